@@ -1,0 +1,240 @@
+/*
+ * moe_ffn.h -- C ABI of the GB300 (sm_103a) grouped MXFP8 MoE expert FFN.
+ *
+ * The library computes the Mixture-of-Experts expert FFN as one grouped
+ * operation instead of a per-expert loop: top-k routing, an expert-major
+ * permutation driven by per-expert token counts (split_sizes), MXFP8
+ * quantization, a grouped gate_up GEMM with ScaledSwiGLU fused into its
+ * epilogue, a grouped down GEMM, the combine, and the matching backward
+ * (dgrad and wgrad).
+ *
+ * Sources.  Page "Efficient MoE Training for Biological Foundation Models"
+ * (summary of the NVIDIA technical blog on the BioNeMo MoE recipe):
+ *   - section "GroupedLinear：把逐专家循环改成一次分组GEMM": one grouped call
+ *     takes the tokens collected per expert plus split_sizes; every expert
+ *     keeps its own weight; gate_up has out_features = 2*intermediate,
+ *     bias=False;
+ *   - section "MXFP8与融合MLP：减少显存并跳过独立量化步骤": gate_up ->
+ *     ScaledSwiGLU (SwiGLU times the router probabilities) -> down, with
+ *     quantization, SwiGLU and the probability scaling fused, forward and
+ *     backward;
+ *   - section "MoE训练的瓶颈与TE的对应能力": MXFP8 holds values in 8 bits with
+ *     one scale per 32 consecutive values; 16-bit master weights are
+ *     quantized before each low-precision GEMM.
+ * Page "英伟达开源MoE加速神器：一行代码，微调快3.7倍", section "三板斧": each
+ * token goes to a few of many experts; the expert FFN is the compute bulk.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library allocates nothing and keeps no state beyond a per-process
+ *     cache of the driver entry point that encodes TMA descriptors.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  No call synchronises the host except
+ *     moe_get_device_error.  split_sizes is never read on the host.
+ *   - Host-checkable errors (sizes, alignment, null pointers) return before
+ *     anything is launched.  Errors detected by a kernel (a bounded wait
+ *     that ran out, an index out of range) are recorded in the workspace
+ *     error word and read with moe_get_device_error; kernels never trap.
+ *   - bf16 means IEEE bfloat16 stored as 2 bytes; f32 is IEEE float.
+ *   - Every pointer must be 16-byte aligned.
+ *
+ * Sizes: T tokens (>= 1), H hidden, I intermediate (H and I multiples of
+ * 128), E experts (1..256), k experts per token (1..min(E, 8)).
+ * R = T*k routed rows.  Permuted buffers have CAP = moe_rows_capacity()
+ * rows: the expert segments are laid out expert-major from row 0, segment e
+ * has roundup(split_sizes[e], 128) rows (rows past split_sizes[e] are zero
+ * padding), and CAP bounds the padded total for every routing.
+ *
+ * MXFP8 tensors.  An MX tensor is (codes, scales):
+ *   codes  uint8 E4M3 (sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ *          max 448, 0x7F/0xFF NaN), row-major [rows][K];
+ *   scales uint8 power-of-two exponents c (scale = 2^(c-127), 255 = NaN),
+ *          one per 32 consecutive elements along K, in the MMA tile layout:
+ *          the scale of (row r, block b = k/32) is stored at byte
+ *              ((r/128)*(K/128) + b/4)*512 + (r%32)*16 + ((r/32)%4)*4 + b%4
+ *          (rows a multiple of 128, K a multiple of 128).  A batch of
+ *          matrices [B][rows][K] uses the same formula on [B*rows][K].
+ *   Quantization rule: e = smallest integer with amax <= 448*2^e (no element
+ *   saturates), clamped to [-127,127], all-zero block -> code 0; elements
+ *   are x*2^-e rounded to nearest-even E4M3 (subnormals and the sign of
+ *   zero kept); a block holding NaN/Inf gets scale 255 and codes 0x7F.
+ *   The page fixes "8 bits" and "one scale per 32 consecutive values"; the
+ *   E4M3 element, the power-of-two scale and this rounding rule are the
+ *   readings this library implements.
+ */
+#ifndef MOE_FFN_H
+#define MOE_FFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,     /* a size or pointer argument is out of range */
+  MOE_ERR_UNSUPPORTED = 2,     /* a valid configuration this build does not handle */
+  MOE_ERR_ALIGNMENT = 3,       /* a pointer is not 16-byte aligned */
+  MOE_ERR_WORKSPACE = 4,       /* workspace missing or smaller than moe_workspace_size */
+  MOE_ERR_CUDA = 5,            /* a CUDA runtime/driver call failed (launch, attribute, TMA encode) */
+  MOE_ERR_DEVICE_TIMEOUT = 6,  /* (device) a bounded wait inside a kernel ran out */
+  MOE_ERR_DEVICE_BOUNDS = 7    /* (device) an index read from device data was out of range */
+} moe_status;
+
+typedef void* moe_stream_t;    /* a cudaStream_t */
+
+typedef struct moe_dims {
+  int32_t T;            /* tokens */
+  int32_t H;            /* hidden size, multiple of 128 */
+  int32_t I;            /* intermediate size, multiple of 128 (gate_up has 2*I outputs) */
+  int32_t E;            /* experts, 1..256 */
+  int32_t k;            /* experts per token, 1..min(E,8) */
+  int32_t renormalize;  /* 1: prob = softmax over the k selected logits; 0: softmax over all E */
+} moe_dims;
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status s);
+
+/* Text of the last host-side error on the calling thread ("" if none). */
+const char* moe_last_error_message(void);
+
+/* Rows of every permuted buffer: roundup(T*k, 128) + 128*E.  Host only. */
+size_t moe_rows_capacity(const moe_dims* d);
+
+/* Bytes of workspace needed by moe_route_permute, grouped_mlp_fwd and (when
+ * training != 0) grouped_mlp_bwd for these sizes.  The workspace is caller
+ * memory, 256-byte aligned, zero-filled once before first use (that clears
+ * the device error word); it may be reused by later calls on the same
+ * stream.  Host only. */
+size_t moe_workspace_size(const moe_dims* d, int32_t training);
+
+/*
+ * mxfp8_quantize -- bf16 -> MX tensor (the quantize step before each GEMM;
+ * page "Efficient MoE Training for Biological Foundation Models", section
+ * "MoE训练的瓶颈与TE的对应能力").  Used for the 16-bit master weights, once
+ * per optimizer step.
+ *   src     bf16 [batch][rows][cols], row-major.
+ *   axis 0: blocks of 32 along cols -> codes [batch][rows][cols],
+ *           scales in the tile layout of [batch*rows][cols].
+ *   axis 1: blocks of 32 along rows -> codes [batch][cols][rows] (each
+ *           matrix transposed), scales in the tile layout of [batch*cols][rows].
+ *   rows and cols multiples of 128, batch >= 1.
+ */
+moe_status mxfp8_quantize(const void* src, int32_t batch, int32_t rows, int32_t cols, int32_t axis,
+                          uint8_t* codes, uint8_t* scales, moe_stream_t stream);
+
+/*
+ * moe_route_permute -- top-k routing, expert-major permutation, gather and
+ * quantization of the tokens (page "Efficient MoE Training for Biological
+ * Foundation Models", section "GroupedLinear": tokens are collected per
+ * expert, split_sizes counts them; page "英伟达开源MoE加速神器", section
+ * "三板斧": each token is routed to a few experts).
+ *   logits      f32 [T][E] (finite)
+ *   x           bf16 [T][H]
+ *   idx         out int32 [T][k]: top-k experts by logit, descending, ties to
+ *               the lower expert index
+ *   prob        out f32 [T][k]: softmax of the selected logits (see renormalize)
+ *   split_sizes out int32 [E]: tokens per expert (sum = T*k)
+ *   row_of      out int32 [T][k]: permuted row of (token, slot); inside an
+ *               expert segment rows follow ascending token index
+ *   src_of      out int32 [CAP]: source token of each row, -1 on padding
+ *               (rows past the padded total are not written)
+ *   prob_perm   out f32 [CAP]: prob of each row, 0 on padding
+ *   xq,xq_scale out MX [CAP][H] of x rows, blocks along H (padding rows zero)
+ *   xq_col,xq_col_scale  optional (both NULL or both set): MX [H][CAP], x
+ *               permuted and quantized in blocks of 32 rows along the token
+ *               axis (blocks start at segment starts; padding is zero) --
+ *               the B operand of the gate_up weight gradient.
+ *   workspace   >= moe_workspace_size(d, xq_col != NULL) bytes.
+ */
+moe_status moe_route_permute(const moe_dims* d, const float* logits, const void* x,
+                             int32_t* idx, float* prob, int32_t* split_sizes,
+                             int32_t* row_of, int32_t* src_of, float* prob_perm,
+                             uint8_t* xq, uint8_t* xq_scale, uint8_t* xq_col, uint8_t* xq_col_scale,
+                             void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * grouped_mlp_fwd -- grouped gate_up GEMM + ScaledSwiGLU + grouped down GEMM
+ * (page "Efficient MoE Training for Biological Foundation Models", sections
+ * "GroupedLinear" and "MXFP8与融合MLP").  One launch per GEMM covers every
+ * expert; the tile schedule is derived on the device from split_sizes.
+ *   xq,xq_scale   MX [CAP][H] from moe_route_permute
+ *   split_sizes   int32 [E] (device)
+ *   prob_perm     f32 [CAP]
+ *   wgu_q,wgu_s   MX [E][2I][H] (mxfp8_quantize axis 0 of W_gu; rows 0..I-1
+ *                 gate, I..2I-1 up)
+ *   wd_q,wd_s     MX [E][H][I]  (mxfp8_quantize axis 0 of W_d)
+ *   y             out bf16 [CAP][H]: expert output of every row (padding 0)
+ *   saved_gu      optional out bf16 [CAP][2I]: g (cols 0..I-1) and u (I..2I-1)
+ *                 as bf16, for the backward
+ *   aq_col,aq_col_scale  optional out MX [I][CAP]: a = silu(g)*u*p quantized
+ *                 along tokens, for the down weight gradient
+ *   Epilogue of the gate_up GEMM: a = silu(g)*u*prob_perm[row], quantized
+ *   rowwise along I into the workspace; no f32/bf16 copy of a is stored.
+ */
+moe_status grouped_mlp_fwd(const moe_dims* d, const uint8_t* xq, const uint8_t* xq_scale,
+                           const int32_t* split_sizes, const float* prob_perm,
+                           const uint8_t* wgu_q, const uint8_t* wgu_s,
+                           const uint8_t* wd_q, const uint8_t* wd_s,
+                           void* y, void* saved_gu, uint8_t* aq_col, uint8_t* aq_col_scale,
+                           void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * grouped_mlp_bwd -- backward of grouped_mlp_fwd with straight-through
+ * quantizers (page "Efficient MoE Training for Biological Foundation
+ * Models", section "MXFP8与融合MLP": the fused op has a matching backward).
+ *   dout          bf16 [T][H]: gradient of the combined output
+ *   split_sizes, row_of, src_of, prob_perm: from moe_route_permute
+ *   saved_gu      bf16 [CAP][2I] from grouped_mlp_fwd
+ *   aq_col,aq_col_scale  MX [I][CAP] from grouped_mlp_fwd
+ *   xq_col,xq_col_scale  MX [H][CAP] from moe_route_permute
+ *   wguT_q,wguT_s MX [E][H][2I] (mxfp8_quantize axis 1 of W_gu)
+ *   wdT_q,wdT_s   MX [E][I][H]  (mxfp8_quantize axis 1 of W_d)
+ *   dx_perm       out bf16 [CAP][H]: input gradient of every row; combine
+ *                 it with moe_unpermute_combine to get dx [T][H]
+ *   dwgu          out bf16 [E][2I][H]; dwd out bf16 [E][H][I] (zeros for
+ *                 experts without tokens)
+ *   dprob         out f32 [T][k]: gradient of prob
+ * Steps: dY = dout gathered to rows and quantized along H and along tokens;
+ * dA = dY*W_d (GEMM, K=H) with the SwiGLU backward fused in its epilogue
+ * (dg = dA*p*u*silu'(g), du = dA*p*silu(g), dp = sum dA*silu(g)*u), writing
+ * dH = [dg|du] quantized along 2I and along tokens; dW_d = dY^T*a (K = each
+ * expert's tokens); dX = dH*W_gu (K = 2I); dW_gu = dH^T*x (K = tokens).
+ */
+moe_status grouped_mlp_bwd(const moe_dims* d, const void* dout,
+                           const int32_t* split_sizes, const int32_t* row_of, const int32_t* src_of,
+                           const float* prob_perm, const void* saved_gu,
+                           const uint8_t* aq_col, const uint8_t* aq_col_scale,
+                           const uint8_t* xq_col, const uint8_t* xq_col_scale,
+                           const uint8_t* wguT_q, const uint8_t* wguT_s,
+                           const uint8_t* wdT_q, const uint8_t* wdT_s,
+                           void* dx_perm, void* dwgu, void* dwd, float* dprob,
+                           void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * moe_unpermute_combine -- out[t] = sum over j of y_perm[row_of[t][j]]
+ * (times prob[t][j] when prob != NULL), f32 sum in slot order, rounded to
+ * bf16.  With the probability already applied in ScaledSwiGLU, prob is NULL
+ * (page "Efficient MoE Training for Biological Foundation Models", section
+ * "MXFP8与融合MLP").  Also combines dx_perm into dx.
+ *   y_perm bf16 [CAP][H], row_of int32 [T][k], prob f32 [T][k] or NULL,
+ *   out bf16 [T][H].
+ */
+moe_status moe_unpermute_combine(const moe_dims* d, const void* y_perm, const int32_t* row_of,
+                                 const float* prob, void* out, moe_stream_t stream);
+
+/* Read (and keep) the device error word of a workspace: *code is a
+ * moe_status (MOE_OK if none), *site identifies the kernel and wait.
+ * Synchronises `stream`. */
+moe_status moe_get_device_error(const void* workspace, int32_t* code, int32_t* site, moe_stream_t stream);
+
+/* Zero the device error word of a workspace (asynchronous on stream). */
+moe_status moe_clear_device_error(void* workspace, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H */

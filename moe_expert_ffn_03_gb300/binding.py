@@ -1,0 +1,146 @@
+"""Thin ctypes binding of libmoeffn.so: one Python function per C entry point,
+same names, argument marshalling only (torch tensors -> device pointers, the
+current CUDA stream).  Every step of the computation runs in the library's
+CUDA kernels; there is no fallback -- a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+c_int32, c_size_t, c_void_p = ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p
+
+EXPORTS = (
+    "moe_status_string", "moe_last_error_message", "moe_rows_capacity", "moe_workspace_size",
+    "mxfp8_quantize", "moe_route_permute", "grouped_mlp_fwd", "grouped_mlp_bwd",
+    "moe_unpermute_combine", "moe_get_device_error", "moe_clear_device_error",
+)
+
+MOE_OK = 0
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
+          4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_DEVICE_TIMEOUT", 7: "MOE_ERR_DEVICE_BOUNDS"}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class MoeDims(ctypes.Structure):
+    _fields_ = [("T", c_int32), ("H", c_int32), ("I", c_int32), ("E", c_int32), ("k", c_int32),
+                ("renormalize", c_int32)]
+
+
+def dims(T, H, I, E, k, renormalize=1) -> MoeDims:
+    return MoeDims(T, H, I, E, k, renormalize)
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoeffn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with moe_expert_ffn_03_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        D = ctypes.POINTER(MoeDims)
+        P = c_void_p
+        sig = {
+            "moe_status_string": ([c_int32], ctypes.c_char_p),
+            "moe_last_error_message": ([], ctypes.c_char_p),
+            "moe_rows_capacity": ([D], c_size_t),
+            "moe_workspace_size": ([D, c_int32], c_size_t),
+            "mxfp8_quantize": ([P, c_int32, c_int32, c_int32, c_int32, P, P, P], c_int32),
+            "moe_route_permute": ([D, P, P, P, P, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
+            "grouped_mlp_fwd": ([D, P, P, P, P, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
+            "grouped_mlp_bwd": ([D] + [P] * 19 + [c_size_t, P], c_int32),
+            "moe_unpermute_combine": ([D, P, P, P, P, P], c_int32),
+            "moe_get_device_error": ([P, ctypes.POINTER(c_int32), ctypes.POINTER(c_int32), P], c_int32),
+            "moe_clear_device_error": ([P, P], c_int32),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def _p(t):
+    if t is None:
+        return None
+    return c_void_p(t.data_ptr())
+
+
+def _st(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return c_void_p(stream.cuda_stream)
+
+
+def _check(status: int):
+    if status != MOE_OK:
+        msg = lib().moe_last_error_message().decode()
+        raise MoeError(status, msg)
+
+
+def moe_rows_capacity(d: MoeDims) -> int:
+    return int(lib().moe_rows_capacity(ctypes.byref(d)))
+
+
+def moe_workspace_size(d: MoeDims, training: bool) -> int:
+    return int(lib().moe_workspace_size(ctypes.byref(d), int(training)))
+
+
+def mxfp8_quantize(src, batch, rows, cols, axis, codes, scales, stream=None):
+    _check(lib().mxfp8_quantize(_p(src), batch, rows, cols, axis, _p(codes), _p(scales), _st(stream)))
+
+
+def moe_route_permute(d, logits, x, idx, prob, split_sizes, row_of, src_of, prob_perm, xq, xq_scale,
+                      xq_col, xq_col_scale, workspace, stream=None):
+    _check(lib().moe_route_permute(ctypes.byref(d), _p(logits), _p(x), _p(idx), _p(prob), _p(split_sizes),
+                                   _p(row_of), _p(src_of), _p(prob_perm), _p(xq), _p(xq_scale), _p(xq_col),
+                                   _p(xq_col_scale), _p(workspace), workspace.numel() * workspace.element_size(),
+                                   _st(stream)))
+
+
+def grouped_mlp_fwd(d, xq, xq_scale, split_sizes, prob_perm, wgu_q, wgu_s, wd_q, wd_s, y, saved_gu, aq_col,
+                    aq_col_scale, workspace, stream=None):
+    _check(lib().grouped_mlp_fwd(ctypes.byref(d), _p(xq), _p(xq_scale), _p(split_sizes), _p(prob_perm), _p(wgu_q),
+                                 _p(wgu_s), _p(wd_q), _p(wd_s), _p(y), _p(saved_gu), _p(aq_col), _p(aq_col_scale),
+                                 _p(workspace), workspace.numel() * workspace.element_size(), _st(stream)))
+
+
+def grouped_mlp_bwd(d, dout, split_sizes, row_of, src_of, prob_perm, saved_gu, aq_col, aq_col_scale, xq_col,
+                    xq_col_scale, wguT_q, wguT_s, wdT_q, wdT_s, dx_perm, dwgu, dwd, dprob, workspace, stream=None):
+    _check(lib().grouped_mlp_bwd(ctypes.byref(d), _p(dout), _p(split_sizes), _p(row_of), _p(src_of), _p(prob_perm),
+                                 _p(saved_gu), _p(aq_col), _p(aq_col_scale), _p(xq_col), _p(xq_col_scale),
+                                 _p(wguT_q), _p(wguT_s), _p(wdT_q), _p(wdT_s), _p(dx_perm), _p(dwgu), _p(dwd),
+                                 _p(dprob), _p(workspace), workspace.numel() * workspace.element_size(),
+                                 _st(stream)))
+
+
+def moe_unpermute_combine(d, y_perm, row_of, prob, out, stream=None):
+    _check(lib().moe_unpermute_combine(ctypes.byref(d), _p(y_perm), _p(row_of), _p(prob), _p(out), _st(stream)))
+
+
+def moe_get_device_error(workspace, stream=None):
+    code, site = c_int32(0), c_int32(0)
+    _check(lib().moe_get_device_error(_p(workspace), ctypes.byref(code), ctypes.byref(site), _st(stream)))
+    return int(code.value), int(site.value)
+
+
+def moe_clear_device_error(workspace, stream=None):
+    _check(lib().moe_clear_device_error(_p(workspace), _st(stream)))

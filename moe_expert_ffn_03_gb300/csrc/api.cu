@@ -1,0 +1,465 @@
+// C ABI of libmoeffn (declared and documented in include/moe_ffn.h): argument
+// checks, workspace layout and the launch sequence of every entry point.
+#include <cstdarg>
+#include <cstdio>
+
+#include "kernels.cuh"
+
+using namespace moe;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+moe_status fail(moe_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+int64_t capacity(const moe_dims* d) { return round_up(int64_t(d->T) * d->k, 128) + 128 * int64_t(d->E); }
+
+moe_status check_dims(const moe_dims* d) {
+  if (d == nullptr) return fail(MOE_ERR_INVALID_ARG, "dims is NULL");
+  if (d->T < 1) return fail(MOE_ERR_INVALID_ARG, "T=%d must be >= 1", d->T);
+  if (d->H < 128 || d->H % 128) return fail(MOE_ERR_UNSUPPORTED, "H=%d must be a positive multiple of 128", d->H);
+  if (d->I < 128 || d->I % 128) return fail(MOE_ERR_UNSUPPORTED, "I=%d must be a positive multiple of 128", d->I);
+  if (d->E < 1 || d->E > 256) return fail(MOE_ERR_UNSUPPORTED, "E=%d must be in 1..256", d->E);
+  if (d->k < 1 || d->k > 8 || d->k > d->E) return fail(MOE_ERR_UNSUPPORTED, "k=%d must be in 1..min(E,8)", d->k);
+  if (d->H > 65536 || d->I > 65536) return fail(MOE_ERR_UNSUPPORTED, "H and I must be <= 65536");
+  const int64_t cap = capacity(d);
+  if (cap > (int64_t(1) << 30)) return fail(MOE_ERR_UNSUPPORTED, "T*k too large (row capacity %lld)", (long long)cap);
+  if (int64_t(d->E) * 2 * d->I > (int64_t(1) << 30) || int64_t(d->E) * d->H > (int64_t(1) << 30))
+    return fail(MOE_ERR_UNSUPPORTED, "E*2I or E*H too large for 32-bit TMA coordinates");
+  return MOE_OK;
+}
+
+struct WsLayout {
+  size_t err, masks, bases, aq, aq_s;
+  size_t dyq, dyq_s, dyqc, dyqc_s, dhq, dhq_s, dhqc, dhqc_s, dp;
+  size_t total;
+};
+
+WsLayout ws_layout(const moe_dims* d, bool training) {
+  WsLayout w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) & ~size_t(255);
+    return o;
+  };
+  const size_t cap = size_t(capacity(d));
+  const size_t G = size_t((d->T + 31) / 32);
+  const size_t H = size_t(d->H), I = size_t(d->I), E = size_t(d->E);
+  w.err = take(256);
+  w.masks = take(E * G * 4);
+  w.bases = take(E * G * 4);
+  w.aq = take(cap * I);
+  w.aq_s = take(cap * I / 32);
+  if (training) {
+    const size_t ntI = (I + 255) / 256;
+    w.dyq = take(cap * H);
+    w.dyq_s = take(cap * H / 32);
+    w.dyqc = take(H * cap);
+    w.dyqc_s = take(H * cap / 32);
+    w.dhq = take(cap * 2 * I);
+    w.dhq_s = take(cap * 2 * I / 32);
+    w.dhqc = take(2 * I * cap);
+    w.dhqc_s = take(2 * I * cap / 32);
+    w.dp = take(ntI * cap * 4);
+  }
+  w.total = off;
+  return w;
+}
+
+moe_status check_ws(const moe_dims* d, const void* ws, size_t bytes, bool training) {
+  if (ws == nullptr) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  const size_t need = ws_layout(d, training).total;
+  if (bytes < need) return fail(MOE_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", bytes, need);
+  return MOE_OK;
+}
+
+#define REQUIRE_PTR(p)                                                                         \
+  do {                                                                                         \
+    if ((p) == nullptr) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", #p);                   \
+    if (!al16(p)) return fail(MOE_ERR_ALIGNMENT, "%s is not 16-byte aligned", #p);            \
+  } while (0)
+
+#define CUDA_TRY(expr, what)                                                                   \
+  do {                                                                                         \
+    cudaError_t e_ = (expr);                                                                   \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what);                                         \
+  } while (0)
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_ALIGNMENT: return "MOE_ERR_ALIGNMENT";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+    case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+const char* moe_last_error_message(void) { return g_msg; }
+
+size_t moe_rows_capacity(const moe_dims* d) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return size_t(capacity(d));
+}
+
+size_t moe_workspace_size(const moe_dims* d, int32_t training) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return ws_layout(d, training != 0).total;
+}
+
+moe_status mxfp8_quantize(const void* src, int32_t batch, int32_t rows, int32_t cols, int32_t axis,
+                          uint8_t* codes, uint8_t* scales, moe_stream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE_PTR(src);
+  REQUIRE_PTR(codes);
+  REQUIRE_PTR(scales);
+  if (batch < 1 || rows < 128 || cols < 128 || rows % 128 || cols % 128)
+    return fail(MOE_ERR_UNSUPPORTED, "batch=%d rows=%d cols=%d: need batch>=1 and rows, cols multiples of 128",
+                batch, rows, cols);
+  if (axis != 0 && axis != 1) return fail(MOE_ERR_INVALID_ARG, "axis=%d must be 0 or 1", axis);
+  if (int64_t(batch) * rows > (int64_t(1) << 31) / 1 || int64_t(batch) * cols > (int64_t(1) << 31))
+    return fail(MOE_ERR_UNSUPPORTED, "tensor too large");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (axis == 0) {
+    const int64_t n = int64_t(batch) * rows;
+    CUDA_TRY(launch_quant_rowwise(src, n, cols, nullptr, 1, n, codes, scales, nullptr, st), "quant_rowwise");
+  } else {
+    CUDA_TRY(launch_quant_colwise(src, nullptr, int64_t(batch) * rows, batch, rows, cols, nullptr, 0, codes, scales,
+                                  nullptr, st),
+             "quant_colwise");
+  }
+  return MOE_OK;
+}
+
+moe_status moe_route_permute(const moe_dims* d, const float* logits, const void* x, int32_t* idx, float* prob,
+                             int32_t* split_sizes, int32_t* row_of, int32_t* src_of, float* prob_perm,
+                             uint8_t* xq, uint8_t* xq_scale, uint8_t* xq_col, uint8_t* xq_col_scale,
+                             void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  REQUIRE_PTR(logits);
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(idx);
+  REQUIRE_PTR(prob);
+  REQUIRE_PTR(split_sizes);
+  REQUIRE_PTR(row_of);
+  REQUIRE_PTR(src_of);
+  REQUIRE_PTR(prob_perm);
+  REQUIRE_PTR(xq);
+  REQUIRE_PTR(xq_scale);
+  if ((xq_col == nullptr) != (xq_col_scale == nullptr))
+    return fail(MOE_ERR_INVALID_ARG, "xq_col and xq_col_scale must both be set or both be NULL");
+  if (xq_col != nullptr) {
+    REQUIRE_PTR(xq_col);
+    REQUIRE_PTR(xq_col_scale);
+  }
+  s = check_ws(d, workspace, workspace_bytes, false);
+  if (s != MOE_OK) return s;
+  const WsLayout w = ws_layout(d, false);
+  int* err = at<int>(workspace, w.err);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t cap = capacity(d);
+  CUDA_TRY(launch_route_permute(logits, d->T, d->E, d->k, d->renormalize, idx, prob, at<uint32_t>(workspace, w.masks),
+                                at<int>(workspace, w.bases), split_sizes, row_of, src_of, prob_perm, err, st),
+           "route_permute");
+  CUDA_TRY(launch_quant_rowwise(x, d->T, d->H, row_of, d->k, cap, xq, xq_scale, err, st), "gather_quant_rowwise");
+  CUDA_TRY(launch_fill_pad_rows(split_sizes, d->E, d->H, xq, xq_scale, st), "fill_pad_rows");
+  if (xq_col != nullptr)
+    CUDA_TRY(launch_quant_colwise(x, src_of, d->T, 1, int(cap), d->H, split_sizes, d->E, xq_col, xq_col_scale, err,
+                                  st),
+             "gather_quant_colwise");
+  return MOE_OK;
+}
+
+moe_status grouped_mlp_fwd(const moe_dims* d, const uint8_t* xq, const uint8_t* xq_scale, const int32_t* split_sizes,
+                           const float* prob_perm, const uint8_t* wgu_q, const uint8_t* wgu_s, const uint8_t* wd_q,
+                           const uint8_t* wd_s, void* y, void* saved_gu, uint8_t* aq_col, uint8_t* aq_col_scale,
+                           void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  REQUIRE_PTR(xq);
+  REQUIRE_PTR(xq_scale);
+  REQUIRE_PTR(split_sizes);
+  REQUIRE_PTR(prob_perm);
+  REQUIRE_PTR(wgu_q);
+  REQUIRE_PTR(wgu_s);
+  REQUIRE_PTR(wd_q);
+  REQUIRE_PTR(wd_s);
+  REQUIRE_PTR(y);
+  if (saved_gu != nullptr) REQUIRE_PTR(saved_gu);
+  if ((aq_col == nullptr) != (aq_col_scale == nullptr))
+    return fail(MOE_ERR_INVALID_ARG, "aq_col and aq_col_scale must both be set or both be NULL");
+  if (aq_col != nullptr) {
+    REQUIRE_PTR(aq_col);
+    REQUIRE_PTR(aq_col_scale);
+  }
+  s = check_ws(d, workspace, workspace_bytes, false);
+  if (s != MOE_OK) return s;
+  const WsLayout w = ws_layout(d, false);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t cap = capacity(d);
+  const int H = d->H, I = d->I, E = d->E;
+
+  GemmArgs g1{};
+  g1.mode = 0;
+  g1.E = E;
+  g1.split_sizes = split_sizes;
+  g1.K = H;
+  g1.N = I;
+  g1.n_tiles = I / 128;
+  g1.b_rows_per_expert = 2 * int64_t(I);
+  g1.cap = cap;
+  g1.sfa = xq_scale;
+  g1.sfb = wgu_s;
+  g1.sfa_K = H;
+  g1.sfb_K = H;
+  g1.prob_perm = prob_perm;
+  g1.q_row = at<uint8_t>(workspace, w.aq);
+  g1.q_row_s = at<uint8_t>(workspace, w.aq_s);
+  g1.q_row_K = I;
+  g1.q_col = aq_col;
+  g1.q_col_s = aq_col_scale;
+  g1.gu = static_cast<__nv_bfloat16*>(saved_gu);
+  g1.I = I;
+  g1.err = at<int>(workspace, w.err);
+  CUDA_TRY(launch_grouped_gemm(EPI_FWD_SWIGLU, g1, xq, cap, H, wgu_q, int64_t(E) * 2 * I, H, (cap / 128) * g1.n_tiles,
+                               st, g_msg, sizeof(g_msg)),
+           "grouped gate_up GEMM");
+
+  GemmArgs g2{};
+  g2.mode = 0;
+  g2.E = E;
+  g2.split_sizes = split_sizes;
+  g2.K = I;
+  g2.N = H;
+  g2.n_tiles = (H + 255) / 256;
+  g2.b_rows_per_expert = H;
+  g2.cap = cap;
+  g2.sfa = g1.q_row_s;
+  g2.sfb = wd_s;
+  g2.sfa_K = I;
+  g2.sfb_K = I;
+  g2.out = static_cast<__nv_bfloat16*>(y);
+  g2.ldo = H;
+  g2.I = I;
+  g2.err = g1.err;
+  CUDA_TRY(launch_grouped_gemm(EPI_BF16, g2, g1.q_row, cap, I, wd_q, int64_t(E) * H, I, (cap / 128) * g2.n_tiles, st,
+                               g_msg, sizeof(g_msg)),
+           "grouped down GEMM");
+  return MOE_OK;
+}
+
+moe_status grouped_mlp_bwd(const moe_dims* d, const void* dout, const int32_t* split_sizes, const int32_t* row_of,
+                           const int32_t* src_of, const float* prob_perm, const void* saved_gu, const uint8_t* aq_col,
+                           const uint8_t* aq_col_scale, const uint8_t* xq_col, const uint8_t* xq_col_scale,
+                           const uint8_t* wguT_q, const uint8_t* wguT_s, const uint8_t* wdT_q, const uint8_t* wdT_s,
+                           void* dx_perm, void* dwgu, void* dwd, float* dprob, void* workspace,
+                           size_t workspace_bytes, moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  REQUIRE_PTR(dout);
+  REQUIRE_PTR(split_sizes);
+  REQUIRE_PTR(row_of);
+  REQUIRE_PTR(src_of);
+  REQUIRE_PTR(prob_perm);
+  REQUIRE_PTR(saved_gu);
+  REQUIRE_PTR(aq_col);
+  REQUIRE_PTR(aq_col_scale);
+  REQUIRE_PTR(xq_col);
+  REQUIRE_PTR(xq_col_scale);
+  REQUIRE_PTR(wguT_q);
+  REQUIRE_PTR(wguT_s);
+  REQUIRE_PTR(wdT_q);
+  REQUIRE_PTR(wdT_s);
+  REQUIRE_PTR(dx_perm);
+  REQUIRE_PTR(dwgu);
+  REQUIRE_PTR(dwd);
+  REQUIRE_PTR(dprob);
+  s = check_ws(d, workspace, workspace_bytes, true);
+  if (s != MOE_OK) return s;
+  const WsLayout w = ws_layout(d, true);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t cap = capacity(d);
+  const int H = d->H, I = d->I, E = d->E, k = d->k;
+  int* err = at<int>(workspace, w.err);
+  uint8_t* dyq = at<uint8_t>(workspace, w.dyq);
+  uint8_t* dyq_s = at<uint8_t>(workspace, w.dyq_s);
+  uint8_t* dyqc = at<uint8_t>(workspace, w.dyqc);
+  uint8_t* dyqc_s = at<uint8_t>(workspace, w.dyqc_s);
+  uint8_t* dhq = at<uint8_t>(workspace, w.dhq);
+  uint8_t* dhq_s = at<uint8_t>(workspace, w.dhq_s);
+  uint8_t* dhqc = at<uint8_t>(workspace, w.dhqc);
+  uint8_t* dhqc_s = at<uint8_t>(workspace, w.dhqc_s);
+  float* dp = at<float>(workspace, w.dp);
+
+  // dY rows: gathered dout quantized along H (dgrad) and along tokens (wgrad)
+  CUDA_TRY(launch_quant_rowwise(dout, d->T, H, row_of, k, cap, dyq, dyq_s, err, st), "dout gather_quant_rowwise");
+  CUDA_TRY(launch_fill_pad_rows(split_sizes, E, H, dyq, dyq_s, st), "dout fill_pad_rows");
+  CUDA_TRY(launch_quant_colwise(dout, src_of, d->T, 1, int(cap), H, split_sizes, E, dyqc, dyqc_s, err, st),
+           "dout gather_quant_colwise");
+
+  // down dgrad + fused SwiGLU backward: dA = dY * W_d -> dH (both axes), dp partials
+  GemmArgs g3{};
+  g3.mode = 0;
+  g3.E = E;
+  g3.split_sizes = split_sizes;
+  g3.K = H;
+  g3.N = I;
+  g3.n_tiles = (I + 255) / 256;
+  g3.b_rows_per_expert = I;
+  g3.cap = cap;
+  g3.sfa = dyq_s;
+  g3.sfb = wdT_s;
+  g3.sfa_K = H;
+  g3.sfb_K = H;
+  g3.prob_perm = prob_perm;
+  g3.q_row = dhq;
+  g3.q_row_s = dhq_s;
+  g3.q_row_K = 2 * int64_t(I);
+  g3.q_col = dhqc;
+  g3.q_col_s = dhqc_s;
+  g3.gu = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(saved_gu));
+  g3.dp_part = dp;
+  g3.I = I;
+  g3.err = err;
+  CUDA_TRY(launch_grouped_gemm(EPI_BWD_SWIGLU, g3, dyq, cap, H, wdT_q, int64_t(E) * I, H, (cap / 128) * g3.n_tiles,
+                               st, g_msg, sizeof(g_msg)),
+           "down dgrad GEMM");
+  CUDA_TRY(launch_dprob_reduce(dp, g3.n_tiles, cap, row_of, int64_t(d->T) * k, dprob, err, st), "dprob reduce");
+
+  // down wgrad: dW_d[e] = dY_e^T a_e, K = the expert's tokens
+  GemmArgs g4{};
+  g4.mode = 1;
+  g4.E = E;
+  g4.split_sizes = split_sizes;
+  g4.M = H;
+  g4.N = I;
+  g4.n_tiles = (I + 255) / 256;
+  g4.cap = cap;
+  g4.sfa = dyqc_s;
+  g4.sfb = aq_col_scale;
+  g4.sfa_K = cap;
+  g4.sfb_K = cap;
+  g4.out = static_cast<__nv_bfloat16*>(dwd);
+  g4.ldo = I;
+  g4.I = I;
+  g4.err = err;
+  CUDA_TRY(launch_grouped_gemm(EPI_BF16, g4, dyqc, H, cap, aq_col, I, cap, int64_t(E) * (H / 128) * g4.n_tiles, st,
+                               g_msg, sizeof(g_msg)),
+           "down wgrad GEMM");
+
+  // gate_up dgrad: dX = dH * W_gu (K = 2I)
+  GemmArgs g5{};
+  g5.mode = 0;
+  g5.E = E;
+  g5.split_sizes = split_sizes;
+  g5.K = 2 * I;
+  g5.N = H;
+  g5.n_tiles = (H + 255) / 256;
+  g5.b_rows_per_expert = H;
+  g5.cap = cap;
+  g5.sfa = dhq_s;
+  g5.sfb = wguT_s;
+  g5.sfa_K = 2 * int64_t(I);
+  g5.sfb_K = 2 * int64_t(I);
+  g5.out = static_cast<__nv_bfloat16*>(dx_perm);
+  g5.ldo = H;
+  g5.I = I;
+  g5.err = err;
+  CUDA_TRY(launch_grouped_gemm(EPI_BF16, g5, dhq, cap, 2 * int64_t(I), wguT_q, int64_t(E) * H, 2 * int64_t(I),
+                               (cap / 128) * g5.n_tiles, st, g_msg, sizeof(g_msg)),
+           "gate_up dgrad GEMM");
+
+  // gate_up wgrad: dW_gu[e] = dH_e^T x_e, K = the expert's tokens
+  GemmArgs g6{};
+  g6.mode = 1;
+  g6.E = E;
+  g6.split_sizes = split_sizes;
+  g6.M = 2 * I;
+  g6.N = H;
+  g6.n_tiles = (H + 255) / 256;
+  g6.cap = cap;
+  g6.sfa = dhqc_s;
+  g6.sfb = xq_col_scale;
+  g6.sfa_K = cap;
+  g6.sfb_K = cap;
+  g6.out = static_cast<__nv_bfloat16*>(dwgu);
+  g6.ldo = H;
+  g6.I = I;
+  g6.err = err;
+  CUDA_TRY(launch_grouped_gemm(EPI_BF16, g6, dhqc, 2 * int64_t(I), cap, xq_col, H, cap,
+                               int64_t(E) * (2 * I / 128) * g6.n_tiles, st, g_msg, sizeof(g_msg)),
+           "gate_up wgrad GEMM");
+  return MOE_OK;
+}
+
+moe_status moe_unpermute_combine(const moe_dims* d, const void* y_perm, const int32_t* row_of, const float* prob,
+                                 void* out, moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  REQUIRE_PTR(y_perm);
+  REQUIRE_PTR(row_of);
+  REQUIRE_PTR(out);
+  if (prob != nullptr && (reinterpret_cast<uintptr_t>(prob) & 3u))
+    return fail(MOE_ERR_ALIGNMENT, "prob is not 4-byte aligned");
+  CUDA_TRY(launch_combine(y_perm, row_of, prob, d->T, d->k, d->H, capacity(d), out, nullptr,
+                          static_cast<cudaStream_t>(stream)),
+           "combine");
+  return MOE_OK;
+}
+
+moe_status moe_get_device_error(const void* workspace, int32_t* code, int32_t* site, moe_stream_t stream) {
+  g_msg[0] = 0;
+  if (workspace == nullptr || code == nullptr || site == nullptr)
+    return fail(MOE_ERR_INVALID_ARG, "workspace, code and site must be non-NULL");
+  int32_t h[2] = {0, 0};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CUDA_TRY(cudaMemcpyAsync(h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st), "read error word");
+  CUDA_TRY(cudaStreamSynchronize(st), "synchronize");
+  *code = h[0];
+  *site = h[1];
+  return MOE_OK;
+}
+
+moe_status moe_clear_device_error(void* workspace, moe_stream_t stream) {
+  g_msg[0] = 0;
+  if (workspace == nullptr) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  CUDA_TRY(cudaMemsetAsync(workspace, 0, 8, static_cast<cudaStream_t>(stream)), "clear error word");
+  return MOE_OK;
+}
+
+}  // extern "C"

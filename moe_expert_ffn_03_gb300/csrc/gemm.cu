@@ -1,0 +1,608 @@
+// Grouped block-scaled MXFP8 GEMM on the sm_103a tensor cores (tcgen05).
+//
+// Page "Efficient MoE Training for Biological Foundation Models":
+//   section "GroupedLinear": all experts' GEMMs are submitted as ONE grouped
+//   operation driven by split_sizes instead of one launch per expert;
+//   section "MXFP8与融合MLP": MXFP8 GEMMs run on dedicated Blackwell tensor
+//   core instructions, and quantization, SwiGLU and the router-probability
+//   scaling are fused into the grouped MLP so no intermediate is stored in
+//   high precision.
+//
+// Design (one CTA per SM, persistent):
+//   warp 0      TMA producer: 128x128 A box + one or two 128x128 B boxes
+//               (128B swizzle) and the 512-byte scale atoms (bulk copies)
+//               per 128-deep K step into a 4-stage shared-memory ring.
+//   warp 1      TMEM allocator and MMA issuer: per stage, tcgen05.cp moves
+//               the scale atoms into TMEM, then four
+//               tcgen05.mma.kind::mxf8f6f4.block_scale (M=128, N=256 or 128,
+//               K=32) accumulate in TMEM (fp32, 256 columns); tcgen05.commit
+//               frees the stage and, after the last K step, hands the
+//               accumulator to the epilogue.
+//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter (= 32 rows),
+//               fused epilogue (bf16 store, ScaledSwiGLU + re-quantization,
+//               or SwiGLU backward + re-quantization), then release TMEM.
+// Tiles: mode 0 walks the 128-row blocks of every expert segment (computed on
+// the device from split_sizes; empty experts get no tile) times the N tiles,
+// rasterised in groups of 8 row blocks; mode 1 (weight gradients) walks
+// expert x M tiles x N tiles with K = the expert's padded token range.
+// Every mbarrier wait is bounded; on expiry the CTA records
+// MOE_ERR_DEVICE_TIMEOUT, stops issuing, drains its copies and MMAs, frees
+// TMEM and returns.
+#include <cuda.h>
+
+#include <cstdio>
+
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128;
+constexpr int STAGES = 4;
+constexpr int A_TILE = BM * BK;                 // 16 KB of E4M3
+constexpr int B_HALF = 128 * BK;                // 16 KB
+constexpr int B_TILE = BN * BK;                 // 32 KB
+constexpr int SF_ATOM = 512;                    // 128 rows x 4 scale bytes
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_ACC = 0, TM_SFA = 256, TM_SFB = 260;
+constexpr int GROUP_M = 8;
+
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + STAGES * A_TILE;
+constexpr int OFF_SFA = OFF_B + STAGES * B_TILE;
+constexpr int OFF_SFB = OFF_SFA + STAGES * SF_ATOM;
+constexpr int OFF_BAR = OFF_SFB + STAGES * 2 * SF_ATOM;
+constexpr int NUM_BARS = 2 * STAGES + 3;        // full[S], empty[S], tmem_full, tmem_empty, drain
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int OFF_SEG = OFF_MISC + 16;
+constexpr int SMEM_USED = OFF_SEG + 260 * 4;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;    // slack to align the base to 1024 B
+
+// ---- PTX wrappers -------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tc_mma_mxf8(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+      ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor, K-major operand staged by TMA with 128-byte
+// swizzle: 8-row x 128-byte swizzle atoms stacked every 1024 bytes (SBO);
+// the leading-dimension offset is unused for swizzled K-major layouts.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);
+  d |= uint64_t(1) << 16;                 // LBO (ignored), encoded 16 B
+  d |= uint64_t(1024 >> 4) << 32;         // SBO
+  d |= uint64_t(1) << 46;                 // descriptor version of the sm_100 family
+  d |= uint64_t(2) << 61;                 // SWIZZLE_128B
+  return d;
+}
+// Descriptor of one 512-byte scale atom as 32 rows x 16 bytes, no swizzle:
+// 8-row core matrices every 128 bytes.
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);
+  d |= uint64_t(128 >> 4) << 32;
+  d |= uint64_t(1) << 46;
+  return d;
+}
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: E4M3 x E4M3,
+// both K-major, UE8M0 scales, scale-factor ids select the byte (= 32-block of
+// the 128-deep K step) inside each 32-bit TMEM scale word.
+__device__ __forceinline__ uint32_t idesc_mxf8(int N, int sf_id) {
+  return (uint32_t(sf_id) << 4)            // B scale factor id
+         | (0u << 7) | (0u << 10)          // A, B format E4M3
+         | (uint32_t(N >> 3) << 17)        // N / 8
+         | (1u << 23)                      // scale format UE8M0
+         | (uint32_t(BM >> 4) << 24)       // M / 16
+         | (uint32_t(sf_id) << 29);        // A scale factor id
+}
+
+struct Tile {
+  int e;
+  int nb;
+  int k_tiles;
+  int n0;
+  bool second;            // the second 128-row half of B (columns n0+128.. or the up half) is present
+  int64_t a_row;          // row of A
+  int64_t k0;             // first K element
+  int64_t b_row0, b_row1; // rows of B for the two halves
+  int64_t out_row;        // output row of tile row 0 (mode 1: e*M + a_row)
+};
+
+__device__ __forceinline__ int tile_count(const GemmArgs& a, const int* seg_mb) {
+  if (a.mode == 0) return seg_mb[a.E] * a.n_tiles;
+  return a.E * (a.M / BM) * a.n_tiles;
+}
+
+template <int EPI>
+__device__ __forceinline__ void decode_tile(const GemmArgs& a, const int* seg_mb, int t, Tile& tl) {
+  if (a.mode == 0) {
+    const int total_mb = seg_mb[a.E];
+    const int per_group = GROUP_M * a.n_tiles;
+    const int group = t / per_group;
+    const int first = group * GROUP_M;
+    const int gs = min(GROUP_M, total_mb - first);
+    const int local = t - group * per_group;
+    const int mb = first + local % gs;
+    const int nb = local / gs;
+    int lo = 0, hi = a.E - 1;            // largest e with seg_mb[e] <= mb
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (seg_mb[mid] <= mb) lo = mid; else hi = mid - 1;
+    }
+    tl.e = lo;
+    tl.nb = nb;
+    tl.a_row = int64_t(mb) * BM;
+    tl.k0 = 0;
+    tl.k_tiles = a.K / BK;
+    tl.out_row = tl.a_row;
+    if (EPI == EPI_FWD_SWIGLU) {
+      tl.n0 = nb * 128;
+      tl.b_row0 = int64_t(lo) * a.b_rows_per_expert + tl.n0;
+      tl.b_row1 = tl.b_row0 + a.I;
+      tl.second = true;
+    } else {
+      tl.n0 = nb * BN;
+      tl.b_row0 = int64_t(lo) * a.b_rows_per_expert + tl.n0;
+      tl.b_row1 = tl.b_row0 + 128;
+      tl.second = (tl.n0 + 128) < a.N;
+    }
+  } else {
+    const int m_tiles = a.M / BM;
+    const int per_e = m_tiles * a.n_tiles;
+    const int e = t / per_e;
+    const int rem = t - e * per_e;
+    const int mb = rem / a.n_tiles;
+    const int nb = rem - mb * a.n_tiles;
+    tl.e = e;
+    tl.nb = nb;
+    tl.a_row = int64_t(mb) * BM;
+    tl.k0 = int64_t(seg_mb[e]) * BK;
+    tl.k_tiles = seg_mb[e + 1] - seg_mb[e];
+    tl.n0 = nb * BN;
+    tl.b_row0 = tl.n0;
+    tl.b_row1 = tl.n0 + 128;
+    tl.second = (tl.n0 + 128) < a.N;
+    tl.out_row = int64_t(e) * a.M + tl.a_row;
+  }
+}
+
+// Bounded wait on an mbarrier phase.  Returns false when the CTA aborted or
+// the limit ran out (then records the timeout and raises the abort flag).
+__device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                        int site, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++n & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        report_error(err, MOE_ERR_DEVICE_TIMEOUT, site);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// ---- epilogues ---------------------------------------------------------------------
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, const float (&v)[32]) {
+  uint4* p4 = reinterpret_cast<uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    p4[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                       pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+}
+
+// 32 values of one column block (this thread's row) quantized rowwise; the scale
+// of (row, block) goes to the tile layout with row length K.
+__device__ __forceinline__ void quant_row_block(const float (&v)[32], uint8_t* codes, uint8_t* scales,
+                                                int64_t row, int64_t col, int64_t K) {
+  uint32_t q[8];
+  const uint32_t c = mx_quant32(v, q);
+  store_codes32(codes + row * K + col, q);
+  scales[sf_offset(row, col >> 5, K)] = uint8_t(c);
+}
+
+// The same 32 columns quantized along tokens: the warp's 32 lanes are 32
+// consecutive permuted rows (one MX block).  Column col+i becomes row col+i of
+// the transposed [cols][cap] tensor; lane i stores that row's scale.
+__device__ __forceinline__ void quant_col_block(const float (&v)[32], uint8_t* codes_t, uint8_t* scales_t,
+                                                int64_t row, int64_t row_blk0, int64_t col, int64_t cap,
+                                                int lane) {
+  uint32_t my_c = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t amax = __reduce_max_sync(0xFFFFFFFFu, abs_bits(v[i]));
+    const uint32_t c = mx_scale_code(amax);
+    codes_t[(col + i) * cap + row] = uint8_t(mx_quant1(v[i], c));
+    if (lane == i) my_c = c;
+  }
+  scales_t[sf_offset(col + lane, row_blk0 >> 5, cap)] = uint8_t(my_c);
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+template <int EPI>
+__device__ __forceinline__ void run_epilogue(const GemmArgs& a, const Tile& tl, uint32_t tmem_row, int q,
+                                             int lane) {
+  const int64_t row = tl.out_row + q * 32 + lane;       // output / permuted row of this thread
+  const int64_t row_blk0 = tl.out_row + q * 32;
+  if (EPI == EPI_BF16) {
+    const int nchunks = tl.second ? 8 : 4;
+    __nv_bfloat16* orow = a.out + row * a.ldo + tl.n0;
+    for (int c = 0; c < nchunks; ++c) {
+      float v[32];
+      if (tl.k_tiles > 0) {
+        tmem_ld32(tmem_row + TM_ACC + c * 32, v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      }
+      store_bf16x32(orow + c * 32, v);
+    }
+  } else if (EPI == EPI_FWD_SWIGLU) {
+    const float p = a.prob_perm[row];
+    const int64_t twoI = 2 * int64_t(a.I);
+    for (int c = 0; c < 4; ++c) {
+      float g[32], u[32];
+      tmem_ld32(tmem_row + TM_ACC + c * 32, g);
+      tmem_ld32(tmem_row + TM_ACC + 128 + c * 32, u);
+      const int64_t col = tl.n0 + c * 32;
+      if (a.gu != nullptr) {
+        store_bf16x32(a.gu + row * twoI + col, g);
+        store_bf16x32(a.gu + row * twoI + a.I + col, u);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i] * p;
+      quant_row_block(g, a.q_row, a.q_row_s, row, col, a.q_row_K);
+      if (a.q_col != nullptr) quant_col_block(g, a.q_col, a.q_col_s, row, row_blk0, col, a.cap, lane);
+    }
+  } else {  // EPI_BWD_SWIGLU
+    const float p = a.prob_perm[row];
+    const int64_t twoI = 2 * int64_t(a.I);
+    const int nchunks = tl.second ? 8 : 4;
+    float dp = 0.f;
+    for (int c = 0; c < nchunks; ++c) {
+      float d[32], g[32], u[32];
+      tmem_ld32(tmem_row + TM_ACC + c * 32, d);
+      const int64_t col = tl.n0 + c * 32;
+      load_bf16x32(a.gu + row * twoI + col, g);
+      load_bf16x32(a.gu + row * twoI + a.I + col, u);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float s = 1.0f / (1.0f + __expf(-g[i]));
+        const float sg = g[i] * s;
+        const float ds = s * (1.0f + g[i] * (1.0f - s));
+        const float dpu = d[i] * p;
+        dp += d[i] * sg * u[i];
+        g[i] = dpu * u[i] * ds;     // dg
+        u[i] = dpu * sg;            // du
+      }
+      quant_row_block(g, a.q_row, a.q_row_s, row, col, twoI);
+      quant_row_block(u, a.q_row, a.q_row_s, row, a.I + col, twoI);
+      quant_col_block(g, a.q_col, a.q_col_s, row, row_blk0, col, a.cap, lane);
+      quant_col_block(u, a.q_col, a.q_col_s, row, row_blk0, a.I + col, a.cap, lane);
+    }
+    a.dp_part[int64_t(tl.nb) * a.cap + row] = dp;
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tmem_full = empty + STAGES;
+  uint64_t* tmem_empty = tmem_full + 1;
+  uint64_t* drain = tmem_empty + 1;
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_s = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  int* seg_mb = reinterpret_cast<int*>(smem + OFF_SEG);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, 4);
+    mbar_init(drain, 1);
+    *abort_s = 0;
+    int acc = 0;
+    for (int e = 0; e < args.E; ++e) {
+      seg_mb[e] = acc;
+      acc += (args.split_sizes[e] + 127) >> 7;
+    }
+    seg_mb[args.E] = acc;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_base_s, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_s;
+  const int total = tile_count(args, seg_mb);
+  // the padded segments must fit the permuted capacity (rows in mode 0, K in mode 1)
+  if (int64_t(seg_mb[args.E]) * BM > args.cap) {
+    if (threadIdx.x == 0) report_error(args.err, MOE_ERR_DEVICE_BOUNDS, SITE_GEMM_PRODUCER + 9);
+  } else if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int it = 0;
+      int last_round[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) last_round[s] = -1;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        Tile tl;
+        decode_tile<EPI>(args, seg_mb, t, tl);
+        const int64_t sfa_row_atoms = args.sfa_K / BK;
+        const int64_t sfb_row_atoms = args.sfb_K / BK;
+        const uint8_t* sfa = args.sfa + ((tl.a_row / BM) * sfa_row_atoms + tl.k0 / BK) * SF_ATOM;
+        const uint8_t* sfb0 = args.sfb + ((tl.b_row0 / 128) * sfb_row_atoms + tl.k0 / BK) * SF_ATOM;
+        const uint8_t* sfb1 = args.sfb + ((tl.b_row1 / 128) * sfb_row_atoms + tl.k0 / BK) * SF_ATOM;
+        const uint32_t bytes = A_TILE + SF_ATOM * 2 + (tl.second ? (B_HALF * 2 + SF_ATOM) : B_HALF);
+        for (int kt = 0; kt < tl.k_tiles; ++kt, ++it) {
+          const int s = it % STAGES;
+          const int round = it / STAGES;
+          if (!wait_phase(&empty[s], (round & 1) ^ 1, abort_s, args.err, SITE_GEMM_PRODUCER, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], bytes);
+          last_round[s] = round;
+          const int kc = int(tl.k0) + kt * BK;
+          tma_load_2d(smem + OFF_A + s * A_TILE, &tmA, kc, int(tl.a_row), &full[s]);
+          tma_load_2d(smem + OFF_B + s * B_TILE, &tmB, kc, int(tl.b_row0), &full[s]);
+          if (tl.second) tma_load_2d(smem + OFF_B + s * B_TILE + B_HALF, &tmB, kc, int(tl.b_row1), &full[s]);
+          bulk_load(smem + OFF_SFA + s * SF_ATOM, sfa + kt * SF_ATOM, SF_ATOM, &full[s]);
+          bulk_load(smem + OFF_SFB + s * 2 * SF_ATOM, sfb0 + kt * SF_ATOM, SF_ATOM, &full[s]);
+          if (tl.second) bulk_load(smem + OFF_SFB + s * 2 * SF_ATOM + SF_ATOM, sfb1 + kt * SF_ATOM, SF_ATOM, &full[s]);
+        }
+      }
+      if (!ok) {
+        // let copies already issued land before the CTA exits
+        for (int s = 0; s < STAGES; ++s) {
+          if (last_round[s] < 0) continue;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&full[s], last_round[s] & 1) && globaltimer_ns() - t0 < 20000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int it = 0, tcount = 0;
+      bool ok = true, issued = false;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
+        Tile tl;
+        decode_tile<EPI>(args, seg_mb, t, tl);
+        if (!wait_phase(tmem_empty, (tcount & 1) ^ 1, abort_s, args.err, SITE_GEMM_MMA_ACC, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int n = tl.second ? 256 : 128;
+        for (int kt = 0; kt < tl.k_tiles; ++kt, ++it) {
+          const int s = it % STAGES;
+          const int round = it / STAGES;
+          if (!wait_phase(&full[s], round & 1, abort_s, args.err, SITE_GEMM_MMA, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          tc_cp_sf(tmem + TM_SFA, desc_sf(smem_u32(smem + OFF_SFA + s * SF_ATOM)));
+          tc_cp_sf(tmem + TM_SFB, desc_sf(smem_u32(smem + OFF_SFB + s * 2 * SF_ATOM)));
+          if (tl.second) tc_cp_sf(tmem + TM_SFB + 4, desc_sf(smem_u32(smem + OFF_SFB + s * 2 * SF_ATOM + SF_ATOM)));
+          const uint64_t adesc = desc_sw128(smem_u32(smem + OFF_A + s * A_TILE));
+          const uint64_t bdesc = desc_sw128(smem_u32(smem + OFF_B + s * B_TILE));
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            // +32 bytes along K inside the 128-byte swizzle atom = +2 in the encoded start address
+            tc_mma_mxf8(tmem + TM_ACC, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_mxf8(n, kk),
+                        tmem + TM_SFA, tmem + TM_SFB, (kt | kk) != 0);
+          }
+          issued = true;
+          tc_commit(&empty[s]);
+        }
+        if (!ok) break;
+        tc_commit(tmem_full);
+      }
+      if (!ok && issued) {
+        tc_commit(drain);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < 20000000ull) {
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 ----------------
+    const int q = warp & 3;                    // TMEM lane quarter this warp may access
+    const uint32_t tmem_row = tmem + (uint32_t(q * 32) << 16);
+    int tcount = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
+      Tile tl;
+      decode_tile<EPI>(args, seg_mb, t, tl);
+      if (!wait_phase(tmem_full, tcount & 1, abort_s, args.err, SITE_GEMM_EPILOGUE, kWaitLimitNs)) break;
+      tc_fence_after();
+      run_epilogue<EPI>(args, tl, tmem_row, q, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// ---- host side -----------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D map over a row-major uint8 [rows][K] tensor, 128x128 boxes, 128-byte swizzle.
+bool encode_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(K)};
+  cuuint32_t box[2] = {BK, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI>
+cudaError_t launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a, int grid, cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  grouped_gemm_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ma, mb, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64_t a_rows, int64_t a_K,
+                                const void* B, int64_t b_rows, int64_t b_K, int64_t max_tiles, cudaStream_t st,
+                                char* msg, size_t msg_len) {
+  if (max_tiles <= 0) return cudaSuccess;
+  CUtensorMap ma, mb;
+  if (!encode_map(&ma, A, a_rows, a_K) || !encode_map(&mb, B, b_rows, b_K)) {
+    snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed (A %lld x %lld, B %lld x %lld)", (long long)a_rows,
+             (long long)a_K, (long long)b_rows, (long long)b_K);
+    return cudaErrorInvalidValue;
+  }
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = int(max_tiles < sms ? max_tiles : sms);
+  switch (epi) {
+    case EPI_BF16: return launch_epi<EPI_BF16>(ma, mb, a, grid, st);
+    case EPI_FWD_SWIGLU: return launch_epi<EPI_FWD_SWIGLU>(ma, mb, a, grid, st);
+    case EPI_BWD_SWIGLU: return launch_epi<EPI_BWD_SWIGLU>(ma, mb, a, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moe

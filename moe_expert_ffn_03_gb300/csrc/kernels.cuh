@@ -1,0 +1,66 @@
+// Launchers of the libmoeffn kernels (internal; the public interface is the C
+// ABI in include/moe_ffn.h, implemented in api.cu).
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+cudaError_t launch_quant_rowwise(const void* src, int64_t n_rows, int cols, const int* row_of, int k, int64_t cap,
+                                 uint8_t* codes, uint8_t* scales, int* err, cudaStream_t st);
+cudaError_t launch_fill_pad_rows(const int* split_sizes, int E, int cols, uint8_t* codes, uint8_t* scales,
+                                 cudaStream_t st);
+cudaError_t launch_quant_colwise(const void* src, const int* src_map, int64_t n_src_rows, int batch, int rows,
+                                 int cols, const int* split_sizes, int E, uint8_t* codes_t, uint8_t* scales_t,
+                                 int* err, cudaStream_t st);
+cudaError_t launch_route_permute(const float* logits, int T, int E, int k, int renorm, int* idx, float* prob,
+                                 uint32_t* masks, int* bases, int* split_sizes, int* row_of, int* src_of,
+                                 float* prob_perm, int* err, cudaStream_t st);
+cudaError_t launch_combine(const void* y, const int* row_of, const float* prob, int T, int k, int H, int64_t cap,
+                           void* out, int* err, cudaStream_t st);
+cudaError_t launch_dprob_reduce(const float* dp_part, int n_tiles, int64_t cap, const int* row_of, int64_t R,
+                                float* dprob, int* err, cudaStream_t st);
+
+// ---- grouped block-scaled MXFP8 GEMM (tcgen05) ------------------------------------
+// C[M][N] = A[M][K] * B[N][K]^T, both operands K-major MX tensors.
+//   mode 0 (grouped rows): A rows are the permuted token rows, split into
+//     128-row blocks per expert segment (from split_sizes); B = expert e's
+//     weight rows.  K fixed.
+//   mode 1 (grouped K, weight gradients): for each expert e an independent
+//     [M][N] output with K = the expert's padded token range of A and B.
+enum Epilogue : int { EPI_BF16 = 0, EPI_FWD_SWIGLU = 1, EPI_BWD_SWIGLU = 2 };
+
+struct GemmArgs {
+  int mode;
+  int E;
+  const int* split_sizes;
+  int K;                     // mode 0 contraction length (multiple of 128)
+  int N;                     // output columns (per expert in mode 1); SwiGLU epilogues: I
+  int M;                     // mode 1: output rows per expert (multiple of 128)
+  int n_tiles;               // tiles along N
+  int64_t b_rows_per_expert; // mode 0: rows of B per expert
+  int64_t cap;               // permuted row capacity
+  const uint8_t* sfa;        // tile-layout scales of A
+  const uint8_t* sfb;        // tile-layout scales of B
+  int64_t sfa_K;             // K of A's scale layout
+  int64_t sfb_K;             // K of B's scale layout
+  // epilogue operands
+  __nv_bfloat16* out;        // EPI_BF16 output
+  int64_t ldo;
+  const float* prob_perm;    // SwiGLU epilogues
+  uint8_t* q_row;            // rowwise MX output (codes) [cap][q_row_K]
+  uint8_t* q_row_s;
+  int64_t q_row_K;
+  uint8_t* q_col;            // colwise MX output (codes) [cols][cap], optional
+  uint8_t* q_col_s;
+  __nv_bfloat16* gu;         // saved g,u [cap][2I]: written by FWD (optional), read by BWD
+  float* dp_part;            // BWD: [n_tiles][cap] partial row sums of dA*silu(g)*u
+  int I;
+  int* err;
+};
+
+cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64_t a_rows, int64_t a_K,
+                                const void* B, int64_t b_rows, int64_t b_K, int64_t max_tiles, cudaStream_t st,
+                                char* msg, size_t msg_len);
+
+}  // namespace moe

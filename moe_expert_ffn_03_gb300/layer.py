@@ -1,0 +1,94 @@
+"""One expert-FFN layer step on the device: buffer allocation (torch) plus the
+C entry points called in order.  No arithmetic happens here.
+
+Forward:  moe_route_permute -> grouped_mlp_fwd -> moe_unpermute_combine
+Backward: grouped_mlp_bwd -> moe_unpermute_combine (dx_perm -> dx)
+Weights:  mxfp8_quantize of the bf16 master weights (axis 0 for the forward,
+          axis 1 for the backward copies), once per optimizer step.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+U8 = torch.uint8
+
+
+class ExpertFFN:
+    """Buffers of one layer for fixed sizes (T, H, I, E, k) on one device."""
+
+    def __init__(self, T, H, I, E, k, training=True, renormalize=True, device="cuda"):
+        self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
+        self.training = training
+        self.d = B.dims(T, H, I, E, k, int(renormalize))
+        self.cap = B.moe_rows_capacity(self.d)
+        if self.cap == 0:
+            raise B.MoeError(2, f"unsupported sizes T={T} H={H} I={I} E={E} k={k}")
+        cap = self.cap
+        dev = torch.device(device)
+        z = lambda *s, dt: torch.zeros(*s, dtype=dt, device=dev)  # noqa: E731
+        e = lambda *s, dt: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
+        self.ws = z(B.moe_workspace_size(self.d, training), dt=U8)
+        self.idx = e(T, k, dt=torch.int32)
+        self.prob = e(T, k, dt=torch.float32)
+        self.split_sizes = e(E, dt=torch.int32)
+        self.row_of = e(T, k, dt=torch.int32)
+        self.src_of = e(cap, dt=torch.int32)
+        self.prob_perm = e(cap, dt=torch.float32)
+        self.xq = e(cap, H, dt=U8)
+        self.xq_s = e(cap * H // 32, dt=U8)
+        self.y = e(cap, H, dt=torch.bfloat16)
+        self.out = e(T, H, dt=torch.bfloat16)
+        self.wgu_q = e(E, 2 * I, H, dt=U8)
+        self.wgu_s = e(E * 2 * I * H // 32, dt=U8)
+        self.wd_q = e(E, H, I, dt=U8)
+        self.wd_s = e(E * H * I // 32, dt=U8)
+        if training:
+            self.xq_col = e(H, cap, dt=U8)
+            self.xq_col_s = e(H * cap // 32, dt=U8)
+            self.saved_gu = e(cap, 2 * I, dt=torch.bfloat16)
+            self.aq_col = e(I, cap, dt=U8)
+            self.aq_col_s = e(I * cap // 32, dt=U8)
+            self.dx_perm = e(cap, H, dt=torch.bfloat16)
+            self.dx = e(T, H, dt=torch.bfloat16)
+            self.dwgu = e(E, 2 * I, H, dt=torch.bfloat16)
+            self.dwd = e(E, H, I, dt=torch.bfloat16)
+            self.dprob = e(T, k, dt=torch.float32)
+            self.wguT_q = e(E, H, 2 * I, dt=U8)
+            self.wguT_s = e(E * H * 2 * I // 32, dt=U8)
+            self.wdT_q = e(E, I, H, dt=U8)
+            self.wdT_s = e(E * I * H // 32, dt=U8)
+        else:
+            self.xq_col = self.xq_col_s = self.saved_gu = self.aq_col = self.aq_col_s = None
+
+    # ---- steps -------------------------------------------------------------------
+    def quantize_weights(self, w_gu, w_d, stream=None):
+        E, H, I = self.E, self.H, self.I
+        B.mxfp8_quantize(w_gu, E, 2 * I, H, 0, self.wgu_q, self.wgu_s, stream)
+        B.mxfp8_quantize(w_d, E, H, I, 0, self.wd_q, self.wd_s, stream)
+        if self.training:
+            B.mxfp8_quantize(w_gu, E, 2 * I, H, 1, self.wguT_q, self.wguT_s, stream)
+            B.mxfp8_quantize(w_d, E, H, I, 1, self.wdT_q, self.wdT_s, stream)
+
+    def forward(self, logits, x, stream=None):
+        B.moe_route_permute(self.d, logits, x, self.idx, self.prob, self.split_sizes, self.row_of, self.src_of,
+                            self.prob_perm, self.xq, self.xq_s, self.xq_col, self.xq_col_s, self.ws, stream)
+        B.grouped_mlp_fwd(self.d, self.xq, self.xq_s, self.split_sizes, self.prob_perm, self.wgu_q, self.wgu_s,
+                          self.wd_q, self.wd_s, self.y, self.saved_gu, self.aq_col, self.aq_col_s, self.ws, stream)
+        B.moe_unpermute_combine(self.d, self.y, self.row_of, None, self.out, stream)
+        return self.out
+
+    def backward(self, dout, stream=None):
+        B.grouped_mlp_bwd(self.d, dout, self.split_sizes, self.row_of, self.src_of, self.prob_perm, self.saved_gu,
+                          self.aq_col, self.aq_col_s, self.xq_col, self.xq_col_s, self.wguT_q, self.wguT_s,
+                          self.wdT_q, self.wdT_s, self.dx_perm, self.dwgu, self.dwd, self.dprob, self.ws, stream)
+        B.moe_unpermute_combine(self.d, self.dx_perm, self.row_of, None, self.dx, stream)
+        return self.dx
+
+    def device_error(self, stream=None):
+        return B.moe_get_device_error(self.ws, stream)
+
+    def padded_rows(self) -> int:
+        s = self.split_sizes.to("cpu", torch.int64)
+        return int(((s + 127) // 128 * 128).sum())

@@ -1,0 +1,81 @@
+"""The C-ABI library loads and exports every entry point the header declares;
+host-side argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from moe_expert_ffn_03_gb300 import binding as B
+from moe_expert_ffn_03_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_ffn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return B.lib()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("mxfp8_quantize", "moe_route_permute", "grouped_mlp_fwd", "grouped_mlp_bwd",
+              "moe_unpermute_combine", "moe_workspace_size", "moe_get_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert set(B.EXPORTS) == set(declared_functions())
+
+
+def test_capacity_and_workspace_sizes(lib):
+    d = B.dims(16384, 4096, 14336, 8, 2)
+    cap = B.moe_rows_capacity(d)
+    assert cap == 32768 + 128 * 8
+    fwd = B.moe_workspace_size(d, False)
+    bwd = B.moe_workspace_size(d, True)
+    assert fwd >= cap * 14336 * (1 + 1 / 32)
+    assert bwd > fwd + 2 * cap * 2 * 14336
+    assert B.moe_rows_capacity(B.dims(10, 100, 128, 4, 2)) == 0       # H not a multiple of 128
+    assert B.moe_rows_capacity(B.dims(10, 128, 128, 4, 9)) == 0       # k > 8
+
+
+def test_host_checks_fail_before_launch(lib):
+    s = lib.mxfp8_quantize(None, 1, 128, 128, 0, None, None, None)
+    assert s == 1
+    assert b"NULL" in lib.moe_last_error_message()
+    s = lib.mxfp8_quantize(ctypes.c_void_p(16), 1, 100, 128, 0, ctypes.c_void_p(16), ctypes.c_void_p(16), None)
+    assert s == 2
+    s = lib.mxfp8_quantize(ctypes.c_void_p(8), 1, 128, 128, 0, ctypes.c_void_p(16), ctypes.c_void_p(16), None)
+    assert s == 3
+    d = B.dims(64, 128, 128, 4, 2)
+    s = lib.grouped_mlp_fwd(ctypes.byref(d), *([ctypes.c_void_p(256)] * 9), None, None, None,
+                            ctypes.c_void_p(256), 16, None)
+    assert s == 4                                                     # workspace too small
+    assert lib.moe_status_string(6) == b"MOE_ERR_DEVICE_TIMEOUT"
+
+
+def header_param_counts():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(\w+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_header(lib):
+    counts = header_param_counts()
+    for name in B.EXPORTS:
+        assert len(getattr(lib, name).argtypes) == counts[name], name

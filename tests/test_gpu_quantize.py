@@ -1,0 +1,87 @@
+"""GPU mxfp8_quantize vs the oracle codec: bit-exact codes and scales."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import untile_scales
+from moe_expert_ffn_03_gb300 import binding as B
+from moe_expert_ffn_03_gb300 import build
+from oracle import mxfp8 as mx
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    B.lib()
+
+
+def bf16_from_bits(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(bits.astype(np.uint16).view(np.int16).copy()).view(torch.bfloat16)
+
+
+def as_f64(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def run_quant(x: torch.Tensor, batch: int, rows: int, cols: int, axis: int):
+    xd = x.cuda().contiguous()
+    codes = torch.empty(x.numel(), dtype=torch.uint8, device="cuda")
+    scales = torch.full((x.numel() // 32,), 0xAB, dtype=torch.uint8, device="cuda")
+    B.mxfp8_quantize(xd, batch, rows, cols, axis, codes, scales)
+    torch.cuda.synchronize()
+    return codes.cpu().numpy(), scales.cpu().numpy()
+
+
+def all_patterns_matrix(seed: int) -> np.ndarray:
+    """Every bf16 bit pattern once (sorted or shuffled), as a [512][128] matrix."""
+    bits = np.arange(65536, dtype=np.uint32)
+    if seed:
+        bits = np.random.default_rng(seed).permutation(bits)
+    return bits.reshape(512, 128)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_rowwise_every_bf16_pattern(seed):
+    bits = all_patterns_matrix(seed)
+    x = bf16_from_bits(bits)
+    codes, scales = run_quant(x, 1, 512, 128, 0)
+    with np.errstate(invalid="ignore"):
+        ref_c, ref_s = mx.quantize_blocks(as_f64(x), axis=1)
+    got_s = untile_scales(scales, 512, 128)
+    assert np.array_equal(got_s, ref_s), np.argwhere(got_s != ref_s)[:5]
+    bad = np.argwhere(codes.reshape(512, 128) != ref_c)
+    assert bad.size == 0, [(tuple(i), hex(bits[tuple(i)]), codes.reshape(512, 128)[tuple(i)], ref_c[tuple(i)])
+                           for i in bad[:8]]
+
+
+@pytest.mark.parametrize("seed", [0, 5])
+def test_colwise_every_bf16_pattern(seed):
+    bits = all_patterns_matrix(seed)
+    x = bf16_from_bits(bits)
+    codes, scales = run_quant(x, 1, 512, 128, 1)
+    with np.errstate(invalid="ignore"):
+        ref_c, ref_s = mx.quantize_blocks(as_f64(x), axis=0)     # blocks along rows
+    got_c = codes.reshape(128, 512)                               # transposed
+    got_s = untile_scales(scales, 128, 512)
+    assert np.array_equal(got_s, ref_s.T)
+    assert np.array_equal(got_c, ref_c.T)
+
+
+@pytest.mark.parametrize("scale_pow", [-60, -20, 0, 12])
+def test_batched_weights_both_axes(scale_pow):
+    E, R, C = 3, 256, 384
+    g = torch.Generator().manual_seed(scale_pow + 100)
+    w = (torch.randn(E, R, C, generator=g) * (2.0 ** scale_pow)).to(torch.bfloat16)
+    w[1, 5, :64] = 0                                              # all-zero blocks
+    w[2, :32, 7] = 0
+    wf = as_f64(w)
+    codes, scales = run_quant(w, E, R, C, 0)
+    ref_c, ref_s = mx.quantize_blocks(wf, axis=2)
+    assert np.array_equal(codes.reshape(E, R, C), ref_c)
+    assert np.array_equal(untile_scales(scales, E * R, C), ref_s.reshape(E * R, C // 32))
+    codes, scales = run_quant(w, E, R, C, 1)
+    ref_c, ref_s = mx.quantize_blocks(wf, axis=1)
+    assert np.array_equal(codes.reshape(E, C, R), np.swapaxes(ref_c, 1, 2))
+    assert np.array_equal(untile_scales(scales, E * C, R), np.swapaxes(ref_s, 1, 2).reshape(E * C, R // 32))
