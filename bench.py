@@ -1,0 +1,378 @@
+"""Benchmark of the grouped MXFP8 expert-FFN layer step on GB300.
+
+One step = weight quantization of the bf16 masters (both orientations) +
+route/permute/quantize + grouped gate_up GEMM with fused ScaledSwiGLU +
+grouped down GEMM + combine + the full backward (dY quantization, down dgrad
+with fused SwiGLU backward, down wgrad, gate_up dgrad, gate_up wgrad, dprob)
++ combine of dX.  Workload: Mixtral-8x7B-shaped expert MLP forward+backward
+(T=16384, H=4096, I=14336, E=8, top-2), synthetic seeded inputs.
+
+Metric: algorithmic TFLOP/s of the grouped expert MLP (18*R*H*I per step,
+R = T*k) over the whole step time; also tokens/s and the fraction of the
+dense MXFP8 tensor-core peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 (torchrun): every rank runs its own replica of the workload (the path
+has no exchange step), timing is the max over ranks, value = all ranks' FLOPs
+/ that time.  ``--impl reference`` times the CPU oracle on a bounded sample of
+the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "mixtral_fwdbwd_T16384_H4096_I14336_E8_k2"
+METRIC = "grouped expert-MLP fwd+bwd TFLOP/s (MXFP8, algorithmic 18*R*H*I per step)"
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the gate_up forward
+# GEMM from the ncu capture summarised in profiles/ (None until captured for
+# the current kernel)
+GEMM_TRAFFIC_BYTES = None
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        loaded = [s for s, p in zip(sm, power) if p > 200.0] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def dist_setup(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if gpus > 0 else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------
+def run_cuda(args):
+    import torch
+
+    from moe_expert_ffn_03_gb300 import build, configs, synth
+    from moe_expert_ffn_03_gb300.layer import LAUNCHES_PER_FORWARD_STEP, LAUNCHES_PER_TRAINING_STEP, ExpertFFN
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    build.build()
+    wl = pick_workload(args)
+    train = wl.backward
+    dev = torch.device("cuda", local)
+    inp = synth.make_inputs(wl, seed=0, device=dev)
+    L = ExpertFFN(wl.T, wl.H, wl.I, wl.E, wl.k, training=train, device=dev)
+    stream = torch.cuda.current_stream()
+
+    ev = {}
+
+    def step(record=False):
+        def mark(name):
+            if record:
+                e = torch.cuda.Event(enable_timing=True)
+                e.record(stream)
+                ev.setdefault(name, []).append(e)
+        mark("start")
+        L.quantize_weights(inp["w_gu"], inp["w_d"])
+        mark("wquant")
+        L.route(inp["logits"], inp["x"])
+        mark("route")
+        L.ffn_forward()
+        mark("fwd")
+        L.combine_out()
+        mark("comb")
+        if train:
+            L.ffn_backward(inp["dout"])
+        mark("bwd")
+        if train:
+            L.combine_dx()
+        mark("end")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    code, site = L.device_error()
+    if code != 0:
+        raise RuntimeError(f"device error {code} at site {site}")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms_total = t0.elapsed_time(t1)
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / args.steps
+
+    def seg(a, b):
+        return sum(x.elapsed_time(y) for x, y in zip(ev[a], ev[b])) / args.steps
+
+    parts = {"weight_quant_ms": seg("start", "wquant"), "route_permute_ms": seg("wquant", "route"),
+             "grouped_mlp_fwd_ms": seg("route", "fwd"), "combine_ms": seg("fwd", "comb"),
+             "grouped_mlp_bwd_ms": seg("comb", "bwd"), "combine_dx_ms": seg("bwd", "end")}
+    code, site = L.device_error()
+    if code != 0:
+        raise RuntimeError(f"device error {code} at site {site}")
+
+    flops = wl.flops_total()
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    peaks, src = read_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+    gemm_ms = parts["grouped_mlp_fwd_ms"] + parts["grouped_mlp_bwd_ms"]
+    gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
+    n_gemm = 6 if train else 2
+
+    # ---- end to end through the public API with pinned host buffers ----
+    host = {k: inp[k].cpu().pin_memory() for k in (("x", "logits", "dout") if train else ("x", "logits"))}
+    dev_in = {k: torch.empty_like(inp[k]) for k in host}
+    out_h = torch.empty(L.out.shape, dtype=L.out.dtype).pin_memory()
+    dx_h = torch.empty(L.dx.shape, dtype=L.dx.dtype).pin_memory() if train else None
+    bi = sum(t.numel() * t.element_size() for t in host.values())
+    bo = out_h.numel() * 2 + (dx_h.numel() * 2 if train else 0)
+
+    def e2e_step():
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        L.quantize_weights(inp["w_gu"], inp["w_d"])
+        L.forward(dev_in["logits"], dev_in["x"])
+        out_h.copy_(L.out, non_blocking=True)
+        if train:
+            L.backward(dev_in["dout"])
+            dx_h.copy_(L.dx, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_tokens, wl)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "mxfp8-e4m3 (ue8m0 block-32 scales, fp32 accumulate)",
+        "data": "synthetic (seeded SplitMix64/Box-Muller: x~N(0,1), W~N(0,0.02^2), dout~N(0,0.01^2), logits~N(0,1))",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                   "pass": "fwd+bwd" if train else "fwd", "global_batch_tokens": wl.T * world,
+                   "l2": "inputs larger than L2 (2.8 GB bf16 weights re-read every step); no flush",
+                   "parallelism": f"replicas x{world} (no exchange step)"},
+        "tokens_per_s": round(world * wl.T / (ms_step * 1e-3), 1),
+        "frac_of_mxfp8_peak": round(value / world / fp8_peak, 4),
+        "breakdown_ms": {k: round(v, 4) for k, v in parts.items()},
+        "roofline": {"bound": "tensor", "kernel": f"grouped_gemm_kernel ({n_gemm} launches per step)",
+                     "achieved": round(gemm_tflops, 2), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / fp8_peak, 4), "traffic": GEMM_TRAFFIC_BYTES,
+                     "peak_source": f"{src}: 2 x bf16_tflops_sustained (fp8/bf16 nominal ratio 4.5/2.25)",
+                     "timed": "grouped_mlp_fwd + grouped_mlp_bwd calls (the backward call also holds "
+                              "4 small quantize/reduce launches)",
+                     "launches_per_step": n_gemm},
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+        "gpu_launches": (LAUNCHES_PER_TRAINING_STEP if train else LAUNCHES_PER_FORWARD_STEP) * args.steps,
+        "clocks": clocks,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------------------------
+def cpu_baseline(tokens: int, wl=None):
+    """The oracle (numpy, float64) on a bounded sample: `tokens` tokens of the
+    workload's routing over its first two experts, full H and I, forward and
+    (when the workload trains) backward, weight quantization included."""
+    import numpy as np
+    import torch
+
+    from moe_expert_ffn_03_gb300 import configs, synth
+    from oracle import expert_ffn as ef
+    from oracle import routing as rt
+
+    wl = wl or configs.get(WORKLOAD)
+    E_s = 2
+    sub = configs.small(tokens, wl.H, wl.I, wl.E, wl.k, routing=wl.routing, backward=True)
+    inp = synth.make_inputs(sub, seed=0, device="cpu")
+    f64 = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+    logits = inp["logits"].numpy().copy()
+    logits[:, E_s:] = -1e30                                   # route over the sampled experts only
+    x, dout = f64(inp["x"]), f64(inp["dout"])
+    w_gu, w_d = f64(inp["w_gu"][:E_s]), f64(inp["w_d"][:E_s])
+    t0 = time.perf_counter()
+    k = min(wl.k, E_s)
+    idx, prob = rt.route_topk(logits[:, :E_s], k)
+    fwd = ef.forward(x, idx, prob.astype(np.float64), w_gu, w_d)
+    if wl.backward:
+        ef.backward(fwd, dout)
+    dt = time.perf_counter() - t0
+    flops = (18.0 if wl.backward else 6.0) * tokens * k * wl.H * wl.I
+    return {"value": round(flops / dt / 1e12, 5), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"{tokens} tokens x top-{k} over 2 of the {wl.E} experts, H={wl.H}, I={wl.I}, "
+                      f"{'fwd+bwd' if wl.backward else 'fwd'} incl. weight quantization "
+                      f"(numpy float64, BLAS threads = all host cores)"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup(0)
+    if rank != 0:
+        return
+    wl = pick_workload(args)
+    for _ in range(args.warmup):
+        cpu_baseline(max(32, args.cpu_tokens // 4), wl)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        r = cpu_baseline(args.cpu_tokens, wl)
+        vals.append(r["value"])
+        secs.append(r["seconds"])
+    v = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * statistics.median(secs), 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic", "config": {"workload": wl.name, "sample_tokens": args.cpu_tokens},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": r["sample"]},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def pick_workload(args):
+    from moe_expert_ffn_03_gb300 import configs
+    wl = configs.get(args.workload)
+    if args.tokens or args.experts:
+        T = args.tokens or wl.T
+        E = args.experts or wl.E
+        wl = configs.small(T, wl.H, wl.I, E, min(wl.k, E), routing=wl.routing, backward=wl.backward,
+                           name=f"{wl.name}_T{T}_E{E}")
+    return wl
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default=WORKLOAD, help="a workload name from moe_expert_ffn_03_gb300.configs")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (smaller cases for profiling)")
+    ap.add_argument("--experts", type=int, default=0, help="override E (smaller cases for profiling)")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "cuda":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_cuda(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -14,6 +14,15 @@ from . import binding as B
 
 U8 = torch.uint8
 
+# kernel launches of one training step (quantize_weights + forward + backward):
+# weights 4 (two rowwise, two colwise), route/permute 6 (top-k, scan, scatter,
+# gather+quantize rows, padding rows, gather+quantize along tokens), forward 2
+# GEMMs, combine 1, backward 8 (dY rowwise, padding rows, dY along tokens, down
+# dgrad, dprob reduce, down wgrad, gate_up dgrad, gate_up wgrad), combine 1.
+LAUNCHES_PER_TRAINING_STEP = 22
+# forward-only step: weights 2, route/permute 5, forward 2, combine 1
+LAUNCHES_PER_FORWARD_STEP = 10
+
 
 class ExpertFFN:
     """Buffers of one layer for fixed sizes (T, H, I, E, k) on one device."""
@@ -71,19 +80,34 @@ class ExpertFFN:
             B.mxfp8_quantize(w_gu, E, 2 * I, H, 1, self.wguT_q, self.wguT_s, stream)
             B.mxfp8_quantize(w_d, E, H, I, 1, self.wdT_q, self.wdT_s, stream)
 
-    def forward(self, logits, x, stream=None):
+    def route(self, logits, x, stream=None):
         B.moe_route_permute(self.d, logits, x, self.idx, self.prob, self.split_sizes, self.row_of, self.src_of,
                             self.prob_perm, self.xq, self.xq_s, self.xq_col, self.xq_col_s, self.ws, stream)
+
+    def ffn_forward(self, stream=None):
         B.grouped_mlp_fwd(self.d, self.xq, self.xq_s, self.split_sizes, self.prob_perm, self.wgu_q, self.wgu_s,
                           self.wd_q, self.wd_s, self.y, self.saved_gu, self.aq_col, self.aq_col_s, self.ws, stream)
+
+    def combine_out(self, stream=None):
         B.moe_unpermute_combine(self.d, self.y, self.row_of, None, self.out, stream)
+
+    def forward(self, logits, x, stream=None):
+        self.route(logits, x, stream)
+        self.ffn_forward(stream)
+        self.combine_out(stream)
         return self.out
 
-    def backward(self, dout, stream=None):
+    def ffn_backward(self, dout, stream=None):
         B.grouped_mlp_bwd(self.d, dout, self.split_sizes, self.row_of, self.src_of, self.prob_perm, self.saved_gu,
                           self.aq_col, self.aq_col_s, self.xq_col, self.xq_col_s, self.wguT_q, self.wguT_s,
                           self.wdT_q, self.wdT_s, self.dx_perm, self.dwgu, self.dwd, self.dprob, self.ws, stream)
+
+    def combine_dx(self, stream=None):
         B.moe_unpermute_combine(self.d, self.dx_perm, self.row_of, None, self.dx, stream)
+
+    def backward(self, dout, stream=None):
+        self.ffn_backward(dout, stream)
+        self.combine_dx(stream)
         return self.dx
 
     def device_error(self, stream=None):
