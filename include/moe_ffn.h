@@ -233,6 +233,42 @@ moe_status moe_get_device_error(const void* workspace, int32_t* code, int32_t* s
 /* Zero the device error word of a workspace (asynchronous on stream). */
 moe_status moe_clear_device_error(void* workspace, moe_stream_t stream);
 
+/*
+ * moe_route_permute_noalloc -- moe_route_permute for callers that cannot
+ * allocate device memory for the library.  The pages have no counterpart of
+ * this entry point; it is an interface addition of this library.
+ *
+ * Some callers own no allocator they may use here: a plugin inside a host
+ * framework that hands over only the layer's inputs and outputs, or a serving
+ * loop whose memory is planned at start-up and where a cudaMalloc (which can
+ * synchronise the device) is not allowed.  They cannot supply the workspace
+ * that moe_route_permute needs for its two permutation tables (a 32-bit ballot
+ * mask and a 32-bit running count per expert and 32-token group), so this
+ * variant takes them from a fixed array compiled into the library.
+ *
+ * Arguments and results are exactly those of moe_route_permute, minus the
+ * workspace.  Limits: everything moe_route_permute accepts, and in addition
+ * E * ceil(T/32) <= 262144 (for example T = 32768 tokens with E up to 256
+ * experts); larger sizes return MOE_ERR_UNSUPPORTED with a message naming the
+ * limit.  The array takes 2 MiB + 256 bytes of device memory on every GPU
+ * that loads the library, held until the process exits.  The call allocates
+ * nothing.
+ *
+ * The first call on each device looks up the array's device address with that
+ * device current and caches it; make that first call before any stream
+ * capture.  All calls share the one array and each call rewrites it (only its
+ * error word is cleared at the start of a call): calls whose kernels overlap on
+ * the GPU -- different streams, or threads without ordering between them --
+ * race and corrupt each other's permutation, so order them.  Index errors the
+ * kernels detect are recorded in the array's own error word (not readable
+ * through this interface) and the offending entries are skipped.
+ */
+moe_status moe_route_permute_noalloc(const moe_dims* d, const float* logits, const void* x,
+                                     int32_t* idx, float* prob, int32_t* split_sizes,
+                                     int32_t* row_of, int32_t* src_of, float* prob_perm,
+                                     uint8_t* xq, uint8_t* xq_scale, uint8_t* xq_col, uint8_t* xq_col_scale,
+                                     moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,7 +17,7 @@ c_int32, c_size_t, c_void_p = ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p
 EXPORTS = (
     "moe_status_string", "moe_last_error_message", "moe_rows_capacity", "moe_workspace_size",
     "mxfp8_quantize", "moe_route_permute", "grouped_mlp_fwd", "grouped_mlp_bwd",
-    "moe_unpermute_combine", "moe_get_device_error", "moe_clear_device_error",
+    "moe_unpermute_combine", "moe_get_device_error", "moe_clear_device_error", "moe_route_permute_noalloc",
 )
 
 MOE_OK = 0
@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
             "moe_unpermute_combine": ([D, P, P, P, P, P], c_int32),
             "moe_get_device_error": ([P, ctypes.POINTER(c_int32), ctypes.POINTER(c_int32), P], c_int32),
             "moe_clear_device_error": ([P, P], c_int32),
+            "moe_route_permute_noalloc": ([D, P, P, P, P, P, P, P, P, P, P, P, P, P], c_int32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -114,6 +115,13 @@ def moe_route_permute(d, logits, x, idx, prob, split_sizes, row_of, src_of, prob
                                    _p(row_of), _p(src_of), _p(prob_perm), _p(xq), _p(xq_scale), _p(xq_col),
                                    _p(xq_col_scale), _p(workspace), workspace.numel() * workspace.element_size(),
                                    _st(stream)))
+
+
+def moe_route_permute_noalloc(d, logits, x, idx, prob, split_sizes, row_of, src_of, prob_perm, xq, xq_scale,
+                              xq_col, xq_col_scale, stream=None):
+    _check(lib().moe_route_permute_noalloc(ctypes.byref(d), _p(logits), _p(x), _p(idx), _p(prob), _p(split_sizes),
+                                           _p(row_of), _p(src_of), _p(prob_perm), _p(xq), _p(xq_scale), _p(xq_col),
+                                           _p(xq_col_scale), _st(stream)))
 
 
 def grouped_mlp_fwd(d, xq, xq_scale, split_sizes, prob_perm, wgu_q, wgu_s, wd_q, wd_s, y, saved_gu, aq_col,

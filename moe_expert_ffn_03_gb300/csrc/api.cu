@@ -9,7 +9,7 @@ using namespace moe;
 
 namespace {
 
-thread_local char g_msg[512] = "";
+thread_local char g_msg[kLastErrorBytes] = "";
 
 moe_status fail(moe_status s, const char* fmt, ...) {
   va_list ap;
@@ -108,6 +108,8 @@ T* at(void* ws, size_t off) {
 }
 
 }  // namespace
+
+char* moe::last_error_buffer() { return g_msg; }
 
 extern "C" {
 

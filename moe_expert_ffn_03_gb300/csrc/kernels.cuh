@@ -6,6 +6,10 @@
 
 namespace moe {
 
+// Per-thread text of the last host-side error, returned by moe_last_error_message().
+constexpr size_t kLastErrorBytes = 512;
+char* last_error_buffer();
+
 cudaError_t launch_quant_rowwise(const void* src, int64_t n_rows, int cols, const int* row_of, int k, int64_t cap,
                                  uint8_t* codes, uint8_t* scales, int* err, cudaStream_t st);
 cudaError_t launch_fill_pad_rows(const int* split_sizes, int E, int cols, uint8_t* codes, uint8_t* scales,
