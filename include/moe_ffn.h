@@ -126,6 +126,20 @@ moe_status mxfp8_quantize(const void* src, int32_t batch, int32_t rows, int32_t 
                           uint8_t* codes, uint8_t* scales, moe_stream_t stream);
 
 /*
+ * mxfp8_quantize_dual -- both results of mxfp8_quantize (axis 0 into
+ * codes/scales, axis 1 into codes_t/scales_t) from ONE read of src.  This is
+ * the training-time weight quantization: the forward GEMMs consume W blocked
+ * along its columns, the backward (dgrad) GEMMs consume W^T blocked along its
+ * rows (page "Efficient MoE Training for Biological Foundation Models",
+ * section "MoE训练的瓶颈与TE的对应能力": 16-bit master weights are quantized
+ * before the low-precision GEMMs).  Same sizes, layouts and errors as
+ * mxfp8_quantize; batch <= 65535.
+ */
+moe_status mxfp8_quantize_dual(const void* src, int32_t batch, int32_t rows, int32_t cols,
+                               uint8_t* codes, uint8_t* scales, uint8_t* codes_t, uint8_t* scales_t,
+                               moe_stream_t stream);
+
+/*
  * moe_route_permute -- top-k routing, expert-major permutation, gather and
  * quantization of the tokens (page "Efficient MoE Training for Biological
  * Foundation Models", section "GroupedLinear": tokens are collected per

@@ -16,7 +16,7 @@ c_int32, c_size_t, c_void_p = ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p
 
 EXPORTS = (
     "moe_status_string", "moe_last_error_message", "moe_rows_capacity", "moe_workspace_size",
-    "mxfp8_quantize", "moe_route_permute", "grouped_mlp_fwd", "grouped_mlp_bwd",
+    "mxfp8_quantize", "mxfp8_quantize_dual", "moe_route_permute", "grouped_mlp_fwd", "grouped_mlp_bwd",
     "moe_unpermute_combine", "moe_get_device_error", "moe_clear_device_error", "moe_route_permute_noalloc",
 )
 
@@ -63,6 +63,7 @@ def lib() -> ctypes.CDLL:
             "moe_rows_capacity": ([D], c_size_t),
             "moe_workspace_size": ([D, c_int32], c_size_t),
             "mxfp8_quantize": ([P, c_int32, c_int32, c_int32, c_int32, P, P, P], c_int32),
+            "mxfp8_quantize_dual": ([P, c_int32, c_int32, c_int32, P, P, P, P, P], c_int32),
             "moe_route_permute": ([D, P, P, P, P, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
             "grouped_mlp_fwd": ([D, P, P, P, P, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
             "grouped_mlp_bwd": ([D] + [P] * 19 + [c_size_t, P], c_int32),
@@ -107,6 +108,11 @@ def moe_workspace_size(d: MoeDims, training: bool) -> int:
 
 def mxfp8_quantize(src, batch, rows, cols, axis, codes, scales, stream=None):
     _check(lib().mxfp8_quantize(_p(src), batch, rows, cols, axis, _p(codes), _p(scales), _st(stream)))
+
+
+def mxfp8_quantize_dual(src, batch, rows, cols, codes, scales, codes_t, scales_t, stream=None):
+    _check(lib().mxfp8_quantize_dual(_p(src), batch, rows, cols, _p(codes), _p(scales), _p(codes_t), _p(scales_t),
+                                     _st(stream)))
 
 
 def moe_route_permute(d, logits, x, idx, prob, split_sizes, row_of, src_of, prob_perm, xq, xq_scale,

@@ -67,7 +67,7 @@ WsLayout ws_layout(const moe_dims* d, bool training) {
   w.aq = take(cap * I);
   w.aq_s = take(cap * I / 32);
   if (training) {
-    const size_t ntI = (I + 255) / 256;
+    const size_t ntI = I / 128;                     // 128-column tiles of the SwiGLU-backward GEMM
     w.dyq = take(cap * H);
     w.dyq_s = take(cap * H / 32);
     w.dyqc = take(H * cap);
@@ -76,7 +76,7 @@ WsLayout ws_layout(const moe_dims* d, bool training) {
     w.dhq_s = take(cap * 2 * I / 32);
     w.dhqc = take(2 * I * cap);
     w.dhqc_s = take(2 * I * cap / 32);
-    w.dp = take(ntI * cap * 4);
+    w.dp = take(ntI * 4 * cap * 4);                 // one partial row sum per 64-column group
   }
   w.total = off;
   return w;
@@ -160,6 +160,25 @@ moe_status mxfp8_quantize(const void* src, int32_t batch, int32_t rows, int32_t 
                                   nullptr, st),
              "quant_colwise");
   }
+  return MOE_OK;
+}
+
+moe_status mxfp8_quantize_dual(const void* src, int32_t batch, int32_t rows, int32_t cols, uint8_t* codes,
+                               uint8_t* scales, uint8_t* codes_t, uint8_t* scales_t, moe_stream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE_PTR(src);
+  REQUIRE_PTR(codes);
+  REQUIRE_PTR(scales);
+  REQUIRE_PTR(codes_t);
+  REQUIRE_PTR(scales_t);
+  if (batch < 1 || rows < 128 || cols < 128 || rows % 128 || cols % 128)
+    return fail(MOE_ERR_UNSUPPORTED, "batch=%d rows=%d cols=%d: need batch>=1 and rows, cols multiples of 128",
+                batch, rows, cols);
+  if (int64_t(batch) * rows > (int64_t(1) << 31) || int64_t(batch) * cols > (int64_t(1) << 31) || batch > 65535)
+    return fail(MOE_ERR_UNSUPPORTED, "tensor too large");
+  CUDA_TRY(launch_quant_dual(src, batch, rows, cols, codes, scales, codes_t, scales_t,
+                             static_cast<cudaStream_t>(stream)),
+           "quant_dual");
   return MOE_OK;
 }
 
@@ -340,7 +359,7 @@ moe_status grouped_mlp_bwd(const moe_dims* d, const void* dout, const int32_t* s
   g3.split_sizes = split_sizes;
   g3.K = H;
   g3.N = I;
-  g3.n_tiles = (I + 255) / 256;
+  g3.n_tiles = I / 128;
   g3.b_rows_per_expert = I;
   g3.cap = cap;
   g3.sfa = dyq_s;
@@ -360,7 +379,7 @@ moe_status grouped_mlp_bwd(const moe_dims* d, const void* dout, const int32_t* s
   CUDA_TRY(launch_grouped_gemm(EPI_BWD_SWIGLU, g3, dyq, cap, H, wdT_q, int64_t(E) * I, H, (cap / 128) * g3.n_tiles,
                                st, g_msg, sizeof(g_msg)),
            "down dgrad GEMM");
-  CUDA_TRY(launch_dprob_reduce(dp, g3.n_tiles, cap, row_of, int64_t(d->T) * k, dprob, err, st), "dprob reduce");
+  CUDA_TRY(launch_dprob_reduce(dp, g3.n_tiles * 4, cap, row_of, int64_t(d->T) * k, dprob, err, st), "dprob reduce");
 
   // down wgrad: dW_d[e] = dY_e^T a_e, K = the expert's tokens
   GemmArgs g4{};

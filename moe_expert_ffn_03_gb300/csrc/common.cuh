@@ -66,7 +66,7 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
 }
 
 // Quantize 32 floats (already loaded) to 32 codes packed in 8 words; returns the scale code.
-__device__ __forceinline__ uint32_t mx_quant32(const float (&v)[32], uint32_t (&q)[8]) {
+__device__ __forceinline__ uint32_t mx_quant32(const float* v, uint32_t* q) {
   uint32_t amax = 0;
 #pragma unroll
   for (int i = 0; i < 32; ++i) amax = max(amax, abs_bits(v[i]));

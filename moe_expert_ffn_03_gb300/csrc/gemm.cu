@@ -18,9 +18,11 @@
 //               K=32) accumulate in TMEM (fp32, 256 columns); tcgen05.commit
 //               frees the stage and, after the last K step, hands the
 //               accumulator to the epilogue.
-//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter (= 32 rows),
-//               fused epilogue (bf16 store, ScaledSwiGLU + re-quantization,
-//               or SwiGLU backward + re-quantization), then release TMEM.
+//   warps 2..17 epilogue, four per TMEM lane quarter (32 rows), 64 accumulator
+//               columns each: tcgen05.ld into registers, release the
+//               accumulator at once (the next tile's MMAs start), then the
+//               fused epilogue math (bf16 store, ScaledSwiGLU + re-quantization
+//               along both axes, or SwiGLU backward + re-quantization).
 // Tiles: mode 0 walks the 128-row blocks of every expert segment (computed on
 // the device from split_sizes; empty experts get no tile) times the N tiles,
 // rasterised in groups of 8 row blocks; mode 1 (weight gradients) walks
@@ -43,7 +45,8 @@ constexpr int A_TILE = BM * BK;                 // 16 KB of E4M3
 constexpr int B_HALF = 128 * BK;                // 16 KB
 constexpr int B_TILE = BN * BK;                 // 32 KB
 constexpr int SF_ATOM = 512;                    // 128 rows x 4 scale bytes
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_WARPS = 16;                // 4 per TMEM lane quarter, 64 accumulator columns each
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_ACC = 0, TM_SFA = 256, TM_SFB = 260;
 constexpr int GROUP_M = 8;
@@ -56,7 +59,10 @@ constexpr int OFF_BAR = OFF_SFB + STAGES * 2 * SF_ATOM;
 constexpr int NUM_BARS = 2 * STAGES + 3;        // full[S], empty[S], tmem_full, tmem_empty, drain
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_SEG = OFF_MISC + 16;
-constexpr int SMEM_USED = OFF_SEG + 260 * 4;
+constexpr int TR_PITCH = 9;                     // floats per row of a warp's 32x8 transpose buffer
+constexpr int TR_WARP_FLOATS = 32 * TR_PITCH;
+constexpr int OFF_TR = OFF_SEG + 260 * 4;       // 16 epilogue warps x 32 x 9 floats
+constexpr int SMEM_USED = OFF_TR + NUM_EPI_WARPS * TR_WARP_FLOATS * 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;    // slack to align the base to 1024 B
 
 // ---- PTX wrappers -------------------------------------------------------------------
@@ -129,9 +135,9 @@ __device__ __forceinline__ void tc_mma_mxf8(uint32_t d, uint64_t adesc, uint64_t
       ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
       : "memory");
 }
-// 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base + i).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base + i).  The
+// registers are valid only after tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -142,9 +148,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
       : "memory");
+}
+// Wait for this thread's outstanding tcgen05.ld; the empty asm statements tie
+// every loaded register to the wait so no use is scheduled before it.
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld(uint32_t* r) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
 // Shared-memory matrix descriptor, K-major operand staged by TMA with 128-byte
@@ -224,6 +235,12 @@ __device__ __forceinline__ void decode_tile(const GemmArgs& a, const int* seg_mb
       tl.b_row0 = int64_t(lo) * a.b_rows_per_expert + tl.n0;
       tl.b_row1 = tl.b_row0 + a.I;
       tl.second = true;
+    } else if (EPI == EPI_BWD_SWIGLU) {
+      // 128-column tiles: each epilogue warp then holds 32 dA columns
+      tl.n0 = nb * 128;
+      tl.b_row0 = int64_t(lo) * a.b_rows_per_expert + tl.n0;
+      tl.b_row1 = tl.b_row0;
+      tl.second = false;
     } else {
       tl.n0 = nb * BN;
       tl.b_row0 = int64_t(lo) * a.b_rows_per_expert + tl.n0;
@@ -271,7 +288,7 @@ __device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile
 }
 
 // ---- epilogues ---------------------------------------------------------------------
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, const float (&v)[32]) {
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, const float* v) {
   uint4* p4 = reinterpret_cast<uint4*>(p);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -281,95 +298,149 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, const float (&v)
 
 // 32 values of one column block (this thread's row) quantized rowwise; the scale
 // of (row, block) goes to the tile layout with row length K.
-__device__ __forceinline__ void quant_row_block(const float (&v)[32], uint8_t* codes, uint8_t* scales,
-                                                int64_t row, int64_t col, int64_t K) {
+__device__ __forceinline__ void quant_row_block(const float* v, uint8_t* codes, uint8_t* scales, int64_t row,
+                                                int64_t col, int64_t K) {
   uint32_t q[8];
   const uint32_t c = mx_quant32(v, q);
   store_codes32(codes + row * K + col, q);
   scales[sf_offset(row, col >> 5, K)] = uint8_t(c);
 }
 
-// The same 32 columns quantized along tokens: the warp's 32 lanes are 32
-// consecutive permuted rows (one MX block).  Column col+i becomes row col+i of
-// the transposed [cols][cap] tensor; lane i stores that row's scale.
-__device__ __forceinline__ void quant_col_block(const float (&v)[32], uint8_t* codes_t, uint8_t* scales_t,
-                                                int64_t row, int64_t row_blk0, int64_t col, int64_t cap,
-                                                int lane) {
-  uint32_t my_c = 0;
+// The same 32 columns quantized along tokens.  The warp's 32 lanes are 32
+// consecutive permuted rows (one MX block along tokens); column col+i becomes
+// row col+i of the transposed [cols][cap] tensor.  Eight columns at a time go
+// through the warp's shared-memory buffer (32 rows x 9 floats, conflict-free
+// both ways): lane (c = lane/4, g = lane%4) then holds rows 8g..8g+7 of column c,
+// takes the block amax with two shuffles and stores its 8 codes as one 8-byte
+// word; the g == 0 lane stores the column's scale.
+__device__ __forceinline__ void quant_col_block(const float* v, uint8_t* codes_t, uint8_t* scales_t,
+                                                int64_t row_blk0, int64_t col, int64_t cap, int lane,
+                                                float* tr) {
+  const int c = lane >> 2, g = lane & 3;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const uint32_t amax = __reduce_max_sync(0xFFFFFFFFu, abs_bits(v[i]));
-    const uint32_t c = mx_scale_code(amax);
-    codes_t[(col + i) * cap + row] = uint8_t(mx_quant1(v[i], c));
-    if (lane == i) my_c = c;
+  for (int rnd = 0; rnd < 4; ++rnd) {
+#pragma unroll
+    for (int t = 0; t < 8; ++t) tr[lane * TR_PITCH + t] = v[8 * rnd + t];
+    __syncwarp();
+    float w[8];
+    uint32_t amax = 0;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      w[t] = tr[(8 * g + t) * TR_PITCH + c];
+      amax = max(amax, abs_bits(w[t]));
+    }
+    __syncwarp();
+    amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    const uint32_t sc = mx_scale_code(amax);
+    uint32_t lo, hi;
+    if (sc == 255u) {
+      lo = hi = 0x7F7F7F7Fu;
+    } else {
+      const float m = mx_inv_scale(sc);
+      lo = cvt_e4m3x2(w[0] * m, w[1] * m) | (cvt_e4m3x2(w[2] * m, w[3] * m) << 16);
+      hi = cvt_e4m3x2(w[4] * m, w[5] * m) | (cvt_e4m3x2(w[6] * m, w[7] * m) << 16);
+    }
+    const int64_t crow = col + 8 * rnd + c;               // row of the transposed tensor
+    *reinterpret_cast<uint2*>(codes_t + crow * cap + row_blk0 + 8 * g) = make_uint2(lo, hi);
+    if (g == 0) scales_t[sf_offset(crow, row_blk0 >> 5, cap)] = uint8_t(sc);
   }
-  scales_t[sf_offset(col + lane, row_blk0 >> 5, cap)] = uint8_t(my_c);
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
+// One epilogue warp on one tile.  The warp owns TMEM lane quarter q (32 rows) and
+// column group cg: 64 accumulator columns cg*64.. of an N=256 tile, gate columns
+// cg*32.. and up columns 128+cg*32.. of a ScaledSwiGLU tile, or columns cg*32..
+// of the 128-column SwiGLU-backward tile.  It pulls its
+// columns into registers, releases the accumulator (tmem_empty) and only then
+// runs the epilogue math, so the next tile's MMAs overlap it.
 template <int EPI>
-__device__ __forceinline__ void run_epilogue(const GemmArgs& a, const Tile& tl, uint32_t tmem_row, int q,
-                                             int lane) {
-  const int64_t row = tl.out_row + q * 32 + lane;       // output / permuted row of this thread
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl, uint32_t tmem_row, int q, int cg,
+                                              int lane, uint64_t* tmem_empty, float* tr) {
+  const int64_t row = tl.out_row + q * 32 + lane;        // output / permuted row of this thread
   const int64_t row_blk0 = tl.out_row + q * 32;
+  const int ncols = tl.second ? 256 : 128;                // valid accumulator columns
+  const int c0 = (EPI == EPI_BWD_SWIGLU) ? cg * 32 : cg * 64;
+  uint32_t r[64];
+  bool have;
+  if (EPI == EPI_FWD_SWIGLU) {
+    have = true;
+    tmem_ld32_async(tmem_row + TM_ACC + cg * 32, r);
+    tmem_ld32_async(tmem_row + TM_ACC + 128 + cg * 32, r + 32);
+    tmem_wait_ld<64>(r);
+  } else if (EPI == EPI_BWD_SWIGLU) {
+    have = true;
+    tmem_ld32_async(tmem_row + TM_ACC + c0, r);
+    tmem_wait_ld<32>(r);
+  } else {
+    have = c0 < ncols && tl.k_tiles > 0;
+    if (have) {
+      tmem_ld32_async(tmem_row + TM_ACC + c0, r);
+      tmem_ld32_async(tmem_row + TM_ACC + c0 + 32, r + 32);
+    }
+    tmem_wait_ld<64>(r);
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(tmem_empty);
+
   if (EPI == EPI_BF16) {
-    const int nchunks = tl.second ? 8 : 4;
-    __nv_bfloat16* orow = a.out + row * a.ldo + tl.n0;
-    for (int c = 0; c < nchunks; ++c) {
-      float v[32];
-      if (tl.k_tiles > 0) {
-        tmem_ld32(tmem_row + TM_ACC + c * 32, v);
-      } else {
+    if (c0 >= ncols) return;
+    __nv_bfloat16* orow = a.out + row * a.ldo + tl.n0 + c0;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.f;
-      }
-      store_bf16x32(orow + c * 32, v);
+    for (int h = 0; h < 2; ++h) {
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = have ? __uint_as_float(r[32 * h + i]) : 0.f;
+      store_bf16x32(orow + 32 * h, v);
     }
   } else if (EPI == EPI_FWD_SWIGLU) {
     const float p = a.prob_perm[row];
     const int64_t twoI = 2 * int64_t(a.I);
-    for (int c = 0; c < 4; ++c) {
-      float g[32], u[32];
-      tmem_ld32(tmem_row + TM_ACC + c * 32, g);
-      tmem_ld32(tmem_row + TM_ACC + 128 + c * 32, u);
-      const int64_t col = tl.n0 + c * 32;
-      if (a.gu != nullptr) {
-        store_bf16x32(a.gu + row * twoI + col, g);
-        store_bf16x32(a.gu + row * twoI + a.I + col, u);
-      }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i] * p;
-      quant_row_block(g, a.q_row, a.q_row_s, row, col, a.q_row_K);
-      if (a.q_col != nullptr) quant_col_block(g, a.q_col, a.q_col_s, row, row_blk0, col, a.cap, lane);
+    const int64_t col = tl.n0 + cg * 32;                  // column inside I
+    float* f = reinterpret_cast<float*>(r);
+    if (a.gu != nullptr) {
+      store_bf16x32(a.gu + row * twoI + col, f);
+      store_bf16x32(a.gu + row * twoI + a.I + col, f + 32);
     }
-  } else {  // EPI_BWD_SWIGLU
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = silu_f(f[i]) * f[32 + i] * p;
+    quant_row_block(f, a.q_row, a.q_row_s, row, col, a.q_row_K);
+    if (a.q_col != nullptr) quant_col_block(f, a.q_col, a.q_col_s, row_blk0, col, a.cap, lane, tr);
+  } else {  // EPI_BWD_SWIGLU: this warp's 32 columns of dA
+    float dp = 0.f;
     const float p = a.prob_perm[row];
     const int64_t twoI = 2 * int64_t(a.I);
-    const int nchunks = tl.second ? 8 : 4;
-    float dp = 0.f;
-    for (int c = 0; c < nchunks; ++c) {
-      float d[32], g[32], u[32];
-      tmem_ld32(tmem_row + TM_ACC + c * 32, d);
-      const int64_t col = tl.n0 + c * 32;
-      load_bf16x32(a.gu + row * twoI + col, g);
-      load_bf16x32(a.gu + row * twoI + a.I + col, u);
+    const __nv_bfloat16* grow = a.gu + row * twoI;
+    const int64_t col = tl.n0 + c0;
+    float o[32];
+    // dg = dA*p*u*silu'(g) and the row sum dp += dA*silu(g)*u
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float s = 1.0f / (1.0f + __expf(-g[i]));
-        const float sg = g[i] * s;
-        const float ds = s * (1.0f + g[i] * (1.0f - s));
-        const float dpu = d[i] * p;
-        dp += d[i] * sg * u[i];
-        g[i] = dpu * u[i] * ds;     // dg
-        u[i] = dpu * sg;            // du
+    for (int j = 0; j < 4; ++j) {
+      const uint4 gw = *reinterpret_cast<const uint4*>(grow + col + 8 * j);
+      const uint4 uw = *reinterpret_cast<const uint4*>(grow + a.I + col + 8 * j);
+      const uint32_t gs[4] = {gw.x, gw.y, gw.z, gw.w};
+      const uint32_t us[4] = {uw.x, uw.y, uw.z, uw.w};
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int i = 8 * j + t;
+        const float g = (t & 1) ? bf16_hi(gs[t >> 1]) : bf16_lo(gs[t >> 1]);
+        const float u = (t & 1) ? bf16_hi(us[t >> 1]) : bf16_lo(us[t >> 1]);
+        const float d = __uint_as_float(r[i]);
+        const float sgm = 1.0f / (1.0f + __expf(-g));
+        const float sg = g * sgm;
+        dp += d * sg * u;
+        o[i] = d * p * u * (sgm * (1.0f + g * (1.0f - sgm)));
+        r[i] = __float_as_uint(d * p * sg);            // du = dA*p*silu(g)
       }
-      quant_row_block(g, a.q_row, a.q_row_s, row, col, twoI);
-      quant_row_block(u, a.q_row, a.q_row_s, row, a.I + col, twoI);
-      quant_col_block(g, a.q_col, a.q_col_s, row, row_blk0, col, a.cap, lane);
-      quant_col_block(u, a.q_col, a.q_col_s, row, row_blk0, a.I + col, a.cap, lane);
     }
-    a.dp_part[int64_t(tl.nb) * a.cap + row] = dp;
+    quant_row_block(o, a.q_row, a.q_row_s, row, col, twoI);
+    quant_col_block(o, a.q_col, a.q_col_s, row_blk0, col, a.cap, lane, tr);
+    const float* du = reinterpret_cast<const float*>(r);
+    quant_row_block(du, a.q_row, a.q_row_s, row, a.I + col, twoI);
+    quant_col_block(du, a.q_col, a.q_col_s, row_blk0, a.I + col, a.cap, lane, tr);
+    a.dp_part[(int64_t(tl.nb) * 4 + cg) * a.cap + row] = dp;
   }
 }
 
@@ -397,7 +468,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 4);
+    mbar_init(tmem_empty, NUM_EPI_WARPS);
     mbar_init(drain, 1);
     *abort_s = 0;
     int acc = 0;
@@ -516,19 +587,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else {
-    // ---------------- epilogue warps 2..5 ----------------
+    // ---------------- epilogue warps 2..17 ----------------
     const int q = warp & 3;                    // TMEM lane quarter this warp may access
+    const int cg = (warp - 2) >> 2;            // column group 0..3
     const uint32_t tmem_row = tmem + (uint32_t(q * 32) << 16);
+    float* tr = reinterpret_cast<float*>(smem + OFF_TR) + (warp - 2) * TR_WARP_FLOATS;
     int tcount = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
       Tile tl;
       decode_tile<EPI>(args, seg_mb, t, tl);
+      if (EPI == EPI_BWD_SWIGLU) {
+        // pull this thread's saved g and u (64 B each) toward L2 while the MMAs run
+        const __nv_bfloat16* grow = args.gu + (tl.out_row + q * 32 + lane) * (2 * int64_t(args.I)) + tl.n0 + cg * 32;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(grow));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(grow + args.I));
+      }
       if (!wait_phase(tmem_full, tcount & 1, abort_s, args.err, SITE_GEMM_EPILOGUE, kWaitLimitNs)) break;
       tc_fence_after();
-      run_epilogue<EPI>(args, tl, tmem_row, q, lane);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tmem_empty);
+      epilogue_tile<EPI>(args, tl, tmem_row, q, cg, lane, tmem_empty, tr);
     }
   }
   tc_fence_before();

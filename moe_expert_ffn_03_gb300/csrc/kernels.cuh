@@ -17,6 +17,8 @@ cudaError_t launch_fill_pad_rows(const int* split_sizes, int E, int cols, uint8_
 cudaError_t launch_quant_colwise(const void* src, const int* src_map, int64_t n_src_rows, int batch, int rows,
                                  int cols, const int* split_sizes, int E, uint8_t* codes_t, uint8_t* scales_t,
                                  int* err, cudaStream_t st);
+cudaError_t launch_quant_dual(const void* src, int batch, int rows, int cols, uint8_t* codes, uint8_t* scales,
+                              uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st);
 cudaError_t launch_route_permute(const float* logits, int T, int E, int k, int renorm, int* idx, float* prob,
                                  uint32_t* masks, int* bases, int* split_sizes, int* row_of, int* src_of,
                                  float* prob_perm, int* err, cudaStream_t st);

@@ -144,6 +144,58 @@ __global__ void __launch_bounds__(256) quant_colwise_kernel(
 }
 
 // ---------------------------------------------------------------------------------
+// Both orientations from one read: a 128x128 tile of src[batch] is staged once;
+// thread tasks then quantize (row, 32-column block) pairs into codes[rows][cols]
+// and (column, 32-row block) pairs into codes_t[cols][rows].  Each bf16 weight is
+// read once and both MX copies written: 2 B in, 2*(1 + 1/32) B out per element.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) quant_dual_kernel(
+    const __nv_bfloat16* __restrict__ src, int rows, int cols, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t) {
+  __shared__ __align__(16) __nv_bfloat16 tile[QC_TILE * QC_PITCH];
+  const int row0 = blockIdx.x * QC_TILE;
+  const int col0 = blockIdx.y * QC_TILE;
+  const int64_t batch = blockIdx.z;
+  const int64_t srow0 = batch * rows + row0;
+  for (int i = threadIdx.x; i < QC_TILE * 16; i += blockDim.x) {
+    const int r = i >> 4, c16 = i & 15;
+    const uint4 w = reinterpret_cast<const uint4*>(src + (srow0 + r) * cols + col0)[c16];
+    *reinterpret_cast<uint4*>(&tile[r * QC_PITCH + c16 * 8]) = w;
+  }
+  __syncthreads();
+  // rowwise: task = (row r, block b), 128 x 4
+  for (int task = threadIdx.x; task < QC_TILE * 4; task += blockDim.x) {
+    const int r = task >> 2, b = task & 3;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 w = *reinterpret_cast<const uint4*>(&tile[r * QC_PITCH + b * 32 + i * 8]);
+      v[8 * i + 0] = bf16_lo(w.x); v[8 * i + 1] = bf16_hi(w.x);
+      v[8 * i + 2] = bf16_lo(w.y); v[8 * i + 3] = bf16_hi(w.y);
+      v[8 * i + 4] = bf16_lo(w.z); v[8 * i + 5] = bf16_hi(w.z);
+      v[8 * i + 6] = bf16_lo(w.w); v[8 * i + 7] = bf16_hi(w.w);
+    }
+    uint32_t q[8];
+    const uint32_t sc = mx_quant32(v, q);
+    const int64_t drow = srow0 + r;
+    store_codes32(codes + drow * cols + col0 + b * 32, q);
+    scales[sf_offset(drow, (col0 >> 5) + b, cols)] = uint8_t(sc);
+  }
+  // colwise: task = (column c, row block rb), 128 x 4
+  for (int task = threadIdx.x; task < QC_TILE * 4; task += blockDim.x) {
+    const int c = task & 127, rb = task >> 7;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(tile[(rb * 32 + i) * QC_PITCH + c]);
+    uint32_t q[8];
+    const uint32_t sc = mx_quant32(v, q);
+    const int64_t drow = batch * cols + col0 + c;
+    store_codes32(codes_t + drow * rows + row0 + rb * 32, q);
+    scales_t[sf_offset(drow, (row0 >> 5) + rb, rows)] = uint8_t(sc);
+  }
+}
+
+// ---------------------------------------------------------------------------------
 // host launchers
 // ---------------------------------------------------------------------------------
 cudaError_t launch_quant_rowwise(const void* src, int64_t n_rows, int cols, const int* row_of, int k,
@@ -172,6 +224,14 @@ cudaError_t launch_quant_colwise(const void* src, const int* src_map, int64_t n_
   dim3 grid(rows / QC_TILE, cols / QC_TILE, batch);
   quant_colwise_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), src_map, n_src_rows, rows,
                                              cols, split_sizes, E, codes_t, scales_t, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_dual(const void* src, int batch, int rows, int cols, uint8_t* codes, uint8_t* scales,
+                              uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st) {
+  dim3 grid(rows / QC_TILE, cols / QC_TILE, batch);
+  quant_dual_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, codes, scales, codes_t,
+                                          scales_t);
   return cudaGetLastError();
 }
 

@@ -15,11 +15,11 @@ from . import binding as B
 U8 = torch.uint8
 
 # kernel launches of one training step (quantize_weights + forward + backward):
-# weights 4 (two rowwise, two colwise), route/permute 6 (top-k, scan, scatter,
+# weights 2 (both orientations of W_gu and of W_d), route/permute 6 (top-k, scan, scatter,
 # gather+quantize rows, padding rows, gather+quantize along tokens), forward 2
 # GEMMs, combine 1, backward 8 (dY rowwise, padding rows, dY along tokens, down
 # dgrad, dprob reduce, down wgrad, gate_up dgrad, gate_up wgrad), combine 1.
-LAUNCHES_PER_TRAINING_STEP = 22
+LAUNCHES_PER_TRAINING_STEP = 20
 # forward-only step: weights 2, route/permute 5, forward 2, combine 1
 LAUNCHES_PER_FORWARD_STEP = 10
 
@@ -74,11 +74,12 @@ class ExpertFFN:
     # ---- steps -------------------------------------------------------------------
     def quantize_weights(self, w_gu, w_d, stream=None):
         E, H, I = self.E, self.H, self.I
-        B.mxfp8_quantize(w_gu, E, 2 * I, H, 0, self.wgu_q, self.wgu_s, stream)
-        B.mxfp8_quantize(w_d, E, H, I, 0, self.wd_q, self.wd_s, stream)
         if self.training:
-            B.mxfp8_quantize(w_gu, E, 2 * I, H, 1, self.wguT_q, self.wguT_s, stream)
-            B.mxfp8_quantize(w_d, E, H, I, 1, self.wdT_q, self.wdT_s, stream)
+            B.mxfp8_quantize_dual(w_gu, E, 2 * I, H, self.wgu_q, self.wgu_s, self.wguT_q, self.wguT_s, stream)
+            B.mxfp8_quantize_dual(w_d, E, H, I, self.wd_q, self.wd_s, self.wdT_q, self.wdT_s, stream)
+        else:
+            B.mxfp8_quantize(w_gu, E, 2 * I, H, 0, self.wgu_q, self.wgu_s, stream)
+            B.mxfp8_quantize(w_d, E, H, I, 0, self.wd_q, self.wd_s, stream)
 
     def route(self, logits, x, stream=None):
         B.moe_route_permute(self.d, logits, x, self.idx, self.prob, self.split_sizes, self.row_of, self.src_of,

@@ -85,3 +85,19 @@ def test_batched_weights_both_axes(scale_pow):
     ref_c, ref_s = mx.quantize_blocks(wf, axis=1)
     assert np.array_equal(codes.reshape(E, C, R), np.swapaxes(ref_c, 1, 2))
     assert np.array_equal(untile_scales(scales, E * C, R), np.swapaxes(ref_s, 1, 2).reshape(E * C, R // 32))
+
+
+def test_dual_equals_the_two_single_axis_calls():
+    E, R, C = 3, 256, 384
+    g = torch.Generator().manual_seed(7)
+    w = (torch.randn(E, R, C, generator=g) * 0.02).to(torch.bfloat16).cuda()
+    w[0, 3, :] = 0
+    c0 = torch.empty(E * R * C, dtype=torch.uint8, device="cuda")
+    s0 = torch.empty(E * R * C // 32, dtype=torch.uint8, device="cuda")
+    c1, s1 = torch.empty_like(c0), torch.empty_like(s0)
+    d0, t0, d1, t1 = (torch.empty_like(c0), torch.empty_like(s0), torch.empty_like(c0), torch.empty_like(s0))
+    B.mxfp8_quantize(w, E, R, C, 0, c0, s0)
+    B.mxfp8_quantize(w, E, R, C, 1, c1, s1)
+    B.mxfp8_quantize_dual(w, E, R, C, d0, t0, d1, t1)
+    torch.cuda.synchronize()
+    assert torch.equal(c0, d0) and torch.equal(s0, t0) and torch.equal(c1, d1) and torch.equal(s1, t1)
