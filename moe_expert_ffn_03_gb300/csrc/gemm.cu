@@ -12,8 +12,9 @@
 //   warp 0      TMA producer: 128x128 A box + one or two 128x128 B boxes
 //               (128B swizzle) and the 512-byte scale atoms (bulk copies)
 //               per 128-deep K step into a 4-stage shared-memory ring.
-//   warp 1      TMEM allocator and MMA issuer: per stage, tcgen05.cp moves
-//               the scale atoms into TMEM, then four
+//   warp 18     scale factors: per stage, tcgen05.cp moves the scale atoms
+//               into that stage's TMEM columns, then commits to sf_ready.
+//   warp 1      TMEM allocator and MMA issuer: per stage, after sf_ready, four
 //               tcgen05.mma.kind::mxf8f6f4.block_scale (M=128, N=256 or 128,
 //               K=32) accumulate in TMEM (fp32, 256 columns); tcgen05.commit
 //               frees the stage and, after the last K step, hands the
@@ -40,30 +41,42 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128;
-constexpr int STAGES = 4;
 constexpr int A_TILE = BM * BK;                 // 16 KB of E4M3
-constexpr int B_HALF = 128 * BK;                // 16 KB
-constexpr int B_TILE = BN * BK;                 // 32 KB
+constexpr int B_HALF = 128 * BK;                // 16 KB: one 128-row box of B
 constexpr int SF_ATOM = 512;                    // 128 rows x 4 scale bytes
-constexpr int NUM_EPI_WARPS = 16;                // 4 per TMEM lane quarter, 64 accumulator columns each
-constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int NUM_EPI_WARPS = 16;               // 4 per TMEM lane quarter
+constexpr int SF_WARP = 2 + NUM_EPI_WARPS;      // warp 18: scale-factor copies into TMEM
+constexpr int NUM_THREADS = 32 * (SF_WARP + 1);
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_ACC = 0, TM_SFA = 256, TM_SFB = 260;
+constexpr uint32_t TM_ACC = 0;                  // accumulator: columns 0..255
+constexpr uint32_t TM_SF0 = 256, TM_SF_STRIDE = 12;  // per stage: SFA 4 columns + SFB 8 columns
 constexpr int GROUP_M = 8;
-
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_TILE;
-constexpr int OFF_SFA = OFF_B + STAGES * B_TILE;
-constexpr int OFF_SFB = OFF_SFA + STAGES * SF_ATOM;
-constexpr int OFF_BAR = OFF_SFB + STAGES * 2 * SF_ATOM;
-constexpr int NUM_BARS = 2 * STAGES + 3;        // full[S], empty[S], tmem_full, tmem_empty, drain
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int OFF_SEG = OFF_MISC + 16;
 constexpr int TR_PITCH = 9;                     // floats per row of a warp's 32x8 transpose buffer
 constexpr int TR_WARP_FLOATS = 32 * TR_PITCH;
-constexpr int OFF_TR = OFF_SEG + 260 * 4;       // 16 epilogue warps x 32 x 9 floats
-constexpr int SMEM_USED = OFF_TR + NUM_EPI_WARPS * TR_WARP_FLOATS * 4;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;    // slack to align the base to 1024 B
+
+// Shared-memory layout per epilogue kind.  The SwiGLU-backward GEMM uses
+// 128-column tiles (one B box per stage), so the same bytes hold 6 stages.
+template <int EPI>
+struct Lay {
+  static constexpr int BNT = (EPI == EPI_BWD_SWIGLU) ? 128 : 256;
+  static constexpr int STG = (BNT == 256) ? 4 : 6;
+  static constexpr int B_T = BNT * BK;
+  static constexpr int SFB_T = (BNT / 128) * SF_ATOM;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STG * A_TILE;
+  static constexpr int OFF_SFA = OFF_B + STG * B_T;
+  static constexpr int OFF_SFB = OFF_SFA + STG * SF_ATOM;
+  static constexpr int OFF_BAR = OFF_SFB + STG * SFB_T;
+  // full[S], empty[S], sf_ready[S], tmem_full, tmem_empty, drain (MMA), drain (scale copies)
+  static constexpr int NUM_BARS = 3 * STG + 4;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int OFF_SEG = OFF_MISC + 16;
+  static constexpr int OFF_TR = OFF_SEG + 260 * 4;
+  static constexpr int SMEM_USED = OFF_TR + NUM_EPI_WARPS * TR_WARP_FLOATS * 4;
+  static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 B
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(TM_SF0 + STG * TM_SF_STRIDE <= TMEM_COLS, "TMEM budget");
+};
 
 // ---- PTX wrappers -------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -267,6 +280,30 @@ __device__ __forceinline__ void decode_tile(const GemmArgs& a, const int* seg_mb
   }
 }
 
+// Global sources of one tile's K steps (TMA coordinates and scale atoms).
+struct TileSrc {
+  int a_row, b_row0, b_row1, k0, k_tiles;
+  bool second;
+  const uint8_t *sfa, *sfb0, *sfb1;
+};
+
+template <int EPI>
+__device__ __forceinline__ void tile_src(const GemmArgs& a, const int* seg_mb, int t, TileSrc& ts) {
+  Tile tl;
+  decode_tile<EPI>(a, seg_mb, t, tl);
+  const int64_t sfa_row_atoms = a.sfa_K / BK;
+  const int64_t sfb_row_atoms = a.sfb_K / BK;
+  ts.a_row = int(tl.a_row);
+  ts.b_row0 = int(tl.b_row0);
+  ts.b_row1 = int(tl.b_row1);
+  ts.k0 = int(tl.k0);
+  ts.k_tiles = tl.k_tiles;
+  ts.second = tl.second;
+  ts.sfa = a.sfa + ((tl.a_row / BM) * sfa_row_atoms + tl.k0 / BK) * SF_ATOM;
+  ts.sfb0 = a.sfb + ((tl.b_row0 / 128) * sfb_row_atoms + tl.k0 / BK) * SF_ATOM;
+  ts.sfb1 = a.sfb + ((tl.b_row1 / 128) * sfb_row_atoms + tl.k0 / BK) * SF_ATOM;
+}
+
 // Bounded wait on an mbarrier phase.  Returns false when the CTA aborted or
 // the limit ran out (then records the timeout and raises the abort flag).
 __device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
@@ -448,28 +485,33 @@ template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs args) {
+  using L = Lay<EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* empty = full + STAGES;
-  uint64_t* tmem_full = empty + STAGES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* empty = full + L::STG;
+  uint64_t* sf_ready = empty + L::STG;
+  uint64_t* tmem_full = sf_ready + L::STG;
   uint64_t* tmem_empty = tmem_full + 1;
   uint64_t* drain = tmem_empty + 1;
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-  volatile int* abort_s = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-  int* seg_mb = reinterpret_cast<int*>(smem + OFF_SEG);
+  uint64_t* drain_sf = drain + 1;
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_s = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  int* seg_mb = reinterpret_cast<int*>(smem + L::OFF_SEG);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < L::STG; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&sf_ready[s], 1);
     }
     mbar_init(tmem_full, 1);
     mbar_init(tmem_empty, NUM_EPI_WARPS);
     mbar_init(drain, 1);
+    mbar_init(drain_sf, 1);
     *abort_s = 0;
     int acc = 0;
     for (int e = 0; e < args.E; ++e) {
@@ -499,40 +541,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       // ---------------- TMA producer ----------------
       int it = 0;
-      int last_round[STAGES];
+      int last_round[L::STG];
 #pragma unroll
-      for (int s = 0; s < STAGES; ++s) last_round[s] = -1;
+      for (int s = 0; s < L::STG; ++s) last_round[s] = -1;
       bool ok = true;
+      TileSrc cur, nxt;
+      if (blockIdx.x < total) tile_src<EPI>(args, seg_mb, blockIdx.x, cur);
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        Tile tl;
-        decode_tile<EPI>(args, seg_mb, t, tl);
-        const int64_t sfa_row_atoms = args.sfa_K / BK;
-        const int64_t sfb_row_atoms = args.sfb_K / BK;
-        const uint8_t* sfa = args.sfa + ((tl.a_row / BM) * sfa_row_atoms + tl.k0 / BK) * SF_ATOM;
-        const uint8_t* sfb0 = args.sfb + ((tl.b_row0 / 128) * sfb_row_atoms + tl.k0 / BK) * SF_ATOM;
-        const uint8_t* sfb1 = args.sfb + ((tl.b_row1 / 128) * sfb_row_atoms + tl.k0 / BK) * SF_ATOM;
-        const uint32_t bytes = A_TILE + SF_ATOM * 2 + (tl.second ? (B_HALF * 2 + SF_ATOM) : B_HALF);
-        for (int kt = 0; kt < tl.k_tiles; ++kt, ++it) {
-          const int s = it % STAGES;
-          const int round = it / STAGES;
+        if (t + int(gridDim.x) < total) tile_src<EPI>(args, seg_mb, t + gridDim.x, nxt);
+        const uint32_t bytes = A_TILE + SF_ATOM * 2 + (cur.second ? (B_HALF * 2 + SF_ATOM) : B_HALF);
+        for (int kt = 0; kt < cur.k_tiles; ++kt, ++it) {
+          const int s = it % L::STG;
+          const int round = it / L::STG;
           if (!wait_phase(&empty[s], (round & 1) ^ 1, abort_s, args.err, SITE_GEMM_PRODUCER, kWaitLimitNs)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&full[s], bytes);
           last_round[s] = round;
-          const int kc = int(tl.k0) + kt * BK;
-          tma_load_2d(smem + OFF_A + s * A_TILE, &tmA, kc, int(tl.a_row), &full[s]);
-          tma_load_2d(smem + OFF_B + s * B_TILE, &tmB, kc, int(tl.b_row0), &full[s]);
-          if (tl.second) tma_load_2d(smem + OFF_B + s * B_TILE + B_HALF, &tmB, kc, int(tl.b_row1), &full[s]);
-          bulk_load(smem + OFF_SFA + s * SF_ATOM, sfa + kt * SF_ATOM, SF_ATOM, &full[s]);
-          bulk_load(smem + OFF_SFB + s * 2 * SF_ATOM, sfb0 + kt * SF_ATOM, SF_ATOM, &full[s]);
-          if (tl.second) bulk_load(smem + OFF_SFB + s * 2 * SF_ATOM + SF_ATOM, sfb1 + kt * SF_ATOM, SF_ATOM, &full[s]);
+          const int kc = cur.k0 + kt * BK;
+          tma_load_2d(smem + L::OFF_A + s * A_TILE, &tmA, kc, cur.a_row, &full[s]);
+          tma_load_2d(smem + L::OFF_B + s * L::B_T, &tmB, kc, cur.b_row0, &full[s]);
+          if (cur.second) tma_load_2d(smem + L::OFF_B + s * L::B_T + B_HALF, &tmB, kc, cur.b_row1, &full[s]);
+          bulk_load(smem + L::OFF_SFA + s * SF_ATOM, cur.sfa + kt * SF_ATOM, SF_ATOM, &full[s]);
+          bulk_load(smem + L::OFF_SFB + s * L::SFB_T, cur.sfb0 + kt * SF_ATOM, SF_ATOM, &full[s]);
+          if (cur.second) bulk_load(smem + L::OFF_SFB + s * L::SFB_T + SF_ATOM, cur.sfb1 + kt * SF_ATOM, SF_ATOM, &full[s]);
         }
+        cur = nxt;
       }
       if (!ok) {
         // let copies already issued land before the CTA exits
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < L::STG; ++s) {
           if (last_round[s] < 0) continue;
           const uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait(&full[s], last_round[s] & 1) && globaltimer_ns() - t0 < 20000000ull) {
@@ -555,23 +594,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         const int n = tl.second ? 256 : 128;
         for (int kt = 0; kt < tl.k_tiles; ++kt, ++it) {
-          const int s = it % STAGES;
-          const int round = it / STAGES;
-          if (!wait_phase(&full[s], round & 1, abort_s, args.err, SITE_GEMM_MMA, kWaitLimitNs)) {
+          const int s = it % L::STG;
+          const int round = it / L::STG;
+          // the stage's operands have landed and its scale factors sit in TMEM
+          if (!wait_phase(&sf_ready[s], round & 1, abort_s, args.err, SITE_GEMM_MMA, kWaitLimitNs)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          tc_cp_sf(tmem + TM_SFA, desc_sf(smem_u32(smem + OFF_SFA + s * SF_ATOM)));
-          tc_cp_sf(tmem + TM_SFB, desc_sf(smem_u32(smem + OFF_SFB + s * 2 * SF_ATOM)));
-          if (tl.second) tc_cp_sf(tmem + TM_SFB + 4, desc_sf(smem_u32(smem + OFF_SFB + s * 2 * SF_ATOM + SF_ATOM)));
-          const uint64_t adesc = desc_sw128(smem_u32(smem + OFF_A + s * A_TILE));
-          const uint64_t bdesc = desc_sw128(smem_u32(smem + OFF_B + s * B_TILE));
+          const uint32_t tm_sfa = tmem + TM_SF0 + uint32_t(s) * TM_SF_STRIDE;
+          const uint32_t tm_sfb = tm_sfa + 4;
+          const uint64_t adesc = desc_sw128(smem_u32(smem + L::OFF_A + s * A_TILE));
+          const uint64_t bdesc = desc_sw128(smem_u32(smem + L::OFF_B + s * L::B_T));
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk) {
             // +32 bytes along K inside the 128-byte swizzle atom = +2 in the encoded start address
             tc_mma_mxf8(tmem + TM_ACC, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_mxf8(n, kk),
-                        tmem + TM_SFA, tmem + TM_SFB, (kt | kk) != 0);
+                        tm_sfa, tm_sfb, (kt | kk) != 0);
           }
           issued = true;
           tc_commit(&empty[s]);
@@ -586,12 +625,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
+  } else if (warp == SF_WARP) {
+    if (lane == 0) {
+      // ---------------- scale factors: shared memory -> TMEM ----------------
+      // Issued from their own thread, so the copies are not queued behind the
+      // MMA stream; each stage has its own TMEM columns.
+      int it = 0;
+      bool ok = true, issued = false;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        Tile tl;
+        decode_tile<EPI>(args, seg_mb, t, tl);
+        for (int kt = 0; kt < tl.k_tiles; ++kt, ++it) {
+          const int s = it % L::STG;
+          const int round = it / L::STG;
+          if (!wait_phase(&full[s], round & 1, abort_s, args.err, SITE_GEMM_MMA + 1, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t tm_sfa = tmem + TM_SF0 + uint32_t(s) * TM_SF_STRIDE;
+          const uint32_t tm_sfb = tm_sfa + 4;
+          tc_cp_sf(tm_sfa, desc_sf(smem_u32(smem + L::OFF_SFA + s * SF_ATOM)));
+          tc_cp_sf(tm_sfb, desc_sf(smem_u32(smem + L::OFF_SFB + s * L::SFB_T)));
+          if (tl.second) tc_cp_sf(tm_sfb + 4, desc_sf(smem_u32(smem + L::OFF_SFB + s * L::SFB_T + SF_ATOM)));
+          tc_commit(&sf_ready[s]);
+          issued = true;
+        }
+      }
+      if (!ok && issued) {
+        tc_commit(drain_sf);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(drain_sf, 0) && globaltimer_ns() - t0 < 20000000ull) {
+        }
+      }
+    }
   } else {
     // ---------------- epilogue warps 2..17 ----------------
     const int q = warp & 3;                    // TMEM lane quarter this warp may access
     const int cg = (warp - 2) >> 2;            // column group 0..3
     const uint32_t tmem_row = tmem + (uint32_t(q * 32) << 16);
-    float* tr = reinterpret_cast<float*>(smem + OFF_TR) + (warp - 2) * TR_WARP_FLOATS;
+    float* tr = reinterpret_cast<float*>(smem + L::OFF_TR) + (warp - 2) * TR_WARP_FLOATS;
     int tcount = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
       Tile tl;
@@ -649,11 +722,11 @@ cudaError_t launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, const GemmA
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_BYTES);
+                                         Lay<EPI>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  grouped_gemm_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ma, mb, a);
+  grouped_gemm_kernel<EPI><<<grid, NUM_THREADS, Lay<EPI>::SMEM_BYTES, st>>>(ma, mb, a);
   return cudaGetLastError();
 }
 
