@@ -67,7 +67,7 @@ WsLayout ws_layout(const moe_dims* d, bool training) {
   w.aq = take(cap * I);
   w.aq_s = take(cap * I / 32);
   if (training) {
-    const size_t ntI = I / 128;                     // 128-column tiles of the SwiGLU-backward GEMM
+    const size_t ntI = (I + 255) / 256;             // 256-column tiles of the SwiGLU-backward GEMM
     w.dyq = take(cap * H);
     w.dyq_s = take(cap * H / 32);
     w.dyqc = take(H * cap);
@@ -359,7 +359,7 @@ moe_status grouped_mlp_bwd(const moe_dims* d, const void* dout, const int32_t* s
   g3.split_sizes = split_sizes;
   g3.K = H;
   g3.N = I;
-  g3.n_tiles = I / 128;
+  g3.n_tiles = (I + 255) / 256;
   g3.b_rows_per_expert = I;
   g3.cap = cap;
   g3.sfa = dyq_s;

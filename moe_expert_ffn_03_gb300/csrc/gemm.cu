@@ -50,15 +50,18 @@ constexpr int NUM_THREADS = 32 * (SF_WARP + 1);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_ACC = 0;                  // accumulator: columns 0..255
 constexpr uint32_t TM_SF0 = 256, TM_SF_STRIDE = 12;  // per stage: SFA 4 columns + SFB 8 columns
+// Columns 320..447: per epilogue warp a 32-column parking place (lanes of its quarter)
+// for the second half of its accumulator columns in the SwiGLU-backward epilogue.
+constexpr uint32_t TM_STASH = 320;
 constexpr int GROUP_M = 8;
 constexpr int TR_PITCH = 9;                     // floats per row of a warp's 32x8 transpose buffer
 constexpr int TR_WARP_FLOATS = 32 * TR_PITCH;
 
-// Shared-memory layout per epilogue kind.  The SwiGLU-backward GEMM uses
-// 128-column tiles (one B box per stage), so the same bytes hold 6 stages.
+// Shared-memory layout per epilogue kind (all use 256-column tiles today; a
+// 128-column tile would take one B box per stage and 6 stages).
 template <int EPI>
 struct Lay {
-  static constexpr int BNT = (EPI == EPI_BWD_SWIGLU) ? 128 : 256;
+  static constexpr int BNT = 256;
   static constexpr int STG = (BNT == 256) ? 4 : 6;
   static constexpr int B_T = BNT * BK;
   static constexpr int SFB_T = (BNT / 128) * SF_ATOM;
@@ -75,7 +78,7 @@ struct Lay {
   static constexpr int SMEM_USED = OFF_TR + NUM_EPI_WARPS * TR_WARP_FLOATS * 4;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 B
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(TM_SF0 + STG * TM_SF_STRIDE <= TMEM_COLS, "TMEM budget");
+  static_assert(TM_SF0 + STG * TM_SF_STRIDE <= TM_STASH, "TMEM budget");
 };
 
 // ---- PTX wrappers -------------------------------------------------------------------
@@ -162,6 +165,20 @@ __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t* r) {
       : "r"(taddr)
       : "memory");
 }
+// 32 lanes x 32 consecutive 32-bit columns from registers into TMEM.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+      "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Wait for this thread's outstanding tcgen05.ld; the empty asm statements tie
 // every loaded register to the wait so no use is scheduled before it.
 template <int N>
@@ -248,12 +265,6 @@ __device__ __forceinline__ void decode_tile(const GemmArgs& a, const int* seg_mb
       tl.b_row0 = int64_t(lo) * a.b_rows_per_expert + tl.n0;
       tl.b_row1 = tl.b_row0 + a.I;
       tl.second = true;
-    } else if (EPI == EPI_BWD_SWIGLU) {
-      // 128-column tiles: each epilogue warp then holds 32 dA columns
-      tl.n0 = nb * 128;
-      tl.b_row0 = int64_t(lo) * a.b_rows_per_expert + tl.n0;
-      tl.b_row1 = tl.b_row0;
-      tl.second = false;
     } else {
       tl.n0 = nb * BN;
       tl.b_row0 = int64_t(lo) * a.b_rows_per_expert + tl.n0;
@@ -387,9 +398,8 @@ __device__ __forceinline__ void quant_col_block(const float* v, uint8_t* codes_t
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
 // One epilogue warp on one tile.  The warp owns TMEM lane quarter q (32 rows) and
-// column group cg: 64 accumulator columns cg*64.. of an N=256 tile, gate columns
-// cg*32.. and up columns 128+cg*32.. of a ScaledSwiGLU tile, or columns cg*32..
-// of the 128-column SwiGLU-backward tile.  It pulls its
+// column group cg: 64 accumulator columns cg*64.. of an N=256 tile, or gate
+// columns cg*32.. and up columns 128+cg*32.. of a ScaledSwiGLU tile.  It pulls its
 // columns into registers, releases the accumulator (tmem_empty) and only then
 // runs the epilogue math, so the next tile's MMAs overlap it.
 template <int EPI>
@@ -398,7 +408,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
   const int64_t row = tl.out_row + q * 32 + lane;        // output / permuted row of this thread
   const int64_t row_blk0 = tl.out_row + q * 32;
   const int ncols = tl.second ? 256 : 128;                // valid accumulator columns
-  const int c0 = (EPI == EPI_BWD_SWIGLU) ? cg * 32 : cg * 64;
+  const int c0 = cg * 64;
   uint32_t r[64];
   bool have;
   if (EPI == EPI_FWD_SWIGLU) {
@@ -407,9 +417,17 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     tmem_ld32_async(tmem_row + TM_ACC + 128 + cg * 32, r + 32);
     tmem_wait_ld<64>(r);
   } else if (EPI == EPI_BWD_SWIGLU) {
-    have = true;
-    tmem_ld32_async(tmem_row + TM_ACC + c0, r);
-    tmem_wait_ld<32>(r);
+    // 64 columns do not fit the register budget next to the SwiGLU-backward math:
+    // park the second 32 in this warp's spare TMEM columns, then free the accumulator
+    have = c0 < ncols;
+    if (have) {
+      tmem_ld32_async(tmem_row + TM_ACC + c0 + 32, r);
+      tmem_wait_ld<32>(r);
+      tmem_st32(tmem_row + TM_STASH + cg * 32, r);
+      tmem_ld32_async(tmem_row + TM_ACC + c0, r);
+      tmem_wait_ld<32>(r);
+      tmem_wait_st();
+    }
   } else {
     have = c0 < ncols && tl.k_tiles > 0;
     if (have) {
@@ -445,38 +463,46 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     for (int i = 0; i < 32; ++i) f[i] = silu_f(f[i]) * f[32 + i] * p;
     quant_row_block(f, a.q_row, a.q_row_s, row, col, a.q_row_K);
     if (a.q_col != nullptr) quant_col_block(f, a.q_col, a.q_col_s, row_blk0, col, a.cap, lane, tr);
-  } else {  // EPI_BWD_SWIGLU: this warp's 32 columns of dA
+  } else {  // EPI_BWD_SWIGLU: this warp's 64 columns of dA, as two halves of 32
     float dp = 0.f;
-    const float p = a.prob_perm[row];
-    const int64_t twoI = 2 * int64_t(a.I);
-    const __nv_bfloat16* grow = a.gu + row * twoI;
-    const int64_t col = tl.n0 + c0;
-    float o[32];
-    // dg = dA*p*u*silu'(g) and the row sum dp += dA*silu(g)*u
+    if (have) {
+      const float p = a.prob_perm[row];
+      const int64_t twoI = 2 * int64_t(a.I);
+      const __nv_bfloat16* grow = a.gu + row * twoI;
+      for (int h = 0; h < 2; ++h) {
+        if (h == 1) {
+          tmem_ld32_async(tmem_row + TM_STASH + cg * 32, r);
+          tmem_wait_ld<32>(r);
+        }
+        const int64_t col = tl.n0 + c0 + 32 * h;
+        float o[32];
+        // dg = dA*p*u*silu'(g) and the row sum dp += dA*silu(g)*u
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 gw = *reinterpret_cast<const uint4*>(grow + col + 8 * j);
-      const uint4 uw = *reinterpret_cast<const uint4*>(grow + a.I + col + 8 * j);
-      const uint32_t gs[4] = {gw.x, gw.y, gw.z, gw.w};
-      const uint32_t us[4] = {uw.x, uw.y, uw.z, uw.w};
+        for (int j = 0; j < 4; ++j) {
+          const uint4 gw = *reinterpret_cast<const uint4*>(grow + col + 8 * j);
+          const uint4 uw = *reinterpret_cast<const uint4*>(grow + a.I + col + 8 * j);
+          const uint32_t gs[4] = {gw.x, gw.y, gw.z, gw.w};
+          const uint32_t us[4] = {uw.x, uw.y, uw.z, uw.w};
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int i = 8 * j + t;
-        const float g = (t & 1) ? bf16_hi(gs[t >> 1]) : bf16_lo(gs[t >> 1]);
-        const float u = (t & 1) ? bf16_hi(us[t >> 1]) : bf16_lo(us[t >> 1]);
-        const float d = __uint_as_float(r[i]);
-        const float sgm = 1.0f / (1.0f + __expf(-g));
-        const float sg = g * sgm;
-        dp += d * sg * u;
-        o[i] = d * p * u * (sgm * (1.0f + g * (1.0f - sgm)));
-        r[i] = __float_as_uint(d * p * sg);            // du = dA*p*silu(g)
+          for (int t = 0; t < 8; ++t) {
+            const int i = 8 * j + t;
+            const float g = (t & 1) ? bf16_hi(gs[t >> 1]) : bf16_lo(gs[t >> 1]);
+            const float u = (t & 1) ? bf16_hi(us[t >> 1]) : bf16_lo(us[t >> 1]);
+            const float d = __uint_as_float(r[i]);
+            const float sgm = 1.0f / (1.0f + __expf(-g));
+            const float sg = g * sgm;
+            dp += d * sg * u;
+            o[i] = d * p * u * (sgm * (1.0f + g * (1.0f - sgm)));
+            r[i] = __float_as_uint(d * p * sg);            // du = dA*p*silu(g)
+          }
+        }
+        quant_row_block(o, a.q_row, a.q_row_s, row, col, twoI);
+        quant_col_block(o, a.q_col, a.q_col_s, row_blk0, col, a.cap, lane, tr);
+        const float* du = reinterpret_cast<const float*>(r);
+        quant_row_block(du, a.q_row, a.q_row_s, row, a.I + col, twoI);
+        quant_col_block(du, a.q_col, a.q_col_s, row_blk0, a.I + col, a.cap, lane, tr);
       }
     }
-    quant_row_block(o, a.q_row, a.q_row_s, row, col, twoI);
-    quant_col_block(o, a.q_col, a.q_col_s, row_blk0, col, a.cap, lane, tr);
-    const float* du = reinterpret_cast<const float*>(r);
-    quant_row_block(du, a.q_row, a.q_row_s, row, a.I + col, twoI);
-    quant_col_block(du, a.q_col, a.q_col_s, row_blk0, a.I + col, a.cap, lane, tr);
     a.dp_part[(int64_t(tl.nb) * 4 + cg) * a.cap + row] = dp;
   }
 }
@@ -670,8 +696,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       Tile tl;
       decode_tile<EPI>(args, seg_mb, t, tl);
       if (EPI == EPI_BWD_SWIGLU) {
-        // pull this thread's saved g and u (64 B each) toward L2 while the MMAs run
-        const __nv_bfloat16* grow = args.gu + (tl.out_row + q * 32 + lane) * (2 * int64_t(args.I)) + tl.n0 + cg * 32;
+        // pull this thread's saved g and u (128 B each) toward L2 while the MMAs run
+        const __nv_bfloat16* grow = args.gu + (tl.out_row + q * 32 + lane) * (2 * int64_t(args.I)) + tl.n0 + cg * 64;
         asm volatile("prefetch.global.L2 [%0];" ::"l"(grow));
         asm volatile("prefetch.global.L2 [%0];" ::"l"(grow + args.I));
       }
