@@ -122,13 +122,20 @@ def barrier(world):
 
 
 def max_over_ranks(v: float, world: int) -> float:
+    """The slowest rank's time: every replica's timed region ends with the barrier."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_throughput(units_per_replica: float, ms_max: float, world: int) -> float:
+    """Whole-job rate of `world` independent replicas (weak scaling): all ranks' units / slowest time."""
+    return world * units_per_replica / (ms_max * 1e-3)
 
 
 # ------------------------------------------------------------------------------------
@@ -207,7 +214,7 @@ def run_cuda(args):
         raise RuntimeError(f"device error {code} at site {site}")
 
     flops = wl.flops_total()
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = replica_throughput(flops, ms_step, world) / 1e12
     peaks, src = read_peaks()
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
     gemm_ms = parts["grouped_mlp_fwd_ms"] + parts["grouped_mlp_bwd_ms"]
@@ -244,7 +251,7 @@ def run_cuda(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
-    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+    e2e_value = replica_throughput(flops, e2e_ms, world) / 1e12
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -262,7 +269,7 @@ def run_cuda(args):
                    "pass": "fwd+bwd" if train else "fwd", "global_batch_tokens": wl.T * world,
                    "l2": "inputs larger than L2 (2.8 GB bf16 weights re-read every step); no flush",
                    "parallelism": f"replicas x{world} (no exchange step)"},
-        "tokens_per_s": round(world * wl.T / (ms_step * 1e-3), 1),
+        "tokens_per_s": round(replica_throughput(wl.T, ms_step, world), 1),
         "frac_of_mxfp8_peak": round(value / world / fp8_peak, 4),
         "breakdown_ms": {k: round(v, 4) for k, v in parts.items()},
         "roofline": {"bound": "tensor", "kernel": f"grouped_gemm_kernel ({n_gemm} launches per step)",
