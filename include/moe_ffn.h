@@ -239,6 +239,18 @@ moe_status grouped_mlp_bwd(const moe_dims* d, const void* dout,
 moe_status moe_unpermute_combine(const moe_dims* d, const void* y_perm, const int32_t* row_of,
                                  const float* prob, void* out, moe_stream_t stream);
 
+/* moe_selftest_wait_timeout -- exercises the device-side failure path without
+ * faulting anything.  One launch of the grouped GEMM kernel over a single
+ * 128x256x128 tile whose producer is told to issue no loads: the MMA, scale
+ * copy and epilogue warps wait for data that never comes, each wait runs out
+ * after limit_ns (1 ms .. 2 s), the kernel records MOE_ERR_DEVICE_TIMEOUT and a
+ * site id, frees its tensor memory and returns.  Synchronises `stream` and
+ * returns the recorded *code and *site (expected: MOE_ERR_DEVICE_TIMEOUT and a
+ * site in 500..599).  scratch: >= 96 KB of device memory, 256-byte aligned,
+ * overwritten.  The context stays usable afterwards. */
+moe_status moe_selftest_wait_timeout(void* scratch, size_t scratch_bytes, int64_t limit_ns, int32_t* code,
+                                     int32_t* site, moe_stream_t stream);
+
 /* Read (and keep) the device error word of a workspace: *code is a
  * moe_status (MOE_OK if none), *site identifies the kernel and wait.
  * Synchronises `stream`. */

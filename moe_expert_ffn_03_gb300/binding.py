@@ -18,6 +18,7 @@ EXPORTS = (
     "moe_status_string", "moe_last_error_message", "moe_rows_capacity", "moe_workspace_size",
     "mxfp8_quantize", "mxfp8_quantize_dual", "moe_route_permute", "grouped_mlp_fwd", "grouped_mlp_bwd",
     "moe_unpermute_combine", "moe_get_device_error", "moe_clear_device_error", "moe_route_permute_noalloc",
+    "moe_selftest_wait_timeout",
 )
 
 MOE_OK = 0
@@ -71,6 +72,8 @@ def lib() -> ctypes.CDLL:
             "moe_get_device_error": ([P, ctypes.POINTER(c_int32), ctypes.POINTER(c_int32), P], c_int32),
             "moe_clear_device_error": ([P, P], c_int32),
             "moe_route_permute_noalloc": ([D, P, P, P, P, P, P, P, P, P, P, P, P, P], c_int32),
+            "moe_selftest_wait_timeout": ([P, c_size_t, ctypes.c_int64, ctypes.POINTER(c_int32),
+                                           ctypes.POINTER(c_int32), P], c_int32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -153,6 +156,13 @@ def moe_unpermute_combine(d, y_perm, row_of, prob, out, stream=None):
 def moe_get_device_error(workspace, stream=None):
     code, site = c_int32(0), c_int32(0)
     _check(lib().moe_get_device_error(_p(workspace), ctypes.byref(code), ctypes.byref(site), _st(stream)))
+    return int(code.value), int(site.value)
+
+
+def moe_selftest_wait_timeout(scratch, limit_ns, stream=None):
+    code, site = c_int32(0), c_int32(0)
+    _check(lib().moe_selftest_wait_timeout(_p(scratch), scratch.numel() * scratch.element_size(), int(limit_ns),
+                                           ctypes.byref(code), ctypes.byref(site), _st(stream)))
     return int(code.value), int(site.value)
 
 

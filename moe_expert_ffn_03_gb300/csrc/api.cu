@@ -463,6 +463,52 @@ moe_status moe_unpermute_combine(const moe_dims* d, const void* y_perm, const in
   return MOE_OK;
 }
 
+moe_status moe_selftest_wait_timeout(void* scratch, size_t scratch_bytes, int64_t limit_ns, int32_t* code,
+                                     int32_t* site, moe_stream_t stream) {
+  g_msg[0] = 0;
+  constexpr size_t kNeed = 96 * 1024;
+  if (scratch == nullptr || code == nullptr || site == nullptr)
+    return fail(MOE_ERR_INVALID_ARG, "scratch, code and site must be non-NULL");
+  if ((reinterpret_cast<uintptr_t>(scratch) & 255u) != 0) return fail(MOE_ERR_ALIGNMENT, "scratch must be 256-byte aligned");
+  if (scratch_bytes < kNeed) return fail(MOE_ERR_WORKSPACE, "scratch needs %zu bytes", kNeed);
+  if (limit_ns < 1000000 || limit_ns > 2000000000) return fail(MOE_ERR_INVALID_ARG, "limit_ns must be in [1 ms, 2 s]");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // layout: [0,256) error word, [256,512) split_sizes, [4 KB, +16 KB) A codes 128x128,
+  // [20 KB, +32 KB) B codes 256x128, [52 KB, +512) A scales, [53 KB, +1 KB) B scales
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  CUDA_TRY(cudaMemsetAsync(scratch, 0, kNeed, st), "clear scratch");
+  static const int32_t one_expert_rows = 128;
+  CUDA_TRY(cudaMemcpyAsync(base + 256, &one_expert_rows, sizeof(int32_t), cudaMemcpyHostToDevice, st),
+           "split_sizes");
+  GemmArgs g{};
+  g.mode = 0;
+  g.E = 1;
+  g.split_sizes = reinterpret_cast<const int*>(base + 256);
+  g.K = 128;
+  g.N = 256;
+  g.n_tiles = 1;
+  g.b_rows_per_expert = 256;
+  g.cap = 128;
+  g.sfa = base + 52 * 1024;
+  g.sfb = base + 53 * 1024;
+  g.sfa_K = 128;
+  g.sfb_K = 128;
+  g.out = reinterpret_cast<__nv_bfloat16*>(base + 60 * 1024);   // 128 x 128 bf16 would fit; never written
+  g.ldo = 128;
+  g.err = reinterpret_cast<int*>(base);
+  g.wait_limit_ns = uint64_t(limit_ns);
+  g.selftest_no_loads = 1;
+  CUDA_TRY(launch_grouped_gemm(EPI_BF16, g, base + 4 * 1024, 128, 128, base + 20 * 1024, 256, 128, 1, st, g_msg,
+                               sizeof(g_msg)),
+           "self-test GEMM");
+  int32_t h[2] = {0, 0};
+  CUDA_TRY(cudaMemcpyAsync(h, scratch, sizeof(h), cudaMemcpyDeviceToHost, st), "read error word");
+  CUDA_TRY(cudaStreamSynchronize(st), "synchronize");
+  *code = h[0];
+  *site = h[1];
+  return MOE_OK;
+}
+
 moe_status moe_get_device_error(const void* workspace, int32_t* code, int32_t* site, moe_stream_t stream) {
   g_msg[0] = 0;
   if (workspace == nullptr || code == nullptr || site == nullptr)

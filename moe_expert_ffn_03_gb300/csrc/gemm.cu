@@ -560,11 +560,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
   const int total = tile_count(args, seg_mb);
+  const uint64_t lim = args.wait_limit_ns != 0 ? args.wait_limit_ns : kWaitLimitNs;
   // the padded segments must fit the permuted capacity (rows in mode 0, K in mode 1)
   if (int64_t(seg_mb[args.E]) * BM > args.cap) {
     if (threadIdx.x == 0) report_error(args.err, MOE_ERR_DEVICE_BOUNDS, SITE_GEMM_PRODUCER + 9);
   } else if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && !args.selftest_no_loads) {
       // ---------------- TMA producer ----------------
       int it = 0;
       int last_round[L::STG];
@@ -579,7 +580,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int kt = 0; kt < cur.k_tiles; ++kt, ++it) {
           const int s = it % L::STG;
           const int round = it / L::STG;
-          if (!wait_phase(&empty[s], (round & 1) ^ 1, abort_s, args.err, SITE_GEMM_PRODUCER, kWaitLimitNs)) {
+          if (!wait_phase(&empty[s], (round & 1) ^ 1, abort_s, args.err, SITE_GEMM_PRODUCER, lim)) {
             ok = false;
             break;
           }
@@ -613,7 +614,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
         Tile tl;
         decode_tile<EPI>(args, seg_mb, t, tl);
-        if (!wait_phase(tmem_empty, (tcount & 1) ^ 1, abort_s, args.err, SITE_GEMM_MMA_ACC, kWaitLimitNs)) {
+        if (!wait_phase(tmem_empty, (tcount & 1) ^ 1, abort_s, args.err, SITE_GEMM_MMA_ACC, lim)) {
           ok = false;
           break;
         }
@@ -623,7 +624,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int s = it % L::STG;
           const int round = it / L::STG;
           // the stage's operands have landed and its scale factors sit in TMEM
-          if (!wait_phase(&sf_ready[s], round & 1, abort_s, args.err, SITE_GEMM_MMA, kWaitLimitNs)) {
+          if (!wait_phase(&sf_ready[s], round & 1, abort_s, args.err, SITE_GEMM_MMA, lim)) {
             ok = false;
             break;
           }
@@ -664,7 +665,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int kt = 0; kt < tl.k_tiles; ++kt, ++it) {
           const int s = it % L::STG;
           const int round = it / L::STG;
-          if (!wait_phase(&full[s], round & 1, abort_s, args.err, SITE_GEMM_MMA + 1, kWaitLimitNs)) {
+          if (!wait_phase(&full[s], round & 1, abort_s, args.err, SITE_GEMM_MMA + 1, lim)) {
             ok = false;
             break;
           }
@@ -701,7 +702,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(grow));
         asm volatile("prefetch.global.L2 [%0];" ::"l"(grow + args.I));
       }
-      if (!wait_phase(tmem_full, tcount & 1, abort_s, args.err, SITE_GEMM_EPILOGUE, kWaitLimitNs)) break;
+      if (!wait_phase(tmem_full, tcount & 1, abort_s, args.err, SITE_GEMM_EPILOGUE, lim)) break;
       tc_fence_after();
       epilogue_tile<EPI>(args, tl, tmem_row, q, cg, lane, tmem_empty, tr);
     }

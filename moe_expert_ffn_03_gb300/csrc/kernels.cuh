@@ -63,6 +63,8 @@ struct GemmArgs {
   float* dp_part;            // BWD: [n_tiles][cap] partial row sums of dA*silu(g)*u
   int I;
   int* err;
+  uint64_t wait_limit_ns;    // bound of every mbarrier wait (0: the default kWaitLimitNs)
+  int selftest_no_loads;     // self-test only: the producer issues nothing, so the waits run out
 };
 
 cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64_t a_rows, int64_t a_K,

@@ -79,3 +79,13 @@ def test_binding_signatures_match_header(lib):
     counts = header_param_counts()
     for name in B.EXPORTS:
         assert len(getattr(lib, name).argtypes) == counts[name], name
+
+
+def test_selftest_checks_arguments_before_launch(lib):
+    code, site = ctypes.c_int32(0), ctypes.c_int32(0)
+    s = lib.moe_selftest_wait_timeout(ctypes.c_void_p(256), 1024, 20_000_000, ctypes.byref(code),
+                                      ctypes.byref(site), None)
+    assert s == 4                                                     # scratch too small
+    s = lib.moe_selftest_wait_timeout(ctypes.c_void_p(256), 1 << 20, 10, ctypes.byref(code),
+                                      ctypes.byref(site), None)
+    assert s == 1                                                     # limit out of range
