@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(256) quant_colwise_kernel(
     int rows, int cols, const int* __restrict__ split_sizes, int E,
     uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t, int* err) {
   __shared__ __align__(16) __nv_bfloat16 tile[QC_TILE * QC_PITCH];
+  __shared__ __align__(16) uint8_t sc_atom[512];
   __shared__ int s_rows_used;
   const int row0 = blockIdx.x * QC_TILE;
   const int col0 = blockIdx.y * QC_TILE;
@@ -112,8 +113,10 @@ __global__ void __launch_bounds__(256) quant_colwise_kernel(
     __syncthreads();
     if (row0 >= s_rows_used) return;
   }
-  // stage: 128 rows x 256 bytes = 16 uint4 per row
-  for (int i = threadIdx.x; i < QC_TILE * 16; i += blockDim.x) {
+  // stage: 128 rows x 256 bytes = 16 uint4 per row; all eight loads of a thread in flight together
+#pragma unroll
+  for (int it = 0; it < QC_TILE * 16 / 256; ++it) {
+    const int i = threadIdx.x + it * 256;
     const int r = i >> 4, c16 = i & 15;
     int64_t sr;
     if (src_map != nullptr) {
@@ -139,7 +142,13 @@ __global__ void __launch_bounds__(256) quant_colwise_kernel(
     uint32_t q[8];
     const uint32_t sc = mx_quant32(v, q);
     store_codes32(codes_t + drow * rows + row0 + rb * 32, q);
-    scales_t[sf_offset(drow, (row0 >> 5) + rb, rows)] = uint8_t(sc);
+    sc_atom[((c & 31) << 4) + (((c >> 5) & 3) << 2) + rb] = uint8_t(sc);
+  }
+  __syncthreads();
+  // the tile's scales are exactly one 512-byte atom of the transposed tensor
+  if (threadIdx.x < 32) {
+    const int64_t atom = ((batch * cols + col0) >> 7) * (rows >> 7) + (row0 >> 7);
+    reinterpret_cast<uint4*>(scales_t + (atom << 9))[threadIdx.x] = reinterpret_cast<const uint4*>(sc_atom)[threadIdx.x];
   }
 }
 
@@ -153,11 +162,15 @@ __global__ void __launch_bounds__(256) quant_dual_kernel(
     const __nv_bfloat16* __restrict__ src, int rows, int cols, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t) {
   __shared__ __align__(16) __nv_bfloat16 tile[QC_TILE * QC_PITCH];
+  __shared__ __align__(16) uint8_t sc_row[512];
+  __shared__ __align__(16) uint8_t sc_col[512];
   const int row0 = blockIdx.x * QC_TILE;
   const int col0 = blockIdx.y * QC_TILE;
   const int64_t batch = blockIdx.z;
   const int64_t srow0 = batch * rows + row0;
-  for (int i = threadIdx.x; i < QC_TILE * 16; i += blockDim.x) {
+#pragma unroll
+  for (int it = 0; it < QC_TILE * 16 / 256; ++it) {
+    const int i = threadIdx.x + it * 256;
     const int r = i >> 4, c16 = i & 15;
     const uint4 w = reinterpret_cast<const uint4*>(src + (srow0 + r) * cols + col0)[c16];
     *reinterpret_cast<uint4*>(&tile[r * QC_PITCH + c16 * 8]) = w;
@@ -179,7 +192,7 @@ __global__ void __launch_bounds__(256) quant_dual_kernel(
     const uint32_t sc = mx_quant32(v, q);
     const int64_t drow = srow0 + r;
     store_codes32(codes + drow * cols + col0 + b * 32, q);
-    scales[sf_offset(drow, (col0 >> 5) + b, cols)] = uint8_t(sc);
+    sc_row[((r & 31) << 4) + (((r >> 5) & 3) << 2) + b] = uint8_t(sc);
   }
   // colwise: task = (column c, row block rb), 128 x 4
   for (int task = threadIdx.x; task < QC_TILE * 4; task += blockDim.x) {
@@ -191,7 +204,17 @@ __global__ void __launch_bounds__(256) quant_dual_kernel(
     const uint32_t sc = mx_quant32(v, q);
     const int64_t drow = batch * cols + col0 + c;
     store_codes32(codes_t + drow * rows + row0 + rb * 32, q);
-    scales_t[sf_offset(drow, (row0 >> 5) + rb, rows)] = uint8_t(sc);
+    sc_col[((c & 31) << 4) + (((c >> 5) & 3) << 2) + rb] = uint8_t(sc);
+  }
+  __syncthreads();
+  // each orientation's scales of this tile are exactly one 512-byte atom
+  if (threadIdx.x < 32) {
+    const int64_t atom = (srow0 >> 7) * (cols >> 7) + (col0 >> 7);
+    reinterpret_cast<uint4*>(scales + (atom << 9))[threadIdx.x] = reinterpret_cast<const uint4*>(sc_row)[threadIdx.x];
+  } else if (threadIdx.x < 64) {
+    const int64_t atom = ((batch * cols + col0) >> 7) * (rows >> 7) + (row0 >> 7);
+    reinterpret_cast<uint4*>(scales_t + (atom << 9))[threadIdx.x - 32] =
+        reinterpret_cast<const uint4*>(sc_col)[threadIdx.x - 32];
   }
 }
 
