@@ -253,6 +253,30 @@ def run_cuda(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
     e2e_value = replica_throughput(flops, e2e_ms, world) / 1e12
 
+    # ---- router on both sides (timed on its own; the step above starts from logits) ----
+    router = None
+    if train:
+        w_r = synth.make_router_weight(wl, seed=0, device=dev)
+        L.router_forward(inp["x"], w_r)
+        L.router_backward(inp["x"], w_r)
+        torch.cuda.synchronize()
+        r0, r1, r2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        n_r = 10
+        r0.record(stream)
+        for _ in range(n_r):
+            L.router_forward(inp["x"], w_r)
+        r1.record(stream)
+        for _ in range(n_r):
+            L.router_backward(inp["x"], w_r)
+        r2.record(stream)
+        torch.cuda.synchronize()
+        fwd_ms, bwd_ms = r0.elapsed_time(r1) / n_r, r1.elapsed_time(r2) / n_r
+        xb = wl.T * wl.H * 2
+        router = {"fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4),
+                  "fwd_gbs": round((xb + wl.E * wl.H * 2 + wl.T * wl.E * 4) / fwd_ms / 1e6, 1),
+                  "bwd_gbs": round((3 * xb + 2 * wl.T * wl.E * 4) / bwd_ms / 1e6, 1),
+                  "bytes": "fwd: x + W_r + logits; bwd: x (dW_r) + dx read and written + dlogits"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_tokens, wl)
@@ -284,6 +308,8 @@ def run_cuda(args):
         "gpu_launches": (LAUNCHES_PER_TRAINING_STEP if train else LAUNCHES_PER_FORWARD_STEP) * args.steps,
         "clocks": clocks,
     }
+    if router is not None:
+        line["router"] = router
     if cpu is not None:
         line["cpu_baseline"] = cpu
     print(json.dumps(line))

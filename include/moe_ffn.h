@@ -239,6 +239,36 @@ moe_status grouped_mlp_bwd(const moe_dims* d, const void* dout,
 moe_status moe_unpermute_combine(const moe_dims* d, const void* y_perm, const int32_t* row_of,
                                  const float* prob, void* out, moe_stream_t stream);
 
+/*
+ * moe_router_fwd -- router logits of a linear router: logits[t][e] =
+ * sum_h x[t][h] * w_r[e][h], f32 sums in ascending h (page
+ * "英伟达开源MoE加速神器", section "三板斧": each token is routed to a few
+ * experts; the pages give no router formula, a bias-free linear map is the
+ * reading).
+ *   x bf16 [T][H]; w_r bf16 [E][H]; logits out f32 [T][E].
+ */
+moe_status moe_router_fwd(const moe_dims* d, const void* x, const void* w_r, float* logits, moe_stream_t stream);
+
+/*
+ * moe_router_bwd -- gradient of the router from dprob (grouped_mlp_bwd),
+ * through the top-k softmax with the selection held fixed (page "Efficient
+ * MoE Training for Biological Foundation Models", section "MXFP8与融合MLP":
+ * the probabilities scale the SwiGLU output, so their gradient reaches the
+ * router).
+ *   renormalize=1: dlogits[t][e_j] = p_j (dp_j - sum_i p_i dp_i), 0 elsewhere;
+ *   renormalize=0: dlogits[t][e] = s_e (g_e - sum_j p_j dp_j), s = softmax of the
+ *                  row, g = dprob scattered to idx.
+ *   logits f32 [T][E], idx int32 [T][k], prob f32 [T][k] (from
+ *   moe_route_permute), dprob f32 [T][k]; dlogits out f32 [T][E];
+ *   dx in/out bf16 [T][H]: dx[t] += sum_e dlogits[t][e] w_r[e] (f32 sum, one
+ *   rounding to bf16); dw_r out f32 [E][H] = dlogits^T x, summed over fixed
+ *   token chunks in chunk order (deterministic).
+ *   workspace: as for grouped_mlp_bwd (moe_workspace_size with training).
+ */
+moe_status moe_router_bwd(const moe_dims* d, const void* x, const void* w_r, const float* logits,
+                          const int32_t* idx, const float* prob, const float* dprob, float* dlogits,
+                          void* dx, float* dw_r, void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* moe_selftest_wait_timeout -- exercises the device-side failure path without
  * faulting anything.  One launch of the grouped GEMM kernel over a single
  * 128x256x128 tile whose producer is told to issue no loads: the MMA, scale

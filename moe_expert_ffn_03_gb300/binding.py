@@ -18,7 +18,7 @@ EXPORTS = (
     "moe_status_string", "moe_last_error_message", "moe_rows_capacity", "moe_workspace_size",
     "mxfp8_quantize", "mxfp8_quantize_dual", "moe_route_permute", "grouped_mlp_fwd", "grouped_mlp_bwd",
     "moe_unpermute_combine", "moe_get_device_error", "moe_clear_device_error", "moe_route_permute_noalloc",
-    "moe_selftest_wait_timeout",
+    "moe_selftest_wait_timeout", "moe_router_fwd", "moe_router_bwd",
 )
 
 MOE_OK = 0
@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
             "moe_get_device_error": ([P, ctypes.POINTER(c_int32), ctypes.POINTER(c_int32), P], c_int32),
             "moe_clear_device_error": ([P, P], c_int32),
             "moe_route_permute_noalloc": ([D, P, P, P, P, P, P, P, P, P, P, P, P, P], c_int32),
+            "moe_router_fwd": ([D, P, P, P, P], c_int32),
+            "moe_router_bwd": ([D, P, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
             "moe_selftest_wait_timeout": ([P, c_size_t, ctypes.c_int64, ctypes.POINTER(c_int32),
                                            ctypes.POINTER(c_int32), P], c_int32),
         }
@@ -157,6 +159,16 @@ def moe_get_device_error(workspace, stream=None):
     code, site = c_int32(0), c_int32(0)
     _check(lib().moe_get_device_error(_p(workspace), ctypes.byref(code), ctypes.byref(site), _st(stream)))
     return int(code.value), int(site.value)
+
+
+def moe_router_fwd(d, x, w_r, logits, stream=None):
+    _check(lib().moe_router_fwd(ctypes.byref(d), _p(x), _p(w_r), _p(logits), _st(stream)))
+
+
+def moe_router_bwd(d, x, w_r, logits, idx, prob, dprob, dlogits, dx, dw_r, workspace, stream=None):
+    _check(lib().moe_router_bwd(ctypes.byref(d), _p(x), _p(w_r), _p(logits), _p(idx), _p(prob), _p(dprob),
+                                _p(dlogits), _p(dx), _p(dw_r), _p(workspace),
+                                workspace.numel() * workspace.element_size(), _st(stream)))
 
 
 def moe_selftest_wait_timeout(scratch, limit_ns, stream=None):

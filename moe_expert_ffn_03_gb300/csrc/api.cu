@@ -46,7 +46,7 @@ moe_status check_dims(const moe_dims* d) {
 
 struct WsLayout {
   size_t err, masks, bases, aq, aq_s;
-  size_t dyq, dyq_s, dyqc, dyqc_s, dhq, dhq_s, dhqc, dhqc_s, dp;
+  size_t dyq, dyq_s, dyqc, dyqc_s, dhq, dhq_s, dhqc, dhqc_s, dp, rpart;
   size_t total;
 };
 
@@ -77,6 +77,7 @@ WsLayout ws_layout(const moe_dims* d, bool training) {
     w.dhqc = take(2 * I * cap);
     w.dhqc_s = take(2 * I * cap / 32);
     w.dp = take(ntI * 4 * cap * 4);                 // one partial row sum per 64-column group
+    w.rpart = take(router_partial_bytes(d->E, d->H));   // router weight-gradient partials
   }
   w.total = off;
   return w;
@@ -460,6 +461,42 @@ moe_status moe_unpermute_combine(const moe_dims* d, const void* y_perm, const in
   CUDA_TRY(launch_combine(y_perm, row_of, prob, d->T, d->k, d->H, capacity(d), out, nullptr,
                           static_cast<cudaStream_t>(stream)),
            "combine");
+  return MOE_OK;
+}
+
+moe_status moe_router_fwd(const moe_dims* d, const void* x, const void* w_r, float* logits, moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(w_r);
+  REQUIRE_PTR(logits);
+  CUDA_TRY(launch_router_fwd(x, w_r, d->T, d->H, d->E, logits, static_cast<cudaStream_t>(stream)), "router fwd");
+  return MOE_OK;
+}
+
+moe_status moe_router_bwd(const moe_dims* d, const void* x, const void* w_r, const float* logits, const int32_t* idx,
+                          const float* prob, const float* dprob, float* dlogits, void* dx, float* dw_r,
+                          void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(w_r);
+  REQUIRE_PTR(logits);
+  REQUIRE_PTR(idx);
+  REQUIRE_PTR(prob);
+  REQUIRE_PTR(dprob);
+  REQUIRE_PTR(dlogits);
+  REQUIRE_PTR(dx);
+  REQUIRE_PTR(dw_r);
+  s = check_ws(d, workspace, workspace_bytes, true);
+  if (s != MOE_OK) return s;
+  const WsLayout w = ws_layout(d, true);
+  CUDA_TRY(launch_router_bwd(x, w_r, logits, idx, prob, dprob, d->T, d->H, d->E, d->k, d->renormalize, dlogits, dx,
+                             dw_r, at<float>(workspace, w.rpart), at<int>(workspace, w.err),
+                             static_cast<cudaStream_t>(stream)),
+           "router bwd");
   return MOE_OK;
 }
 

@@ -19,6 +19,11 @@ cudaError_t launch_quant_colwise(const void* src, const int* src_map, int64_t n_
                                  int* err, cudaStream_t st);
 cudaError_t launch_quant_dual(const void* src, int batch, int rows, int cols, uint8_t* codes, uint8_t* scales,
                               uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st);
+size_t router_partial_bytes(int E, int H);
+cudaError_t launch_router_fwd(const void* x, const void* w, int T, int H, int E, float* logits, cudaStream_t st);
+cudaError_t launch_router_bwd(const void* x, const void* w, const float* logits, const int* idx, const float* prob,
+                              const float* dprob, int T, int H, int E, int k, int renorm, float* dl, void* dx,
+                              float* dw, float* partial, int* err, cudaStream_t st);
 cudaError_t launch_route_permute(const float* logits, int T, int E, int k, int renorm, int* idx, float* prob,
                                  uint32_t* masks, int* bases, int* split_sizes, int* row_of, int* src_of,
                                  float* prob_perm, int* err, cudaStream_t st);

@@ -111,6 +111,23 @@ class ExpertFFN:
         self.combine_dx(stream)
         return self.dx
 
+    # ---- router (optional: when the logits come from x) ------------------------------
+    def router_forward(self, x, w_r, stream=None):
+        """logits = x W_r^T into self.logits (allocated on first use)."""
+        if not hasattr(self, "logits"):
+            self.logits = torch.empty(self.T, self.E, dtype=torch.float32, device=self.ws.device)
+        B.moe_router_fwd(self.d, x, w_r, self.logits, stream)
+        return self.logits
+
+    def router_backward(self, x, w_r, stream=None):
+        """After backward(): dlogits, dW_r, and the router's term added into self.dx."""
+        if not hasattr(self, "dlogits"):
+            self.dlogits = torch.empty(self.T, self.E, dtype=torch.float32, device=self.ws.device)
+            self.dw_r = torch.empty(self.E, self.H, dtype=torch.float32, device=self.ws.device)
+        B.moe_router_bwd(self.d, x, w_r, self.logits, self.idx, self.prob, self.dprob, self.dlogits, self.dx,
+                         self.dw_r, self.ws, stream)
+        return self.dx
+
     def device_error(self, stream=None):
         return B.moe_get_device_error(self.ws, stream)
 

@@ -112,7 +112,7 @@ def normal_bf16(key: int, shape, std: float, device) -> torch.Tensor:
 
 
 # tensor ids of the streams
-TID_X, TID_LOGITS, TID_WGU, TID_WD, TID_DOUT, TID_BIAS = 1, 2, 3, 4, 5, 6
+TID_X, TID_LOGITS, TID_WGU, TID_WD, TID_DOUT, TID_BIAS, TID_WR = 1, 2, 3, 4, 5, 6, 7
 
 
 def make_logits(cfg, seed: int, device) -> torch.Tensor:
@@ -165,3 +165,8 @@ def make_inputs(cfg, seed: int = 0, device="cpu", with_grad: bool | None = None)
     if with_grad:
         d["dout"] = normal_bf16(stream_key(seed, TID_DOUT), (T, H), cfg.g_std, device)
     return d
+
+
+def make_router_weight(cfg, seed: int = 0, device="cpu") -> torch.Tensor:
+    """W_r [E][H] bf16 ~ N(0, 0.02^2) for the linear router."""
+    return normal_bf16(stream_key(seed, TID_WR), (cfg.E, cfg.H), cfg.w_std, device)

@@ -1,0 +1,66 @@
+"""GPU router (forward logits, backward through the top-k softmax) vs the oracle.
+
+The routing decisions come from logits, so the oracle takes the device's logits
+as its input for everything downstream (both sides then select the same
+experts); the logits themselves are compared with the float tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import assert_close
+from moe_expert_ffn_03_gb300 import build, configs, synth
+from moe_expert_ffn_03_gb300.layer import ExpertFFN
+from oracle import expert_ffn as ef
+from oracle import router as ro
+from oracle import routing as rt
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+
+
+def f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("T,H,E", [(300, 256, 8), (70, 128, 64), (1000, 384, 256), (16384, 4096, 8)])
+def test_router_logits(T, H, E):
+    wl = configs.small(T, H, 128, E, 2, backward=False)
+    x = synth.make_inputs(wl, 0, device="cuda")["x"]
+    w_r = synth.make_router_weight(wl, 0, device="cuda")
+    L = ExpertFFN(T, H, 128, E, 2, training=False)
+    logits = L.router_forward(x, w_r)
+    torch.cuda.synchronize()
+    assert_close(logits.cpu().numpy(), ro.router_logits(f64(x), f64(w_r)), "logits")
+
+
+@pytest.mark.parametrize("renorm", [1, 0])
+@pytest.mark.parametrize("T,H,I,E,k", [(256, 128, 256, 4, 2), (600, 256, 384, 16, 4)])
+def test_trainable_layer_with_router(T, H, I, E, k, renorm):
+    wl = configs.small(T, H, I, E, k, routing="normal", backward=True)
+    inp = {kk: v.cuda() for kk, v in synth.make_inputs(wl, 0).items()}
+    w_r = synth.make_router_weight(wl, 0, device="cuda")
+    L = ExpertFFN(T, H, I, E, k, training=True, renormalize=bool(renorm))
+    L.quantize_weights(inp["w_gu"], inp["w_d"])
+    logits = L.router_forward(inp["x"], w_r)
+    L.forward(logits, inp["x"])
+    L.backward(inp["dout"])
+    L.router_backward(inp["x"], w_r)
+    torch.cuda.synchronize()
+    assert L.device_error() == (0, 0)
+
+    lg = logits.cpu().numpy()
+    idx, prob = rt.route_topk(lg, k, renormalize=bool(renorm))
+    assert np.array_equal(L.idx.cpu().numpy(), idx)
+    x, w_gu, w_d, dout = f64(inp["x"]), f64(inp["w_gu"]), f64(inp["w_d"]), f64(inp["dout"])
+    fwd = ef.forward(x, idx, prob.astype(np.float64), w_gu, w_d)
+    bwd = ef.backward(fwd, dout)
+    dl = ro.router_backward(lg, idx, prob, bwd["dprob"], bool(renorm))
+    dx_r, dw_r = ro.router_input_grads(dl, x, f64(w_r))
+    assert_close(L.dlogits.cpu().numpy(), dl, "dlogits")
+    assert_close(L.dw_r.cpu().numpy(), dw_r, "dW_r")
+    assert_close(f64(L.dx), ro.add_to_bf16(bwd["dx"], dx_r), "dx (experts + router)")
