@@ -277,6 +277,29 @@ def run_cuda(args):
                   "bwd_gbs": round((3 * xb + 2 * wl.T * wl.E * 4) / bwd_ms / 1e6, 1),
                   "bytes": "fwd: x + W_r + logits; bwd: x (dW_r) + dx read and written + dlogits"}
 
+    # ---- the same forward with bf16 operands (no quantization), for comparison ----
+    L.forward_bf16(inp["x"], inp["w_gu"], inp["w_d"])
+    torch.cuda.synchronize()
+    from moe_expert_ffn_03_gb300 import binding as Bn
+    b0, b1, b2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    n_b = 5
+    gat = gem = 0.0
+    for _ in range(n_b):
+        b0.record(stream)
+        Bn.moe_gather_rows(L.d, inp["x"], L.row_of, L.split_sizes, L.x_perm, L.ws)
+        b1.record(stream)
+        Bn.grouped_mlp_fwd_bf16(L.d, L.x_perm, L.split_sizes, L.prob_perm, inp["w_gu"], inp["w_d"], L.a_perm,
+                                L.y_b16, L.ws)
+        b2.record(stream)
+        torch.cuda.synchronize()
+        gat += b0.elapsed_time(b1)
+        gem += b1.elapsed_time(b2)
+    fwd_flops = 6.0 * wl.R * wl.H * wl.I
+    bf16_fwd = {"gather_ms": round(gat / n_b, 4), "grouped_mlp_fwd_bf16_ms": round(gem / n_b, 4),
+                "gemm_tflops": round(fwd_flops / (gem / n_b * 1e-3) / 1e12, 1),
+                "frac_of_bf16_peak": round(fwd_flops / (gem / n_b * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"], 4),
+                "mxfp8_grouped_mlp_fwd_ms": round(parts["grouped_mlp_fwd_ms"], 4)}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_tokens, wl)
@@ -308,6 +331,7 @@ def run_cuda(args):
         "gpu_launches": (LAUNCHES_PER_TRAINING_STEP if train else LAUNCHES_PER_FORWARD_STEP) * args.steps,
         "clocks": clocks,
     }
+    line["bf16_forward"] = bf16_fwd
     if router is not None:
         line["router"] = router
     if cpu is not None:

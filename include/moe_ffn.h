@@ -196,6 +196,31 @@ moe_status grouped_mlp_fwd(const moe_dims* d, const uint8_t* xq, const uint8_t* 
                            void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * moe_gather_rows -- bf16 path: x_perm[row_of[t][j]] = x[t] for every (token,
+ * slot); padding rows of each expert segment are zeroed.  x bf16 [T][H],
+ * row_of and split_sizes from moe_route_permute, x_perm out bf16 [CAP][H].
+ * workspace: as for grouped_mlp_fwd (its error word records bad rows).
+ */
+moe_status moe_gather_rows(const moe_dims* d, const void* x, const int32_t* row_of, const int32_t* split_sizes,
+                           void* x_perm, void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * grouped_mlp_fwd_bf16 -- the same grouped gate_up GEMM + ScaledSwiGLU + grouped
+ * down GEMM with bf16 operands and no quantization (page "Efficient MoE
+ * Training for Biological Foundation Models", section "运行要求、基准与验证步骤":
+ * the recipe runs in BF16 or in MXFP8).  tcgen05 kind::f16 MMA, f32 accumulate.
+ *   x_perm   bf16 [CAP][H] (moe_gather_rows); split_sizes, prob_perm as for
+ *            grouped_mlp_fwd; w_gu bf16 [E][2I][H], w_d bf16 [E][H][I] (the master
+ *            weights as they are);
+ *   a_perm   out bf16 [CAP][I]: a = silu(g)*u*p rounded to bf16 (the down
+ *            GEMM's input);
+ *   y        out bf16 [CAP][H].
+ */
+moe_status grouped_mlp_fwd_bf16(const moe_dims* d, const void* x_perm, const int32_t* split_sizes,
+                                const float* prob_perm, const void* w_gu, const void* w_d, void* a_perm, void* y,
+                                void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
  * grouped_mlp_bwd -- backward of grouped_mlp_fwd with straight-through
  * quantizers (page "Efficient MoE Training for Biological Foundation
  * Models", section "MXFP8与融合MLP": the fused op has a matching backward).

@@ -18,7 +18,7 @@ EXPORTS = (
     "moe_status_string", "moe_last_error_message", "moe_rows_capacity", "moe_workspace_size",
     "mxfp8_quantize", "mxfp8_quantize_dual", "moe_route_permute", "grouped_mlp_fwd", "grouped_mlp_bwd",
     "moe_unpermute_combine", "moe_get_device_error", "moe_clear_device_error", "moe_route_permute_noalloc",
-    "moe_selftest_wait_timeout", "moe_router_fwd", "moe_router_bwd",
+    "moe_selftest_wait_timeout", "moe_router_fwd", "moe_router_bwd", "moe_gather_rows", "grouped_mlp_fwd_bf16",
 )
 
 MOE_OK = 0
@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
             "moe_clear_device_error": ([P, P], c_int32),
             "moe_route_permute_noalloc": ([D, P, P, P, P, P, P, P, P, P, P, P, P, P], c_int32),
             "moe_router_fwd": ([D, P, P, P, P], c_int32),
+            "moe_gather_rows": ([D, P, P, P, P, P, c_size_t, P], c_int32),
+            "grouped_mlp_fwd_bf16": ([D, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
             "moe_router_bwd": ([D, P, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
             "moe_selftest_wait_timeout": ([P, c_size_t, ctypes.c_int64, ctypes.POINTER(c_int32),
                                            ctypes.POINTER(c_int32), P], c_int32),
@@ -159,6 +161,17 @@ def moe_get_device_error(workspace, stream=None):
     code, site = c_int32(0), c_int32(0)
     _check(lib().moe_get_device_error(_p(workspace), ctypes.byref(code), ctypes.byref(site), _st(stream)))
     return int(code.value), int(site.value)
+
+
+def moe_gather_rows(d, x, row_of, split_sizes, x_perm, workspace, stream=None):
+    _check(lib().moe_gather_rows(ctypes.byref(d), _p(x), _p(row_of), _p(split_sizes), _p(x_perm), _p(workspace),
+                                 workspace.numel() * workspace.element_size(), _st(stream)))
+
+
+def grouped_mlp_fwd_bf16(d, x_perm, split_sizes, prob_perm, w_gu, w_d, a_perm, y, workspace, stream=None):
+    _check(lib().grouped_mlp_fwd_bf16(ctypes.byref(d), _p(x_perm), _p(split_sizes), _p(prob_perm), _p(w_gu),
+                                      _p(w_d), _p(a_perm), _p(y), _p(workspace),
+                                      workspace.numel() * workspace.element_size(), _st(stream)))
 
 
 def moe_router_fwd(d, x, w_r, logits, stream=None):

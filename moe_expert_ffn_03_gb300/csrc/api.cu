@@ -303,6 +303,79 @@ moe_status grouped_mlp_fwd(const moe_dims* d, const uint8_t* xq, const uint8_t* 
   return MOE_OK;
 }
 
+moe_status moe_gather_rows(const moe_dims* d, const void* x, const int32_t* row_of, const int32_t* split_sizes,
+                           void* x_perm, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(row_of);
+  REQUIRE_PTR(split_sizes);
+  REQUIRE_PTR(x_perm);
+  s = check_ws(d, workspace, workspace_bytes, false);
+  if (s != MOE_OK) return s;
+  const WsLayout w = ws_layout(d, false);
+  CUDA_TRY(launch_gather_rows(x, row_of, split_sizes, d->T, d->k, d->H, d->E, capacity(d), x_perm,
+                              at<int>(workspace, w.err), static_cast<cudaStream_t>(stream)),
+           "gather rows");
+  return MOE_OK;
+}
+
+moe_status grouped_mlp_fwd_bf16(const moe_dims* d, const void* x_perm, const int32_t* split_sizes,
+                                const float* prob_perm, const void* w_gu, const void* w_d, void* a_perm, void* y,
+                                void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  REQUIRE_PTR(x_perm);
+  REQUIRE_PTR(split_sizes);
+  REQUIRE_PTR(prob_perm);
+  REQUIRE_PTR(w_gu);
+  REQUIRE_PTR(w_d);
+  REQUIRE_PTR(a_perm);
+  REQUIRE_PTR(y);
+  s = check_ws(d, workspace, workspace_bytes, false);
+  if (s != MOE_OK) return s;
+  const WsLayout w = ws_layout(d, false);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t cap = capacity(d);
+  const int H = d->H, I = d->I, E = d->E;
+  GemmArgs g1{};
+  g1.mode = 0;
+  g1.E = E;
+  g1.split_sizes = split_sizes;
+  g1.K = H;
+  g1.N = I;
+  g1.n_tiles = I / 128;
+  g1.b_rows_per_expert = 2 * int64_t(I);
+  g1.cap = cap;
+  g1.prob_perm = prob_perm;
+  g1.out = static_cast<__nv_bfloat16*>(a_perm);
+  g1.ldo = I;
+  g1.I = I;
+  g1.err = at<int>(workspace, w.err);
+  CUDA_TRY(launch_grouped_gemm(EPI_B16_FWD_SWIGLU, g1, x_perm, cap, H, w_gu, int64_t(E) * 2 * I, H,
+                               (cap / 128) * g1.n_tiles, st, g_msg, sizeof(g_msg)),
+           "bf16 grouped gate_up GEMM");
+  GemmArgs g2{};
+  g2.mode = 0;
+  g2.E = E;
+  g2.split_sizes = split_sizes;
+  g2.K = I;
+  g2.N = H;
+  g2.n_tiles = (H + 255) / 256;
+  g2.b_rows_per_expert = H;
+  g2.cap = cap;
+  g2.out = static_cast<__nv_bfloat16*>(y);
+  g2.ldo = H;
+  g2.I = I;
+  g2.err = g1.err;
+  CUDA_TRY(launch_grouped_gemm(EPI_B16_OUT, g2, a_perm, cap, I, w_d, int64_t(E) * H, I, (cap / 128) * g2.n_tiles,
+                               st, g_msg, sizeof(g_msg)),
+           "bf16 grouped down GEMM");
+  return MOE_OK;
+}
+
 moe_status grouped_mlp_bwd(const moe_dims* d, const void* dout, const int32_t* split_sizes, const int32_t* row_of,
                            const int32_t* src_of, const float* prob_perm, const void* saved_gu, const uint8_t* aq_col,
                            const uint8_t* aq_col_scale, const uint8_t* xq_col, const uint8_t* xq_col_scale,

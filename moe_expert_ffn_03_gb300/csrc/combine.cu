@@ -69,6 +69,54 @@ __global__ void __launch_bounds__(256) dprob_reduce_kernel(
   dprob[i] = acc;
 }
 
+// bf16 path: x_perm[row_of[t][j]] = x[t] (one warp per token, 16-byte copies).
+__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
+                                                          const int* __restrict__ row_of, int T, int k, int H,
+                                                          int64_t cap, __nv_bfloat16* __restrict__ x_perm, int* err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
+  for (int j = 0; j < k; ++j) {
+    const int r = row_of[t * k + j];
+    if (r < 0 || r >= cap) {
+      report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_COMBINE + 3);
+      continue;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + int64_t(r) * H);
+    for (int c = lane; c < H / 8; c += 32) dst[c] = src[c];
+  }
+}
+
+// Zero the padding rows (split_sizes[e] .. roundup(split_sizes[e],128)-1 of segment e)
+// of a permuted buffer whose rows are row_bytes long (a multiple of 16).
+__global__ void __launch_bounds__(256) zero_pad_rows_kernel(const int* __restrict__ split_sizes, int E,
+                                                            int64_t row_bytes, uint8_t* __restrict__ buf) {
+  __shared__ int seg_start;
+  const int e = blockIdx.x;
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int i = 0; i < e; ++i) acc += (split_sizes[i] + 127) & ~127;
+    seg_start = acc;
+  }
+  __syncthreads();
+  const int m = split_sizes[e];
+  const int64_t n16 = (((m + 127) & ~127) - m) * (row_bytes / 16);
+  uint4* p = reinterpret_cast<uint4*>(buf + (int64_t(seg_start) + m) * row_bytes);
+  for (int64_t i = int64_t(blockIdx.y) * blockDim.x + threadIdx.x; i < n16; i += int64_t(gridDim.y) * blockDim.x)
+    p[i] = make_uint4(0, 0, 0, 0);
+}
+
+cudaError_t launch_gather_rows(const void* x, const int* row_of, const int* split_sizes, int T, int k, int H, int E,
+                               int64_t cap, void* x_perm, int* err, cudaStream_t st) {
+  gather_rows_kernel<<<unsigned((int64_t(T) * 32 + 255) / 256), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(x), row_of, T, k, H, cap, static_cast<__nv_bfloat16*>(x_perm), err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  zero_pad_rows_kernel<<<dim3(E, 8), 256, 0, st>>>(split_sizes, E, int64_t(H) * 2, static_cast<uint8_t*>(x_perm));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const void* y, const int* row_of, const float* prob, int T, int k, int H, int64_t cap,
                            void* out, int* err, cudaStream_t st) {
   const int64_t threads = int64_t(T) * 32;

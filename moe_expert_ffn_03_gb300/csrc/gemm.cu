@@ -57,6 +57,13 @@ constexpr int GROUP_M = 8;
 constexpr int TR_PITCH = 9;                     // floats per row of a warp's 32x8 transpose buffer
 constexpr int TR_WARP_FLOATS = 32 * TR_PITCH;
 
+// bf16-operand kinds: 64 K elements per 128-byte stage row, kind::f16 MMA, no scales.
+template <int EPI>
+struct Ops {
+  static constexpr bool B16 = (EPI == EPI_B16_OUT || EPI == EPI_B16_FWD_SWIGLU);
+  static constexpr int KSTEP = B16 ? 64 : 128;    // K elements per stage
+};
+
 // Shared-memory layout per epilogue kind (all use 256-column tiles today; a
 // 128-column tile would take one B box per stage and 6 stages).
 template <int EPI>
@@ -221,6 +228,23 @@ __device__ __forceinline__ uint32_t idesc_mxf8(int N, int sf_id) {
          | (uint32_t(sf_id) << 29);        // A scale factor id
 }
 
+// Instruction descriptor of kind::f16: bf16 x bf16 -> f32, both K-major.
+__device__ __forceinline__ uint32_t idesc_bf16(int N) {
+  return (1u << 4)                         // D format F32
+         | (1u << 7) | (1u << 10)          // A, B format BF16
+         | (uint32_t(N >> 3) << 17)        // N / 8
+         | (uint32_t(BM >> 4) << 24);      // M / 16
+}
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 struct Tile {
   int e;
   int nb;
@@ -258,9 +282,9 @@ __device__ __forceinline__ void decode_tile(const GemmArgs& a, const int* seg_mb
     tl.nb = nb;
     tl.a_row = int64_t(mb) * BM;
     tl.k0 = 0;
-    tl.k_tiles = a.K / BK;
+    tl.k_tiles = a.K / Ops<EPI>::KSTEP;
     tl.out_row = tl.a_row;
-    if (EPI == EPI_FWD_SWIGLU) {
+    if (EPI == EPI_FWD_SWIGLU || EPI == EPI_B16_FWD_SWIGLU) {
       tl.n0 = nb * 128;
       tl.b_row0 = int64_t(lo) * a.b_rows_per_expert + tl.n0;
       tl.b_row1 = tl.b_row0 + a.I;
@@ -281,8 +305,8 @@ __device__ __forceinline__ void decode_tile(const GemmArgs& a, const int* seg_mb
     tl.e = e;
     tl.nb = nb;
     tl.a_row = int64_t(mb) * BM;
-    tl.k0 = int64_t(seg_mb[e]) * BK;
-    tl.k_tiles = seg_mb[e + 1] - seg_mb[e];
+    tl.k0 = int64_t(seg_mb[e]) * 128;
+    tl.k_tiles = (seg_mb[e + 1] - seg_mb[e]) * (128 / Ops<EPI>::KSTEP);
     tl.n0 = nb * BN;
     tl.b_row0 = tl.n0;
     tl.b_row1 = tl.n0 + 128;
@@ -411,7 +435,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
   const int c0 = cg * 64;
   uint32_t r[64];
   bool have;
-  if (EPI == EPI_FWD_SWIGLU) {
+  if (EPI == EPI_FWD_SWIGLU || EPI == EPI_B16_FWD_SWIGLU) {
     have = true;
     tmem_ld32_async(tmem_row + TM_ACC + cg * 32, r);
     tmem_ld32_async(tmem_row + TM_ACC + 128 + cg * 32, r + 32);
@@ -440,7 +464,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
   __syncwarp();
   if (lane == 0) mbar_arrive(tmem_empty);
 
-  if (EPI == EPI_BF16) {
+  if (EPI == EPI_BF16 || EPI == EPI_B16_OUT) {
     if (c0 >= ncols) return;
     __nv_bfloat16* orow = a.out + row * a.ldo + tl.n0 + c0;
 #pragma unroll
@@ -450,6 +474,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
       for (int i = 0; i < 32; ++i) v[i] = have ? __uint_as_float(r[32 * h + i]) : 0.f;
       store_bf16x32(orow + 32 * h, v);
     }
+  } else if (EPI == EPI_B16_FWD_SWIGLU) {
+    // bf16 path: a = silu(g)*u*p stored as bf16 [cap][I] in out
+    const float p = a.prob_perm[row];
+    const int64_t col = tl.n0 + cg * 32;
+    float* f = reinterpret_cast<float*>(r);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = silu_f(f[i]) * f[32 + i] * p;
+    store_bf16x32(a.out + row * a.ldo + col, f);
   } else if (EPI == EPI_FWD_SWIGLU) {
     const float p = a.prob_perm[row];
     const int64_t twoI = 2 * int64_t(a.I);
@@ -576,7 +608,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (blockIdx.x < total) tile_src<EPI>(args, seg_mb, blockIdx.x, cur);
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         if (t + int(gridDim.x) < total) tile_src<EPI>(args, seg_mb, t + gridDim.x, nxt);
-        const uint32_t bytes = A_TILE + SF_ATOM * 2 + (cur.second ? (B_HALF * 2 + SF_ATOM) : B_HALF);
+        const uint32_t bytes = Ops<EPI>::B16 ? A_TILE + (cur.second ? B_HALF * 2 : B_HALF)
+                                             : A_TILE + SF_ATOM * 2 + (cur.second ? (B_HALF * 2 + SF_ATOM) : B_HALF);
         for (int kt = 0; kt < cur.k_tiles; ++kt, ++it) {
           const int s = it % L::STG;
           const int round = it / L::STG;
@@ -586,13 +619,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           mbar_arrive_expect_tx(&full[s], bytes);
           last_round[s] = round;
-          const int kc = cur.k0 + kt * BK;
+          const int kc = cur.k0 + kt * Ops<EPI>::KSTEP;
           tma_load_2d(smem + L::OFF_A + s * A_TILE, &tmA, kc, cur.a_row, &full[s]);
           tma_load_2d(smem + L::OFF_B + s * L::B_T, &tmB, kc, cur.b_row0, &full[s]);
           if (cur.second) tma_load_2d(smem + L::OFF_B + s * L::B_T + B_HALF, &tmB, kc, cur.b_row1, &full[s]);
-          bulk_load(smem + L::OFF_SFA + s * SF_ATOM, cur.sfa + kt * SF_ATOM, SF_ATOM, &full[s]);
-          bulk_load(smem + L::OFF_SFB + s * L::SFB_T, cur.sfb0 + kt * SF_ATOM, SF_ATOM, &full[s]);
-          if (cur.second) bulk_load(smem + L::OFF_SFB + s * L::SFB_T + SF_ATOM, cur.sfb1 + kt * SF_ATOM, SF_ATOM, &full[s]);
+          if (!Ops<EPI>::B16) {
+            bulk_load(smem + L::OFF_SFA + s * SF_ATOM, cur.sfa + kt * SF_ATOM, SF_ATOM, &full[s]);
+            bulk_load(smem + L::OFF_SFB + s * L::SFB_T, cur.sfb0 + kt * SF_ATOM, SF_ATOM, &full[s]);
+            if (cur.second) bulk_load(smem + L::OFF_SFB + s * L::SFB_T + SF_ATOM, cur.sfb1 + kt * SF_ATOM, SF_ATOM, &full[s]);
+          }
         }
         cur = nxt;
       }
@@ -636,6 +671,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk) {
             // +32 bytes along K inside the 128-byte swizzle atom = +2 in the encoded start address
+            if (Ops<EPI>::B16) {
+              tc_mma_bf16(tmem + TM_ACC, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_bf16(n),
+                          (kt | kk) != 0);
+              continue;
+            }
             tc_mma_mxf8(tmem + TM_ACC, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_mxf8(n, kk),
                         tm_sfa, tm_sfb, (kt | kk) != 0);
           }
@@ -672,9 +712,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t tm_sfa = tmem + TM_SF0 + uint32_t(s) * TM_SF_STRIDE;
           const uint32_t tm_sfb = tm_sfa + 4;
-          tc_cp_sf(tm_sfa, desc_sf(smem_u32(smem + L::OFF_SFA + s * SF_ATOM)));
-          tc_cp_sf(tm_sfb, desc_sf(smem_u32(smem + L::OFF_SFB + s * L::SFB_T)));
-          if (tl.second) tc_cp_sf(tm_sfb + 4, desc_sf(smem_u32(smem + L::OFF_SFB + s * L::SFB_T + SF_ATOM)));
+          if (!Ops<EPI>::B16) {
+            tc_cp_sf(tm_sfa, desc_sf(smem_u32(smem + L::OFF_SFA + s * SF_ATOM)));
+            tc_cp_sf(tm_sfb, desc_sf(smem_u32(smem + L::OFF_SFB + s * L::SFB_T)));
+            if (tl.second) tc_cp_sf(tm_sfb + 4, desc_sf(smem_u32(smem + L::OFF_SFB + s * L::SFB_T + SF_ATOM)));
+          }
           tc_commit(&sf_ready[s]);
           issued = true;
         }
@@ -732,14 +774,16 @@ EncodeTiledFn get_encode_fn() {
 }
 
 // 2-D map over a row-major uint8 [rows][K] tensor, 128x128 boxes, 128-byte swizzle.
-bool encode_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K) {
+bool encode_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, bool b16) {
   EncodeTiledFn fn = get_encode_fn();
   if (fn == nullptr) return false;
+  const int64_t esize = b16 ? 2 : 1;
   cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
-  cuuint64_t strides[1] = {cuuint64_t(K)};
-  cuuint32_t box[2] = {BK, 128};
+  cuuint64_t strides[1] = {cuuint64_t(K * esize)};
+  cuuint32_t box[2] = {cuuint32_t(BK / esize), 128};     // 128 bytes of K per row
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+  return fn(m, b16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base),
+            dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -764,7 +808,8 @@ cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64
                                 char* msg, size_t msg_len) {
   if (max_tiles <= 0) return cudaSuccess;
   CUtensorMap ma, mb;
-  if (!encode_map(&ma, A, a_rows, a_K) || !encode_map(&mb, B, b_rows, b_K)) {
+  const bool b16 = (epi == EPI_B16_OUT || epi == EPI_B16_FWD_SWIGLU);
+  if (!encode_map(&ma, A, a_rows, a_K, b16) || !encode_map(&mb, B, b_rows, b_K, b16)) {
     snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed (A %lld x %lld, B %lld x %lld)", (long long)a_rows,
              (long long)a_K, (long long)b_rows, (long long)b_K);
     return cudaErrorInvalidValue;
@@ -777,6 +822,8 @@ cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64
     case EPI_BF16: return launch_epi<EPI_BF16>(ma, mb, a, grid, st);
     case EPI_FWD_SWIGLU: return launch_epi<EPI_FWD_SWIGLU>(ma, mb, a, grid, st);
     case EPI_BWD_SWIGLU: return launch_epi<EPI_BWD_SWIGLU>(ma, mb, a, grid, st);
+    case EPI_B16_OUT: return launch_epi<EPI_B16_OUT>(ma, mb, a, grid, st);
+    case EPI_B16_FWD_SWIGLU: return launch_epi<EPI_B16_FWD_SWIGLU>(ma, mb, a, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -27,6 +27,8 @@ cudaError_t launch_router_bwd(const void* x, const void* w, const float* logits,
 cudaError_t launch_route_permute(const float* logits, int T, int E, int k, int renorm, int* idx, float* prob,
                                  uint32_t* masks, int* bases, int* split_sizes, int* row_of, int* src_of,
                                  float* prob_perm, int* err, cudaStream_t st);
+cudaError_t launch_gather_rows(const void* x, const int* row_of, const int* split_sizes, int T, int k, int H, int E,
+                               int64_t cap, void* x_perm, int* err, cudaStream_t st);
 cudaError_t launch_combine(const void* y, const int* row_of, const float* prob, int T, int k, int H, int64_t cap,
                            void* out, int* err, cudaStream_t st);
 cudaError_t launch_dprob_reduce(const float* dp_part, int n_tiles, int64_t cap, const int* row_of, int64_t R,
@@ -39,7 +41,10 @@ cudaError_t launch_dprob_reduce(const float* dp_part, int n_tiles, int64_t cap, 
 //     weight rows.  K fixed.
 //   mode 1 (grouped K, weight gradients): for each expert e an independent
 //     [M][N] output with K = the expert's padded token range of A and B.
-enum Epilogue : int { EPI_BF16 = 0, EPI_FWD_SWIGLU = 1, EPI_BWD_SWIGLU = 2 };
+// EPI_BF16 .. EPI_BWD_SWIGLU take MXFP8 operands (block-scaled MMA); the B16 kinds take
+// bf16 operands (kind::f16 MMA, no scales): plain bf16 output, or ScaledSwiGLU with a
+// bf16 `a` written to out [cap][I].
+enum Epilogue : int { EPI_BF16 = 0, EPI_FWD_SWIGLU = 1, EPI_BWD_SWIGLU = 2, EPI_B16_OUT = 3, EPI_B16_FWD_SWIGLU = 4 };
 
 struct GemmArgs {
   int mode;

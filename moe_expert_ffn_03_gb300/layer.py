@@ -111,6 +111,21 @@ class ExpertFFN:
         self.combine_dx(stream)
         return self.dx
 
+    # ---- bf16 forward (no quantization), on the routing of route() ----------------------
+    def forward_bf16(self, x, w_gu, w_d, stream=None):
+        """After route(): gather x rows, bf16 grouped gate_up + ScaledSwiGLU + down, combine."""
+        if not hasattr(self, "x_perm"):
+            dev = self.ws.device
+            self.x_perm = torch.empty(self.cap, self.H, dtype=torch.bfloat16, device=dev)
+            self.a_perm = torch.empty(self.cap, self.I, dtype=torch.bfloat16, device=dev)
+            self.y_b16 = torch.empty(self.cap, self.H, dtype=torch.bfloat16, device=dev)
+            self.out_b16 = torch.empty(self.T, self.H, dtype=torch.bfloat16, device=dev)
+        B.moe_gather_rows(self.d, x, self.row_of, self.split_sizes, self.x_perm, self.ws, stream)
+        B.grouped_mlp_fwd_bf16(self.d, self.x_perm, self.split_sizes, self.prob_perm, w_gu, w_d, self.a_perm,
+                               self.y_b16, self.ws, stream)
+        B.moe_unpermute_combine(self.d, self.y_b16, self.row_of, None, self.out_b16, stream)
+        return self.out_b16
+
     # ---- router (optional: when the logits come from x) ------------------------------
     def router_forward(self, x, w_r, stream=None):
         """logits = x W_r^T into self.logits (allocated on first use)."""

@@ -41,13 +41,17 @@ from .routing import permute
 class Numerics:
     """quantized: MXFP8 quantizers on (False = identity quantizers).
     rounded: float32 quantizer inputs, bf16 saved g/u and bf16 outputs
-    (False = pure float64, used by the finite-difference checks)."""
+    (False = pure float64, used by the finite-difference checks).
+    act_bf16: with quantizers off, the activations between the GEMMs are
+    rounded to bf16 instead (the BF16 path of the recipe)."""
     quantized: bool = True
     rounded: bool = True
+    act_bf16: bool = False
 
 
 MXFP8 = Numerics(True, True)
 UNQUANTIZED_BF16 = Numerics(False, True)
+BF16_PATH = Numerics(False, True, True)
 EXACT = Numerics(False, False)
 
 
@@ -70,7 +74,7 @@ def _bf16(v, nm: Numerics):
 def q_rowwise(v, nm: Numerics):
     """Quantize-dequantize along the last axis (identity when quantizers are off)."""
     if not nm.quantized:
-        return np.asarray(v, dtype=np.float64)
+        return mx.bf16(v) if nm.act_bf16 else np.asarray(v, dtype=np.float64)
     c, s = mx.quantize_blocks(v, axis=-1)
     return mx.dequantize_blocks(c, s, axis=-1)
 
