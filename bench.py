@@ -300,6 +300,32 @@ def run_cuda(args):
                 "frac_of_bf16_peak": round(fwd_flops / (gem / n_b * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"], 4),
                 "mxfp8_grouped_mlp_fwd_ms": round(parts["grouped_mlp_fwd_ms"], 4)}
 
+    # ---- the same forward with per-tensor FP8 operands (one dynamic scale per expert tensor) ----
+    L.quantize_weights_fp8_tensor(inp["w_gu"], inp["w_d"])
+    L.forward_fp8_tensor(inp["x"])
+    torch.cuda.synchronize()
+    t0_, t1_, t2_, t3_ = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+    wq_t = qx_t = gm_t = 0.0
+    for _ in range(n_b):
+        t0_.record(stream)
+        L.quantize_weights_fp8_tensor(inp["w_gu"], inp["w_d"])
+        t1_.record(stream)
+        Bn.moe_fp8_tensor_quantize_tokens(L.d, inp["x"], L.idx, L.row_of, L.split_sizes, L.t8_xq, L.t8_amax_x, L.ws)
+        t2_.record(stream)
+        Bn.grouped_mlp_fwd_fp8_tensor(L.d, L.t8_xq, L.t8_amax_x, L.split_sizes, L.prob_perm, L.t8_wgu,
+                                      L.t8_amax_gu, L.t8_wd, L.t8_amax_d, L.t8_a, L.t8_aq, L.t8_amax_a, L.t8_y, L.ws)
+        t3_.record(stream)
+        torch.cuda.synchronize()
+        wq_t += t0_.elapsed_time(t1_)
+        qx_t += t1_.elapsed_time(t2_)
+        gm_t += t2_.elapsed_time(t3_)
+    t8_fwd = {"weight_quant_ms": round(wq_t / n_b, 4), "x_quant_ms": round(qx_t / n_b, 4),
+              "grouped_mlp_fwd_fp8_tensor_ms": round(gm_t / n_b, 4),
+              "tflops": round(fwd_flops / (gm_t / n_b * 1e-3) / 1e12, 1),
+              "frac_of_fp8_peak": round(fwd_flops / (gm_t / n_b * 1e-3) / 1e12 / fp8_peak, 4),
+              "timed": "gate_up GEMM (bf16 a + amax) + per-tensor quantize of a + down GEMM",
+              "mxfp8_grouped_mlp_fwd_ms": round(parts["grouped_mlp_fwd_ms"], 4)}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_tokens, wl)
@@ -332,6 +358,7 @@ def run_cuda(args):
         "clocks": clocks,
     }
     line["bf16_forward"] = bf16_fwd
+    line["fp8_tensor_forward"] = t8_fwd
     if router is not None:
         line["router"] = router
     if cpu is not None:
@@ -420,7 +447,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=256)
+    ap.add_argument("--cpu-tokens", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "cuda":

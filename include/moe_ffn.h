@@ -221,6 +221,67 @@ moe_status grouped_mlp_fwd_bf16(const moe_dims* d, const void* x_perm, const int
                                 void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * Per-tensor FP8 with dynamic scaling (page "英伟达开源MoE加速神器", section
+ * "3. Transformer Engine：FP8 训练加速": the Hopper recipe scales every tensor by
+ * its current range; page "Efficient MoE Training for Biological Foundation
+ * Models", section "MoE训练的瓶颈与TE的对应能力": FP8 keeps one scale per tensor
+ * where MXFP8 keeps one per 32 values).  The tensors are the operands of each
+ * expert's GEMMs: expert e's token rows of x, its W_gu[e] and W_d[e], and its
+ * rows of the activation a.  For such a tensor with amax = max |v|:
+ *   s = 448 / amax rounded to float32 (s = 1 for an all-zero tensor),
+ *   code = E4M3 of the float32 product v * s, nearest-even, saturating to
+ *   +-448 (sign of zero kept); value = code / s.
+ * The amax arrays are float32 [E] on the device, non-negative; the calls that
+ * fill them first set them to zero.  Tensors holding NaN or Inf are outside
+ * this path.
+ */
+
+/*
+ * fp8_tensor_quantize -- per-slice amax and E4M3 codes of src bf16
+ * [batch][rows][cols] (cols a multiple of 8): amax out float32 [batch],
+ * codes out uint8 [batch][rows][cols] (the same layout).  For the weights:
+ * W_gu as batch E, rows 2I, cols H; W_d as batch E, rows H, cols I.  Device
+ * pointers 16-byte aligned.
+ */
+moe_status fp8_tensor_quantize(const void* src, int batch, int rows, int cols, uint8_t* codes, float* amax,
+                               moe_stream_t stream);
+
+/*
+ * moe_fp8_tensor_quantize_tokens -- the x operand of the per-tensor path:
+ * amax_x[e] = max |x[t][h]| over the tokens t routed to e, then for every
+ * (token, slot j) with expert e = idx[t][j] the codes of x[t] * s_x[e] in
+ * permuted row row_of[t][j] of xq (uint8 [CAP][H]); padding rows of every
+ * segment get zero codes.  idx, row_of, split_sizes from moe_route_permute;
+ * amax_x out float32 [E]; workspace as for grouped_mlp_fwd (its error word
+ * records out-of-range experts or rows).
+ */
+moe_status moe_fp8_tensor_quantize_tokens(const moe_dims* d, const void* x, const int32_t* idx,
+                                          const int32_t* row_of, const int32_t* split_sizes, uint8_t* xq,
+                                          float* amax_x, void* workspace, size_t workspace_bytes,
+                                          moe_stream_t stream);
+
+/*
+ * grouped_mlp_fwd_fp8_tensor -- the grouped gate_up GEMM + ScaledSwiGLU +
+ * grouped down GEMM on per-tensor FP8 operands: tcgen05 kind::f8f6f4 MMA
+ * (E4M3 x E4M3, no block scales), f32 accumulate, the accumulator multiplied
+ * by 1/(s_a[e] * s_b[e]) in the epilogue.
+ *   xq, amax_x      from moe_fp8_tensor_quantize_tokens
+ *   split_sizes, prob_perm from moe_route_permute
+ *   wgu_q, amax_gu  fp8_tensor_quantize of W_gu; wd_q, amax_d of W_d
+ *   a_perm          out bf16 [CAP][I]: a = silu(g)*u*p rounded to bf16 (the
+ *                   activation is stored because its scale needs the
+ *                   tensor's amax before any element is quantized)
+ *   aq              out uint8 [CAP][I]: codes of a with s_a[e]
+ *   amax_a          out float32 [E]: amax of every expert's rows of a_perm
+ *   y               out bf16 [CAP][H]; combine with moe_unpermute_combine.
+ */
+moe_status grouped_mlp_fwd_fp8_tensor(const moe_dims* d, const uint8_t* xq, const float* amax_x,
+                                      const int32_t* split_sizes, const float* prob_perm, const uint8_t* wgu_q,
+                                      const float* amax_gu, const uint8_t* wd_q, const float* amax_d, void* a_perm,
+                                      uint8_t* aq, float* amax_a, void* y, void* workspace, size_t workspace_bytes,
+                                      moe_stream_t stream);
+
+/*
  * grouped_mlp_bwd -- backward of grouped_mlp_fwd with straight-through
  * quantizers (page "Efficient MoE Training for Biological Foundation
  * Models", section "MXFP8与融合MLP": the fused op has a matching backward).

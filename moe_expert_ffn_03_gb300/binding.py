@@ -19,6 +19,7 @@ EXPORTS = (
     "mxfp8_quantize", "mxfp8_quantize_dual", "moe_route_permute", "grouped_mlp_fwd", "grouped_mlp_bwd",
     "moe_unpermute_combine", "moe_get_device_error", "moe_clear_device_error", "moe_route_permute_noalloc",
     "moe_selftest_wait_timeout", "moe_router_fwd", "moe_router_bwd", "moe_gather_rows", "grouped_mlp_fwd_bf16",
+    "fp8_tensor_quantize", "moe_fp8_tensor_quantize_tokens", "grouped_mlp_fwd_fp8_tensor",
 )
 
 MOE_OK = 0
@@ -76,6 +77,9 @@ def lib() -> ctypes.CDLL:
             "moe_gather_rows": ([D, P, P, P, P, P, c_size_t, P], c_int32),
             "grouped_mlp_fwd_bf16": ([D, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
             "moe_router_bwd": ([D, P, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
+            "fp8_tensor_quantize": ([P, c_int32, c_int32, c_int32, P, P, P], c_int32),
+            "moe_fp8_tensor_quantize_tokens": ([D, P, P, P, P, P, P, P, c_size_t, P], c_int32),
+            "grouped_mlp_fwd_fp8_tensor": ([D] + [P] * 13 + [c_size_t, P], c_int32),
             "moe_selftest_wait_timeout": ([P, c_size_t, ctypes.c_int64, ctypes.POINTER(c_int32),
                                            ctypes.POINTER(c_int32), P], c_int32),
         }
@@ -193,3 +197,21 @@ def moe_selftest_wait_timeout(scratch, limit_ns, stream=None):
 
 def moe_clear_device_error(workspace, stream=None):
     _check(lib().moe_clear_device_error(_p(workspace), _st(stream)))
+
+
+def fp8_tensor_quantize(src, batch, rows, cols, codes, amax, stream=None):
+    _check(lib().fp8_tensor_quantize(_p(src), batch, rows, cols, _p(codes), _p(amax), _st(stream)))
+
+
+def moe_fp8_tensor_quantize_tokens(d, x, idx, row_of, split_sizes, xq, amax_x, workspace, stream=None):
+    _check(lib().moe_fp8_tensor_quantize_tokens(ctypes.byref(d), _p(x), _p(idx), _p(row_of), _p(split_sizes), _p(xq),
+                                                _p(amax_x), _p(workspace),
+                                                workspace.numel() * workspace.element_size(), _st(stream)))
+
+
+def grouped_mlp_fwd_fp8_tensor(d, xq, amax_x, split_sizes, prob_perm, wgu_q, amax_gu, wd_q, amax_d, a_perm, aq,
+                               amax_a, y, workspace, stream=None):
+    _check(lib().grouped_mlp_fwd_fp8_tensor(ctypes.byref(d), _p(xq), _p(amax_x), _p(split_sizes), _p(prob_perm),
+                                            _p(wgu_q), _p(amax_gu), _p(wd_q), _p(amax_d), _p(a_perm), _p(aq),
+                                            _p(amax_a), _p(y), _p(workspace),
+                                            workspace.numel() * workspace.element_size(), _st(stream)))

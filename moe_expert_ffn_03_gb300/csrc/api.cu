@@ -376,6 +376,119 @@ moe_status grouped_mlp_fwd_bf16(const moe_dims* d, const void* x_perm, const int
   return MOE_OK;
 }
 
+moe_status fp8_tensor_quantize(const void* src, int32_t batch, int32_t rows, int32_t cols, uint8_t* codes,
+                               float* amax, moe_stream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE_PTR(src);
+  REQUIRE_PTR(codes);
+  if (amax == nullptr) return fail(MOE_ERR_INVALID_ARG, "amax is NULL");
+  if (batch < 1 || rows < 1 || cols < 8 || cols % 8)
+    return fail(MOE_ERR_UNSUPPORTED, "batch=%d rows=%d cols=%d: need batch, rows >= 1 and cols a multiple of 8",
+                batch, rows, cols);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t per = int64_t(rows) * cols;
+  uint32_t* am = reinterpret_cast<uint32_t*>(amax);
+  CUDA_TRY(cudaMemsetAsync(am, 0, sizeof(uint32_t) * size_t(batch), st), "clear amax");
+  CUDA_TRY(launch_t8_amax_batches(src, batch, per, am, st), "per-tensor amax");
+  CUDA_TRY(launch_t8_quant_batches(src, batch, per, am, codes, st), "per-tensor quantize");
+  return MOE_OK;
+}
+
+moe_status moe_fp8_tensor_quantize_tokens(const moe_dims* d, const void* x, const int32_t* idx,
+                                          const int32_t* row_of, const int32_t* split_sizes, uint8_t* xq,
+                                          float* amax_x, void* workspace, size_t workspace_bytes,
+                                          moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(idx);
+  REQUIRE_PTR(row_of);
+  REQUIRE_PTR(split_sizes);
+  REQUIRE_PTR(xq);
+  if (amax_x == nullptr) return fail(MOE_ERR_INVALID_ARG, "amax_x is NULL");
+  s = check_ws(d, workspace, workspace_bytes, false);
+  if (s != MOE_OK) return s;
+  const WsLayout w = ws_layout(d, false);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* err = at<int>(workspace, w.err);
+  uint32_t* am = reinterpret_cast<uint32_t*>(amax_x);
+  CUDA_TRY(cudaMemsetAsync(am, 0, sizeof(uint32_t) * size_t(d->E), st), "clear amax_x");
+  CUDA_TRY(launch_t8_amax_tokens(x, d->T, d->H, idx, d->k, d->E, am, err, st), "per-expert amax of x");
+  CUDA_TRY(launch_t8_quant_tokens(x, d->T, d->H, idx, row_of, d->k, d->E, capacity(d), am, xq, err, st),
+           "per-tensor quantize of x rows");
+  CUDA_TRY(launch_fill_pad_rows(split_sizes, d->E, d->H, xq, nullptr, st), "padding rows of xq");
+  return MOE_OK;
+}
+
+moe_status grouped_mlp_fwd_fp8_tensor(const moe_dims* d, const uint8_t* xq, const float* amax_x,
+                                      const int32_t* split_sizes, const float* prob_perm, const uint8_t* wgu_q,
+                                      const float* amax_gu, const uint8_t* wd_q, const float* amax_d, void* a_perm,
+                                      uint8_t* aq, float* amax_a, void* y, void* workspace, size_t workspace_bytes,
+                                      moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  REQUIRE_PTR(xq);
+  REQUIRE_PTR(split_sizes);
+  REQUIRE_PTR(prob_perm);
+  REQUIRE_PTR(wgu_q);
+  REQUIRE_PTR(wd_q);
+  REQUIRE_PTR(a_perm);
+  REQUIRE_PTR(aq);
+  REQUIRE_PTR(y);
+  if (amax_x == nullptr || amax_gu == nullptr || amax_d == nullptr || amax_a == nullptr)
+    return fail(MOE_ERR_INVALID_ARG, "an amax array is NULL");
+  s = check_ws(d, workspace, workspace_bytes, false);
+  if (s != MOE_OK) return s;
+  const WsLayout w = ws_layout(d, false);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t cap = capacity(d);
+  const int H = d->H, I = d->I, E = d->E;
+  uint32_t* am_a = reinterpret_cast<uint32_t*>(amax_a);
+  CUDA_TRY(cudaMemsetAsync(am_a, 0, sizeof(uint32_t) * size_t(E), st), "clear amax_a");
+  GemmArgs g1{};
+  g1.mode = 0;
+  g1.E = E;
+  g1.split_sizes = split_sizes;
+  g1.K = H;
+  g1.N = I;
+  g1.n_tiles = I / 128;
+  g1.b_rows_per_expert = 2 * int64_t(I);
+  g1.cap = cap;
+  g1.prob_perm = prob_perm;
+  g1.out = static_cast<__nv_bfloat16*>(a_perm);
+  g1.ldo = I;
+  g1.I = I;
+  g1.amax_a = reinterpret_cast<const uint32_t*>(amax_x);
+  g1.amax_b = reinterpret_cast<const uint32_t*>(amax_gu);
+  g1.amax_out = am_a;
+  g1.err = at<int>(workspace, w.err);
+  CUDA_TRY(launch_grouped_gemm(EPI_T8_FWD_SWIGLU, g1, xq, cap, H, wgu_q, int64_t(E) * 2 * I, H,
+                               (cap / 128) * g1.n_tiles, st, g_msg, sizeof(g_msg)),
+           "per-tensor FP8 grouped gate_up GEMM");
+  CUDA_TRY(launch_t8_quant_segments(a_perm, split_sizes, E, cap, I, am_a, aq, st), "per-tensor quantize of a");
+  GemmArgs g2{};
+  g2.mode = 0;
+  g2.E = E;
+  g2.split_sizes = split_sizes;
+  g2.K = I;
+  g2.N = H;
+  g2.n_tiles = (H + 255) / 256;
+  g2.b_rows_per_expert = H;
+  g2.cap = cap;
+  g2.out = static_cast<__nv_bfloat16*>(y);
+  g2.ldo = H;
+  g2.I = I;
+  g2.amax_a = am_a;
+  g2.amax_b = reinterpret_cast<const uint32_t*>(amax_d);
+  g2.err = g1.err;
+  CUDA_TRY(launch_grouped_gemm(EPI_T8_OUT, g2, aq, cap, I, wd_q, int64_t(E) * H, I, (cap / 128) * g2.n_tiles, st,
+                               g_msg, sizeof(g_msg)),
+           "per-tensor FP8 grouped down GEMM");
+  return MOE_OK;
+}
+
 moe_status grouped_mlp_bwd(const moe_dims* d, const void* dout, const int32_t* split_sizes, const int32_t* row_of,
                            const int32_t* src_of, const float* prob_perm, const void* saved_gu, const uint8_t* aq_col,
                            const uint8_t* aq_col_scale, const uint8_t* xq_col, const uint8_t* xq_col_scale,

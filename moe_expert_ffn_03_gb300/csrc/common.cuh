@@ -86,14 +86,75 @@ __device__ __forceinline__ uint32_t mx_quant32(const float* v, uint32_t* q) {
   return c;
 }
 
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// mx_quant32 for 32 bf16 values packed two per word (value 2i in the low half
+// of w[i]).  The block max is taken on the 16-bit |x| patterns of both halves
+// at once; codes and scale are bit-identical to mx_quant32 on the same values.
+__device__ __forceinline__ uint32_t mx_quant32_bf16(const uint32_t* w, uint32_t* q) {
+  uint32_t mx = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) mx = __vmaxu2(mx, w[i] & 0x7FFF7FFFu);
+  const uint32_t c = mx_scale_code(max(mx << 16, mx & 0xFFFF0000u));
+  if (c == 255u) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = 0x7F7F7F7Fu;
+    return c;
+  }
+  const float m = mx_inv_scale(c);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t a = cvt_e4m3x2(bf16_lo(w[2 * i]) * m, bf16_hi(w[2 * i]) * m);
+    const uint32_t b = cvt_e4m3x2(bf16_lo(w[2 * i + 1]) * m, bf16_hi(w[2 * i + 1]) * m);
+    q[i] = a | (b << 16);
+  }
+  return c;
+}
+
+// Two adjacent columns of 32 rows at once: word i of the column pair is
+// p[i * stride] (low half = left column).  Codes of the left column go to
+// q_lo, of the right one to q_hi; returns both scale codes (left in bits 0-7,
+// right in bits 8-15).  Bit-identical to mx_quant32 on each column.
+__device__ __forceinline__ uint32_t mx_quant32_bf16_colpair(const uint32_t* p, int stride, uint32_t* q_lo,
+                                                            uint32_t* q_hi) {
+  uint32_t mx = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) mx = __vmaxu2(mx, p[i * stride] & 0x7FFF7FFFu);
+  const uint32_t c_lo = mx_scale_code(mx << 16), c_hi = mx_scale_code(mx & 0xFFFF0000u);
+  const float m_lo = mx_inv_scale(c_lo == 255u ? 0u : c_lo), m_hi = mx_inv_scale(c_hi == 255u ? 0u : c_hi);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t w0 = p[(4 * i + 0) * stride], w1 = p[(4 * i + 1) * stride];
+    const uint32_t w2 = p[(4 * i + 2) * stride], w3 = p[(4 * i + 3) * stride];
+    q_lo[i] = cvt_e4m3x2(bf16_lo(w0) * m_lo, bf16_lo(w1) * m_lo) |
+              (cvt_e4m3x2(bf16_lo(w2) * m_lo, bf16_lo(w3) * m_lo) << 16);
+    q_hi[i] = cvt_e4m3x2(bf16_hi(w0) * m_hi, bf16_hi(w1) * m_hi) |
+              (cvt_e4m3x2(bf16_hi(w2) * m_hi, bf16_hi(w3) * m_hi) << 16);
+  }
+  if (c_lo == 255u) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q_lo[i] = 0x7F7F7F7Fu;
+  }
+  if (c_hi == 255u) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q_hi[i] = 0x7F7F7F7Fu;
+  }
+  return c_lo | (c_hi << 8);
+}
+
+// Per-tensor FP8 scale of a tensor with max |v| = amax (float bits):
+// s = 448 / amax rounded to float32 (IEEE division), 1 for an all-zero tensor.
+__device__ __forceinline__ float t8_scale(uint32_t amax_bits) {
+  const float a = __uint_as_float(amax_bits);
+  return a == 0.0f ? 1.0f : __fdiv_rn(448.0f, a);
+}
+
 // One value quantized with a known scale code (for blocks reduced across lanes).
 __device__ __forceinline__ uint32_t mx_quant1(float v, uint32_t c) {
   if (c == 255u) return 0x7Fu;
   return cvt_e4m3x2(v * mx_inv_scale(c), 0.0f) & 0xFFu;
 }
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -117,6 +178,17 @@ __device__ __forceinline__ void store_codes32(uint8_t* p, const uint32_t (&q)[8]
   p4[0] = make_uint4(q[0], q[1], q[2], q[3]);
   p4[1] = make_uint4(q[4], q[5], q[6], q[7]);
 }
+
+// 16-byte global -> shared copy that bypasses registers (cp.async, L1 not
+// allocated).  valid == false writes 16 zero bytes and reads nothing.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+// Waits for all of this thread's cp.async copies (a hardware wait, not a spin loop).
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;

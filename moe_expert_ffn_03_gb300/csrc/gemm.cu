@@ -58,9 +58,13 @@ constexpr int TR_PITCH = 9;                     // floats per row of a warp's 32
 constexpr int TR_WARP_FLOATS = 32 * TR_PITCH;
 
 // bf16-operand kinds: 64 K elements per 128-byte stage row, kind::f16 MMA, no scales.
+// Per-tensor E4M3 kinds: 128 K elements per stage, kind::f8f6f4 MMA, no block scales.
 template <int EPI>
 struct Ops {
   static constexpr bool B16 = (EPI == EPI_B16_OUT || EPI == EPI_B16_FWD_SWIGLU);
+  static constexpr bool T8 = (EPI == EPI_T8_OUT || EPI == EPI_T8_FWD_SWIGLU);
+  static constexpr bool NOSF = B16 || T8;         // no scale-factor loads or copies
+  static constexpr bool SWIGLU_FWD = (EPI == EPI_FWD_SWIGLU || EPI == EPI_B16_FWD_SWIGLU || EPI == EPI_T8_FWD_SWIGLU);
   static constexpr int KSTEP = B16 ? 64 : 128;    // K elements per stage
 };
 
@@ -235,6 +239,22 @@ __device__ __forceinline__ uint32_t idesc_bf16(int N) {
          | (uint32_t(N >> 3) << 17)        // N / 8
          | (uint32_t(BM >> 4) << 24);      // M / 16
 }
+// Instruction descriptor of kind::f8f6f4 without block scaling: E4M3 x E4M3 -> f32, both K-major.
+__device__ __forceinline__ uint32_t idesc_f8(int N) {
+  return (1u << 4)                         // D format F32
+         | (0u << 7) | (0u << 10)          // A, B format E4M3
+         | (uint32_t(N >> 3) << 17)        // N / 8
+         | (uint32_t(BM >> 4) << 24);      // M / 16
+}
+__device__ __forceinline__ void tc_mma_f8(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void tc_mma_bf16(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
@@ -284,7 +304,7 @@ __device__ __forceinline__ void decode_tile(const GemmArgs& a, const int* seg_mb
     tl.k0 = 0;
     tl.k_tiles = a.K / Ops<EPI>::KSTEP;
     tl.out_row = tl.a_row;
-    if (EPI == EPI_FWD_SWIGLU || EPI == EPI_B16_FWD_SWIGLU) {
+    if (Ops<EPI>::SWIGLU_FWD) {
       tl.n0 = nb * 128;
       tl.b_row0 = int64_t(lo) * a.b_rows_per_expert + tl.n0;
       tl.b_row1 = tl.b_row0 + a.I;
@@ -419,7 +439,11 @@ __device__ __forceinline__ void quant_col_block(const float* v, uint8_t* codes_t
   }
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+// SiLU with the fast divide (__fdividef, about 2 ulp): the result feeds an E4M3
+// quantizer (3 mantissa bits) or a bf16 store.  For g below about -87 the
+// denominator passes 2^126 and it returns 0 (the exact value there is below
+// 1e-35 in magnitude).
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // One epilogue warp on one tile.  The warp owns TMEM lane quarter q (32 rows) and
 // column group cg: 64 accumulator columns cg*64.. of an N=256 tile, or gate
@@ -435,7 +459,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
   const int c0 = cg * 64;
   uint32_t r[64];
   bool have;
-  if (EPI == EPI_FWD_SWIGLU || EPI == EPI_B16_FWD_SWIGLU) {
+  if (Ops<EPI>::SWIGLU_FWD) {
     have = true;
     tmem_ld32_async(tmem_row + TM_ACC + cg * 32, r);
     tmem_ld32_async(tmem_row + TM_ACC + 128 + cg * 32, r + 32);
@@ -464,16 +488,37 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
   __syncwarp();
   if (lane == 0) mbar_arrive(tmem_empty);
 
-  if (EPI == EPI_BF16 || EPI == EPI_B16_OUT) {
+  if (EPI == EPI_BF16 || EPI == EPI_B16_OUT || EPI == EPI_T8_OUT) {
     if (c0 >= ncols) return;
+    // per-tensor E4M3 operands: dequantize the accumulator with 1/(s_a s_b) of this expert
+    const float alpha = Ops<EPI>::T8 ? __frcp_rn(t8_scale(a.amax_a[tl.e])) * __frcp_rn(t8_scale(a.amax_b[tl.e]))
+                                     : 1.0f;
     __nv_bfloat16* orow = a.out + row * a.ldo + tl.n0 + c0;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       float v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = have ? __uint_as_float(r[32 * h + i]) : 0.f;
+      for (int i = 0; i < 32; ++i) v[i] = have ? __uint_as_float(r[32 * h + i]) * alpha : 0.f;
       store_bf16x32(orow + 32 * h, v);
     }
+  } else if (EPI == EPI_T8_FWD_SWIGLU) {
+    // per-tensor path: a = silu(g)*u*p stored as bf16 [cap][I] in out; the expert's amax of
+    // the stored values is raised in amax_out (bf16 rounding is monotonic: the largest
+    // stored magnitude is the rounded largest fp32 magnitude)
+    const float p = a.prob_perm[row];
+    const float alpha = __frcp_rn(t8_scale(a.amax_a[tl.e])) * __frcp_rn(t8_scale(a.amax_b[tl.e]));
+    const int64_t col = tl.n0 + cg * 32;
+    float* f = reinterpret_cast<float*>(r);
+    uint32_t amax = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      f[i] = silu_f(f[i] * alpha) * (f[32 + i] * alpha) * p;
+      amax = max(amax, abs_bits(f[i]));
+    }
+    store_bf16x32(a.out + row * a.ldo + col, f);
+    amax = __float_as_uint(__bfloat162float(__float2bfloat16_rn(__uint_as_float(amax))));
+    amax = __reduce_max_sync(0xFFFFFFFFu, amax);
+    if (lane == 0 && amax != 0u) atomicMax(a.amax_out + tl.e, amax);
   } else if (EPI == EPI_B16_FWD_SWIGLU) {
     // bf16 path: a = silu(g)*u*p stored as bf16 [cap][I] in out
     const float p = a.prob_perm[row];
@@ -521,6 +566,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
             const float g = (t & 1) ? bf16_hi(gs[t >> 1]) : bf16_lo(gs[t >> 1]);
             const float u = (t & 1) ? bf16_hi(us[t >> 1]) : bf16_lo(us[t >> 1]);
             const float d = __uint_as_float(r[i]);
+            // the IEEE divide here: with the fast one this fully unrolled loop spills more
             const float sgm = 1.0f / (1.0f + __expf(-g));
             const float sg = g * sgm;
             dp += d * sg * u;
@@ -608,8 +654,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (blockIdx.x < total) tile_src<EPI>(args, seg_mb, blockIdx.x, cur);
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         if (t + int(gridDim.x) < total) tile_src<EPI>(args, seg_mb, t + gridDim.x, nxt);
-        const uint32_t bytes = Ops<EPI>::B16 ? A_TILE + (cur.second ? B_HALF * 2 : B_HALF)
-                                             : A_TILE + SF_ATOM * 2 + (cur.second ? (B_HALF * 2 + SF_ATOM) : B_HALF);
+        const uint32_t bytes = Ops<EPI>::NOSF ? A_TILE + (cur.second ? B_HALF * 2 : B_HALF)
+                                              : A_TILE + SF_ATOM * 2 + (cur.second ? (B_HALF * 2 + SF_ATOM) : B_HALF);
         for (int kt = 0; kt < cur.k_tiles; ++kt, ++it) {
           const int s = it % L::STG;
           const int round = it / L::STG;
@@ -623,7 +669,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tma_load_2d(smem + L::OFF_A + s * A_TILE, &tmA, kc, cur.a_row, &full[s]);
           tma_load_2d(smem + L::OFF_B + s * L::B_T, &tmB, kc, cur.b_row0, &full[s]);
           if (cur.second) tma_load_2d(smem + L::OFF_B + s * L::B_T + B_HALF, &tmB, kc, cur.b_row1, &full[s]);
-          if (!Ops<EPI>::B16) {
+          if (!Ops<EPI>::NOSF) {
             bulk_load(smem + L::OFF_SFA + s * SF_ATOM, cur.sfa + kt * SF_ATOM, SF_ATOM, &full[s]);
             bulk_load(smem + L::OFF_SFB + s * L::SFB_T, cur.sfb0 + kt * SF_ATOM, SF_ATOM, &full[s]);
             if (cur.second) bulk_load(smem + L::OFF_SFB + s * L::SFB_T + SF_ATOM, cur.sfb1 + kt * SF_ATOM, SF_ATOM, &full[s]);
@@ -676,6 +722,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                           (kt | kk) != 0);
               continue;
             }
+            if (Ops<EPI>::T8) {
+              tc_mma_f8(tmem + TM_ACC, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_f8(n),
+                        (kt | kk) != 0);
+              continue;
+            }
             tc_mma_mxf8(tmem + TM_ACC, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_mxf8(n, kk),
                         tm_sfa, tm_sfb, (kt | kk) != 0);
           }
@@ -712,7 +763,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t tm_sfa = tmem + TM_SF0 + uint32_t(s) * TM_SF_STRIDE;
           const uint32_t tm_sfb = tm_sfa + 4;
-          if (!Ops<EPI>::B16) {
+          if (!Ops<EPI>::NOSF) {
             tc_cp_sf(tm_sfa, desc_sf(smem_u32(smem + L::OFF_SFA + s * SF_ATOM)));
             tc_cp_sf(tm_sfb, desc_sf(smem_u32(smem + L::OFF_SFB + s * L::SFB_T)));
             if (tl.second) tc_cp_sf(tm_sfb + 4, desc_sf(smem_u32(smem + L::OFF_SFB + s * L::SFB_T + SF_ATOM)));
@@ -824,6 +875,8 @@ cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64
     case EPI_BWD_SWIGLU: return launch_epi<EPI_BWD_SWIGLU>(ma, mb, a, grid, st);
     case EPI_B16_OUT: return launch_epi<EPI_B16_OUT>(ma, mb, a, grid, st);
     case EPI_B16_FWD_SWIGLU: return launch_epi<EPI_B16_FWD_SWIGLU>(ma, mb, a, grid, st);
+    case EPI_T8_OUT: return launch_epi<EPI_T8_OUT>(ma, mb, a, grid, st);
+    case EPI_T8_FWD_SWIGLU: return launch_epi<EPI_T8_FWD_SWIGLU>(ma, mb, a, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -31,6 +31,16 @@ cudaError_t launch_gather_rows(const void* x, const int* row_of, const int* spli
                                int64_t cap, void* x_perm, int* err, cudaStream_t st);
 cudaError_t launch_combine(const void* y, const int* row_of, const float* prob, int T, int k, int H, int64_t cap,
                            void* out, int* err, cudaStream_t st);
+// Per-tensor FP8 (one scale per expert operand tensor): amax reductions and E4M3 codes.
+cudaError_t launch_t8_amax_tokens(const void* x, int T, int H, const int* idx, int k, int E, uint32_t* amax,
+                                  int* err, cudaStream_t st);
+cudaError_t launch_t8_quant_tokens(const void* x, int T, int H, const int* idx, const int* row_of, int k, int E,
+                                   int64_t cap, const uint32_t* amax, uint8_t* codes, int* err, cudaStream_t st);
+cudaError_t launch_t8_amax_batches(const void* src, int batch, int64_t per_batch, uint32_t* amax, cudaStream_t st);
+cudaError_t launch_t8_quant_batches(const void* src, int batch, int64_t per_batch, const uint32_t* amax,
+                                    uint8_t* codes, cudaStream_t st);
+cudaError_t launch_t8_quant_segments(const void* src, const int* split_sizes, int E, int64_t cap, int cols,
+                                     const uint32_t* amax, uint8_t* codes, cudaStream_t st);
 cudaError_t launch_dprob_reduce(const float* dp_part, int n_tiles, int64_t cap, const int* row_of, int64_t R,
                                 float* dprob, int* err, cudaStream_t st);
 
@@ -43,8 +53,20 @@ cudaError_t launch_dprob_reduce(const float* dp_part, int n_tiles, int64_t cap, 
 //     [M][N] output with K = the expert's padded token range of A and B.
 // EPI_BF16 .. EPI_BWD_SWIGLU take MXFP8 operands (block-scaled MMA); the B16 kinds take
 // bf16 operands (kind::f16 MMA, no scales): plain bf16 output, or ScaledSwiGLU with a
-// bf16 `a` written to out [cap][I].
-enum Epilogue : int { EPI_BF16 = 0, EPI_FWD_SWIGLU = 1, EPI_BWD_SWIGLU = 2, EPI_B16_OUT = 3, EPI_B16_FWD_SWIGLU = 4 };
+// bf16 `a` written to out [cap][I].  The T8 kinds take per-tensor scaled E4M3 operands
+// (kind::f8f6f4 MMA, no block scales): the accumulator is multiplied by
+// 1 / (s_a[e] * s_b[e]) with s = 448 / amax of the expert's operand tensors, then a
+// plain bf16 output, or ScaledSwiGLU with a bf16 `a` in out [cap][I] and the amax of
+// every expert's bf16 `a` raised into amax_out[e].
+enum Epilogue : int {
+  EPI_BF16 = 0,
+  EPI_FWD_SWIGLU = 1,
+  EPI_BWD_SWIGLU = 2,
+  EPI_B16_OUT = 3,
+  EPI_B16_FWD_SWIGLU = 4,
+  EPI_T8_OUT = 5,
+  EPI_T8_FWD_SWIGLU = 6,
+};
 
 struct GemmArgs {
   int mode;
@@ -72,6 +94,9 @@ struct GemmArgs {
   __nv_bfloat16* gu;         // saved g,u [cap][2I]: written by FWD (optional), read by BWD
   float* dp_part;            // BWD: [n_tiles][cap] partial row sums of dA*silu(g)*u
   int I;
+  const uint32_t* amax_a;    // T8 kinds: per-expert amax (float bits) of A's and B's tensors
+  const uint32_t* amax_b;
+  uint32_t* amax_out;        // EPI_T8_FWD_SWIGLU: per-expert amax of the bf16 `a` (raised, not set)
   int* err;
   uint64_t wait_limit_ns;    // bound of every mbarrier wait (0: the default kWaitLimitNs)
   int selftest_no_loads;     // self-test only: the producer issues nothing, so the waits run out

@@ -23,62 +23,75 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(
   const int64_t s = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (s >= n_rows) return;
   const int nblk = cols >> 5;
-  int64_t dst[8];
+  // lane j < k holds the destination row of slot j (shuffled to the warp when storing)
+  int my_dst = 0;
   int nd = 1;
   if (SCATTER) {
     nd = k;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j < k) {
-        const int r = row_of[s * k + j];
-        if (r < 0 || r >= cap) {
-          report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_QUANT + 1);
-          return;
-        }
-        dst[j] = r;
-      }
+    bool bad = false;
+    if (lane < k) {
+      my_dst = row_of[s * k + lane];
+      bad = my_dst < 0 || my_dst >= cap;
     }
-  } else {
-    dst[0] = s;
+    if (__any_sync(0xFFFFFFFFu, bad)) {
+      if (lane == 0) report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_QUANT + 1);
+      return;
+    }
   }
   for (int b = lane; b < nblk; b += 32) {
-    float v[32];
-    load_bf16x32(src + s * cols + (int64_t)b * 32, v);
+    uint32_t w[16];
+    const uint4* p4 = reinterpret_cast<const uint4*>(src + s * cols + (int64_t)b * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 x = p4[i];
+      w[4 * i + 0] = x.x;
+      w[4 * i + 1] = x.y;
+      w[4 * i + 2] = x.z;
+      w[4 * i + 3] = x.w;
+    }
     uint32_t q[8];
-    const uint32_t c = mx_quant32(v, q);
-    for (int j = 0; j < nd; ++j) {
-      store_codes32(codes + dst[j] * cols + (int64_t)b * 32, q);
-      scales[sf_offset(dst[j], b, cols)] = uint8_t(c);
+    const uint32_t c = mx_quant32_bf16(w, q);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < nd) {
+        const int64_t row = SCATTER ? int64_t(__shfl_sync(0xFFFFFFFFu, my_dst, j)) : s;
+        store_codes32(codes + row * cols + (int64_t)b * 32, q);
+        scales[sf_offset(row, b, cols)] = uint8_t(c);
+      }
     }
   }
 }
 
-// Zero codes and zero scale codes for the padding rows of every expert segment
-// (rows split_sizes[e] .. roundup(split_sizes[e],128)-1 of segment e).
+// Zero codes and zero scale codes (scales may be null: codes only) for the
+// padding rows of every expert segment (rows split_sizes[e] ..
+// roundup(split_sizes[e],128)-1 of segment e).
+// Grid (E, FP_SLICES): slice y of expert e clears padding rows y, y + FP_SLICES, ...
+constexpr int FP_SLICES = 16;
+
 __global__ void __launch_bounds__(256) fill_pad_rows_kernel(
     const int* __restrict__ split_sizes, int E, int cols,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
   __shared__ int seg_start;
   const int e = blockIdx.x;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {
     int acc = 0;
-    for (int i = 0; i < e; ++i) acc += (split_sizes[i] + 127) & ~127;
-    seg_start = acc;
+    for (int i = threadIdx.x; i < e; i += 32) acc += (split_sizes[i] + 127) & ~127;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+    if (threadIdx.x == 0) seg_start = acc;
   }
   __syncthreads();
   const int m = split_sizes[e];
   const int npad = ((m + 127) & ~127) - m;
   const int64_t r0 = int64_t(seg_start) + m;
   const int vec_per_row = cols >> 4;                 // uint4 per row
-  for (int64_t i = threadIdx.x; i < int64_t(npad) * vec_per_row; i += blockDim.x) {
-    const int64_t r = r0 + i / vec_per_row;
-    const int c = int(i % vec_per_row);
-    reinterpret_cast<uint4*>(codes + r * cols)[c] = make_uint4(0, 0, 0, 0);
-  }
   const int nblk = cols >> 5;
-  for (int64_t i = threadIdx.x; i < int64_t(npad) * nblk; i += blockDim.x) {
-    const int64_t r = r0 + i / nblk;
-    scales[sf_offset(r, i % nblk, cols)] = 0;
+  for (int pr = blockIdx.y; pr < npad; pr += FP_SLICES) {
+    const int64_t r = r0 + pr;
+    uint4* row = reinterpret_cast<uint4*>(codes + r * cols);
+    for (int c = threadIdx.x; c < vec_per_row; c += blockDim.x) row[c] = make_uint4(0, 0, 0, 0);
+    if (scales != nullptr)
+      for (int b = threadIdx.x; b < nblk; b += blockDim.x) scales[sf_offset(r, b, cols)] = 0;
   }
 }
 
@@ -94,7 +107,7 @@ __global__ void __launch_bounds__(256) fill_pad_rows_kernel(
 constexpr int QC_TILE = 128;
 constexpr int QC_PITCH = QC_TILE + 8;                // bf16 per smem row (16 B pad)
 
-__global__ void __launch_bounds__(256) quant_colwise_kernel(
+__global__ void __launch_bounds__(256, 6) quant_colwise_kernel(
     const __nv_bfloat16* __restrict__ src, const int* __restrict__ src_map, int64_t n_src_rows,
     int rows, int cols, const int* __restrict__ split_sizes, int E,
     uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t, int* err) {
@@ -104,45 +117,56 @@ __global__ void __launch_bounds__(256) quant_colwise_kernel(
   const int row0 = blockIdx.x * QC_TILE;
   const int col0 = blockIdx.y * QC_TILE;
   const int64_t batch = blockIdx.z;
+  // Thread stages 16-byte chunk c16 of tile rows rbase + 16*it.  The gather
+  // indices are loaded before the padded total is known, so both round trips
+  // overlap; entries past the total are never used.
+  const int c16 = threadIdx.x & 15, rbase = threadIdx.x >> 4;
+  int sr[QC_TILE / 16];
+  if (src_map != nullptr) {
+#pragma unroll
+    for (int it = 0; it < QC_TILE / 16; ++it) sr[it] = src_map[row0 + rbase + 16 * it];
+  }
   if (split_sizes != nullptr) {
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < 32) {
       int acc = 0;
-      for (int e = 0; e < E; ++e) acc += (split_sizes[e] + 127) & ~127;
-      s_rows_used = acc;
+      for (int e = threadIdx.x; e < E; e += 32) acc += (split_sizes[e] + 127) & ~127;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+      if (threadIdx.x == 0) s_rows_used = acc;
     }
     __syncthreads();
     if (row0 >= s_rows_used) return;
   }
-  // stage: 128 rows x 256 bytes = 16 uint4 per row; all eight loads of a thread in flight together
 #pragma unroll
-  for (int it = 0; it < QC_TILE * 16 / 256; ++it) {
-    const int i = threadIdx.x + it * 256;
-    const int r = i >> 4, c16 = i & 15;
-    int64_t sr;
+  for (int it = 0; it < QC_TILE / 16; ++it) {
+    const int r = rbase + 16 * it;
+    int64_t s;
     if (src_map != nullptr) {
-      sr = src_map[row0 + r];
-      if (sr >= n_src_rows) {
+      s = sr[it];
+      if (s >= n_src_rows) {
         report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_QUANT + 2);
-        sr = -1;
+        s = -1;
       }
     } else {
-      sr = batch * rows + row0 + r;
+      s = batch * rows + row0 + r;
     }
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (sr >= 0) w = reinterpret_cast<const uint4*>(src + sr * cols + col0)[c16];
-    *reinterpret_cast<uint4*>(&tile[r * QC_PITCH + c16 * 8]) = w;
+    const bool valid = s >= 0;
+    cp_async16(&tile[r * QC_PITCH + c16 * 8], valid ? static_cast<const void*>(src + s * cols + col0 + c16 * 8) : src,
+               valid);
   }
+  cp_async_wait_all();
   __syncthreads();
-  const int c = threadIdx.x & 127;
-  const int64_t drow = batch * cols + col0 + c;      // row of the transposed tensor
-  for (int rb = threadIdx.x >> 7; rb < 4; rb += 2) {
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(tile[(rb * 32 + i) * QC_PITCH + c]);
-    uint32_t q[8];
-    const uint32_t sc = mx_quant32(v, q);
-    store_codes32(codes_t + drow * rows + row0 + rb * 32, q);
+  // task: columns (c, c+1) x 32-row block rb -- one per thread
+  {
+    const int c = 2 * (threadIdx.x & 63), rb = threadIdx.x >> 6;
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(&tile[(rb * 32) * QC_PITCH + c]);
+    uint32_t q_lo[8], q_hi[8];
+    const uint32_t sc = mx_quant32_bf16_colpair(p, QC_PITCH / 2, q_lo, q_hi);
+    const int64_t drow = batch * cols + col0 + c;    // row of the transposed tensor
+    store_codes32(codes_t + drow * rows + row0 + rb * 32, q_lo);
+    store_codes32(codes_t + (drow + 1) * rows + row0 + rb * 32, q_hi);
     sc_atom[((c & 31) << 4) + (((c >> 5) & 3) << 2) + rb] = uint8_t(sc);
+    sc_atom[(((c + 1) & 31) << 4) + ((((c + 1) >> 5) & 3) << 2) + rb] = uint8_t(sc >> 8);
   }
   __syncthreads();
   // the tile's scales are exactly one 512-byte atom of the transposed tensor
@@ -158,7 +182,7 @@ __global__ void __launch_bounds__(256) quant_colwise_kernel(
 // and (column, 32-row block) pairs into codes_t[cols][rows].  Each bf16 weight is
 // read once and both MX copies written: 2 B in, 2*(1 + 1/32) B out per element.
 // ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) quant_dual_kernel(
+__global__ void __launch_bounds__(256, 6) quant_dual_kernel(
     const __nv_bfloat16* __restrict__ src, int rows, int cols, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t) {
   __shared__ __align__(16) __nv_bfloat16 tile[QC_TILE * QC_PITCH];
@@ -168,43 +192,46 @@ __global__ void __launch_bounds__(256) quant_dual_kernel(
   const int col0 = blockIdx.y * QC_TILE;
   const int64_t batch = blockIdx.z;
   const int64_t srow0 = batch * rows + row0;
+  {
+    const int c16 = threadIdx.x & 15, rbase = threadIdx.x >> 4;
 #pragma unroll
-  for (int it = 0; it < QC_TILE * 16 / 256; ++it) {
-    const int i = threadIdx.x + it * 256;
-    const int r = i >> 4, c16 = i & 15;
-    const uint4 w = reinterpret_cast<const uint4*>(src + (srow0 + r) * cols + col0)[c16];
-    *reinterpret_cast<uint4*>(&tile[r * QC_PITCH + c16 * 8]) = w;
+    for (int it = 0; it < QC_TILE / 16; ++it) {
+      const int r = rbase + 16 * it;
+      cp_async16(&tile[r * QC_PITCH + c16 * 8], src + (srow0 + r) * cols + col0 + c16 * 8, true);
+    }
   }
+  cp_async_wait_all();
   __syncthreads();
   // rowwise: task = (row r, block b), 128 x 4
   for (int task = threadIdx.x; task < QC_TILE * 4; task += blockDim.x) {
     const int r = task >> 2, b = task & 3;
-    float v[32];
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(&tile[r * QC_PITCH + b * 32]);
+    uint32_t w[16];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint4 w = *reinterpret_cast<const uint4*>(&tile[r * QC_PITCH + b * 32 + i * 8]);
-      v[8 * i + 0] = bf16_lo(w.x); v[8 * i + 1] = bf16_hi(w.x);
-      v[8 * i + 2] = bf16_lo(w.y); v[8 * i + 3] = bf16_hi(w.y);
-      v[8 * i + 4] = bf16_lo(w.z); v[8 * i + 5] = bf16_hi(w.z);
-      v[8 * i + 6] = bf16_lo(w.w); v[8 * i + 7] = bf16_hi(w.w);
+      const uint4 x = reinterpret_cast<const uint4*>(p)[i];
+      w[4 * i + 0] = x.x;
+      w[4 * i + 1] = x.y;
+      w[4 * i + 2] = x.z;
+      w[4 * i + 3] = x.w;
     }
     uint32_t q[8];
-    const uint32_t sc = mx_quant32(v, q);
+    const uint32_t sc = mx_quant32_bf16(w, q);
     const int64_t drow = srow0 + r;
     store_codes32(codes + drow * cols + col0 + b * 32, q);
     sc_row[((r & 31) << 4) + (((r >> 5) & 3) << 2) + b] = uint8_t(sc);
   }
-  // colwise: task = (column c, row block rb), 128 x 4
-  for (int task = threadIdx.x; task < QC_TILE * 4; task += blockDim.x) {
-    const int c = task & 127, rb = task >> 7;
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(tile[(rb * 32 + i) * QC_PITCH + c]);
-    uint32_t q[8];
-    const uint32_t sc = mx_quant32(v, q);
+  // colwise: task = (columns c, c+1) x 32-row block rb -- one per thread
+  {
+    const int c = 2 * (threadIdx.x & 63), rb = threadIdx.x >> 6;
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(&tile[(rb * 32) * QC_PITCH + c]);
+    uint32_t q_lo[8], q_hi[8];
+    const uint32_t sc = mx_quant32_bf16_colpair(p, QC_PITCH / 2, q_lo, q_hi);
     const int64_t drow = batch * cols + col0 + c;
-    store_codes32(codes_t + drow * rows + row0 + rb * 32, q);
+    store_codes32(codes_t + drow * rows + row0 + rb * 32, q_lo);
+    store_codes32(codes_t + (drow + 1) * rows + row0 + rb * 32, q_hi);
     sc_col[((c & 31) << 4) + (((c >> 5) & 3) << 2) + rb] = uint8_t(sc);
+    sc_col[(((c + 1) & 31) << 4) + ((((c + 1) >> 5) & 3) << 2) + rb] = uint8_t(sc >> 8);
   }
   __syncthreads();
   // each orientation's scales of this tile are exactly one 512-byte atom
@@ -237,7 +264,7 @@ cudaError_t launch_quant_rowwise(const void* src, int64_t n_rows, int cols, cons
 
 cudaError_t launch_fill_pad_rows(const int* split_sizes, int E, int cols, uint8_t* codes, uint8_t* scales,
                                  cudaStream_t st) {
-  fill_pad_rows_kernel<<<E, 256, 0, st>>>(split_sizes, E, cols, codes, scales);
+  fill_pad_rows_kernel<<<dim3(E, FP_SLICES), 256, 0, st>>>(split_sizes, E, cols, codes, scales);
   return cudaGetLastError();
 }
 

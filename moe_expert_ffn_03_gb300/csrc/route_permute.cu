@@ -3,11 +3,11 @@
 // Training for Biological Foundation Models", section "GroupedLinear": the
 // grouped call takes the tokens collected per expert plus split_sizes).
 //
-// Deterministic without sorting or atomics:
-//   1. route_topk_kernel: one warp per 32-token group selects the top-k
-//      experts of each token by exact logit comparisons and writes, per expert
-//      e and group g, the 32-bit ballot mask[e][g] of the group's tokens that
-//      picked e.
+// Deterministic without sorting and without global atomics:
+//   1. route_topk_kernel: one thread per token keeps its k best (logit,
+//      expert) pairs in a sorted register list (exact comparisons, ties to the
+//      lower expert id); the warp then writes, per expert e and 32-token group
+//      g, the bit mask[e][g] of the group's tokens that picked e.
 //   2. permute_scan_kernel: one CTA per expert scans popc(mask[e][g]) over g:
 //      base[e][g] = tokens of e in groups before g; split_sizes[e] = total.
 //   3. permute_scatter_kernel: row of (t, slot) = padded start of e +
@@ -24,90 +24,76 @@ __device__ __forceinline__ bool better(float va, int ea, float vb, int eb) {
   return va > vb || (va == vb && ea < eb);
 }
 
-__global__ void __launch_bounds__(256) route_topk_kernel(
+constexpr int RT_THREADS = 128;
+
+// Bubble (v, e) into the sorted list (best first); the last entry falls off.
+__device__ __forceinline__ void topk_insert(float v, int e, float (&sv)[kMaxK], int (&se)[kMaxK]) {
+#pragma unroll
+  for (int s = 0; s < kMaxK; ++s) {
+    if (better(v, e, sv[s], se[s])) {
+      const float tv = sv[s];
+      const int te = se[s];
+      sv[s] = v;
+      se[s] = e;
+      v = tv;
+      e = te;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(RT_THREADS) route_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renorm,
     int* __restrict__ idx, float* __restrict__ prob, uint32_t* __restrict__ masks, int G) {
-  const int lane = threadIdx.x & 31;
-  const int g = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (g >= G) return;
-  const int nchunk = (E + 31) >> 5;                    // <= 8 logits per lane
-  int my_sel[kMaxK];
-#pragma unroll
-  for (int s = 0; s < kMaxK; ++s) my_sel[s] = -1;
-  for (int i = 0; i < 32; ++i) {
-    const int t = g * 32 + i;
-    if (t >= T) break;                                 // warp-uniform
-    float v[8];
-    unsigned taken = 0;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const int e = lane + 32 * c;
-      v[c] = (c < nchunk && e < E) ? logits[(int64_t)t * E + e] : -INFINITY;
-    }
-    int sel_e[kMaxK];
-    float sel_v[kMaxK];
+  __shared__ uint32_t smask[RT_THREADS / 32][kMaxE];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int t = blockIdx.x * RT_THREADS + threadIdx.x;
+  const int g = t >> 5;                                // the warp's 32-token group
+  if (g >= G) return;                                  // warp-uniform
+  for (int e = lane; e < E; e += 32) smask[w][e] = 0u;
+  __syncwarp();
+  if (t < T) {
+    float sv[kMaxK];
+    int se[kMaxK];
 #pragma unroll
     for (int s = 0; s < kMaxK; ++s) {
-      sel_e[s] = -1;
-      sel_v[s] = -INFINITY;
-      if (s < k) {
-        float bv = -INFINITY;
-        int be = 0x7FFFFFFF;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int e = lane + 32 * c;
-          if (c < nchunk && e < E && !((taken >> c) & 1u) && better(v[c], e, bv, be)) {
-            bv = v[c];
-            be = e;
-          }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-          const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
-          if (better(ov, oe, bv, be)) {
-            bv = ov;
-            be = oe;
-          }
-        }
-        sel_e[s] = be;
-        sel_v[s] = bv;
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      sv[s] = -INFINITY;
+      se[s] = 0x7FFFFFFF;
+    }
+    const float* row = logits + (int64_t)t * E;
+    if ((E & 3) == 0) {
+      const float4* row4 = reinterpret_cast<const float4*>(row);
+      for (int e4 = 0; e4 < (E >> 2); ++e4) {
+        const float4 q = row4[e4];
+        topk_insert(q.x, 4 * e4 + 0, sv, se);
+        topk_insert(q.y, 4 * e4 + 1, sv, se);
+        topk_insert(q.z, 4 * e4 + 2, sv, se);
+        topk_insert(q.w, 4 * e4 + 3, sv, se);
       }
+    } else {
+      for (int e = 0; e < E; ++e) topk_insert(row[e], e, sv, se);
     }
     // probabilities: softmax of the selected logits (renorm) or of all E
-    const float m = sel_v[0];
+    const float m = sv[0];
     float den = 0.f;
     if (renorm) {
 #pragma unroll
       for (int s = 0; s < kMaxK; ++s)
-        if (s < k) den += expf(sel_v[s] - m);
+        if (s < k) den += expf(sv[s] - m);
     } else {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int e = lane + 32 * c;
-        if (c < nchunk && e < E) den += expf(v[c] - m);
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, off);
+      for (int e = 0; e < E; ++e) den += expf(row[e] - m);
     }
 #pragma unroll
     for (int s = 0; s < kMaxK; ++s) {
-      if (s < k && lane == s) {
-        idx[(int64_t)t * k + s] = sel_e[s];
-        prob[(int64_t)t * k + s] = expf(sel_v[s] - m) / den;
+      if (s < k) {
+        idx[(int64_t)t * k + s] = se[s];
+        prob[(int64_t)t * k + s] = expf(sv[s] - m) / den;
+        atomicOr(&smask[w][se[s]], 1u << lane);
       }
-      if (lane == i) my_sel[s] = (s < k) ? sel_e[s] : -1;
     }
   }
-  // ballot masks: bit l of mask[e][g] = token g*32+l picked expert e
-  for (int e = 0; e < E; ++e) {
-    bool pick = false;
-#pragma unroll
-    for (int s = 0; s < kMaxK; ++s) pick |= (my_sel[s] == e);
-    const unsigned msk = __ballot_sync(0xFFFFFFFFu, pick);
-    if (lane == 0) masks[(int64_t)e * G + g] = msk;
-  }
+  __syncwarp();
+  // bit l of mask[e][g] = token g*32+l picked expert e
+  for (int e = lane; e < E; e += 32) masks[(int64_t)e * G + g] = smask[w][e];
 }
 
 // One CTA per expert: exclusive scan over groups of popc(mask).
@@ -196,7 +182,8 @@ cudaError_t launch_route_permute(const float* logits, int T, int E, int k, int r
                                  uint32_t* masks, int* bases, int* split_sizes, int* row_of, int* src_of,
                                  float* prob_perm, int* err, cudaStream_t st) {
   const int G = (T + 31) / 32;
-  route_topk_kernel<<<(G * 32 + 255) / 256, 256, 0, st>>>(logits, T, E, k, renorm, idx, prob, masks, G);
+  route_topk_kernel<<<(G * 32 + RT_THREADS - 1) / RT_THREADS, RT_THREADS, 0, st>>>(logits, T, E, k, renorm, idx,
+                                                                                   prob, masks, G);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   permute_scan_kernel<<<E, 1024, 0, st>>>(masks, G, bases, split_sizes);

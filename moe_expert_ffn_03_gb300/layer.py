@@ -126,6 +126,38 @@ class ExpertFFN:
         B.moe_unpermute_combine(self.d, self.y_b16, self.row_of, None, self.out_b16, stream)
         return self.out_b16
 
+    # ---- per-tensor FP8 forward (one scale per expert operand tensor) ------------------
+    def quantize_weights_fp8_tensor(self, w_gu, w_d, stream=None):
+        """E4M3 codes of W_gu and W_d with one dynamic scale per expert weight."""
+        if not hasattr(self, "t8_wgu"):
+            dev = self.ws.device
+            self.t8_wgu = torch.empty(self.E, 2 * self.I, self.H, dtype=U8, device=dev)
+            self.t8_wd = torch.empty(self.E, self.H, self.I, dtype=U8, device=dev)
+            self.t8_amax_gu = torch.empty(self.E, dtype=torch.float32, device=dev)
+            self.t8_amax_d = torch.empty(self.E, dtype=torch.float32, device=dev)
+        B.fp8_tensor_quantize(w_gu, self.E, 2 * self.I, self.H, self.t8_wgu, self.t8_amax_gu, stream)
+        B.fp8_tensor_quantize(w_d, self.E, self.H, self.I, self.t8_wd, self.t8_amax_d, stream)
+
+    def forward_fp8_tensor(self, x, stream=None):
+        """After route() and quantize_weights_fp8_tensor(): per-tensor FP8 x rows, grouped
+        gate_up + ScaledSwiGLU (bf16 a), per-tensor FP8 a, grouped down, combine."""
+        if not hasattr(self, "t8_xq"):
+            dev = self.ws.device
+            self.t8_xq = torch.empty(self.cap, self.H, dtype=U8, device=dev)
+            self.t8_a = torch.empty(self.cap, self.I, dtype=torch.bfloat16, device=dev)
+            self.t8_aq = torch.empty(self.cap, self.I, dtype=U8, device=dev)
+            self.t8_y = torch.empty(self.cap, self.H, dtype=torch.bfloat16, device=dev)
+            self.t8_out = torch.empty(self.T, self.H, dtype=torch.bfloat16, device=dev)
+            self.t8_amax_x = torch.empty(self.E, dtype=torch.float32, device=dev)
+            self.t8_amax_a = torch.empty(self.E, dtype=torch.float32, device=dev)
+        B.moe_fp8_tensor_quantize_tokens(self.d, x, self.idx, self.row_of, self.split_sizes, self.t8_xq,
+                                         self.t8_amax_x, self.ws, stream)
+        B.grouped_mlp_fwd_fp8_tensor(self.d, self.t8_xq, self.t8_amax_x, self.split_sizes, self.prob_perm, self.t8_wgu,
+                                     self.t8_amax_gu, self.t8_wd, self.t8_amax_d, self.t8_a, self.t8_aq,
+                                     self.t8_amax_a, self.t8_y, self.ws, stream)
+        B.moe_unpermute_combine(self.d, self.t8_y, self.row_of, None, self.t8_out, stream)
+        return self.t8_out
+
     # ---- router (optional: when the logits come from x) ------------------------------
     def router_forward(self, x, w_r, stream=None):
         """logits = x W_r^T into self.logits (allocated on first use)."""

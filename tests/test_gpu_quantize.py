@@ -101,3 +101,22 @@ def test_dual_equals_the_two_single_axis_calls():
     B.mxfp8_quantize_dual(w, E, R, C, d0, t0, d1, t1)
     torch.cuda.synchronize()
     assert torch.equal(c0, d0) and torch.equal(s0, t0) and torch.equal(c1, d1) and torch.equal(s1, t1)
+
+
+@pytest.mark.parametrize("seed", [0, 9])
+def test_dual_every_bf16_pattern(seed):
+    """Both orientations of one read, on every bf16 bit pattern (NaN, Inf, zeros, subnormals)."""
+    bits = all_patterns_matrix(seed)
+    x = bf16_from_bits(bits).cuda()
+    codes = torch.empty(65536, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(2048, dtype=torch.uint8, device="cuda")
+    codes_t, scales_t = torch.empty_like(codes), torch.empty_like(scales)
+    B.mxfp8_quantize_dual(x, 1, 512, 128, codes, scales, codes_t, scales_t)
+    torch.cuda.synchronize()
+    with np.errstate(invalid="ignore"):
+        rc, rs = mx.quantize_blocks(as_f64(x), axis=1)
+        cc, cs = mx.quantize_blocks(as_f64(x), axis=0)
+    assert np.array_equal(codes.cpu().numpy().reshape(512, 128), rc)
+    assert np.array_equal(untile_scales(scales.cpu().numpy(), 512, 128), rs)
+    assert np.array_equal(codes_t.cpu().numpy().reshape(128, 512), cc.T)
+    assert np.array_equal(untile_scales(scales_t.cpu().numpy(), 128, 512), cs.T)
