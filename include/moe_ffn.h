@@ -221,6 +221,21 @@ moe_status grouped_mlp_fwd_bf16(const moe_dims* d, const void* x_perm, const int
                                 void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * mxfp8_quantize_experts -- mxfp8_quantize_dual for weights held as one tensor
+ * per expert (page "Efficient MoE Training for Biological Foundation Models",
+ * section "GroupedLinear": every expert keeps its own weight tensor, weight0,
+ * weight1, ...).  w is a HOST array of E device pointers, each to a bf16
+ * [rows][cols] row-major matrix, 16-byte aligned; the results are the stacked
+ * tensors of mxfp8_quantize_dual with batch = E, so the grouped GEMMs read
+ * them unchanged.  codes_t/scales_t may both be NULL (forward-only: the
+ * rowwise copy alone).  1 <= E <= 256; the pointers are read during the call
+ * only.
+ */
+moe_status mxfp8_quantize_experts(const void* const* w, int32_t E, int32_t rows, int32_t cols, uint8_t* codes,
+                                  uint8_t* scales, uint8_t* codes_t, uint8_t* scales_t, moe_stream_t stream);
+
+/*
+ * Per-tensor FP8 with dynamic scaling/*
  * Per-tensor FP8 with dynamic scaling (page "英伟达开源MoE加速神器", section
  * "3. Transformer Engine：FP8 训练加速": the Hopper recipe scales every tensor by
  * its current range; page "Efficient MoE Training for Biological Foundation
@@ -245,6 +260,15 @@ moe_status grouped_mlp_fwd_bf16(const moe_dims* d, const void* x_perm, const int
  */
 moe_status fp8_tensor_quantize(const void* src, int batch, int rows, int cols, uint8_t* codes, float* amax,
                                moe_stream_t stream);
+
+/*
+ * fp8_tensor_quantize_experts -- fp8_tensor_quantize for one weight tensor per
+ * expert: w is a HOST array of E device pointers (bf16 [rows][cols] each,
+ * 16-byte aligned), 1 <= E <= 256; codes out stacked uint8 [E][rows][cols],
+ * amax out float32 [E].
+ */
+moe_status fp8_tensor_quantize_experts(const void* const* w, int32_t E, int32_t rows, int32_t cols, uint8_t* codes,
+                                       float* amax, moe_stream_t stream);
 
 /*
  * moe_fp8_tensor_quantize_tokens -- the x operand of the per-tensor path:

@@ -20,6 +20,7 @@ EXPORTS = (
     "moe_unpermute_combine", "moe_get_device_error", "moe_clear_device_error", "moe_route_permute_noalloc",
     "moe_selftest_wait_timeout", "moe_router_fwd", "moe_router_bwd", "moe_gather_rows", "grouped_mlp_fwd_bf16",
     "fp8_tensor_quantize", "moe_fp8_tensor_quantize_tokens", "grouped_mlp_fwd_fp8_tensor",
+    "mxfp8_quantize_experts", "fp8_tensor_quantize_experts",
 )
 
 MOE_OK = 0
@@ -80,6 +81,8 @@ def lib() -> ctypes.CDLL:
             "fp8_tensor_quantize": ([P, c_int32, c_int32, c_int32, P, P, P], c_int32),
             "moe_fp8_tensor_quantize_tokens": ([D, P, P, P, P, P, P, P, c_size_t, P], c_int32),
             "grouped_mlp_fwd_fp8_tensor": ([D] + [P] * 13 + [c_size_t, P], c_int32),
+            "mxfp8_quantize_experts": ([ctypes.POINTER(P), c_int32, c_int32, c_int32, P, P, P, P, P], c_int32),
+            "fp8_tensor_quantize_experts": ([ctypes.POINTER(P), c_int32, c_int32, c_int32, P, P, P], c_int32),
             "moe_selftest_wait_timeout": ([P, c_size_t, ctypes.c_int64, ctypes.POINTER(c_int32),
                                            ctypes.POINTER(c_int32), P], c_int32),
         }
@@ -215,3 +218,18 @@ def grouped_mlp_fwd_fp8_tensor(d, xq, amax_x, split_sizes, prob_perm, wgu_q, ama
                                             _p(wgu_q), _p(amax_gu), _p(wd_q), _p(amax_d), _p(a_perm), _p(aq),
                                             _p(amax_a), _p(y), _p(workspace),
                                             workspace.numel() * workspace.element_size(), _st(stream)))
+
+
+def _ptr_array(tensors):
+    """Host array of the device pointers of a list of tensors (one per expert)."""
+    return (c_void_p * len(tensors))(*[t.data_ptr() for t in tensors])
+
+
+def mxfp8_quantize_experts(w_list, rows, cols, codes, scales, codes_t=None, scales_t=None, stream=None):
+    _check(lib().mxfp8_quantize_experts(_ptr_array(w_list), len(w_list), rows, cols, _p(codes), _p(scales),
+                                        _p(codes_t), _p(scales_t), _st(stream)))
+
+
+def fp8_tensor_quantize_experts(w_list, rows, cols, codes, amax, stream=None):
+    _check(lib().fp8_tensor_quantize_experts(_ptr_array(w_list), len(w_list), rows, cols, _p(codes), _p(amax),
+                                             _st(stream)))

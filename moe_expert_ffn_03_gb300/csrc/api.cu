@@ -183,6 +183,68 @@ moe_status mxfp8_quantize_dual(const void* src, int32_t batch, int32_t rows, int
   return MOE_OK;
 }
 
+}  // extern "C"
+
+namespace {
+// The host array of per-expert weight pointers, checked and copied into a kernel parameter table.
+moe_status expert_table(const void* const* w, int32_t E, ExpertSrc* tbl) {
+  if (w == nullptr) return fail(MOE_ERR_INVALID_ARG, "the expert pointer array is NULL");
+  if (E < 1 || E > kMaxExpertPtrs) return fail(MOE_ERR_UNSUPPORTED, "E=%d must be in 1..%d", E, kMaxExpertPtrs);
+  for (int e = 0; e < E; ++e) {
+    if (w[e] == nullptr) return fail(MOE_ERR_INVALID_ARG, "the weight pointer of expert %d is NULL", e);
+    if (!al16(w[e])) return fail(MOE_ERR_ALIGNMENT, "the weight of expert %d is not 16-byte aligned", e);
+    tbl->p[e] = static_cast<const __nv_bfloat16*>(w[e]);
+  }
+  for (int e = E; e < kMaxExpertPtrs; ++e) tbl->p[e] = nullptr;
+  return MOE_OK;
+}
+}  // namespace
+
+extern "C" {
+
+moe_status mxfp8_quantize_experts(const void* const* w, int32_t E, int32_t rows, int32_t cols, uint8_t* codes,
+                                  uint8_t* scales, uint8_t* codes_t, uint8_t* scales_t, moe_stream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE_PTR(codes);
+  REQUIRE_PTR(scales);
+  if ((codes_t == nullptr) != (scales_t == nullptr))
+    return fail(MOE_ERR_INVALID_ARG, "codes_t and scales_t must both be given or both be NULL");
+  if (codes_t != nullptr) {
+    REQUIRE_PTR(codes_t);
+    REQUIRE_PTR(scales_t);
+  }
+  if (rows < 128 || cols < 128 || rows % 128 || cols % 128)
+    return fail(MOE_ERR_UNSUPPORTED, "rows=%d cols=%d: need multiples of 128", rows, cols);
+  if (int64_t(E) * rows > (int64_t(1) << 31) || int64_t(E) * cols > (int64_t(1) << 31))
+    return fail(MOE_ERR_UNSUPPORTED, "tensor too large");
+  ExpertSrc tbl;
+  moe_status s = expert_table(w, E, &tbl);
+  if (s != MOE_OK) return s;
+  CUDA_TRY(launch_quant_dual_experts(tbl, E, rows, cols, codes, scales, codes_t, scales_t,
+                                     static_cast<cudaStream_t>(stream)),
+           "quant_dual (per-expert pointers)");
+  return MOE_OK;
+}
+
+moe_status fp8_tensor_quantize_experts(const void* const* w, int32_t E, int32_t rows, int32_t cols, uint8_t* codes,
+                                       float* amax, moe_stream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE_PTR(codes);
+  if (amax == nullptr) return fail(MOE_ERR_INVALID_ARG, "amax is NULL");
+  if (rows < 1 || cols < 8 || cols % 8)
+    return fail(MOE_ERR_UNSUPPORTED, "rows=%d cols=%d: need rows >= 1 and cols a multiple of 8", rows, cols);
+  ExpertSrc tbl;
+  moe_status s = expert_table(w, E, &tbl);
+  if (s != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t per = int64_t(rows) * cols;
+  uint32_t* am = reinterpret_cast<uint32_t*>(amax);
+  CUDA_TRY(cudaMemsetAsync(am, 0, sizeof(uint32_t) * size_t(E), st), "clear amax");
+  CUDA_TRY(launch_t8_amax_experts(tbl, E, per, am, st), "per-tensor amax (per-expert pointers)");
+  CUDA_TRY(launch_t8_quant_experts(tbl, E, per, am, codes, st), "per-tensor quantize (per-expert pointers)");
+  return MOE_OK;
+}
+
 moe_status moe_route_permute(const moe_dims* d, const float* logits, const void* x, int32_t* idx, float* prob,
                              int32_t* split_sizes, int32_t* row_of, int32_t* src_of, float* prob_perm,
                              uint8_t* xq, uint8_t* xq_scale, uint8_t* xq_col, uint8_t* xq_col_scale,

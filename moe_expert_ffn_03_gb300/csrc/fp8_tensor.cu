@@ -113,11 +113,13 @@ __global__ void __launch_bounds__(256) t8_quant_tokens_kernel(
 }
 
 // ---- per-slice amax and codes of a batch of tensors (the experts' weights) -------------
-__global__ void __launch_bounds__(256) t8_amax_batches_kernel(const __nv_bfloat16* __restrict__ src,
-                                                              int64_t per_batch, uint32_t* __restrict__ amax) {
+// Src: StackedSrc or ExpertSrc (one pointer per expert's tensor).
+template <class Src>
+__global__ void __launch_bounds__(256) t8_amax_batches_kernel(const __grid_constant__ Src src, int64_t per_batch,
+                                                              uint32_t* __restrict__ amax) {
   __shared__ uint32_t s_warp[8];
   const int64_t b = blockIdx.y;
-  const uint4* p = reinterpret_cast<const uint4*>(src + b * per_batch);
+  const uint4* p = reinterpret_cast<const uint4*>(src.mat(b));
   const int64_t n = per_batch / 8;
   uint32_t m2 = 0;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
@@ -131,12 +133,13 @@ __global__ void __launch_bounds__(256) t8_amax_batches_kernel(const __nv_bfloat1
   }
 }
 
-__global__ void __launch_bounds__(256) t8_quant_batches_kernel(const __nv_bfloat16* __restrict__ src,
-                                                               int64_t per_batch, const uint32_t* __restrict__ amax,
+template <class Src>
+__global__ void __launch_bounds__(256) t8_quant_batches_kernel(const __grid_constant__ Src src, int64_t per_batch,
+                                                               const uint32_t* __restrict__ amax,
                                                                uint8_t* __restrict__ codes) {
   const int64_t b = blockIdx.y;
   const float s = t8_scale(amax[b]);
-  const uint4* p = reinterpret_cast<const uint4*>(src + b * per_batch);
+  const uint4* p = reinterpret_cast<const uint4*>(src.mat(b));
   uint2* q = reinterpret_cast<uint2*>(codes + b * per_batch);
   const int64_t n = per_batch / 8;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
@@ -210,19 +213,42 @@ cudaError_t launch_t8_quant_tokens(const void* x, int T, int H, const int* idx, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_t8_amax_batches(const void* src, int batch, int64_t per_batch, uint32_t* amax, cudaStream_t st) {
+namespace {
+template <class Src>
+cudaError_t amax_batches(const Src& src, int batch, int64_t per_batch, uint32_t* amax, cudaStream_t st) {
   const int64_t chunks = (per_batch / 8 + 255) / 256;
   const dim3 grid(unsigned(chunks < 1024 ? chunks : 1024), unsigned(batch));
-  t8_amax_batches_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), per_batch, amax);
+  t8_amax_batches_kernel<Src><<<grid, 256, 0, st>>>(src, per_batch, amax);
   return cudaGetLastError();
+}
+template <class Src>
+cudaError_t quant_batches(const Src& src, int batch, int64_t per_batch, const uint32_t* amax, uint8_t* codes,
+                          cudaStream_t st) {
+  const int64_t chunks = (per_batch / 8 + 255) / 256;
+  const dim3 grid(unsigned(chunks < 2048 ? chunks : 2048), unsigned(batch));
+  t8_quant_batches_kernel<Src><<<grid, 256, 0, st>>>(src, per_batch, amax, codes);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_t8_amax_batches(const void* src, int batch, int64_t per_batch, uint32_t* amax, cudaStream_t st) {
+  return amax_batches(StackedSrc{static_cast<const __nv_bfloat16*>(src), per_batch}, batch, per_batch, amax, st);
 }
 
 cudaError_t launch_t8_quant_batches(const void* src, int batch, int64_t per_batch, const uint32_t* amax,
                                     uint8_t* codes, cudaStream_t st) {
-  const int64_t chunks = (per_batch / 8 + 255) / 256;
-  const dim3 grid(unsigned(chunks < 2048 ? chunks : 2048), unsigned(batch));
-  t8_quant_batches_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), per_batch, amax, codes);
-  return cudaGetLastError();
+  return quant_batches(StackedSrc{static_cast<const __nv_bfloat16*>(src), per_batch}, batch, per_batch, amax, codes,
+                       st);
+}
+
+cudaError_t launch_t8_amax_experts(const ExpertSrc& src, int batch, int64_t per_batch, uint32_t* amax,
+                                   cudaStream_t st) {
+  return amax_batches(src, batch, per_batch, amax, st);
+}
+
+cudaError_t launch_t8_quant_experts(const ExpertSrc& src, int batch, int64_t per_batch, const uint32_t* amax,
+                                    uint8_t* codes, cudaStream_t st) {
+  return quant_batches(src, batch, per_batch, amax, codes, st);
 }
 
 cudaError_t launch_t8_quant_segments(const void* src, const int* split_sizes, int E, int64_t cap, int cols,

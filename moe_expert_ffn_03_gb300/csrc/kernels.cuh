@@ -10,6 +10,19 @@ namespace moe {
 constexpr size_t kLastErrorBytes = 512;
 char* last_error_buffer();
 
+// Sources of a batch of bf16 [rows][cols] matrices: one stacked tensor, or one
+// pointer per matrix (each expert's own weight tensor), passed by value.
+constexpr int kMaxExpertPtrs = 256;
+struct StackedSrc {
+  const __nv_bfloat16* base;
+  int64_t per;                                 // elements per matrix
+  __device__ __forceinline__ const __nv_bfloat16* mat(int64_t b) const { return base + b * per; }
+};
+struct ExpertSrc {
+  const __nv_bfloat16* p[kMaxExpertPtrs];
+  __device__ __forceinline__ const __nv_bfloat16* mat(int64_t b) const { return p[b]; }
+};
+
 cudaError_t launch_quant_rowwise(const void* src, int64_t n_rows, int cols, const int* row_of, int k, int64_t cap,
                                  uint8_t* codes, uint8_t* scales, int* err, cudaStream_t st);
 cudaError_t launch_fill_pad_rows(const int* split_sizes, int E, int cols, uint8_t* codes, uint8_t* scales,
@@ -19,6 +32,9 @@ cudaError_t launch_quant_colwise(const void* src, const int* src_map, int64_t n_
                                  int* err, cudaStream_t st);
 cudaError_t launch_quant_dual(const void* src, int batch, int rows, int cols, uint8_t* codes, uint8_t* scales,
                               uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st);
+// codes_t / scales_t may be null (rows only)
+cudaError_t launch_quant_dual_experts(const ExpertSrc& src, int batch, int rows, int cols, uint8_t* codes,
+                                      uint8_t* scales, uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st);
 size_t router_partial_bytes(int E, int H);
 cudaError_t launch_router_fwd(const void* x, const void* w, int T, int H, int E, float* logits, cudaStream_t st);
 cudaError_t launch_router_bwd(const void* x, const void* w, const float* logits, const int* idx, const float* prob,
@@ -38,6 +54,10 @@ cudaError_t launch_t8_quant_tokens(const void* x, int T, int H, const int* idx, 
                                    int64_t cap, const uint32_t* amax, uint8_t* codes, int* err, cudaStream_t st);
 cudaError_t launch_t8_amax_batches(const void* src, int batch, int64_t per_batch, uint32_t* amax, cudaStream_t st);
 cudaError_t launch_t8_quant_batches(const void* src, int batch, int64_t per_batch, const uint32_t* amax,
+                                    uint8_t* codes, cudaStream_t st);
+cudaError_t launch_t8_amax_experts(const ExpertSrc& src, int batch, int64_t per_batch, uint32_t* amax,
+                                   cudaStream_t st);
+cudaError_t launch_t8_quant_experts(const ExpertSrc& src, int batch, int64_t per_batch, const uint32_t* amax,
                                     uint8_t* codes, cudaStream_t st);
 cudaError_t launch_t8_quant_segments(const void* src, const int* split_sizes, int E, int64_t cap, int cols,
                                      const uint32_t* amax, uint8_t* codes, cudaStream_t st);

@@ -182,8 +182,11 @@ __global__ void __launch_bounds__(256, 6) quant_colwise_kernel(
 // and (column, 32-row block) pairs into codes_t[cols][rows].  Each bf16 weight is
 // read once and both MX copies written: 2 B in, 2*(1 + 1/32) B out per element.
 // ---------------------------------------------------------------------------------
+// Src: StackedSrc (src[batch] of one tensor) or ExpertSrc (one pointer per matrix).
+// codes_t == nullptr: the rowwise orientation only.
+template <class Src>
 __global__ void __launch_bounds__(256, 6) quant_dual_kernel(
-    const __nv_bfloat16* __restrict__ src, int rows, int cols, uint8_t* __restrict__ codes,
+    const __grid_constant__ Src src, int rows, int cols, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t) {
   __shared__ __align__(16) __nv_bfloat16 tile[QC_TILE * QC_PITCH];
   __shared__ __align__(16) uint8_t sc_row[512];
@@ -191,13 +194,14 @@ __global__ void __launch_bounds__(256, 6) quant_dual_kernel(
   const int row0 = blockIdx.x * QC_TILE;
   const int col0 = blockIdx.y * QC_TILE;
   const int64_t batch = blockIdx.z;
-  const int64_t srow0 = batch * rows + row0;
+  const int64_t srow0 = batch * rows + row0;         // row of the stacked outputs
   {
+    const __nv_bfloat16* m = src.mat(batch);
     const int c16 = threadIdx.x & 15, rbase = threadIdx.x >> 4;
 #pragma unroll
     for (int it = 0; it < QC_TILE / 16; ++it) {
       const int r = rbase + 16 * it;
-      cp_async16(&tile[r * QC_PITCH + c16 * 8], src + (srow0 + r) * cols + col0 + c16 * 8, true);
+      cp_async16(&tile[r * QC_PITCH + c16 * 8], m + int64_t(row0 + r) * cols + col0 + c16 * 8, true);
     }
   }
   cp_async_wait_all();
@@ -222,7 +226,7 @@ __global__ void __launch_bounds__(256, 6) quant_dual_kernel(
     sc_row[((r & 31) << 4) + (((r >> 5) & 3) << 2) + b] = uint8_t(sc);
   }
   // colwise: task = (columns c, c+1) x 32-row block rb -- one per thread
-  {
+  if (codes_t != nullptr) {
     const int c = 2 * (threadIdx.x & 63), rb = threadIdx.x >> 6;
     const uint32_t* p = reinterpret_cast<const uint32_t*>(&tile[(rb * 32) * QC_PITCH + c]);
     uint32_t q_lo[8], q_hi[8];
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(256, 6) quant_dual_kernel(
   if (threadIdx.x < 32) {
     const int64_t atom = (srow0 >> 7) * (cols >> 7) + (col0 >> 7);
     reinterpret_cast<uint4*>(scales + (atom << 9))[threadIdx.x] = reinterpret_cast<const uint4*>(sc_row)[threadIdx.x];
-  } else if (threadIdx.x < 64) {
+  } else if (threadIdx.x < 64 && codes_t != nullptr) {
     const int64_t atom = ((batch * cols + col0) >> 7) * (rows >> 7) + (row0 >> 7);
     reinterpret_cast<uint4*>(scales_t + (atom << 9))[threadIdx.x - 32] =
         reinterpret_cast<const uint4*>(sc_col)[threadIdx.x - 32];
@@ -280,8 +284,15 @@ cudaError_t launch_quant_colwise(const void* src, const int* src_map, int64_t n_
 cudaError_t launch_quant_dual(const void* src, int batch, int rows, int cols, uint8_t* codes, uint8_t* scales,
                               uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st) {
   dim3 grid(rows / QC_TILE, cols / QC_TILE, batch);
-  quant_dual_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, cols, codes, scales, codes_t,
-                                          scales_t);
+  const StackedSrc s{static_cast<const __nv_bfloat16*>(src), int64_t(rows) * cols};
+  quant_dual_kernel<StackedSrc><<<grid, 256, 0, st>>>(s, rows, cols, codes, scales, codes_t, scales_t);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_dual_experts(const ExpertSrc& src, int batch, int rows, int cols, uint8_t* codes,
+                                      uint8_t* scales, uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st) {
+  dim3 grid(rows / QC_TILE, cols / QC_TILE, batch);
+  quant_dual_kernel<ExpertSrc><<<grid, 256, 0, st>>>(src, rows, cols, codes, scales, codes_t, scales_t);
   return cudaGetLastError();
 }
 

@@ -73,7 +73,16 @@ class ExpertFFN:
 
     # ---- steps -------------------------------------------------------------------
     def quantize_weights(self, w_gu, w_d, stream=None):
+        """MX copies of the master weights: stacked tensors [E][2I][H] and [E][H][I], or
+        lists of E per-expert tensors [2I][H] and [H][I]."""
         E, H, I = self.E, self.H, self.I
+        if isinstance(w_gu, (list, tuple)):
+            t = self.training
+            B.mxfp8_quantize_experts(w_gu, 2 * I, H, self.wgu_q, self.wgu_s, self.wguT_q if t else None,
+                                     self.wguT_s if t else None, stream)
+            B.mxfp8_quantize_experts(w_d, H, I, self.wd_q, self.wd_s, self.wdT_q if t else None,
+                                     self.wdT_s if t else None, stream)
+            return
         if self.training:
             B.mxfp8_quantize_dual(w_gu, E, 2 * I, H, self.wgu_q, self.wgu_s, self.wguT_q, self.wguT_s, stream)
             B.mxfp8_quantize_dual(w_d, E, H, I, self.wd_q, self.wd_s, self.wdT_q, self.wdT_s, stream)
@@ -135,6 +144,10 @@ class ExpertFFN:
             self.t8_wd = torch.empty(self.E, self.H, self.I, dtype=U8, device=dev)
             self.t8_amax_gu = torch.empty(self.E, dtype=torch.float32, device=dev)
             self.t8_amax_d = torch.empty(self.E, dtype=torch.float32, device=dev)
+        if isinstance(w_gu, (list, tuple)):
+            B.fp8_tensor_quantize_experts(w_gu, 2 * self.I, self.H, self.t8_wgu, self.t8_amax_gu, stream)
+            B.fp8_tensor_quantize_experts(w_d, self.H, self.I, self.t8_wd, self.t8_amax_d, stream)
+            return
         B.fp8_tensor_quantize(w_gu, self.E, 2 * self.I, self.H, self.t8_wgu, self.t8_amax_gu, stream)
         B.fp8_tensor_quantize(w_d, self.E, self.H, self.I, self.t8_wd, self.t8_amax_d, stream)
 

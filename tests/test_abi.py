@@ -89,3 +89,22 @@ def test_selftest_checks_arguments_before_launch(lib):
     s = lib.moe_selftest_wait_timeout(ctypes.c_void_p(256), 1 << 20, 10, ctypes.byref(code),
                                       ctypes.byref(site), None)
     assert s == 1                                                     # limit out of range
+
+
+def test_expert_pointer_arrays_checked_on_the_host(lib):
+    P = ctypes.c_void_p
+    good = (P * 2)(256, 512)
+    s = lib.mxfp8_quantize_experts(None, 2, 128, 128, P(256), P(256), None, None, None)
+    assert s == 1                                                     # no pointer array
+    s = lib.mxfp8_quantize_experts(good, 0, 128, 128, P(256), P(256), None, None, None)
+    assert s == 2                                                     # E out of range
+    s = lib.mxfp8_quantize_experts((P * 2)(256, 520), 2, 128, 128, P(256), P(256), None, None, None)
+    assert s == 3 and b"expert 1" in lib.moe_last_error_message()   # misaligned expert weight
+    s = lib.mxfp8_quantize_experts((P * 2)(256, None), 2, 128, 128, P(256), P(256), None, None, None)
+    assert s == 1 and b"expert 1" in lib.moe_last_error_message()
+    s = lib.mxfp8_quantize_experts(good, 2, 128, 128, P(256), P(256), P(256), None, None)
+    assert s == 1                                                     # codes_t without scales_t
+    s = lib.fp8_tensor_quantize_experts(good, 300, 128, 128, P(256), P(256), None)
+    assert s == 2
+    s = lib.fp8_tensor_quantize_experts(good, 2, 128, 100, P(256), P(256), None)
+    assert s == 2                                                     # cols not a multiple of 8

@@ -175,3 +175,22 @@ def test_quantization_error_against_unquantized_reference():
     err = rel_frob(f64(L.out), ref["out"])
     print(f"quantization error (rel Frobenius, out): {err:.4f}")
     assert err < 0.1
+
+
+def test_per_expert_weight_tensors_give_the_stacked_results():
+    """A training step with one weight tensor per expert (lists) is bit-identical to stacked weights."""
+    wl = configs.small(500, 256, 384, 6, 2, routing="biased", backward=True)
+    inp = {k: v.cuda() for k, v in synth.make_inputs(wl, 0).items()}
+    runs = []
+    for as_list in (False, True):
+        L = ExpertFFN(wl.T, wl.H, wl.I, wl.E, wl.k, training=True)
+        w_gu = [w.clone() for w in inp["w_gu"]] if as_list else inp["w_gu"]
+        w_d = [w.clone() for w in inp["w_d"]] if as_list else inp["w_d"]
+        L.quantize_weights(w_gu, w_d)
+        L.forward(inp["logits"], inp["x"])
+        L.backward(inp["dout"])
+        torch.cuda.synchronize()
+        assert L.device_error() == (0, 0)
+        runs.append([t.clone() for t in (L.out, L.dx, L.dwgu, L.dwd, L.dprob)])
+    for a, b in zip(*runs):
+        assert torch.equal(a, b)

@@ -120,3 +120,45 @@ def test_dual_every_bf16_pattern(seed):
     assert np.array_equal(untile_scales(scales.cpu().numpy(), 512, 128), rs)
     assert np.array_equal(codes_t.cpu().numpy().reshape(128, 512), cc.T)
     assert np.array_equal(untile_scales(scales_t.cpu().numpy(), 128, 512), cs.T)
+
+
+@pytest.mark.parametrize("both", [True, False])
+def test_per_expert_pointers_equal_the_stacked_tensor(both):
+    """One tensor per expert, allocated separately, gives the stacked results bit for bit."""
+    E, R, C = 5, 256, 384
+    g = torch.Generator().manual_seed(11)
+    experts = [(torch.randn(R, C, generator=g) * 0.02 * (e + 1)).to(torch.bfloat16).cuda() for e in range(E)]
+    pad = [torch.empty(1000 + 37 * e, dtype=torch.uint8, device="cuda") for e in range(E)]   # scatter the allocations
+    stacked = torch.stack(experts)
+    c0 = torch.empty(E * R * C, dtype=torch.uint8, device="cuda")
+    s0 = torch.empty(E * R * C // 32, dtype=torch.uint8, device="cuda")
+    c1, s1 = torch.empty_like(c0), torch.empty_like(s0)
+    d0, t0, d1, t1 = (torch.full_like(c0, 0xEE), torch.full_like(s0, 0xEE), torch.full_like(c0, 0xEE),
+                      torch.full_like(s0, 0xEE))
+    B.mxfp8_quantize_dual(stacked, E, R, C, c0, s0, c1, s1)
+    if both:
+        B.mxfp8_quantize_experts(experts, R, C, d0, t0, d1, t1)
+    else:
+        B.mxfp8_quantize_experts(experts, R, C, d0, t0)
+    torch.cuda.synchronize()
+    assert torch.equal(c0, d0) and torch.equal(s0, t0)
+    if both:
+        assert torch.equal(c1, d1) and torch.equal(s1, t1)
+    else:
+        assert bool((d1 == 0xEE).all()) and bool((t1 == 0xEE).all())   # untouched
+    del pad
+
+
+def test_per_tensor_per_expert_pointers_equal_the_stacked_tensor():
+    E, R, C = 4, 128, 256
+    g = torch.Generator().manual_seed(12)
+    experts = [(torch.randn(R, C, generator=g) * 10.0 ** (e - 2)).to(torch.bfloat16).cuda() for e in range(E)]
+    stacked = torch.stack(experts)
+    c0 = torch.empty(E, R, C, dtype=torch.uint8, device="cuda")
+    c1 = torch.empty_like(c0)
+    a0 = torch.empty(E, dtype=torch.float32, device="cuda")
+    a1 = torch.empty_like(a0)
+    B.fp8_tensor_quantize(stacked, E, R, C, c0, a0)
+    B.fp8_tensor_quantize_experts(experts, R, C, c1, a1)
+    torch.cuda.synchronize()
+    assert torch.equal(c0, c1) and torch.equal(a0, a1)
