@@ -18,7 +18,8 @@
 //               tcgen05.mma.kind::mxf8f6f4.block_scale (M=128, N=256 or 128,
 //               K=32) accumulate in TMEM (fp32, 256 columns); tcgen05.commit
 //               frees the stage and, after the last K step, hands the
-//               accumulator to the epilogue.
+//               accumulator to the epilogue.  Kinds without scale factors
+//               (bf16, per-tensor E4M3) alternate two 256-column accumulators.
 //   warps 2..17 epilogue, four per TMEM lane quarter (32 rows), 64 accumulator
 //               columns each: tcgen05.ld into registers, release the
 //               accumulator at once (the next tile's MMAs start), then the
@@ -66,6 +67,9 @@ struct Ops {
   static constexpr bool NOSF = B16 || T8;         // no scale-factor loads or copies
   static constexpr bool SWIGLU_FWD = (EPI == EPI_FWD_SWIGLU || EPI == EPI_B16_FWD_SWIGLU || EPI == EPI_T8_FWD_SWIGLU);
   static constexpr int KSTEP = B16 ? 64 : 128;    // K elements per stage
+  // Kinds without scale factors leave TMEM to the accumulator: two 256-column
+  // buffers, so the next tile's MMAs run while the epilogue drains the last one.
+  static constexpr int ACC_BUFS = NOSF ? 2 : 1;
 };
 
 // Shared-memory layout per epilogue kind (all use 256-column tiles today; a
@@ -81,8 +85,8 @@ struct Lay {
   static constexpr int OFF_SFA = OFF_B + STG * B_T;
   static constexpr int OFF_SFB = OFF_SFA + STG * SF_ATOM;
   static constexpr int OFF_BAR = OFF_SFB + STG * SFB_T;
-  // full[S], empty[S], sf_ready[S], tmem_full, tmem_empty, drain (MMA), drain (scale copies)
-  static constexpr int NUM_BARS = 3 * STG + 4;
+  // full[S], empty[S], sf_ready[S], tmem_full[2], tmem_empty[2], drain (MMA), drain (scale copies)
+  static constexpr int NUM_BARS = 3 * STG + 6;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_SEG = OFF_MISC + 16;
   static constexpr int OFF_TR = OFF_SEG + 260 * 4;
@@ -595,9 +599,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* empty = full + L::STG;
   uint64_t* sf_ready = empty + L::STG;
-  uint64_t* tmem_full = sf_ready + L::STG;
-  uint64_t* tmem_empty = tmem_full + 1;
-  uint64_t* drain = tmem_empty + 1;
+  uint64_t* tmem_full = sf_ready + L::STG;       // one per accumulator buffer
+  uint64_t* tmem_empty = tmem_full + 2;
+  uint64_t* drain = tmem_empty + 2;
   uint64_t* drain_sf = drain + 1;
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_s = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
@@ -612,8 +616,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&empty[s], 1);
       mbar_init(&sf_ready[s], 1);
     }
-    mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, NUM_EPI_WARPS);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], NUM_EPI_WARPS);
+    }
     mbar_init(drain, 1);
     mbar_init(drain_sf, 1);
     *abort_s = 0;
@@ -695,7 +701,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
         Tile tl;
         decode_tile<EPI>(args, seg_mb, t, tl);
-        if (!wait_phase(tmem_empty, (tcount & 1) ^ 1, abort_s, args.err, SITE_GEMM_MMA_ACC, lim)) {
+        // accumulator buffer of this tile and how often it was used before
+        const int ab = Ops<EPI>::ACC_BUFS == 2 ? (tcount & 1) : 0;
+        const int use = Ops<EPI>::ACC_BUFS == 2 ? (tcount >> 1) : tcount;
+        const uint32_t acc = tmem + TM_ACC + uint32_t(ab) * 256u;
+        if (!wait_phase(&tmem_empty[ab], (use & 1) ^ 1, abort_s, args.err, SITE_GEMM_MMA_ACC, lim)) {
           ok = false;
           break;
         }
@@ -718,23 +728,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int kk = 0; kk < BK / 32; ++kk) {
             // +32 bytes along K inside the 128-byte swizzle atom = +2 in the encoded start address
             if (Ops<EPI>::B16) {
-              tc_mma_bf16(tmem + TM_ACC, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_bf16(n),
-                          (kt | kk) != 0);
+              tc_mma_bf16(acc, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_bf16(n), (kt | kk) != 0);
               continue;
             }
             if (Ops<EPI>::T8) {
-              tc_mma_f8(tmem + TM_ACC, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_f8(n),
-                        (kt | kk) != 0);
+              tc_mma_f8(acc, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_f8(n), (kt | kk) != 0);
               continue;
             }
-            tc_mma_mxf8(tmem + TM_ACC, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_mxf8(n, kk),
-                        tm_sfa, tm_sfb, (kt | kk) != 0);
+            tc_mma_mxf8(acc, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_mxf8(n, kk), tm_sfa, tm_sfb,
+                        (kt | kk) != 0);
           }
           issued = true;
           tc_commit(&empty[s]);
         }
         if (!ok) break;
-        tc_commit(tmem_full);
+        tc_commit(&tmem_full[ab]);
       }
       if (!ok && issued) {
         tc_commit(drain);
@@ -795,9 +803,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(grow));
         asm volatile("prefetch.global.L2 [%0];" ::"l"(grow + args.I));
       }
-      if (!wait_phase(tmem_full, tcount & 1, abort_s, args.err, SITE_GEMM_EPILOGUE, lim)) break;
+      const int ab = Ops<EPI>::ACC_BUFS == 2 ? (tcount & 1) : 0;
+      const int use = Ops<EPI>::ACC_BUFS == 2 ? (tcount >> 1) : tcount;
+      if (!wait_phase(&tmem_full[ab], use & 1, abort_s, args.err, SITE_GEMM_EPILOGUE, lim)) break;
       tc_fence_after();
-      epilogue_tile<EPI>(args, tl, tmem_row, q, cg, lane, tmem_empty, tr);
+      epilogue_tile<EPI>(args, tl, tmem_row + uint32_t(ab) * 256u, q, cg, lane, &tmem_empty[ab], tr);
     }
   }
   tc_fence_before();
