@@ -144,6 +144,7 @@ def run_cuda(args):
 
     from moe_expert_ffn_03_gb300 import build, configs, synth
     from moe_expert_ffn_03_gb300.layer import LAUNCHES_PER_FORWARD_STEP, LAUNCHES_PER_TRAINING_STEP, ExpertFFN
+    from moe_expert_ffn_03_gb300.pipeline import HostPipeline
 
     world, rank, local = dist_setup(args.gpus)
     torch.cuda.set_device(local)
@@ -222,36 +223,74 @@ def run_cuda(args):
     n_gemm = 6 if train else 2
 
     # ---- end to end through the public API with pinned host buffers ----
-    host = {k: inp[k].cpu().pin_memory() for k in (("x", "logits", "dout") if train else ("x", "logits"))}
-    dev_in = {k: torch.empty_like(inp[k]) for k in host}
-    out_h = torch.empty(L.out.shape, dtype=L.out.dtype).pin_memory()
-    dx_h = torch.empty(L.dx.shape, dtype=L.dx.dtype).pin_memory() if train else None
-    bi = sum(t.numel() * t.element_size() for t in host.values())
-    bo = out_h.numel() * 2 + (dx_h.numel() * 2 if train else 0)
+    # HostPipeline: every step copies its inputs from pinned host memory and its results back;
+    # the copies of step i+1's inputs and step i's results overlap the kernels on a copy stream.
+    names = ("x", "logits", "dout") if train else ("x", "logits")
+    host_sets = [{k: inp[k].cpu().pin_memory() for k in names} for _ in range(2)]
+    out_sets = [{"out": torch.empty(L.out.shape, dtype=L.out.dtype).pin_memory(),
+                 "dx": torch.empty(L.dx.shape, dtype=L.dx.dtype).pin_memory() if train else None}
+                for _ in range(2)]
+    bi = sum(t.numel() * t.element_size() for t in host_sets[0].values())
+    bo = out_sets[0]["out"].numel() * 2 + (out_sets[0]["dx"].numel() * 2 if train else 0)
+    pipe = HostPipeline(L, inp["w_gu"], inp["w_d"], stream)
 
-    def e2e_step():
-        for k in host:
-            dev_in[k].copy_(host[k], non_blocking=True)
-        L.quantize_weights(inp["w_gu"], inp["w_d"])
-        L.forward(dev_in["logits"], dev_in["x"])
-        out_h.copy_(L.out, non_blocking=True)
-        if train:
-            L.backward(dev_in["dout"])
-            dx_h.copy_(L.dx, non_blocking=True)
+    def host_steps(n):
+        return [host_sets[i % 2] for i in range(n)], [out_sets[i % 2] for i in range(n)]
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    pipe.run(*host_steps(max(1, args.warmup)))
+    pipe.join()
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    pipe.run(*host_steps(args.steps), after=e0)
+    pipe.join()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
     e2e_value = replica_throughput(flops, e2e_ms, world) / 1e12
+
+    # the same steps with every copy in line on one stream, for comparison
+    dev_in = {k: torch.empty_like(inp[k]) for k in names}
+
+    def serial_step():
+        for k in names:
+            dev_in[k].copy_(host_sets[0][k], non_blocking=True)
+        L.quantize_weights(inp["w_gu"], inp["w_d"])
+        L.forward(dev_in["logits"], dev_in["x"])
+        out_sets[0]["out"].copy_(L.out, non_blocking=True)
+        if train:
+            L.backward(dev_in["dout"])
+            out_sets[0]["dx"].copy_(L.dx, non_blocking=True)
+
+    serial_step()
+    torch.cuda.synchronize()
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(args.steps):
+        serial_step()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    serial_ms = max_over_ranks(s0.elapsed_time(s1), world) / args.steps
+
+    # ---- the same step replayed as one CUDA graph (launch gaps removed) ----
+    graph = L.capture_step(inp["w_gu"], inp["w_d"], inp["logits"], inp["x"], inp.get("dout"))
+    for _ in range(max(1, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = max_over_ranks(g0.elapsed_time(g1), world) / args.steps
+    code, site = L.device_error()
+    if code != 0:
+        raise RuntimeError(f"device error {code} at site {site} (graph replay)")
 
     # ---- router on both sides (timed on its own; the step above starts from logits) ----
     router = None
@@ -353,10 +392,15 @@ def run_cuda(args):
                               "4 small quantize/reduce launches)",
                      "launches_per_step": n_gemm},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
-                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+                "api": "HostPipeline.run (copies overlapped on a copy stream)",
+                "serial_copies_ms_per_step": round(serial_ms, 4)},
         "gpu_launches": (LAUNCHES_PER_TRAINING_STEP if train else LAUNCHES_PER_FORWARD_STEP) * args.steps,
         "clocks": clocks,
     }
+    line["graph"] = {"ms_per_step": round(graph_ms, 4),
+                     "value": round(replica_throughput(flops, graph_ms, world) / 1e12, 2), "unit": "TFLOP/s",
+                     "how": "ExpertFFN.capture_step: the whole step as one CUDA graph, replayed"}
     line["bf16_forward"] = bf16_fwd
     line["fp8_tensor_forward"] = t8_fwd
     if router is not None:
@@ -368,9 +412,10 @@ def run_cuda(args):
 
 # ------------------------------------------------------------------------------------
 def cpu_baseline(tokens: int, wl=None):
-    """The oracle (numpy, float64) on a bounded sample: `tokens` tokens of the
-    workload's routing over its first two experts, full H and I, forward and
-    (when the workload trains) backward, weight quantization included."""
+    """The oracle (numpy, float64) on a bounded sample: `tokens` tokens routed to the
+    workload's first expert, full H and I, forward and (when the workload trains)
+    backward, weight quantization included (that quantization of a full expert is most
+    of the sample's time)."""
     import numpy as np
     import torch
 
@@ -379,7 +424,7 @@ def cpu_baseline(tokens: int, wl=None):
     from oracle import routing as rt
 
     wl = wl or configs.get(WORKLOAD)
-    E_s = 2
+    E_s = 1
     sub = configs.small(tokens, wl.H, wl.I, wl.E, wl.k, routing=wl.routing, backward=True)
     inp = synth.make_inputs(sub, seed=0, device="cpu")
     f64 = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
@@ -397,7 +442,7 @@ def cpu_baseline(tokens: int, wl=None):
     flops = (18.0 if wl.backward else 6.0) * tokens * k * wl.H * wl.I
     return {"value": round(flops / dt / 1e12, 5), "unit": "TFLOP/s", "cores": os.cpu_count(),
             "kind": "oracle", "seconds": round(dt, 2),
-            "sample": f"{tokens} tokens x top-{k} over 2 of the {wl.E} experts, H={wl.H}, I={wl.I}, "
+            "sample": f"{tokens} tokens x top-{k} over {E_s} of the {wl.E} experts, H={wl.H}, I={wl.I}, "
                       f"{'fwd+bwd' if wl.backward else 'fwd'} incl. weight quantization "
                       f"(numpy float64, BLAS threads = all host cores)"}
 

@@ -120,6 +120,29 @@ class ExpertFFN:
         self.combine_dx(stream)
         return self.dx
 
+    # ---- one step as a CUDA graph (for launch-bound sizes) -------------------------------
+    def step(self, w_gu, w_d, logits, x, dout=None, stream=None):
+        """quantize_weights + forward (+ backward when training) on the given tensors."""
+        self.quantize_weights(w_gu, w_d, stream)
+        self.forward(logits, x, stream)
+        if self.training:
+            self.backward(dout, stream)
+
+    def capture_step(self, w_gu, w_d, logits, x, dout=None) -> torch.cuda.CUDAGraph:
+        """Record step() on these tensors as one CUDA graph.  Every launch of the step is
+        replayed by graph.replay(); refill the same tensors in place between replays.
+        The step runs once eagerly first (on a side stream) so that one-time setup
+        (kernel attributes, driver entry points) happens outside the capture."""
+        side = torch.cuda.Stream(self.ws.device)
+        side.wait_stream(torch.cuda.current_stream(self.ws.device))
+        with torch.cuda.stream(side):
+            self.step(w_gu, w_d, logits, x, dout)
+        torch.cuda.current_stream(self.ws.device).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.step(w_gu, w_d, logits, x, dout)
+        return graph
+
     # ---- bf16 forward (no quantization), on the routing of route() ----------------------
     def forward_bf16(self, x, w_gu, w_d, stream=None):
         """After route(): gather x rows, bf16 grouped gate_up + ScaledSwiGLU + down, combine."""
