@@ -103,11 +103,13 @@ const char* moe_last_error_message(void);
 /* Rows of every permuted buffer: roundup(T*k, 128) + 128*E.  Host only. */
 size_t moe_rows_capacity(const moe_dims* d);
 
-/* Bytes of workspace needed by moe_route_permute, grouped_mlp_fwd and (when
- * training != 0) grouped_mlp_bwd for these sizes.  The workspace is caller
- * memory, 256-byte aligned, zero-filled once before first use (that clears
- * the device error word); it may be reused by later calls on the same
- * stream.  Host only. */
+/* Bytes of workspace needed for these sizes by moe_route_permute and the
+ * forward calls (training = 0), also by grouped_mlp_bwd and moe_router_bwd
+ * (training = 1), and also by grouped_mlp_bwd_bf16 (training = 2).  The
+ * workspace is caller memory, 256-byte aligned, zero-filled once before first
+ * use (that clears the device error word); it may be reused by later calls on
+ * the same stream.  Returns 0 for invalid sizes or training outside 0..2.
+ * Host only. */
 size_t moe_workspace_size(const moe_dims* d, int32_t training);
 
 /*
@@ -214,11 +216,46 @@ moe_status moe_gather_rows(const moe_dims* d, const void* x, const int32_t* row_
  *            weights as they are);
  *   a_perm   out bf16 [CAP][I]: a = silu(g)*u*p rounded to bf16 (the down
  *            GEMM's input);
- *   y        out bf16 [CAP][H].
+ *   y        out bf16 [CAP][H];
+ *   saved_gu out bf16 [CAP][2I] or NULL: g and u for grouped_mlp_bwd_bf16.
  */
 moe_status grouped_mlp_fwd_bf16(const moe_dims* d, const void* x_perm, const int32_t* split_sizes,
                                 const float* prob_perm, const void* w_gu, const void* w_d, void* a_perm, void* y,
-                                void* workspace, size_t workspace_bytes, moe_stream_t stream);
+                                void* saved_gu, void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * moe_transpose_bf16 -- dst[b][c][r] = src[b][r][c] for bf16 [batch][rows][cols]
+ * (rows, cols multiples of 128; 1 <= batch <= 65535).  The bf16 training path
+ * takes W_gu^T [E][H][2I] and W_d^T [E][I][H] from it, once per step, the way the
+ * MXFP8 path takes its transposed weight copies from mxfp8_quantize_dual.
+ */
+moe_status moe_transpose_bf16(const void* src, int32_t batch, int32_t rows, int32_t cols, void* dst,
+                              moe_stream_t stream);
+
+/*
+ * grouped_mlp_bwd_bf16 -- backward of grouped_mlp_fwd_bf16 (no quantization;
+ * every stored tensor bf16, every GEMM a tcgen05 kind::f16 MMA with f32
+ * accumulation).  The steps are those of grouped_mlp_bwd: dY = dout gathered
+ * to rows; dA = dY*W_d with the SwiGLU backward fused (dg = dA*p*u*silu'(g),
+ * du = dA*p*silu(g), dp = sum dA*silu(g)*u), writing dH = [dg|du] as bf16 rows
+ * and transposed; dW_d = dY^T*a and dW_gu = dH^T*x over each expert's tokens;
+ * dX = dH*W_gu.
+ *   dout            bf16 [T][H]
+ *   split_sizes, row_of, src_of, prob_perm: from moe_route_permute
+ *   saved_gu        bf16 [CAP][2I]: the saved_gu output of grouped_mlp_fwd_bf16
+ *   x_perm, a_perm  bf16 [CAP][H], [CAP][I]: from moe_gather_rows and
+ *                   grouped_mlp_fwd_bf16
+ *   w_guT, w_dT     bf16 [E][H][2I], [E][I][H]: moe_transpose_bf16 of W_gu, W_d
+ *   dx_perm         out bf16 [CAP][H]; combine it with moe_unpermute_combine
+ *   dwgu, dwd       out bf16 [E][2I][H], [E][H][I] (zeros for experts without tokens)
+ *   dprob           out f32 [T][k]
+ *   workspace       moe_workspace_size(d, 2) bytes (holds dY, dH and x, a transposed)
+ */
+moe_status grouped_mlp_bwd_bf16(const moe_dims* d, const void* dout, const int32_t* split_sizes,
+                                const int32_t* row_of, const int32_t* src_of, const float* prob_perm,
+                                const void* saved_gu, const void* x_perm, const void* a_perm, const void* w_guT,
+                                const void* w_dT, void* dx_perm, void* dwgu, void* dwd, float* dprob, void* workspace,
+                                size_t workspace_bytes, moe_stream_t stream);
 
 /*
  * mxfp8_quantize_experts -- mxfp8_quantize_dual for weights held as one tensor

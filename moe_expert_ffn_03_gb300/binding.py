@@ -20,7 +20,7 @@ EXPORTS = (
     "moe_unpermute_combine", "moe_get_device_error", "moe_clear_device_error", "moe_route_permute_noalloc",
     "moe_selftest_wait_timeout", "moe_router_fwd", "moe_router_bwd", "moe_gather_rows", "grouped_mlp_fwd_bf16",
     "fp8_tensor_quantize", "moe_fp8_tensor_quantize_tokens", "grouped_mlp_fwd_fp8_tensor",
-    "mxfp8_quantize_experts", "fp8_tensor_quantize_experts",
+    "mxfp8_quantize_experts", "fp8_tensor_quantize_experts", "moe_transpose_bf16", "grouped_mlp_bwd_bf16",
 )
 
 MOE_OK = 0
@@ -76,7 +76,9 @@ def lib() -> ctypes.CDLL:
             "moe_route_permute_noalloc": ([D, P, P, P, P, P, P, P, P, P, P, P, P, P], c_int32),
             "moe_router_fwd": ([D, P, P, P, P], c_int32),
             "moe_gather_rows": ([D, P, P, P, P, P, c_size_t, P], c_int32),
-            "grouped_mlp_fwd_bf16": ([D, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
+            "grouped_mlp_fwd_bf16": ([D, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
+            "moe_transpose_bf16": ([P, c_int32, c_int32, c_int32, P, P], c_int32),
+            "grouped_mlp_bwd_bf16": ([D] + [P] * 15 + [c_size_t, P], c_int32),
             "moe_router_bwd": ([D, P, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
             "fp8_tensor_quantize": ([P, c_int32, c_int32, c_int32, P, P, P], c_int32),
             "moe_fp8_tensor_quantize_tokens": ([D, P, P, P, P, P, P, P, c_size_t, P], c_int32),
@@ -175,9 +177,22 @@ def moe_gather_rows(d, x, row_of, split_sizes, x_perm, workspace, stream=None):
                                  workspace.numel() * workspace.element_size(), _st(stream)))
 
 
-def grouped_mlp_fwd_bf16(d, x_perm, split_sizes, prob_perm, w_gu, w_d, a_perm, y, workspace, stream=None):
+def grouped_mlp_fwd_bf16(d, x_perm, split_sizes, prob_perm, w_gu, w_d, a_perm, y, workspace, saved_gu=None,
+                         stream=None):
     _check(lib().grouped_mlp_fwd_bf16(ctypes.byref(d), _p(x_perm), _p(split_sizes), _p(prob_perm), _p(w_gu),
-                                      _p(w_d), _p(a_perm), _p(y), _p(workspace),
+                                      _p(w_d), _p(a_perm), _p(y), _p(saved_gu), _p(workspace),
+                                      workspace.numel() * workspace.element_size(), _st(stream)))
+
+
+def moe_transpose_bf16(src, batch, rows, cols, dst, stream=None):
+    _check(lib().moe_transpose_bf16(_p(src), batch, rows, cols, _p(dst), _st(stream)))
+
+
+def grouped_mlp_bwd_bf16(d, dout, split_sizes, row_of, src_of, prob_perm, saved_gu, x_perm, a_perm, w_guT, w_dT,
+                         dx_perm, dwgu, dwd, dprob, workspace, stream=None):
+    _check(lib().grouped_mlp_bwd_bf16(ctypes.byref(d), _p(dout), _p(split_sizes), _p(row_of), _p(src_of),
+                                      _p(prob_perm), _p(saved_gu), _p(x_perm), _p(a_perm), _p(w_guT), _p(w_dT),
+                                      _p(dx_perm), _p(dwgu), _p(dwd), _p(dprob), _p(workspace),
                                       workspace.numel() * workspace.element_size(), _st(stream)))
 
 

@@ -47,10 +47,13 @@ moe_status check_dims(const moe_dims* d) {
 struct WsLayout {
   size_t err, masks, bases, aq, aq_s;
   size_t dyq, dyq_s, dyqc, dyqc_s, dhq, dhq_s, dhqc, dhqc_s, dp, rpart;
+  size_t dy16, dy16c, dh16, dh16c, x16c, a16c;   // bf16 training: dY, dH and x, a transposed
   size_t total;
 };
 
-WsLayout ws_layout(const moe_dims* d, bool training) {
+// mode 0: forward; 1: MXFP8 training; 2: bf16 training (the MXFP8 buffers plus bf16 ones)
+WsLayout ws_layout(const moe_dims* d, int mode) {
+  const bool training = mode != 0;
   WsLayout w{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -79,14 +82,22 @@ WsLayout ws_layout(const moe_dims* d, bool training) {
     w.dp = take(ntI * 4 * cap * 4);                 // one partial row sum per 64-column group
     w.rpart = take(router_partial_bytes(d->E, d->H));   // router weight-gradient partials
   }
+  if (mode == 2) {
+    w.dy16 = take(cap * H * 2);
+    w.dy16c = take(H * cap * 2);
+    w.dh16 = take(cap * 2 * I * 2);
+    w.dh16c = take(2 * I * cap * 2);
+    w.x16c = take(H * cap * 2);
+    w.a16c = take(I * cap * 2);
+  }
   w.total = off;
   return w;
 }
 
-moe_status check_ws(const moe_dims* d, const void* ws, size_t bytes, bool training) {
+moe_status check_ws(const moe_dims* d, const void* ws, size_t bytes, int mode) {
   if (ws == nullptr) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(MOE_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
-  const size_t need = ws_layout(d, training).total;
+  const size_t need = ws_layout(d, mode).total;
   if (bytes < need) return fail(MOE_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", bytes, need);
   return MOE_OK;
 }
@@ -137,7 +148,8 @@ size_t moe_rows_capacity(const moe_dims* d) {
 
 size_t moe_workspace_size(const moe_dims* d, int32_t training) {
   if (check_dims(d) != MOE_OK) return 0;
-  return ws_layout(d, training != 0).total;
+  if (training < 0 || training > 2) return 0;
+  return ws_layout(d, training).total;
 }
 
 moe_status mxfp8_quantize(const void* src, int32_t batch, int32_t rows, int32_t cols, int32_t axis,
@@ -385,7 +397,7 @@ moe_status moe_gather_rows(const moe_dims* d, const void* x, const int32_t* row_
 
 moe_status grouped_mlp_fwd_bf16(const moe_dims* d, const void* x_perm, const int32_t* split_sizes,
                                 const float* prob_perm, const void* w_gu, const void* w_d, void* a_perm, void* y,
-                                void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+                                void* saved_gu, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
   g_msg[0] = 0;
   moe_status s = check_dims(d);
   if (s != MOE_OK) return s;
@@ -414,8 +426,10 @@ moe_status grouped_mlp_fwd_bf16(const moe_dims* d, const void* x_perm, const int
   g1.prob_perm = prob_perm;
   g1.out = static_cast<__nv_bfloat16*>(a_perm);
   g1.ldo = I;
+  g1.gu = static_cast<__nv_bfloat16*>(saved_gu);
   g1.I = I;
   g1.err = at<int>(workspace, w.err);
+  if (saved_gu != nullptr && !al16(saved_gu)) return fail(MOE_ERR_ALIGNMENT, "saved_gu is not 16-byte aligned");
   CUDA_TRY(launch_grouped_gemm(EPI_B16_FWD_SWIGLU, g1, x_perm, cap, H, w_gu, int64_t(E) * 2 * I, H,
                                (cap / 128) * g1.n_tiles, st, g_msg, sizeof(g_msg)),
            "bf16 grouped gate_up GEMM");
@@ -548,6 +562,143 @@ moe_status grouped_mlp_fwd_fp8_tensor(const moe_dims* d, const uint8_t* xq, cons
   CUDA_TRY(launch_grouped_gemm(EPI_T8_OUT, g2, aq, cap, I, wd_q, int64_t(E) * H, I, (cap / 128) * g2.n_tiles, st,
                                g_msg, sizeof(g_msg)),
            "per-tensor FP8 grouped down GEMM");
+  return MOE_OK;
+}
+
+moe_status moe_transpose_bf16(const void* src, int32_t batch, int32_t rows, int32_t cols, void* dst,
+                              moe_stream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE_PTR(src);
+  REQUIRE_PTR(dst);
+  if (batch < 1 || batch > 65535 || rows < 128 || cols < 128 || rows % 128 || cols % 128)
+    return fail(MOE_ERR_UNSUPPORTED, "batch=%d rows=%d cols=%d: need 1 <= batch <= 65535 and rows, cols multiples "
+                "of 128", batch, rows, cols);
+  if (int64_t(batch) * rows > (int64_t(1) << 31) || int64_t(batch) * cols > (int64_t(1) << 31))
+    return fail(MOE_ERR_UNSUPPORTED, "tensor too large");
+  CUDA_TRY(launch_transpose_bf16(src, nullptr, int64_t(batch) * rows, batch, rows, cols, nullptr, 0, dst, nullptr,
+                                 static_cast<cudaStream_t>(stream)),
+           "transpose");
+  return MOE_OK;
+}
+
+moe_status grouped_mlp_bwd_bf16(const moe_dims* d, const void* dout, const int32_t* split_sizes,
+                                const int32_t* row_of, const int32_t* src_of, const float* prob_perm,
+                                const void* saved_gu, const void* x_perm, const void* a_perm, const void* w_guT,
+                                const void* w_dT, void* dx_perm, void* dwgu, void* dwd, float* dprob, void* workspace,
+                                size_t workspace_bytes, moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  REQUIRE_PTR(dout);
+  REQUIRE_PTR(split_sizes);
+  REQUIRE_PTR(row_of);
+  REQUIRE_PTR(src_of);
+  REQUIRE_PTR(prob_perm);
+  REQUIRE_PTR(saved_gu);
+  REQUIRE_PTR(x_perm);
+  REQUIRE_PTR(a_perm);
+  REQUIRE_PTR(w_guT);
+  REQUIRE_PTR(w_dT);
+  REQUIRE_PTR(dx_perm);
+  REQUIRE_PTR(dwgu);
+  REQUIRE_PTR(dwd);
+  REQUIRE_PTR(dprob);
+  s = check_ws(d, workspace, workspace_bytes, 2);
+  if (s != MOE_OK) return s;
+  const WsLayout w = ws_layout(d, 2);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t cap = capacity(d);
+  const int H = d->H, I = d->I, E = d->E, k = d->k;
+  int* err = at<int>(workspace, w.err);
+  void* dy = at<uint8_t>(workspace, w.dy16);
+  void* dyc = at<uint8_t>(workspace, w.dy16c);
+  __nv_bfloat16* dh = at<__nv_bfloat16>(workspace, w.dh16);
+  __nv_bfloat16* dhc = at<__nv_bfloat16>(workspace, w.dh16c);
+  void* xc = at<uint8_t>(workspace, w.x16c);
+  void* ac = at<uint8_t>(workspace, w.a16c);
+  float* dp = at<float>(workspace, w.dp);
+
+  // dY rows (gathered dout) and dY, x, a along tokens (transposed) for the weight gradients
+  CUDA_TRY(launch_gather_rows(dout, row_of, split_sizes, d->T, k, H, E, cap, dy, err, st), "dout gather rows");
+  CUDA_TRY(launch_transpose_bf16(dout, src_of, d->T, 1, int(cap), H, split_sizes, E, dyc, err, st),
+           "dout gather transposed");
+  CUDA_TRY(launch_transpose_bf16(x_perm, nullptr, cap, 1, int(cap), H, split_sizes, E, xc, err, st), "x transposed");
+  CUDA_TRY(launch_transpose_bf16(a_perm, nullptr, cap, 1, int(cap), I, split_sizes, E, ac, err, st), "a transposed");
+
+  // down dgrad + SwiGLU backward: dA = dY * W_d -> dH bf16 (rows and transposed), dp partials
+  GemmArgs g3{};
+  g3.mode = 0;
+  g3.E = E;
+  g3.split_sizes = split_sizes;
+  g3.K = H;
+  g3.N = I;
+  g3.n_tiles = (I + 255) / 256;
+  g3.b_rows_per_expert = I;
+  g3.cap = cap;
+  g3.prob_perm = prob_perm;
+  g3.out = dh;
+  g3.ldo = 2 * int64_t(I);
+  g3.out_t = dhc;
+  g3.gu = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(saved_gu));
+  g3.dp_part = dp;
+  g3.I = I;
+  g3.err = err;
+  CUDA_TRY(launch_grouped_gemm(EPI_B16_BWD_SWIGLU, g3, dy, cap, H, w_dT, int64_t(E) * I, H, (cap / 128) * g3.n_tiles,
+                               st, g_msg, sizeof(g_msg)),
+           "bf16 down dgrad GEMM");
+  CUDA_TRY(launch_dprob_reduce(dp, g3.n_tiles * 4, cap, row_of, int64_t(d->T) * k, dprob, err, st), "dprob reduce");
+
+  // down wgrad: dW_d[e] = dY_e^T a_e (K = the expert's tokens)
+  GemmArgs g4{};
+  g4.mode = 1;
+  g4.E = E;
+  g4.split_sizes = split_sizes;
+  g4.M = H;
+  g4.N = I;
+  g4.n_tiles = (I + 255) / 256;
+  g4.cap = cap;
+  g4.out = static_cast<__nv_bfloat16*>(dwd);
+  g4.ldo = I;
+  g4.I = I;
+  g4.err = err;
+  CUDA_TRY(launch_grouped_gemm(EPI_B16_OUT, g4, dyc, H, cap, ac, I, cap, int64_t(E) * (H / 128) * g4.n_tiles, st,
+                               g_msg, sizeof(g_msg)),
+           "bf16 down wgrad GEMM");
+
+  // gate_up dgrad: dX = dH * W_gu (K = 2I)
+  GemmArgs g5{};
+  g5.mode = 0;
+  g5.E = E;
+  g5.split_sizes = split_sizes;
+  g5.K = 2 * I;
+  g5.N = H;
+  g5.n_tiles = (H + 255) / 256;
+  g5.b_rows_per_expert = H;
+  g5.cap = cap;
+  g5.out = static_cast<__nv_bfloat16*>(dx_perm);
+  g5.ldo = H;
+  g5.I = I;
+  g5.err = err;
+  CUDA_TRY(launch_grouped_gemm(EPI_B16_OUT, g5, dh, cap, 2 * int64_t(I), w_guT, int64_t(E) * H, 2 * int64_t(I),
+                               (cap / 128) * g5.n_tiles, st, g_msg, sizeof(g_msg)),
+           "bf16 gate_up dgrad GEMM");
+
+  // gate_up wgrad: dW_gu[e] = dH_e^T x_e (K = the expert's tokens)
+  GemmArgs g6{};
+  g6.mode = 1;
+  g6.E = E;
+  g6.split_sizes = split_sizes;
+  g6.M = 2 * I;
+  g6.N = H;
+  g6.n_tiles = (H + 255) / 256;
+  g6.cap = cap;
+  g6.out = static_cast<__nv_bfloat16*>(dwgu);
+  g6.ldo = H;
+  g6.I = I;
+  g6.err = err;
+  CUDA_TRY(launch_grouped_gemm(EPI_B16_OUT, g6, dhc, 2 * int64_t(I), cap, xc, H, cap,
+                               int64_t(E) * (2 * I / 128) * g6.n_tiles, st, g_msg, sizeof(g_msg)),
+           "bf16 gate_up wgrad GEMM");
   return MOE_OK;
 }
 

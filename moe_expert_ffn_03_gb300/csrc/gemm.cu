@@ -62,14 +62,16 @@ constexpr int TR_WARP_FLOATS = 32 * TR_PITCH;
 // Per-tensor E4M3 kinds: 128 K elements per stage, kind::f8f6f4 MMA, no block scales.
 template <int EPI>
 struct Ops {
-  static constexpr bool B16 = (EPI == EPI_B16_OUT || EPI == EPI_B16_FWD_SWIGLU);
+  static constexpr bool B16 = (EPI == EPI_B16_OUT || EPI == EPI_B16_FWD_SWIGLU || EPI == EPI_B16_BWD_SWIGLU);
+  static constexpr bool SWIGLU_BWD = (EPI == EPI_BWD_SWIGLU || EPI == EPI_B16_BWD_SWIGLU);
   static constexpr bool T8 = (EPI == EPI_T8_OUT || EPI == EPI_T8_FWD_SWIGLU);
   static constexpr bool NOSF = B16 || T8;         // no scale-factor loads or copies
   static constexpr bool SWIGLU_FWD = (EPI == EPI_FWD_SWIGLU || EPI == EPI_B16_FWD_SWIGLU || EPI == EPI_T8_FWD_SWIGLU);
   static constexpr int KSTEP = B16 ? 64 : 128;    // K elements per stage
   // Kinds without scale factors leave TMEM to the accumulator: two 256-column
   // buffers, so the next tile's MMAs run while the epilogue drains the last one.
-  static constexpr int ACC_BUFS = NOSF ? 2 : 1;
+  // The SwiGLU-backward kinds park half their columns in TMEM and keep one buffer.
+  static constexpr int ACC_BUFS = (NOSF && !SWIGLU_BWD) ? 2 : 1;
 };
 
 // Shared-memory layout per epilogue kind (all use 256-column tiles today; a
@@ -447,6 +449,28 @@ __device__ __forceinline__ void quant_col_block(const float* v, uint8_t* codes_t
 // quantizer (3 mantissa bits) or a bf16 store.  For g below about -87 the
 // denominator passes 2^126 and it returns 0 (the exact value there is below
 // 1e-35 in magnitude).
+// The same 32 columns stored transposed as bf16 (the bf16 path's along-token copy):
+// column col+i becomes row col+i of [cols][cap]; through the warp's transpose
+// buffer eight columns at a time, lane (c = lane/4, g = lane%4) writes rows
+// 8g..8g+7 of column c as one 16-byte store.
+__device__ __forceinline__ void store_col_bf16(const float* v, __nv_bfloat16* out_t, int64_t row_blk0, int64_t col,
+                                               int64_t cap, int lane, float* tr) {
+  const int c = lane >> 2, g = lane & 3;
+#pragma unroll
+  for (int rnd = 0; rnd < 4; ++rnd) {
+#pragma unroll
+    for (int t = 0; t < 8; ++t) tr[lane * TR_PITCH + t] = v[8 * rnd + t];
+    __syncwarp();
+    float w[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) w[t] = tr[(8 * g + t) * TR_PITCH + c];
+    __syncwarp();
+    const int64_t crow = col + 8 * rnd + c;
+    *reinterpret_cast<uint4*>(out_t + crow * cap + row_blk0 + 8 * g) =
+        make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+  }
+}
+
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // One epilogue warp on one tile.  The warp owns TMEM lane quarter q (32 rows) and
@@ -468,7 +492,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     tmem_ld32_async(tmem_row + TM_ACC + cg * 32, r);
     tmem_ld32_async(tmem_row + TM_ACC + 128 + cg * 32, r + 32);
     tmem_wait_ld<64>(r);
-  } else if (EPI == EPI_BWD_SWIGLU) {
+  } else if (Ops<EPI>::SWIGLU_BWD) {
     // 64 columns do not fit the register budget next to the SwiGLU-backward math:
     // park the second 32 in this warp's spare TMEM columns, then free the accumulator
     have = c0 < ncols;
@@ -524,10 +548,15 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     amax = __reduce_max_sync(0xFFFFFFFFu, amax);
     if (lane == 0 && amax != 0u) atomicMax(a.amax_out + tl.e, amax);
   } else if (EPI == EPI_B16_FWD_SWIGLU) {
-    // bf16 path: a = silu(g)*u*p stored as bf16 [cap][I] in out
+    // bf16 path: a = silu(g)*u*p stored as bf16 [cap][I] in out (and g, u saved for the backward)
     const float p = a.prob_perm[row];
     const int64_t col = tl.n0 + cg * 32;
     float* f = reinterpret_cast<float*>(r);
+    if (a.gu != nullptr) {
+      const int64_t twoI = 2 * int64_t(a.I);
+      store_bf16x32(a.gu + row * twoI + col, f);
+      store_bf16x32(a.gu + row * twoI + a.I + col, f + 32);
+    }
 #pragma unroll
     for (int i = 0; i < 32; ++i) f[i] = silu_f(f[i]) * f[32 + i] * p;
     store_bf16x32(a.out + row * a.ldo + col, f);
@@ -544,7 +573,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     for (int i = 0; i < 32; ++i) f[i] = silu_f(f[i]) * f[32 + i] * p;
     quant_row_block(f, a.q_row, a.q_row_s, row, col, a.q_row_K);
     if (a.q_col != nullptr) quant_col_block(f, a.q_col, a.q_col_s, row_blk0, col, a.cap, lane, tr);
-  } else {  // EPI_BWD_SWIGLU: this warp's 64 columns of dA, as two halves of 32
+  } else {  // SwiGLU backward (MX or bf16 dH): this warp's 64 columns of dA, as two halves of 32
     float dp = 0.f;
     if (have) {
       const float p = a.prob_perm[row];
@@ -578,11 +607,18 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
             r[i] = __float_as_uint(d * p * sg);            // du = dA*p*silu(g)
           }
         }
-        quant_row_block(o, a.q_row, a.q_row_s, row, col, twoI);
-        quant_col_block(o, a.q_col, a.q_col_s, row_blk0, col, a.cap, lane, tr);
         const float* du = reinterpret_cast<const float*>(r);
-        quant_row_block(du, a.q_row, a.q_row_s, row, a.I + col, twoI);
-        quant_col_block(du, a.q_col, a.q_col_s, row_blk0, a.I + col, a.cap, lane, tr);
+        if (EPI == EPI_B16_BWD_SWIGLU) {
+          store_bf16x32(a.out + row * twoI + col, o);
+          store_col_bf16(o, a.out_t, row_blk0, col, a.cap, lane, tr);
+          store_bf16x32(a.out + row * twoI + a.I + col, du);
+          store_col_bf16(du, a.out_t, row_blk0, a.I + col, a.cap, lane, tr);
+        } else {
+          quant_row_block(o, a.q_row, a.q_row_s, row, col, twoI);
+          quant_col_block(o, a.q_col, a.q_col_s, row_blk0, col, a.cap, lane, tr);
+          quant_row_block(du, a.q_row, a.q_row_s, row, a.I + col, twoI);
+          quant_col_block(du, a.q_col, a.q_col_s, row_blk0, a.I + col, a.cap, lane, tr);
+        }
       }
     }
     a.dp_part[(int64_t(tl.nb) * 4 + cg) * a.cap + row] = dp;
@@ -797,7 +833,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
       Tile tl;
       decode_tile<EPI>(args, seg_mb, t, tl);
-      if (EPI == EPI_BWD_SWIGLU) {
+      if (Ops<EPI>::SWIGLU_BWD) {
         // pull this thread's saved g and u (128 B each) toward L2 while the MMAs run
         const __nv_bfloat16* grow = args.gu + (tl.out_row + q * 32 + lane) * (2 * int64_t(args.I)) + tl.n0 + cg * 64;
         asm volatile("prefetch.global.L2 [%0];" ::"l"(grow));
@@ -869,7 +905,7 @@ cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64
                                 char* msg, size_t msg_len) {
   if (max_tiles <= 0) return cudaSuccess;
   CUtensorMap ma, mb;
-  const bool b16 = (epi == EPI_B16_OUT || epi == EPI_B16_FWD_SWIGLU);
+  const bool b16 = (epi == EPI_B16_OUT || epi == EPI_B16_FWD_SWIGLU || epi == EPI_B16_BWD_SWIGLU);
   if (!encode_map(&ma, A, a_rows, a_K, b16) || !encode_map(&mb, B, b_rows, b_K, b16)) {
     snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed (A %lld x %lld, B %lld x %lld)", (long long)a_rows,
              (long long)a_K, (long long)b_rows, (long long)b_K);
@@ -887,6 +923,7 @@ cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64
     case EPI_B16_FWD_SWIGLU: return launch_epi<EPI_B16_FWD_SWIGLU>(ma, mb, a, grid, st);
     case EPI_T8_OUT: return launch_epi<EPI_T8_OUT>(ma, mb, a, grid, st);
     case EPI_T8_FWD_SWIGLU: return launch_epi<EPI_T8_FWD_SWIGLU>(ma, mb, a, grid, st);
+    case EPI_B16_BWD_SWIGLU: return launch_epi<EPI_B16_BWD_SWIGLU>(ma, mb, a, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -61,6 +61,12 @@ cudaError_t launch_t8_quant_experts(const ExpertSrc& src, int batch, int64_t per
                                     uint8_t* codes, cudaStream_t st);
 cudaError_t launch_t8_quant_segments(const void* src, const int* split_sizes, int E, int64_t cap, int cols,
                                      const uint32_t* amax, uint8_t* codes, cudaStream_t st);
+// out[b*cols + c][r] = src row (b, r) column c for a batch of [rows][cols] bf16 matrices
+// (rows, cols multiples of 128); with src_map, row r of the single matrix comes from
+// src[src_map[r]] (-1: a zero row); with split_sizes, row tiles past the padded
+// segments are skipped.
+cudaError_t launch_transpose_bf16(const void* src, const int* src_map, int64_t n_src_rows, int batch, int rows,
+                                  int cols, const int* split_sizes, int E, void* out, int* err, cudaStream_t st);
 cudaError_t launch_dprob_reduce(const float* dp_part, int n_tiles, int64_t cap, const int* row_of, int64_t R,
                                 float* dprob, int* err, cudaStream_t st);
 
@@ -86,6 +92,7 @@ enum Epilogue : int {
   EPI_B16_FWD_SWIGLU = 4,
   EPI_T8_OUT = 5,
   EPI_T8_FWD_SWIGLU = 6,
+  EPI_B16_BWD_SWIGLU = 7,    // bf16 operands; SwiGLU backward writing bf16 dH to out [cap][2I] and out_t [2I][cap]
 };
 
 struct GemmArgs {
@@ -105,6 +112,7 @@ struct GemmArgs {
   // epilogue operands
   __nv_bfloat16* out;        // EPI_BF16 output
   int64_t ldo;
+  __nv_bfloat16* out_t;      // EPI_B16_BWD_SWIGLU: dH transposed [2I][cap]
   const float* prob_perm;    // SwiGLU epilogues
   uint8_t* q_row;            // rowwise MX output (codes) [cap][q_row_K]
   uint8_t* q_row_s;

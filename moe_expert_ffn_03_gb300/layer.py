@@ -27,9 +27,11 @@ LAUNCHES_PER_FORWARD_STEP = 10
 class ExpertFFN:
     """Buffers of one layer for fixed sizes (T, H, I, E, k) on one device."""
 
-    def __init__(self, T, H, I, E, k, training=True, renormalize=True, device="cuda"):
+    def __init__(self, T, H, I, E, k, training=True, renormalize=True, device="cuda", bf16_training=False):
+        """bf16_training: also size the workspace for backward_bf16 (the bf16 training path)."""
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
         self.training = training
+        self.bf16_training = bool(training and bf16_training)
         self.d = B.dims(T, H, I, E, k, int(renormalize))
         self.cap = B.moe_rows_capacity(self.d)
         if self.cap == 0:
@@ -38,7 +40,7 @@ class ExpertFFN:
         dev = torch.device(device)
         z = lambda *s, dt: torch.zeros(*s, dtype=dt, device=dev)  # noqa: E731
         e = lambda *s, dt: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
-        self.ws = z(B.moe_workspace_size(self.d, training), dt=U8)
+        self.ws = z(B.moe_workspace_size(self.d, 2 if self.bf16_training else int(training)), dt=U8)
         self.idx = e(T, k, dt=torch.int32)
         self.prob = e(T, k, dt=torch.float32)
         self.split_sizes = e(E, dt=torch.int32)
@@ -154,9 +156,35 @@ class ExpertFFN:
             self.out_b16 = torch.empty(self.T, self.H, dtype=torch.bfloat16, device=dev)
         B.moe_gather_rows(self.d, x, self.row_of, self.split_sizes, self.x_perm, self.ws, stream)
         B.grouped_mlp_fwd_bf16(self.d, self.x_perm, self.split_sizes, self.prob_perm, w_gu, w_d, self.a_perm,
-                               self.y_b16, self.ws, stream)
+                               self.y_b16, self.ws, self.saved_gu if self.bf16_training else None, stream)
         B.moe_unpermute_combine(self.d, self.y_b16, self.row_of, None, self.out_b16, stream)
         return self.out_b16
+
+    # ---- bf16 training path: transposed weights once per step, then the backward ------------
+    def transpose_weights_bf16(self, w_gu, w_d, stream=None):
+        """W_gu^T [E][H][2I] and W_d^T [E][I][H] for backward_bf16 (once per step)."""
+        if not hasattr(self, "wguT16"):
+            dev = self.ws.device
+            self.wguT16 = torch.empty(self.E, self.H, 2 * self.I, dtype=torch.bfloat16, device=dev)
+            self.wdT16 = torch.empty(self.E, self.I, self.H, dtype=torch.bfloat16, device=dev)
+        B.moe_transpose_bf16(w_gu, self.E, 2 * self.I, self.H, self.wguT16, stream)
+        B.moe_transpose_bf16(w_d, self.E, self.H, self.I, self.wdT16, stream)
+
+    def backward_bf16(self, dout, stream=None):
+        """After forward_bf16 and transpose_weights_bf16 (layer built with bf16_training=True)."""
+        if not self.bf16_training:
+            raise RuntimeError("backward_bf16 needs ExpertFFN(..., bf16_training=True)")
+        if not hasattr(self, "dx16"):
+            dev = self.ws.device
+            self.dx16 = torch.empty(self.T, self.H, dtype=torch.bfloat16, device=dev)
+            self.dwgu16 = torch.empty(self.E, 2 * self.I, self.H, dtype=torch.bfloat16, device=dev)
+            self.dwd16 = torch.empty(self.E, self.H, self.I, dtype=torch.bfloat16, device=dev)
+            self.dprob16 = torch.empty(self.T, self.k, dtype=torch.float32, device=dev)
+        B.grouped_mlp_bwd_bf16(self.d, dout, self.split_sizes, self.row_of, self.src_of, self.prob_perm,
+                               self.saved_gu, self.x_perm, self.a_perm, self.wguT16, self.wdT16, self.dx_perm,
+                               self.dwgu16, self.dwd16, self.dprob16, self.ws, stream)
+        B.moe_unpermute_combine(self.d, self.dx_perm, self.row_of, None, self.dx16, stream)
+        return self.dx16
 
     # ---- per-tensor FP8 forward (one scale per expert operand tensor) ------------------
     def quantize_weights_fp8_tensor(self, w_gu, w_d, stream=None):

@@ -42,8 +42,9 @@ class Numerics:
     """quantized: MXFP8 quantizers on (False = identity quantizers).
     rounded: float32 quantizer inputs, bf16 saved g/u and bf16 outputs
     (False = pure float64, used by the finite-difference checks).
-    act_bf16: with quantizers off, the activations between the GEMMs are
-    rounded to bf16 instead (the BF16 path of the recipe)."""
+    act_bf16: with quantizers off, every tensor a GEMM consumes is rounded to
+    bf16 instead, along either axis (the BF16 path of the recipe stores its
+    activations and gradients in bf16)."""
     quantized: bool = True
     rounded: bool = True
     act_bf16: bool = False
@@ -83,10 +84,13 @@ def q_tokens(v, nm: Numerics):
     """Quantize-dequantize one expert's rows along the token axis (axis 0).
 
     Blocks of 32 consecutive rows start at the first row of the expert's
-    segment; a partial last block is padded with zero rows.
+    segment; a partial last block is padded with zero rows.  With quantizers
+    off: the identity, or bf16 rounding in the BF16 path.
     """
     v = np.asarray(v, dtype=np.float64)
-    if not nm.quantized or v.shape[0] == 0:
+    if not nm.quantized:
+        return mx.bf16(v) if nm.act_bf16 else v
+    if v.shape[0] == 0:
         return v
     m = v.shape[0]
     mp = -(-m // mx.BLOCK) * mx.BLOCK

@@ -43,3 +43,43 @@ def test_bf16_forward_matches_oracle(name_or_dims):
     assert_close(f64(L.a_perm)[:rows], ef.q_rowwise(fwd["a"], ef.BF16_PATH), "a (bf16)")
     assert_close(f64(L.y_b16)[:rows], fwd["y"], "y")
     assert_close(f64(out), fwd["out"], "out")
+
+
+@pytest.mark.parametrize("name_or_dims", [
+    configs.TINY,
+    (300, 256, 384, 6, 2, "biased"),
+    (513, 384, 640, 5, 3, "normal"),
+])
+def test_bf16_training_step_matches_oracle(name_or_dims):
+    """bf16 forward (saving g, u) + bf16 backward vs the oracle's BF16-path backward."""
+    wl = configs.get(name_or_dims) if isinstance(name_or_dims, str) else configs.small(*name_or_dims[:5],
+                                                                                         routing=name_or_dims[5])
+    inp = {k: v.cuda() for k, v in synth.make_inputs(wl, 0, with_grad=True).items()}
+    L = ExpertFFN(wl.T, wl.H, wl.I, wl.E, wl.k, training=True, bf16_training=True)
+    L.route(inp["logits"], inp["x"])
+    L.forward_bf16(inp["x"], inp["w_gu"], inp["w_d"])
+    L.transpose_weights_bf16(inp["w_gu"], inp["w_d"])
+    dx = L.backward_bf16(inp["dout"])
+    torch.cuda.synchronize()
+    assert L.device_error() == (0, 0)
+    idx, prob = rt.route_topk(inp["logits"].cpu().numpy(), wl.k)
+    fwd = ef.forward(f64(inp["x"]), idx, prob.astype(np.float64), f64(inp["w_gu"]), f64(inp["w_d"]), ef.BF16_PATH)
+    bwd = ef.backward(fwd, f64(inp["dout"]), ef.BF16_PATH)
+    rows = fwd["perm"]["rows"]
+    I = wl.I
+    assert_close(f64(L.saved_gu)[:rows, :I], fwd["g"], "g")
+    assert_close(f64(L.saved_gu)[:rows, I:], fwd["u"], "u")
+    assert_close(f64(dx), bwd["dx"], "dx")
+    assert_close(f64(L.dwgu16), bwd["dw_gu"], "dW_gu")
+    assert_close(f64(L.dwd16), bwd["dw_d"], "dW_d")
+    assert_close(L.dprob16.cpu().numpy().astype(np.float64), bwd["dprob"], "dprob")
+
+
+def test_transpose_bf16_is_exact():
+    g = torch.Generator().manual_seed(5)
+    w = torch.randn(3, 256, 384, generator=g).to(torch.bfloat16).cuda()
+    out = torch.empty(3, 384, 256, dtype=torch.bfloat16, device="cuda")
+    from moe_expert_ffn_03_gb300 import binding as B
+    B.moe_transpose_bf16(w, 3, 256, 384, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, w.transpose(1, 2))

@@ -184,3 +184,24 @@ def test_quantization_error_is_small_but_nonzero():
     for key in ("dx", "dw_gu", "dw_d", "dprob"):
         rel = np.linalg.norm(bq[key] - br[key]) / np.linalg.norm(br[key])
         assert rel < 0.2, key
+
+
+def test_bf16_path_backward_is_the_exact_backward_up_to_bf16_rounding():
+    """The BF16-path backward rounds every stored tensor to bf16 (dY, dH, a and x along
+    either axis, g/u, the outputs) and nothing else: it lies within a few bf16 steps of
+    the exact (finite-difference-pinned) backward, and differs from it."""
+    rng = np.random.default_rng(21)
+    T, H, I, E, k = 96, 64, 96, 4, 2
+    x = mx.bf16(rng.standard_normal((T, H)))
+    w_gu = mx.bf16(rng.standard_normal((E, 2 * I, H)) * 0.1)
+    w_d = mx.bf16(rng.standard_normal((E, H, I)) * 0.1)
+    dout = mx.bf16(rng.standard_normal((T, H)) * 0.01)
+    idx, prob = rt.route_topk(rng.standard_normal((T, E)).astype(np.float32), k)
+    prob = prob.astype(np.float64)
+    b16 = ef.backward(ef.forward(x, idx, prob, w_gu, w_d, ef.BF16_PATH), dout, ef.BF16_PATH)
+    ex = ef.backward(ef.forward(x, idx, prob, w_gu, w_d, ef.EXACT), dout, ef.EXACT)
+    for key in ("dx", "dw_gu", "dw_d", "dprob"):
+        rel = np.linalg.norm(b16[key] - ex[key]) / np.linalg.norm(ex[key])
+        assert 1e-5 < rel < 2e-2, (key, rel)
+    # the along-token operands are rounded: dW_d sums products of bf16 dY and bf16 a
+    assert np.array_equal(ef.q_tokens(b16["dH"], ef.BF16_PATH), mx.bf16(b16["dH"]))
