@@ -34,10 +34,12 @@ sys.path.insert(0, ROOT)
 
 WORKLOAD = "mixtral_fwdbwd_T16384_H4096_I14336_E8_k2"
 METRIC = "grouped expert-MLP fwd+bwd TFLOP/s (MXFP8, algorithmic 18*R*H*I per step)"
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the gate_up forward
-# GEMM from the ncu capture summarised in profiles/ (None until captured for
-# the current kernel)
-GEMM_TRAFFIC_BYTES = None
+# dram__bytes_read.sum + dram__bytes_write.sum of the six grouped-GEMM launches of
+# one step of the default workload, like `achieved` (which is over the same six
+# launches): 6.851 GB from an ncu capture at T=4096, E=2 (every expert with the
+# full workload's 4096 rows), times 4 for E=8 (profiles/ holds the summary).
+# Set to None when the GEMM kernel changes, until it is captured again.
+GEMM_TRAFFIC_BYTES = 27_406_000_000
 
 
 def read_peaks():
@@ -153,7 +155,7 @@ def run_cuda(args):
     train = wl.backward
     dev = torch.device("cuda", local)
     inp = synth.make_inputs(wl, seed=0, device=dev)
-    L = ExpertFFN(wl.T, wl.H, wl.I, wl.E, wl.k, training=train, device=dev)
+    L = ExpertFFN(wl.T, wl.H, wl.I, wl.E, wl.k, training=train, device=dev, bf16_training=train)
     stream = torch.cuda.current_stream()
 
     ev = {}
@@ -339,6 +341,33 @@ def run_cuda(args):
                 "frac_of_bf16_peak": round(fwd_flops / (gem / n_b * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"], 4),
                 "mxfp8_grouped_mlp_fwd_ms": round(parts["grouped_mlp_fwd_ms"], 4)}
 
+    # ---- the whole training step with bf16 operands (no quantization), for comparison ----
+    bf16_train = None
+    if train:
+        def bf16_step():
+            L.transpose_weights_bf16(inp["w_gu"], inp["w_d"])
+            L.forward_bf16(inp["x"], inp["w_gu"], inp["w_d"])
+            L.backward_bf16(inp["dout"])
+
+        bf16_step()
+        torch.cuda.synchronize()
+        t0b = torch.cuda.Event(enable_timing=True)
+        t1b = torch.cuda.Event(enable_timing=True)
+        t0b.record(stream)
+        for _ in range(n_b):
+            bf16_step()
+        t1b.record(stream)
+        torch.cuda.synchronize()
+        b_ms = t0b.elapsed_time(t1b) / n_b
+        code, site = L.device_error()
+        if code != 0:
+            raise RuntimeError(f"device error {code} at site {site} (bf16 step)")
+        bf16_train = {"ms_per_step": round(b_ms, 4), "tflops": round(flops / (b_ms * 1e-3) / 1e12, 1),
+                      "frac_of_bf16_peak": round(flops / (b_ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"], 4),
+                      "timed": "weight transposes + gather + bf16 forward + bf16 backward + both combines "
+                               "(routing shared with the MXFP8 step, not timed here)",
+                      "mxfp8_ms_per_step": round(ms_step, 4)}
+
     # ---- the same forward with per-tensor FP8 operands (one dynamic scale per expert tensor) ----
     L.quantize_weights_fp8_tensor(inp["w_gu"], inp["w_d"])
     L.forward_fp8_tensor(inp["x"])
@@ -386,7 +415,9 @@ def run_cuda(args):
         "breakdown_ms": {k: round(v, 4) for k, v in parts.items()},
         "roofline": {"bound": "tensor", "kernel": f"grouped_gemm_kernel ({n_gemm} launches per step)",
                      "achieved": round(gemm_tflops, 2), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
-                     "frac": round(gemm_tflops / fp8_peak, 4), "traffic": GEMM_TRAFFIC_BYTES,
+                     "frac": round(gemm_tflops / fp8_peak, 4),
+                     "traffic": GEMM_TRAFFIC_BYTES if wl.name == WORKLOAD else None,
+                     "traffic_unit": "bytes per step over the six GEMM launches",
                      "peak_source": f"{src}: 2 x bf16_tflops_sustained (fp8/bf16 nominal ratio 4.5/2.25)",
                      "timed": "grouped_mlp_fwd + grouped_mlp_bwd calls (the backward call also holds "
                               "4 small quantize/reduce launches)",
@@ -403,6 +434,8 @@ def run_cuda(args):
                      "how": "ExpertFFN.capture_step: the whole step as one CUDA graph, replayed"}
     line["bf16_forward"] = bf16_fwd
     line["fp8_tensor_forward"] = t8_fwd
+    if bf16_train is not None:
+        line["bf16_training_step"] = bf16_train
     if router is not None:
         line["router"] = router
     if cpu is not None:
