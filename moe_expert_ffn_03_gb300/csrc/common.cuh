@@ -150,27 +150,9 @@ __device__ __forceinline__ float t8_scale(uint32_t amax_bits) {
   return a == 0.0f ? 1.0f : __fdiv_rn(448.0f, a);
 }
 
-// One value quantized with a known scale code (for blocks reduced across lanes).
-__device__ __forceinline__ uint32_t mx_quant1(float v, uint32_t c) {
-  if (c == 255u) return 0x7Fu;
-  return cvt_e4m3x2(v * mx_inv_scale(c), 0.0f) & 0xFFu;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, float (&v)[32]) {
-  const uint4* p4 = reinterpret_cast<const uint4*>(p);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 w = p4[i];
-    v[8 * i + 0] = bf16_lo(w.x); v[8 * i + 1] = bf16_hi(w.x);
-    v[8 * i + 2] = bf16_lo(w.y); v[8 * i + 3] = bf16_hi(w.y);
-    v[8 * i + 4] = bf16_lo(w.z); v[8 * i + 5] = bf16_hi(w.z);
-    v[8 * i + 6] = bf16_lo(w.w); v[8 * i + 7] = bf16_hi(w.w);
-  }
 }
 
 __device__ __forceinline__ void store_codes32(uint8_t* p, const uint32_t (&q)[8]) {
