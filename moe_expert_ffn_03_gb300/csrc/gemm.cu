@@ -55,6 +55,8 @@ constexpr uint32_t TM_SF0 = 256, TM_SF_STRIDE = 12;  // per stage: SFA 4 columns
 // for the second half of its accumulator columns in the SwiGLU-backward epilogue.
 constexpr uint32_t TM_STASH = 320;
 constexpr int GROUP_M = 8;
+constexpr int SEG_INTS = 260;                   // per-expert prefix of 128-row blocks (E <= 256, plus the total)
+constexpr int kMaxSegE = 256;                   // mode-1 expert order (heaviest first) follows the prefix
 constexpr int TR_PITCH = 9;                     // floats per row of a warp's 32x8 transpose buffer
 constexpr int TR_WARP_FLOATS = 32 * TR_PITCH;
 
@@ -90,8 +92,8 @@ struct Lay {
   // full[S], empty[S], sf_ready[S], tmem_full[2], tmem_empty[2], drain (MMA), drain (scale copies)
   static constexpr int NUM_BARS = 3 * STG + 6;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int OFF_SEG = OFF_MISC + 16;
-  static constexpr int OFF_TR = OFF_SEG + 260 * 4;
+  static constexpr int OFF_SEG = OFF_MISC + 16;             // seg_mb[SEG_INTS], then order[kMaxSegE]
+  static constexpr int OFF_TR = OFF_SEG + (SEG_INTS + kMaxSegE) * 4;
   static constexpr int SMEM_USED = OFF_TR + NUM_EPI_WARPS * TR_WARP_FLOATS * 4;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 B
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -322,10 +324,13 @@ __device__ __forceinline__ void decode_tile(const GemmArgs& a, const int* seg_mb
       tl.second = (tl.n0 + 128) < a.N;
     }
   } else {
+    // experts in order of decreasing token count (seg_mb is followed by that order), so the
+    // longest tiles are spread over the CTAs first and the short ones fill in at the end
     const int m_tiles = a.M / BM;
     const int per_e = m_tiles * a.n_tiles;
-    const int e = t / per_e;
-    const int rem = t - e * per_e;
+    const int slot = t / per_e;
+    const int e = seg_mb[SEG_INTS + slot];
+    const int rem = t - slot * per_e;
     const int mb = rem / a.n_tiles;
     const int nb = rem - mb * a.n_tiles;
     tl.e = e;
@@ -678,6 +683,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (args.mode == 1) {
+    // rank of expert e: experts with more 128-token blocks, or as many and a lower id, come first
+    int* order = seg_mb + SEG_INTS;
+    for (int e = threadIdx.x; e < args.E; e += blockDim.x) {
+      const int me = seg_mb[e + 1] - seg_mb[e];
+      int rank = 0;
+      for (int f = 0; f < args.E; ++f) {
+        const int other = seg_mb[f + 1] - seg_mb[f];
+        rank += (other > me) || (other == me && f < e);
+      }
+      order[rank] = e;
+    }
+    __syncthreads();
+  }
   const uint32_t tmem = *tmem_base_s;
   const int total = tile_count(args, seg_mb);
   const uint64_t lim = args.wait_limit_ns != 0 ? args.wait_limit_ns : kWaitLimitNs;
