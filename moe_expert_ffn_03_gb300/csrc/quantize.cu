@@ -23,11 +23,14 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(
   const int64_t s = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (s >= n_rows) return;
   const int nblk = cols >> 5;
-  // lane j < k holds the destination row of slot j (shuffled to the warp when storing)
-  int my_dst = 0;
+  // lane j < k loads the destination row of slot j; every lane then takes all k by
+  // shuffles here, where the whole warp is present (fewer than 32 lanes enter the
+  // block loop below when cols < 1024)
   int nd = 1;
+  int dst[8];
   if (SCATTER) {
     nd = k;
+    int my_dst = 0;
     bool bad = false;
     if (lane < k) {
       my_dst = row_of[s * k + lane];
@@ -37,6 +40,8 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(
       if (lane == 0) report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_QUANT + 1);
       return;
     }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) dst[j] = __shfl_sync(0xFFFFFFFFu, my_dst, j);
   }
   for (int b = lane; b < nblk; b += 32) {
     uint32_t w[16];
@@ -54,7 +59,7 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (j < nd) {
-        const int64_t row = SCATTER ? int64_t(__shfl_sync(0xFFFFFFFFu, my_dst, j)) : s;
+        const int64_t row = SCATTER ? int64_t(dst[j]) : s;
         store_codes32(codes + row * cols + (int64_t)b * 32, q);
         scales[sf_offset(row, b, cols)] = uint8_t(c);
       }

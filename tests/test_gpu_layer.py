@@ -105,6 +105,7 @@ def test_tiny_workload_fwd_bwd():
     (200, 128, 128, 1, 1, "normal"),     # one expert: a plain GEMM
     (1000, 256, 256, 64, 6, "biased"),   # fine-grained, skewed, empty experts
     (513, 384, 640, 5, 3, "normal"),
+    (600, 128, 128, 256, 8, "biased"),   # the largest E and k: 256 tiny segments, many empty
 ])
 def test_small_workloads_fwd_bwd(T, H, I, E, k, routing):
     wl = configs.small(T, H, I, E, k, routing=routing, backward=True)

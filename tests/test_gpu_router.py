@@ -1,8 +1,10 @@
 """GPU router (forward logits, backward through the top-k softmax) vs the oracle.
 
-The routing decisions come from logits, so the oracle takes the device's logits
-as its input for everything downstream (both sides then select the same
-experts); the logits themselves are compared with the float tolerance.
+The oracle computes its own logits (float64 sums rounded to float32) and routes
+on them; the device routes on its float32 sums.  The inputs are checked, on the
+oracle side, to keep every token's k-th and (k+1)-th logits further apart than
+the two sides' sums can differ, so both take the same top-k decisions; the
+device's choice must then equal the oracle's exactly.
 """
 import numpy as np
 import pytest
@@ -53,10 +55,15 @@ def test_trainable_layer_with_router(T, H, I, E, k, renorm):
     torch.cuda.synchronize()
     assert L.device_error() == (0, 0)
 
-    lg = logits.cpu().numpy()
-    idx, prob = rt.route_topk(lg, k, renormalize=bool(renorm))
-    assert np.array_equal(L.idx.cpu().numpy(), idx)
     x, w_gu, w_d, dout = f64(inp["x"]), f64(inp["w_gu"]), f64(inp["w_d"]), f64(inp["dout"])
+    lg = ro.router_logits(x, f64(w_r))
+    # float32 sums over H <= 256 products of magnitude <= 0.1 differ from the rounded
+    # float64 sums by far less than 5e-6: no top-k decision of these inputs is that close
+    s = np.sort(lg, axis=1)[:, ::-1]
+    assert (s[:, k - 1] - s[:, k]).min() > 5e-6
+    assert_close(logits.cpu().numpy(), lg, "logits")
+    idx, prob = rt.route_topk(lg.astype(np.float32), k, renormalize=bool(renorm))
+    assert np.array_equal(L.idx.cpu().numpy(), idx)
     fwd = ef.forward(x, idx, prob.astype(np.float64), w_gu, w_d)
     bwd = ef.backward(fwd, dout)
     dl = ro.router_backward(lg, idx, prob, bwd["dprob"], bool(renorm))
