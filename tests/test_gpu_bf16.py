@@ -49,6 +49,7 @@ def test_bf16_forward_matches_oracle(name_or_dims):
     configs.TINY,
     (300, 256, 384, 6, 2, "biased"),
     (513, 384, 640, 5, 3, "normal"),
+    (600, 128, 128, 256, 8, "biased"),
 ])
 def test_bf16_training_step_matches_oracle(name_or_dims):
     """bf16 forward (saving g, u) + bf16 backward vs the oracle's BF16-path backward."""

@@ -64,6 +64,7 @@ def test_all_zero_tensor_has_unit_scale():
     (300, 256, 384, 6, 2, "biased"),
     (513, 384, 640, 5, 3, "normal"),
     (700, 256, 256, 16, 4, "biased"),
+    (600, 128, 128, 256, 8, "biased"),
     configs.UNEVEN,
 ])
 def test_fp8_tensor_forward_matches_oracle(name_or_dims):

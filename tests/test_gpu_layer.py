@@ -106,6 +106,8 @@ def test_tiny_workload_fwd_bwd():
     (1000, 256, 256, 64, 6, "biased"),   # fine-grained, skewed, empty experts
     (513, 384, 640, 5, 3, "normal"),
     (600, 128, 128, 256, 8, "biased"),   # the largest E and k: 256 tiny segments, many empty
+    (1, 128, 128, 4, 2, "normal"),       # one token
+    (100, 128, 256, 4, 4, "normal"),     # k = E: every token in every expert
 ])
 def test_small_workloads_fwd_bwd(T, H, I, E, k, routing):
     wl = configs.small(T, H, I, E, k, routing=routing, backward=True)
