@@ -406,10 +406,7 @@ def run_cuda(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "mxfp8-e4m3 (ue8m0 block-32 scales, fp32 accumulate)",
         "data": "synthetic (seeded SplitMix64/Box-Muller: x~N(0,1), W~N(0,0.02^2), dout~N(0,0.01^2), logits~N(0,1))",
-        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
-                   "pass": "fwd+bwd" if train else "fwd", "global_batch_tokens": wl.T * world,
-                   "l2": "inputs larger than L2 (2.8 GB bf16 weights re-read every step); no flush",
-                   "parallelism": f"replicas x{world} (no exchange step)"},
+        "config": arm_config(wl, world),
         "tokens_per_s": round(replica_throughput(wl.T, ms_step, world), 1),
         "frac_of_mxfp8_peak": round(value / world / fp8_peak, 4),
         "breakdown_ms": {k: round(v, 4) for k, v in parts.items()},
@@ -444,11 +441,15 @@ def run_cuda(args):
 
 
 # ------------------------------------------------------------------------------------
+_SAMPLE_INPUTS: dict = {}
+
+
 def cpu_baseline(tokens: int, wl=None):
     """The oracle (numpy, float64) on a bounded sample: `tokens` tokens routed to the
-    workload's first expert, full H and I, forward and (when the workload trains)
-    backward, weight quantization included (that quantization of a full expert is most
-    of the sample's time)."""
+    workload's first expert, full H and the first half of that expert's intermediate
+    features (I/2 rows of the gate and of the up projection, I/2 columns of the down
+    projection), forward and (when the workload trains) backward, weight quantization
+    included (that quantization is most of the sample's time)."""
     import numpy as np
     import torch
 
@@ -458,13 +459,23 @@ def cpu_baseline(tokens: int, wl=None):
 
     wl = wl or configs.get(WORKLOAD)
     E_s = 1
-    sub = configs.small(tokens, wl.H, wl.I, wl.E, wl.k, routing=wl.routing, backward=True)
-    inp = synth.make_inputs(sub, seed=0, device="cpu")
-    f64 = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
-    logits = inp["logits"].numpy().copy()
-    logits[:, E_s:] = -1e30                                   # route over the sampled experts only
-    x, dout = f64(inp["x"]), f64(inp["dout"])
-    w_gu, w_d = f64(inp["w_gu"][:E_s]), f64(inp["w_d"][:E_s])
+    I_s = max(128, (wl.I // 2) // 128 * 128)
+    key = (tokens, wl.name, I_s)
+    if key not in _SAMPLE_INPUTS:
+        # the first `tokens` tokens and expert 0's weights: the first values of each tensor's
+        # counter-based stream, equal to the same slices of the full workload's tensors
+        f64 = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+        sub = configs.small(tokens, wl.H, wl.I, wl.E, wl.k, routing=wl.routing, backward=True)
+        x = synth.normal_bf16(synth.stream_key(0, synth.TID_X), (tokens, wl.H), 1.0, "cpu")
+        dout = synth.normal_bf16(synth.stream_key(0, synth.TID_DOUT), (tokens, wl.H), sub.g_std, "cpu")
+        w_gu0 = synth.normal_bf16(synth.stream_key(0, synth.TID_WGU), (1, 2 * wl.I, wl.H), sub.w_std, "cpu")
+        w_d0 = synth.normal_bf16(synth.stream_key(0, synth.TID_WD), (1, wl.H, wl.I), sub.w_std, "cpu")
+        logits = synth.make_logits(sub, 0, "cpu").numpy().copy()
+        logits[:, E_s:] = -1e30                               # route over the sampled experts only
+        w_gu = f64(torch.cat([w_gu0[:, :I_s], w_gu0[:, wl.I:wl.I + I_s]], dim=1))
+        _SAMPLE_INPUTS.clear()
+        _SAMPLE_INPUTS[key] = (f64(x), f64(dout), logits, w_gu, f64(w_d0[:, :, :I_s]))
+    x, dout, logits, w_gu, w_d = _SAMPLE_INPUTS[key]
     t0 = time.perf_counter()
     k = min(wl.k, E_s)
     idx, prob = rt.route_topk(logits[:, :E_s], k)
@@ -472,12 +483,21 @@ def cpu_baseline(tokens: int, wl=None):
     if wl.backward:
         ef.backward(fwd, dout)
     dt = time.perf_counter() - t0
-    flops = (18.0 if wl.backward else 6.0) * tokens * k * wl.H * wl.I
+    flops = (18.0 if wl.backward else 6.0) * tokens * k * wl.H * I_s
     return {"value": round(flops / dt / 1e12, 5), "unit": "TFLOP/s", "cores": os.cpu_count(),
             "kind": "oracle", "seconds": round(dt, 2),
-            "sample": f"{tokens} tokens x top-{k} over {E_s} of the {wl.E} experts, H={wl.H}, I={wl.I}, "
+            "sample": f"{tokens} tokens x top-{k} over {E_s} of the {wl.E} experts, H={wl.H}, "
+                      f"{I_s} of its I={wl.I} intermediate features, "
                       f"{'fwd+bwd' if wl.backward else 'fwd'} incl. weight quantization "
                       f"(numpy float64, BLAS threads = all host cores)"}
+
+
+def arm_config(wl, world: int) -> dict:
+    """The workload's config block, the same for both arms."""
+    return {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+            "pass": "fwd+bwd" if wl.backward else "fwd", "global_batch_tokens": wl.T * world,
+            "l2": "inputs larger than L2 (the bf16 weights are re-read every step); no flush",
+            "parallelism": f"replicas x{world} (no exchange step)"}
 
 
 def run_reference(args):
@@ -497,7 +517,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * statistics.median(secs), 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
-        "data": "synthetic", "config": {"workload": wl.name, "sample_tokens": args.cpu_tokens},
+        "data": "synthetic", "config": arm_config(wl, max(1, args.gpus)),
         "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": r["sample"]},
         "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
