@@ -27,49 +27,74 @@ from . import fp8_tensor as pt
 from .routing import route_topk
 
 
-def _forward_weights_mx(w_gu, w_d):
-    """The two forward weight operands of the MXFP8 oracle, quantized expert by expert."""
-    return {"gu": np.stack([ef.q_rowwise(w, ef.MXFP8) for w in w_gu]),
-            "d": np.stack([ef.q_rowwise(w, ef.MXFP8) for w in w_d])}
+def _weights_mx(w_gu, w_d, backward: bool):
+    """The weight operands of the MXFP8 oracle, quantized expert by expert (the two
+    forward ones, and the two transposed ones of the backward when asked)."""
+    wq = {"gu": np.stack([ef.q_rowwise(w, ef.MXFP8) for w in w_gu]),
+          "d": np.stack([ef.q_rowwise(w, ef.MXFP8) for w in w_d])}
+    if backward:
+        wq["guT"] = np.stack([ef.q_rowwise(w.T, ef.MXFP8) for w in w_gu])
+        wq["dT"] = np.stack([ef.q_rowwise(w.T, ef.MXFP8) for w in w_d])
+    return wq
+
+
+def _token_rel(got, ref):
+    """Mean over tokens of |got_t - ref_t| / |ref_t| (tokens with a zero reference skipped)."""
+    n = np.linalg.norm(ref, axis=1)
+    live = n > 0
+    return np.linalg.norm(got - ref, axis=1)[live] / n[live]
 
 
 def rel_fro(a, ref) -> float:
     return float(np.linalg.norm(np.asarray(a) - ref) / np.linalg.norm(ref))
 
 
-def compare(x, logits, w_gu, w_d, k: int) -> dict:
-    """Errors of the three numerics against the exact forward on one input set."""
+def compare(x, logits, w_gu, w_d, k: int, dout=None) -> dict:
+    """Errors of the three numerics against the exact forward (and, given dout, the
+    exact backward) on one input set."""
     idx, prob = route_topk(np.asarray(logits, dtype=np.float32), k)
     prob = prob.astype(np.float64)
+    train = dout is not None
     exact = ef.forward(x, idx, prob, w_gu, w_d, ef.EXACT)
-    rows = {"mxfp8": ef.forward(x, idx, prob, w_gu, w_d, ef.MXFP8, wq=_forward_weights_mx(w_gu, w_d)),
+    rows = {"mxfp8": ef.forward(x, idx, prob, w_gu, w_d, ef.MXFP8, wq=_weights_mx(w_gu, w_d, train)),
             "fp8_per_tensor": pt.forward(x, idx, prob, w_gu, w_d),
             "bf16_activations": ef.forward(x, idx, prob, w_gu, w_d, ef.BF16_PATH)}
     out = {}
     ref = exact["out"]
-    ref_norm = np.linalg.norm(ref, axis=1)
-    live = ref_norm > 0
     for name, f in rows.items():
-        tok = np.linalg.norm(f["out"] - ref, axis=1)[live] / ref_norm[live]
+        tok = _token_rel(f["out"], ref)
         out[name] = {"out_rel_fro": rel_fro(f["out"], ref),
                      "out_token_rel_mean": float(np.mean(tok)),   # every token weighs the same
                      "out_token_rel_max": float(np.max(tok)),
                      "a_rel_fro": rel_fro(f["a"], exact["a"])}   # a as it enters its quantizer
+    if train:
+        exb = ef.backward(exact, dout, ef.EXACT)
+        grads = {"mxfp8": ef.backward(rows["mxfp8"], dout, ef.MXFP8),
+                 "fp8_per_tensor": pt.backward(rows["fp8_per_tensor"], dout),
+                 "bf16_activations": ef.backward(rows["bf16_activations"], dout, ef.BF16_PATH)}
+        for name, g in grads.items():
+            tok = _token_rel(g["dx"], exb["dx"])
+            out[name].update({"dx_rel_fro": rel_fro(g["dx"], exb["dx"]),
+                              "dx_token_rel_mean": float(np.mean(tok)),
+                              "dw_gu_rel_fro": rel_fro(g["dw_gu"], exb["dw_gu"]),
+                              "dw_d_rel_fro": rel_fro(g["dw_d"], exb["dw_d"]),
+                              "dprob_rel_fro": rel_fro(g["dprob"], exb["dprob"])})
     split = exact["perm"]["split_sizes"]
     out["loads"] = {"min": int(split.min()), "max": int(split.max()), "empty": int((split == 0).sum())}
     return out
 
 
 def workload_inputs(wl, tokens: int | None = None):
-    """Float64 views of a workload's seeded inputs (first `tokens` tokens if given)."""
+    """Float64 views of a workload's seeded inputs (first `tokens` tokens if given); the
+    upstream gradient dout is drawn for every workload, also the forward-only ones."""
     import dataclasses
 
     from moe_expert_ffn_03_gb300 import synth
     if tokens is not None and tokens < wl.T:
         wl = dataclasses.replace(wl, T=tokens, name=f"{wl.name}_first{tokens}")
-    d = synth.make_inputs(wl, 0, with_grad=False)
+    d = synth.make_inputs(wl, 0, with_grad=True)
     f = {k: v.double().numpy() for k, v in d.items()}
-    return wl, f["x"], f["logits"], f["w_gu"], f["w_d"]
+    return wl, f["x"], f["logits"], f["w_gu"], f["w_d"], f["dout"]
 
 
 def with_outlier_channels(x, every: int = 128, factor: float = 100.0):
@@ -102,14 +127,17 @@ def main():
     for name, tokens in ((configs.UNEVEN, None), (configs.FINEGRAINED, args.tokens_finegrained)):
         for label, make in variants:
             t0 = time.time()
-            wl, x, logits, w_gu, w_d = workload_inputs(configs.get(name), tokens)
-            r = compare(make(x), logits, w_gu, w_d, wl.k)
+            wl, x, logits, w_gu, w_d, dout = workload_inputs(configs.get(name), tokens)
+            r = compare(make(x), logits, w_gu, w_d, wl.k, dout)
             print(f"{wl.name}{label}  (loads min {r['loads']['min']} max {r['loads']['max']} "
                   f"empty {r['loads']['empty']}; {time.time() - t0:.0f} s)")
             for key in ("mxfp8", "fp8_per_tensor", "bf16_activations"):
                 v = r[key]
                 print(f"    {key:18s} out rel-Fro {v['out_rel_fro']:.3e}  per-token mean {v['out_token_rel_mean']:.3e}"
                       f"  per-token max {v['out_token_rel_max']:.3e}  a rel-Fro {v['a_rel_fro']:.3e}")
+                print(f"    {'':18s} dx rel-Fro {v['dx_rel_fro']:.3e}  per-token mean {v['dx_token_rel_mean']:.3e}"
+                      f"  dW_gu {v['dw_gu_rel_fro']:.3e}  dW_d {v['dw_d_rel_fro']:.3e}"
+                      f"  dprob {v['dprob_rel_fro']:.3e}", flush=True)
 
 
 if __name__ == "__main__":

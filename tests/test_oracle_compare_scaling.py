@@ -29,6 +29,20 @@ def test_gaussian_inputs_both_8bit_paths_alike():
     assert 0.5 < p / m < 2.0
 
 
+def test_gradients_of_small_tokens_degrade_less_than_their_outputs():
+    """With the 4096x tokens, dH grows only linearly with x (dA is the same for every token),
+    so the normal tokens' dH lands partly in E4M3's subnormals instead of vanishing: per-tensor
+    scaling gives worse per-token dx than MX, but not the wiped-out outputs of the forward."""
+    x, logits, w_gu, w_d = _inputs(1)
+    dout = mx.bf16(np.random.default_rng(9).standard_normal(x.shape) * 0.01)
+    r = cs.compare(cs.with_outlier_tokens(x, every=16, factor=4096.0), logits, w_gu, w_d, 2, dout)
+    m, p = r["mxfp8"]["dx_token_rel_mean"], r["fp8_per_tensor"]["dx_token_rel_mean"]
+    assert m < 0.15 and 1.1 * m < p < 0.5
+    assert r["fp8_per_tensor"]["out_token_rel_mean"] > 0.5
+    g = cs.compare(x, logits, w_gu, w_d, 2, dout)
+    assert g["bf16_activations"]["dx_rel_fro"] < g["mxfp8"]["dx_rel_fro"] / 5
+
+
 def test_large_tokens_wipe_out_small_ones_under_per_tensor_scaling_only():
     """Tokens 4096x the rest: a grows quadratically (silu(g)*u), so the expert's one scale
     for a flushes the normal tokens' a below E4M3's smallest subnormal; MX blocks are

@@ -146,3 +146,47 @@ def test_expert_scales_differ_so_one_global_scale_would_fail_the_pins():
     used = full["perm"]["split_sizes"] > 0
     assert len(set(full["s_x"][used])) > 1 and len(set(full["s_a"][used])) > 1
     assert len(set(full["wq"]["gu_s"])) > 1
+
+
+def _workload_bwd(seed):
+    x, idx, prob, w_gu, w_d = _workload(seed)
+    dout = _bf16_tensor(np.random.default_rng(seed + 100), x.shape, 0.01)
+    return x, idx, prob, w_gu, w_d, dout
+
+
+def test_backward_close_to_the_exact_backward_and_different_from_it():
+    x, idx, prob, w_gu, w_d, dout = _workload_bwd(5)
+    got = pt.backward(pt.forward(x, idx, prob, w_gu, w_d), dout)
+    ex = ef.backward(ef.forward(x, idx, prob, w_gu, w_d, ef.EXACT), dout, ef.EXACT)
+    for key in ("dx", "dw_gu", "dw_d", "dprob"):
+        rel = np.linalg.norm(got[key] - ex[key]) / np.linalg.norm(ex[key])
+        assert 1e-3 < rel < 0.15, (key, rel)
+
+
+def test_power_of_two_dout_scales_every_gradient_exactly():
+    """dY, dA, dH are linear in dout and every per-tensor scale follows its tensor, so a 2^m
+    factor on dout passes through every quantizer unchanged."""
+    x, idx, prob, w_gu, w_d, dout = _workload_bwd(6)
+    fwd = pt.forward(x, idx, prob, w_gu, w_d)
+    base = pt.backward(fwd, dout)
+    scaled = pt.backward(fwd, np.ldexp(dout, 4))
+    for key in ("dx", "dw_gu", "dw_d"):
+        assert np.array_equal(scaled[key], np.ldexp(base[key], 4)), key
+    assert np.allclose(scaled["dprob"], np.ldexp(base["dprob"], 4), rtol=1e-6)
+
+
+def test_backward_of_grouped_equals_independent_one_expert_runs():
+    x, idx, prob, w_gu, w_d, dout = _workload_bwd(7)
+    full_f = pt.forward(x, idx, prob, w_gu, w_d)
+    full = pt.backward(full_f, dout)
+    perm = full_f["perm"]
+    for e in range(w_gu.shape[0]):
+        r0, m = int(perm["offsets_pad"][e]), int(perm["split_sizes"][e])
+        if m == 0:
+            continue
+        toks = perm["src_of"][r0:r0 + m]
+        p = full_f["prob_perm"][r0:r0 + m][:, None]
+        one_f = pt.forward(x[toks], np.zeros((m, 1), dtype=np.int32), p, w_gu[e:e + 1], w_d[e:e + 1])
+        one = pt.backward(one_f, dout[toks])
+        assert np.array_equal(one["dw_gu"][0], full["dw_gu"][e])
+        assert np.array_equal(one["dw_d"][0], full["dw_d"][e])
