@@ -394,6 +394,33 @@ def run_cuda(args):
               "timed": "gate_up GEMM (bf16 a + amax) + per-tensor quantize of a + down GEMM",
               "mxfp8_grouped_mlp_fwd_ms": round(parts["grouped_mlp_fwd_ms"], 4)}
 
+    # ---- the whole training step with per-tensor FP8 operands, for comparison ----
+    t8_train = None
+    if train:
+        def t8_step():
+            L.quantize_weights_fp8_tensor(inp["w_gu"], inp["w_d"])
+            L.forward_fp8_tensor(inp["x"])
+            L.backward_fp8_tensor(inp["dout"])
+
+        t8_step()
+        torch.cuda.synchronize()
+        t0t = torch.cuda.Event(enable_timing=True)
+        t1t = torch.cuda.Event(enable_timing=True)
+        t0t.record(stream)
+        for _ in range(n_b):
+            t8_step()
+        t1t.record(stream)
+        torch.cuda.synchronize()
+        tt_ms = t0t.elapsed_time(t1t) / n_b
+        code, site = L.device_error()
+        if code != 0:
+            raise RuntimeError(f"device error {code} at site {site} (per-tensor FP8 step)")
+        t8_train = {"ms_per_step": round(tt_ms, 4), "tflops": round(flops / (tt_ms * 1e-3) / 1e12, 1),
+                    "frac_of_fp8_peak": round(flops / (tt_ms * 1e-3) / 1e12 / fp8_peak, 4),
+                    "timed": "weight amax + codes, x amax + codes, forward (bf16 a + its codes), backward "
+                             "(dY and dH amax + codes, code transposes), both combines (routing shared)",
+                    "mxfp8_ms_per_step": round(ms_step, 4)}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_tokens, wl)
@@ -433,6 +460,8 @@ def run_cuda(args):
     line["fp8_tensor_forward"] = t8_fwd
     if bf16_train is not None:
         line["bf16_training_step"] = bf16_train
+    if t8_train is not None:
+        line["fp8_tensor_training_step"] = t8_train
     if router is not None:
         line["router"] = router
     if cpu is not None:

@@ -105,11 +105,11 @@ size_t moe_rows_capacity(const moe_dims* d);
 
 /* Bytes of workspace needed for these sizes by moe_route_permute and the
  * forward calls (training = 0), also by grouped_mlp_bwd and moe_router_bwd
- * (training = 1), and also by grouped_mlp_bwd_bf16 (training = 2).  The
- * workspace is caller memory, 256-byte aligned, zero-filled once before first
- * use (that clears the device error word); it may be reused by later calls on
- * the same stream.  Returns 0 for invalid sizes or training outside 0..2.
- * Host only. */
+ * (training = 1), and also by grouped_mlp_bwd_bf16 (training = 2) or by
+ * grouped_mlp_bwd_fp8_tensor (training = 3).  The workspace is caller memory,
+ * 256-byte aligned, zero-filled once before first use (that clears the device
+ * error word); it may be reused by later calls on the same stream.  Returns 0
+ * for invalid sizes or training outside 0..3.  Host only. */
 size_t moe_workspace_size(const moe_dims* d, int32_t training);
 
 /*
@@ -334,12 +334,41 @@ moe_status moe_fp8_tensor_quantize_tokens(const moe_dims* d, const void* x, cons
  *                   tensor's amax before any element is quantized)
  *   aq              out uint8 [CAP][I]: codes of a with s_a[e]
  *   amax_a          out float32 [E]: amax of every expert's rows of a_perm
- *   y               out bf16 [CAP][H]; combine with moe_unpermute_combine.
+ *   y               out bf16 [CAP][H]; combine with moe_unpermute_combine;
+ *   saved_gu        out bf16 [CAP][2I] or NULL: g and u for grouped_mlp_bwd_fp8_tensor.
  */
 moe_status grouped_mlp_fwd_fp8_tensor(const moe_dims* d, const uint8_t* xq, const float* amax_x,
                                       const int32_t* split_sizes, const float* prob_perm, const uint8_t* wgu_q,
                                       const float* amax_gu, const uint8_t* wd_q, const float* amax_d, void* a_perm,
-                                      uint8_t* aq, float* amax_a, void* y, void* workspace, size_t workspace_bytes,
+                                      uint8_t* aq, float* amax_a, void* y, void* saved_gu, void* workspace,
+                                      size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * grouped_mlp_bwd_fp8_tensor -- backward of grouped_mlp_fwd_fp8_tensor with
+ * straight-through per-tensor quantizers (one dynamic scale per expert operand
+ * tensor; E4M3 for the gradients too).  A per-tensor scale does not depend on
+ * the axis, so the operands of the weight-gradient GEMMs are the forward's codes
+ * and dY's and dH's codes, transposed.  Steps: dY = dout gathered, its amax per
+ * expert and codes; dA = dY*W_d (kind::f8f6f4) with the SwiGLU backward fused,
+ * writing dH in bf16 and raising each expert's amax of dH; dH codes; dW_d =
+ * dY^T*a and dW_gu = dH^T*x over each expert's tokens; dX = dH*W_gu.
+ *   dout            bf16 [T][H]
+ *   idx, split_sizes, row_of, prob_perm: from moe_route_permute
+ *   saved_gu        bf16 [CAP][2I]: the saved_gu output of grouped_mlp_fwd_fp8_tensor
+ *   xq, amax_x      from moe_fp8_tensor_quantize_tokens
+ *   aq, amax_a      from grouped_mlp_fwd_fp8_tensor
+ *   wgu_q, amax_gu, wd_q, amax_d: fp8_tensor_quantize of W_gu, W_d
+ *   dx_perm         out bf16 [CAP][H]; combine it with moe_unpermute_combine
+ *   dwgu, dwd       out bf16 [E][2I][H], [E][H][I] (zeros for experts without tokens)
+ *   dprob           out f32 [T][k]
+ *   workspace       moe_workspace_size(d, 3) bytes
+ */
+moe_status grouped_mlp_bwd_fp8_tensor(const moe_dims* d, const void* dout, const int32_t* idx,
+                                      const int32_t* split_sizes, const int32_t* row_of, const float* prob_perm,
+                                      const void* saved_gu, const uint8_t* xq, const float* amax_x,
+                                      const uint8_t* aq, const float* amax_a, const uint8_t* wgu_q,
+                                      const float* amax_gu, const uint8_t* wd_q, const float* amax_d, void* dx_perm,
+                                      void* dwgu, void* dwd, float* dprob, void* workspace, size_t workspace_bytes,
                                       moe_stream_t stream);
 
 /*

@@ -21,6 +21,7 @@ EXPORTS = (
     "moe_selftest_wait_timeout", "moe_router_fwd", "moe_router_bwd", "moe_gather_rows", "grouped_mlp_fwd_bf16",
     "fp8_tensor_quantize", "moe_fp8_tensor_quantize_tokens", "grouped_mlp_fwd_fp8_tensor",
     "mxfp8_quantize_experts", "fp8_tensor_quantize_experts", "moe_transpose_bf16", "grouped_mlp_bwd_bf16",
+    "grouped_mlp_bwd_fp8_tensor",
 )
 
 MOE_OK = 0
@@ -82,7 +83,8 @@ def lib() -> ctypes.CDLL:
             "moe_router_bwd": ([D, P, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
             "fp8_tensor_quantize": ([P, c_int32, c_int32, c_int32, P, P, P], c_int32),
             "moe_fp8_tensor_quantize_tokens": ([D, P, P, P, P, P, P, P, c_size_t, P], c_int32),
-            "grouped_mlp_fwd_fp8_tensor": ([D] + [P] * 13 + [c_size_t, P], c_int32),
+            "grouped_mlp_fwd_fp8_tensor": ([D] + [P] * 14 + [c_size_t, P], c_int32),
+            "grouped_mlp_bwd_fp8_tensor": ([D] + [P] * 19 + [c_size_t, P], c_int32),
             "mxfp8_quantize_experts": ([ctypes.POINTER(P), c_int32, c_int32, c_int32, P, P, P, P, P], c_int32),
             "fp8_tensor_quantize_experts": ([ctypes.POINTER(P), c_int32, c_int32, c_int32, P, P, P], c_int32),
             "moe_selftest_wait_timeout": ([P, c_size_t, ctypes.c_int64, ctypes.POINTER(c_int32),
@@ -228,10 +230,19 @@ def moe_fp8_tensor_quantize_tokens(d, x, idx, row_of, split_sizes, xq, amax_x, w
 
 
 def grouped_mlp_fwd_fp8_tensor(d, xq, amax_x, split_sizes, prob_perm, wgu_q, amax_gu, wd_q, amax_d, a_perm, aq,
-                               amax_a, y, workspace, stream=None):
+                               amax_a, y, workspace, saved_gu=None, stream=None):
     _check(lib().grouped_mlp_fwd_fp8_tensor(ctypes.byref(d), _p(xq), _p(amax_x), _p(split_sizes), _p(prob_perm),
                                             _p(wgu_q), _p(amax_gu), _p(wd_q), _p(amax_d), _p(a_perm), _p(aq),
-                                            _p(amax_a), _p(y), _p(workspace),
+                                            _p(amax_a), _p(y), _p(saved_gu), _p(workspace),
+                                            workspace.numel() * workspace.element_size(), _st(stream)))
+
+
+def grouped_mlp_bwd_fp8_tensor(d, dout, idx, split_sizes, row_of, prob_perm, saved_gu, xq, amax_x, aq, amax_a,
+                               wgu_q, amax_gu, wd_q, amax_d, dx_perm, dwgu, dwd, dprob, workspace, stream=None):
+    _check(lib().grouped_mlp_bwd_fp8_tensor(ctypes.byref(d), _p(dout), _p(idx), _p(split_sizes), _p(row_of),
+                                            _p(prob_perm), _p(saved_gu), _p(xq), _p(amax_x), _p(aq), _p(amax_a),
+                                            _p(wgu_q), _p(amax_gu), _p(wd_q), _p(amax_d), _p(dx_perm), _p(dwgu),
+                                            _p(dwd), _p(dprob), _p(workspace),
                                             workspace.numel() * workspace.element_size(), _st(stream)))
 
 

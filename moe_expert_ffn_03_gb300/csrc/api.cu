@@ -48,10 +48,14 @@ struct WsLayout {
   size_t err, masks, bases, aq, aq_s;
   size_t dyq, dyq_s, dyqc, dyqc_s, dhq, dhq_s, dhqc, dhqc_s, dp, rpart;
   size_t dy16, dy16c, dh16, dh16c, x16c, a16c;   // bf16 training: dY, dH and x, a transposed
+  // per-tensor FP8 training: dY codes (rows, transposed), dH (bf16, codes, transposed codes),
+  // x and a codes transposed, the weights' codes transposed, per-expert amax of dY and dH
+  size_t t8dy, t8dyc, t8dh16, t8dh, t8dhc, t8xc, t8ac, t8wdT, t8wguT, t8amax;
   size_t total;
 };
 
-// mode 0: forward; 1: MXFP8 training; 2: bf16 training (the MXFP8 buffers plus bf16 ones)
+// mode 0: forward; 1: MXFP8 training; 2: bf16 training (the MXFP8 buffers plus bf16 ones);
+// 3: per-tensor FP8 training (the MXFP8 buffers plus per-tensor ones)
 WsLayout ws_layout(const moe_dims* d, int mode) {
   const bool training = mode != 0;
   WsLayout w{};
@@ -81,6 +85,18 @@ WsLayout ws_layout(const moe_dims* d, int mode) {
     w.dhqc_s = take(2 * I * cap / 32);
     w.dp = take(ntI * 4 * cap * 4);                 // one partial row sum per 64-column group
     w.rpart = take(router_partial_bytes(d->E, d->H));   // router weight-gradient partials
+  }
+  if (mode == 3) {
+    w.t8dy = take(cap * H);
+    w.t8dyc = take(H * cap);
+    w.t8dh16 = take(cap * 2 * I * 2);
+    w.t8dh = take(cap * 2 * I);
+    w.t8dhc = take(2 * I * cap);
+    w.t8xc = take(H * cap);
+    w.t8ac = take(I * cap);
+    w.t8wdT = take(E * I * H);
+    w.t8wguT = take(E * H * 2 * I);
+    w.t8amax = take(2 * E * 4);
   }
   if (mode == 2) {
     w.dy16 = take(cap * H * 2);
@@ -148,7 +164,7 @@ size_t moe_rows_capacity(const moe_dims* d) {
 
 size_t moe_workspace_size(const moe_dims* d, int32_t training) {
   if (check_dims(d) != MOE_OK) return 0;
-  if (training < 0 || training > 2) return 0;
+  if (training < 0 || training > 3) return 0;
   return ws_layout(d, training).total;
 }
 
@@ -500,8 +516,8 @@ moe_status moe_fp8_tensor_quantize_tokens(const moe_dims* d, const void* x, cons
 moe_status grouped_mlp_fwd_fp8_tensor(const moe_dims* d, const uint8_t* xq, const float* amax_x,
                                       const int32_t* split_sizes, const float* prob_perm, const uint8_t* wgu_q,
                                       const float* amax_gu, const uint8_t* wd_q, const float* amax_d, void* a_perm,
-                                      uint8_t* aq, float* amax_a, void* y, void* workspace, size_t workspace_bytes,
-                                      moe_stream_t stream) {
+                                      uint8_t* aq, float* amax_a, void* y, void* saved_gu, void* workspace,
+                                      size_t workspace_bytes, moe_stream_t stream) {
   g_msg[0] = 0;
   moe_status s = check_dims(d);
   if (s != MOE_OK) return s;
@@ -539,6 +555,8 @@ moe_status grouped_mlp_fwd_fp8_tensor(const moe_dims* d, const uint8_t* xq, cons
   g1.amax_a = reinterpret_cast<const uint32_t*>(amax_x);
   g1.amax_b = reinterpret_cast<const uint32_t*>(amax_gu);
   g1.amax_out = am_a;
+  g1.gu = static_cast<__nv_bfloat16*>(saved_gu);
+  if (saved_gu != nullptr && !al16(saved_gu)) return fail(MOE_ERR_ALIGNMENT, "saved_gu is not 16-byte aligned");
   g1.err = at<int>(workspace, w.err);
   CUDA_TRY(launch_grouped_gemm(EPI_T8_FWD_SWIGLU, g1, xq, cap, H, wgu_q, int64_t(E) * 2 * I, H,
                                (cap / 128) * g1.n_tiles, st, g_msg, sizeof(g_msg)),
@@ -699,6 +717,153 @@ moe_status grouped_mlp_bwd_bf16(const moe_dims* d, const void* dout, const int32
   CUDA_TRY(launch_grouped_gemm(EPI_B16_OUT, g6, dhc, 2 * int64_t(I), cap, xc, H, cap,
                                int64_t(E) * (2 * I / 128) * g6.n_tiles, st, g_msg, sizeof(g_msg)),
            "bf16 gate_up wgrad GEMM");
+  return MOE_OK;
+}
+
+moe_status grouped_mlp_bwd_fp8_tensor(const moe_dims* d, const void* dout, const int32_t* idx,
+                                      const int32_t* split_sizes, const int32_t* row_of, const float* prob_perm,
+                                      const void* saved_gu, const uint8_t* xq, const float* amax_x,
+                                      const uint8_t* aq, const float* amax_a, const uint8_t* wgu_q,
+                                      const float* amax_gu, const uint8_t* wd_q, const float* amax_d, void* dx_perm,
+                                      void* dwgu, void* dwd, float* dprob, void* workspace, size_t workspace_bytes,
+                                      moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  REQUIRE_PTR(dout);
+  REQUIRE_PTR(idx);
+  REQUIRE_PTR(split_sizes);
+  REQUIRE_PTR(row_of);
+  REQUIRE_PTR(prob_perm);
+  REQUIRE_PTR(saved_gu);
+  REQUIRE_PTR(xq);
+  REQUIRE_PTR(aq);
+  REQUIRE_PTR(wgu_q);
+  REQUIRE_PTR(wd_q);
+  REQUIRE_PTR(dx_perm);
+  REQUIRE_PTR(dwgu);
+  REQUIRE_PTR(dwd);
+  REQUIRE_PTR(dprob);
+  if (amax_x == nullptr || amax_a == nullptr || amax_gu == nullptr || amax_d == nullptr)
+    return fail(MOE_ERR_INVALID_ARG, "an amax array is NULL");
+  s = check_ws(d, workspace, workspace_bytes, 3);
+  if (s != MOE_OK) return s;
+  const WsLayout w = ws_layout(d, 3);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t cap = capacity(d);
+  const int H = d->H, I = d->I, E = d->E, k = d->k;
+  int* err = at<int>(workspace, w.err);
+  uint8_t* dyq = at<uint8_t>(workspace, w.t8dy);
+  uint8_t* dyqc = at<uint8_t>(workspace, w.t8dyc);
+  __nv_bfloat16* dh16 = at<__nv_bfloat16>(workspace, w.t8dh16);
+  uint8_t* dhq = at<uint8_t>(workspace, w.t8dh);
+  uint8_t* dhqc = at<uint8_t>(workspace, w.t8dhc);
+  uint8_t* xqc = at<uint8_t>(workspace, w.t8xc);
+  uint8_t* aqc = at<uint8_t>(workspace, w.t8ac);
+  uint8_t* wdT = at<uint8_t>(workspace, w.t8wdT);
+  uint8_t* wguT = at<uint8_t>(workspace, w.t8wguT);
+  uint32_t* am_dy = at<uint32_t>(workspace, w.t8amax);
+  uint32_t* am_dh = am_dy + E;
+  float* dp = at<float>(workspace, w.dp);
+
+  // dY: per-expert amax of the routed dout rows, codes in rows and transposed
+  CUDA_TRY(cudaMemsetAsync(am_dy, 0, 2 * sizeof(uint32_t) * size_t(E), st), "clear amax of dY, dH");
+  CUDA_TRY(launch_t8_amax_tokens(dout, d->T, H, idx, k, E, am_dy, err, st), "per-expert amax of dY");
+  CUDA_TRY(launch_t8_quant_tokens(dout, d->T, H, idx, row_of, k, E, cap, am_dy, dyq, err, st),
+           "per-tensor quantize of dY rows");
+  CUDA_TRY(launch_fill_pad_rows(split_sizes, E, H, dyq, nullptr, st), "padding rows of dY");
+  CUDA_TRY(launch_transpose_u8(dyq, 1, int(cap), H, split_sizes, E, dyqc, st), "dY codes transposed");
+  // the weights' codes transposed (a per-tensor scale does not depend on the axis)
+  CUDA_TRY(launch_transpose_u8(wd_q, E, H, I, nullptr, 0, wdT, st), "W_d codes transposed");
+  CUDA_TRY(launch_transpose_u8(wgu_q, E, 2 * I, H, nullptr, 0, wguT, st), "W_gu codes transposed");
+
+  // down dgrad + SwiGLU backward: dH in bf16 and its per-expert amax, dp partials
+  GemmArgs g3{};
+  g3.mode = 0;
+  g3.E = E;
+  g3.split_sizes = split_sizes;
+  g3.K = H;
+  g3.N = I;
+  g3.n_tiles = (I + 255) / 256;
+  g3.b_rows_per_expert = I;
+  g3.cap = cap;
+  g3.prob_perm = prob_perm;
+  g3.out = dh16;
+  g3.ldo = 2 * int64_t(I);
+  g3.gu = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(saved_gu));
+  g3.dp_part = dp;
+  g3.I = I;
+  g3.amax_a = am_dy;
+  g3.amax_b = reinterpret_cast<const uint32_t*>(amax_d);
+  g3.amax_out = am_dh;
+  g3.err = err;
+  CUDA_TRY(launch_grouped_gemm(EPI_T8_BWD_SWIGLU, g3, dyq, cap, H, wdT, int64_t(E) * I, H, (cap / 128) * g3.n_tiles,
+                               st, g_msg, sizeof(g_msg)),
+           "per-tensor FP8 down dgrad GEMM");
+  CUDA_TRY(launch_dprob_reduce(dp, g3.n_tiles * 4, cap, row_of, int64_t(d->T) * k, dprob, err, st), "dprob reduce");
+  // dH codes with its expert's scale, rows and transposed; x and a codes transposed
+  CUDA_TRY(launch_t8_quant_segments(dh16, split_sizes, E, cap, 2 * I, am_dh, dhq, st), "per-tensor quantize of dH");
+  CUDA_TRY(launch_transpose_u8(dhq, 1, int(cap), 2 * I, split_sizes, E, dhqc, st), "dH codes transposed");
+  CUDA_TRY(launch_transpose_u8(xq, 1, int(cap), H, split_sizes, E, xqc, st), "x codes transposed");
+  CUDA_TRY(launch_transpose_u8(aq, 1, int(cap), I, split_sizes, E, aqc, st), "a codes transposed");
+
+  // down wgrad: dW_d[e] = dY_e^T a_e (K = the expert's tokens)
+  GemmArgs g4{};
+  g4.mode = 1;
+  g4.E = E;
+  g4.split_sizes = split_sizes;
+  g4.M = H;
+  g4.N = I;
+  g4.n_tiles = (I + 255) / 256;
+  g4.cap = cap;
+  g4.out = static_cast<__nv_bfloat16*>(dwd);
+  g4.ldo = I;
+  g4.I = I;
+  g4.amax_a = am_dy;
+  g4.amax_b = reinterpret_cast<const uint32_t*>(amax_a);
+  g4.err = err;
+  CUDA_TRY(launch_grouped_gemm(EPI_T8_OUT, g4, dyqc, H, cap, aqc, I, cap, int64_t(E) * (H / 128) * g4.n_tiles, st,
+                               g_msg, sizeof(g_msg)),
+           "per-tensor FP8 down wgrad GEMM");
+
+  // gate_up dgrad: dX = dH * W_gu (K = 2I)
+  GemmArgs g5{};
+  g5.mode = 0;
+  g5.E = E;
+  g5.split_sizes = split_sizes;
+  g5.K = 2 * I;
+  g5.N = H;
+  g5.n_tiles = (H + 255) / 256;
+  g5.b_rows_per_expert = H;
+  g5.cap = cap;
+  g5.out = static_cast<__nv_bfloat16*>(dx_perm);
+  g5.ldo = H;
+  g5.I = I;
+  g5.amax_a = am_dh;
+  g5.amax_b = reinterpret_cast<const uint32_t*>(amax_gu);
+  g5.err = err;
+  CUDA_TRY(launch_grouped_gemm(EPI_T8_OUT, g5, dhq, cap, 2 * int64_t(I), wguT, int64_t(E) * H, 2 * int64_t(I),
+                               (cap / 128) * g5.n_tiles, st, g_msg, sizeof(g_msg)),
+           "per-tensor FP8 gate_up dgrad GEMM");
+
+  // gate_up wgrad: dW_gu[e] = dH_e^T x_e (K = the expert's tokens)
+  GemmArgs g6{};
+  g6.mode = 1;
+  g6.E = E;
+  g6.split_sizes = split_sizes;
+  g6.M = 2 * I;
+  g6.N = H;
+  g6.n_tiles = (H + 255) / 256;
+  g6.cap = cap;
+  g6.out = static_cast<__nv_bfloat16*>(dwgu);
+  g6.ldo = H;
+  g6.I = I;
+  g6.amax_a = am_dh;
+  g6.amax_b = reinterpret_cast<const uint32_t*>(amax_x);
+  g6.err = err;
+  CUDA_TRY(launch_grouped_gemm(EPI_T8_OUT, g6, dhqc, 2 * int64_t(I), cap, xqc, H, cap,
+                               int64_t(E) * (2 * I / 128) * g6.n_tiles, st, g_msg, sizeof(g_msg)),
+           "per-tensor FP8 gate_up wgrad GEMM");
   return MOE_OK;
 }
 

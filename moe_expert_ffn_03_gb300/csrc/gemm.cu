@@ -65,8 +65,8 @@ constexpr int TR_WARP_FLOATS = 32 * TR_PITCH;
 template <int EPI>
 struct Ops {
   static constexpr bool B16 = (EPI == EPI_B16_OUT || EPI == EPI_B16_FWD_SWIGLU || EPI == EPI_B16_BWD_SWIGLU);
-  static constexpr bool SWIGLU_BWD = (EPI == EPI_BWD_SWIGLU || EPI == EPI_B16_BWD_SWIGLU);
-  static constexpr bool T8 = (EPI == EPI_T8_OUT || EPI == EPI_T8_FWD_SWIGLU);
+  static constexpr bool SWIGLU_BWD = (EPI == EPI_BWD_SWIGLU || EPI == EPI_B16_BWD_SWIGLU || EPI == EPI_T8_BWD_SWIGLU);
+  static constexpr bool T8 = (EPI == EPI_T8_OUT || EPI == EPI_T8_FWD_SWIGLU || EPI == EPI_T8_BWD_SWIGLU);
   static constexpr bool NOSF = B16 || T8;         // no scale-factor loads or copies
   static constexpr bool SWIGLU_FWD = (EPI == EPI_FWD_SWIGLU || EPI == EPI_B16_FWD_SWIGLU || EPI == EPI_T8_FWD_SWIGLU);
   static constexpr int KSTEP = B16 ? 64 : 128;    // K elements per stage
@@ -542,10 +542,17 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     const float alpha = __frcp_rn(t8_scale(a.amax_a[tl.e])) * __frcp_rn(t8_scale(a.amax_b[tl.e]));
     const int64_t col = tl.n0 + cg * 32;
     float* f = reinterpret_cast<float*>(r);
+#pragma unroll
+    for (int i = 0; i < 64; ++i) f[i] *= alpha;            // g | u
+    if (a.gu != nullptr) {                                   // saved for the per-tensor backward
+      const int64_t twoI = 2 * int64_t(a.I);
+      store_bf16x32(a.gu + row * twoI + col, f);
+      store_bf16x32(a.gu + row * twoI + a.I + col, f + 32);
+    }
     uint32_t amax = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      f[i] = silu_f(f[i] * alpha) * (f[32 + i] * alpha) * p;
+      f[i] = silu_f(f[i]) * f[32 + i] * p;
       amax = max(amax, abs_bits(f[i]));
     }
     store_bf16x32(a.out + row * a.ldo + col, f);
@@ -583,6 +590,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     if (have) {
       const float p = a.prob_perm[row];
       const int64_t twoI = 2 * int64_t(a.I);
+      // per-tensor operands: dA = accumulator / (s_dY s_W)
+      const float alpha =
+          Ops<EPI>::T8 ? __frcp_rn(t8_scale(a.amax_a[tl.e])) * __frcp_rn(t8_scale(a.amax_b[tl.e])) : 1.0f;
+      uint32_t amax = 0;
       const __nv_bfloat16* grow = a.gu + row * twoI;
       for (int h = 0; h < 2; ++h) {
         if (h == 1) {
@@ -603,7 +614,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
             const int i = 8 * j + t;
             const float g = (t & 1) ? bf16_hi(gs[t >> 1]) : bf16_lo(gs[t >> 1]);
             const float u = (t & 1) ? bf16_hi(us[t >> 1]) : bf16_lo(us[t >> 1]);
-            const float d = __uint_as_float(r[i]);
+            const float d = __uint_as_float(r[i]) * alpha;
             // the IEEE divide here: with the fast one this fully unrolled loop spills more
             const float sgm = 1.0f / (1.0f + __expf(-g));
             const float sg = g * sgm;
@@ -618,12 +629,24 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
           store_col_bf16(o, a.out_t, row_blk0, col, a.cap, lane, tr);
           store_bf16x32(a.out + row * twoI + a.I + col, du);
           store_col_bf16(du, a.out_t, row_blk0, a.I + col, a.cap, lane, tr);
+        } else if (EPI == EPI_T8_BWD_SWIGLU) {
+          // bf16 dH rows; its per-tensor codes (both orientations) come after the amax
+          store_bf16x32(a.out + row * twoI + col, o);
+          store_bf16x32(a.out + row * twoI + a.I + col, du);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) amax = max(amax, max(abs_bits(o[i]), abs_bits(du[i])));
         } else {
           quant_row_block(o, a.q_row, a.q_row_s, row, col, twoI);
           quant_col_block(o, a.q_col, a.q_col_s, row_blk0, col, a.cap, lane, tr);
           quant_row_block(du, a.q_row, a.q_row_s, row, a.I + col, twoI);
           quant_col_block(du, a.q_col, a.q_col_s, row_blk0, a.I + col, a.cap, lane, tr);
         }
+      }
+      if (EPI == EPI_T8_BWD_SWIGLU) {
+        // amax of the stored bf16 dH (bf16 rounding is monotonic), one atomic per warp
+        amax = __float_as_uint(__bfloat162float(__float2bfloat16_rn(__uint_as_float(amax))));
+        amax = __reduce_max_sync(0xFFFFFFFFu, amax);
+        if (lane == 0 && amax != 0u) atomicMax(a.amax_out + tl.e, amax);
       }
     }
     a.dp_part[(int64_t(tl.nb) * 4 + cg) * a.cap + row] = dp;
@@ -943,6 +966,7 @@ cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64
     case EPI_T8_OUT: return launch_epi<EPI_T8_OUT>(ma, mb, a, grid, st);
     case EPI_T8_FWD_SWIGLU: return launch_epi<EPI_T8_FWD_SWIGLU>(ma, mb, a, grid, st);
     case EPI_B16_BWD_SWIGLU: return launch_epi<EPI_B16_BWD_SWIGLU>(ma, mb, a, grid, st);
+    case EPI_T8_BWD_SWIGLU: return launch_epi<EPI_T8_BWD_SWIGLU>(ma, mb, a, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -67,6 +67,10 @@ cudaError_t launch_t8_quant_segments(const void* src, const int* split_sizes, in
 // segments are skipped.
 cudaError_t launch_transpose_bf16(const void* src, const int* src_map, int64_t n_src_rows, int batch, int rows,
                                   int cols, const int* split_sizes, int E, void* out, int* err, cudaStream_t st);
+// out[b*cols + c][r] = src[b][r][c] for uint8 [batch][rows][cols] (multiples of 128);
+// with split_sizes, row tiles past the padded segments are skipped.
+cudaError_t launch_transpose_u8(const uint8_t* src, int batch, int rows, int cols, const int* split_sizes, int E,
+                                uint8_t* out, cudaStream_t st);
 cudaError_t launch_dprob_reduce(const float* dp_part, int n_tiles, int64_t cap, const int* row_of, int64_t R,
                                 float* dprob, int* err, cudaStream_t st);
 
@@ -93,6 +97,8 @@ enum Epilogue : int {
   EPI_T8_OUT = 5,
   EPI_T8_FWD_SWIGLU = 6,
   EPI_B16_BWD_SWIGLU = 7,    // bf16 operands; SwiGLU backward writing bf16 dH to out [cap][2I] and out_t [2I][cap]
+  EPI_T8_BWD_SWIGLU = 8,     // per-tensor E4M3 operands; SwiGLU backward writing bf16 dH to out [cap][2I]
+                             // and raising every expert's amax of dH into amax_out
 };
 
 struct GemmArgs {

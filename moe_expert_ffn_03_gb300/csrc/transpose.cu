@@ -10,7 +10,8 @@
 // One CTA per 128x128 tile of src[batch]: the tile is staged in shared memory
 // with cp.async (rows gathered through src_map when given, -1 -> zero row),
 // then every thread writes two transposed rows of 32 values (64 contiguous
-// bytes each).  HBM-bound: 2 B read and 2 B written per element.
+// bytes each).  HBM-bound: 2 B read and 2 B written per element.  The byte
+// transpose below serves the per-tensor FP8 path the same way.
 #include "kernels.cuh"
 
 namespace moe {
@@ -83,7 +84,60 @@ __global__ void __launch_bounds__(256, 6) transpose_bf16_kernel(
   }
 }
 
+// Byte transpose of E4M3 codes (the per-tensor FP8 path: a scale per tensor does not
+// depend on the axis, so the along-token operands are the row codes transposed).
+// Tile 128x128 bytes; thread (column c, half h) reads 64 rows of column c from
+// shared memory and writes them as 64 contiguous bytes of transposed row c.
+__global__ void __launch_bounds__(256) transpose_u8_kernel(const uint8_t* __restrict__ src, int rows, int cols,
+                                                           const int* __restrict__ split_sizes, int E,
+                                                           uint8_t* __restrict__ out) {
+  __shared__ __align__(16) uint8_t tile[TT * (TT + 16)];
+  __shared__ int s_rows_used;
+  const int row0 = blockIdx.x * TT;
+  const int col0 = blockIdx.y * TT;
+  const int64_t batch = blockIdx.z;
+  if (split_sizes != nullptr) {
+    if (threadIdx.x < 32) {
+      int acc = 0;
+      for (int e = threadIdx.x; e < E; e += 32) acc += (split_sizes[e] + 127) & ~127;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+      if (threadIdx.x == 0) s_rows_used = acc;
+    }
+    __syncthreads();
+    if (row0 >= s_rows_used) return;
+  }
+  constexpr int P = TT + 16;                           // bytes per shared row
+  const uint8_t* base = src + (batch * rows + row0) * int64_t(cols) + col0;
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {                     // 128 rows x 8 chunks of 16 B
+    const int i = threadIdx.x + 256 * it;
+    const int r = i >> 3, c16 = i & 7;
+    cp_async16(&tile[r * P + c16 * 16], base + int64_t(r) * cols + c16 * 16, true);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  const int c = threadIdx.x & 127, h = threadIdx.x >> 7;
+  uint32_t w[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int r = 64 * h + 4 * q;
+    w[q] = uint32_t(tile[r * P + c]) | (uint32_t(tile[(r + 1) * P + c]) << 8) |
+           (uint32_t(tile[(r + 2) * P + c]) << 16) | (uint32_t(tile[(r + 3) * P + c]) << 24);
+  }
+  uint4* d = reinterpret_cast<uint4*>(out + (batch * cols + col0 + c) * int64_t(rows) + row0 + 64 * h);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) d[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+}
+
 }  // namespace
+
+cudaError_t launch_transpose_u8(const uint8_t* src, int batch, int rows, int cols, const int* split_sizes, int E,
+                                uint8_t* out, cudaStream_t st) {
+  dim3 grid(rows / TT, cols / TT, batch);
+  transpose_u8_kernel<<<grid, 256, 0, st>>>(src, rows, cols, split_sizes, E, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_transpose_bf16(const void* src, const int* src_map, int64_t n_src_rows, int batch, int rows,
                                   int cols, const int* split_sizes, int E, void* out, int* err, cudaStream_t st) {

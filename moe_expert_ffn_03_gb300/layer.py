@@ -218,9 +218,30 @@ class ExpertFFN:
                                          self.t8_amax_x, self.ws, stream)
         B.grouped_mlp_fwd_fp8_tensor(self.d, self.t8_xq, self.t8_amax_x, self.split_sizes, self.prob_perm, self.t8_wgu,
                                      self.t8_amax_gu, self.t8_wd, self.t8_amax_d, self.t8_a, self.t8_aq,
-                                     self.t8_amax_a, self.t8_y, self.ws, stream)
+                                     self.t8_amax_a, self.t8_y, self.ws, self.saved_gu if self.training else None,
+                                     stream)
         B.moe_unpermute_combine(self.d, self.t8_y, self.row_of, None, self.t8_out, stream)
         return self.t8_out
+
+    def backward_fp8_tensor(self, dout, stream=None):
+        """After forward_fp8_tensor on a training layer: the per-tensor FP8 backward
+        (its own workspace, allocated on first use); results in t8_dx, t8_dwgu, t8_dwd,
+        t8_dprob."""
+        if not self.training:
+            raise RuntimeError("backward_fp8_tensor needs a training layer")
+        if not hasattr(self, "ws_t8"):
+            dev = self.ws.device
+            self.ws_t8 = torch.zeros(B.moe_workspace_size(self.d, 3), dtype=U8, device=dev)
+            self.t8_dx = torch.empty(self.T, self.H, dtype=torch.bfloat16, device=dev)
+            self.t8_dwgu = torch.empty(self.E, 2 * self.I, self.H, dtype=torch.bfloat16, device=dev)
+            self.t8_dwd = torch.empty(self.E, self.H, self.I, dtype=torch.bfloat16, device=dev)
+            self.t8_dprob = torch.empty(self.T, self.k, dtype=torch.float32, device=dev)
+        B.grouped_mlp_bwd_fp8_tensor(self.d, dout, self.idx, self.split_sizes, self.row_of, self.prob_perm,
+                                     self.saved_gu, self.t8_xq, self.t8_amax_x, self.t8_aq, self.t8_amax_a,
+                                     self.t8_wgu, self.t8_amax_gu, self.t8_wd, self.t8_amax_d, self.dx_perm,
+                                     self.t8_dwgu, self.t8_dwd, self.t8_dprob, self.ws_t8, stream)
+        B.moe_unpermute_combine(self.d, self.dx_perm, self.row_of, None, self.t8_dx, stream)
+        return self.t8_dx
 
     # ---- router (optional: when the logits come from x) ------------------------------
     def router_forward(self, x, w_r, stream=None):
@@ -240,7 +261,13 @@ class ExpertFFN:
         return self.dx
 
     def device_error(self, stream=None):
-        return B.moe_get_device_error(self.ws, stream)
+        """(code, site) of the first device error recorded in any workspace of this layer."""
+        for ws in (self.ws, getattr(self, "ws_t8", None)):
+            if ws is not None:
+                code, site = B.moe_get_device_error(ws, stream)
+                if code != 0:
+                    return code, site
+        return 0, 0
 
     def padded_rows(self) -> int:
         s = self.split_sizes.to("cpu", torch.int64)

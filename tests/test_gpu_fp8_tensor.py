@@ -131,3 +131,49 @@ def test_padding_rows_of_x_are_zero_codes():
         assert not xq[r0 + m:r0 + m + pad].any()
         r0 += int(m) + pad
     assert not np.isnan(mx.e4m3_decode(xq[:r0])).any()
+
+
+@pytest.mark.parametrize("name_or_dims", [
+    configs.TINY,
+    (300, 256, 384, 6, 2, "biased"),
+    (513, 384, 640, 5, 3, "normal"),
+    (600, 128, 128, 256, 8, "biased"),
+])
+def test_fp8_tensor_training_step_matches_oracle(name_or_dims):
+    """Per-tensor FP8 forward (saving g, u) + backward vs the oracle's per-tensor backward."""
+    wl = configs.get(name_or_dims) if isinstance(name_or_dims, str) else configs.small(*name_or_dims[:5],
+                                                                                         routing=name_or_dims[5])
+    inp = {k: v.cuda() for k, v in synth.make_inputs(wl, 0, with_grad=True).items()}
+    L = ExpertFFN(wl.T, wl.H, wl.I, wl.E, wl.k, training=True)
+    L.route(inp["logits"], inp["x"])
+    L.quantize_weights_fp8_tensor(inp["w_gu"], inp["w_d"])
+    L.forward_fp8_tensor(inp["x"])
+    dx = L.backward_fp8_tensor(inp["dout"])
+    torch.cuda.synchronize()
+    assert L.device_error() == (0, 0)
+    idx, prob = rt.route_topk(inp["logits"].cpu().numpy(), wl.k)
+    fwd = pt.forward(f64(inp["x"]), idx, prob.astype(np.float64), f64(inp["w_gu"]), f64(inp["w_d"]))
+    bwd = pt.backward(fwd, f64(inp["dout"]))
+    rows, I = fwd["perm"]["rows"], wl.I
+    assert_close(f64(L.saved_gu)[:rows, :I], fwd["g"], "g")
+    assert_close(f64(L.saved_gu)[:rows, I:], fwd["u"], "u")
+    assert_close(f64(dx), bwd["dx"], "dx")
+    assert_close(f64(L.t8_dwgu), bwd["dw_gu"], "dW_gu")
+    assert_close(f64(L.t8_dwd), bwd["dw_d"], "dW_d")
+    assert_close(L.t8_dprob.cpu().numpy().astype(np.float64), bwd["dprob"], "dprob")
+
+
+def test_per_tensor_codes_do_not_depend_on_the_axis():
+    """Codes of the transposed tensor are the transposed codes: the byte transposes of the
+    per-tensor backward give the along-token operands exactly."""
+    g = torch.Generator().manual_seed(8)
+    w = (torch.randn(2, 256, 384, generator=g) * 0.1).to(torch.bfloat16).cuda()
+    codes = torch.empty(2, 256, 384, dtype=torch.uint8, device="cuda")
+    amax = torch.empty(2, dtype=torch.float32, device="cuda")
+    B.fp8_tensor_quantize(w, 2, 256, 384, codes, amax)
+    wt = w.transpose(1, 2).contiguous()
+    codes_t = torch.empty(2, 384, 256, dtype=torch.uint8, device="cuda")
+    amax_t = torch.empty(2, dtype=torch.float32, device="cuda")
+    B.fp8_tensor_quantize(wt, 2, 384, 256, codes_t, amax_t)
+    torch.cuda.synchronize()
+    assert torch.equal(amax, amax_t) and torch.equal(codes.transpose(1, 2), codes_t)
