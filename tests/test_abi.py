@@ -108,3 +108,26 @@ def test_expert_pointer_arrays_checked_on_the_host(lib):
     assert s == 2
     s = lib.fp8_tensor_quantize_experts(good, 2, 128, 100, P(256), P(256), None)
     assert s == 2                                                     # cols not a multiple of 8
+
+
+def test_training_path_entry_points_check_arguments_on_the_host(lib):
+    P = ctypes.c_void_p
+    d = B.dims(64, 128, 128, 4, 2)
+    # workspace smaller than the mode each backward needs
+    for name, n_ptr in (("grouped_mlp_bwd_bf16", 15), ("grouped_mlp_bwd_fp8_tensor", 19)):   # pointers incl. ws
+        s = getattr(lib, name)(ctypes.byref(d), *([P(256)] * n_ptr), 16, None)
+        assert s == 4, name
+    assert lib.moe_workspace_size(ctypes.byref(d), 2) > lib.moe_workspace_size(ctypes.byref(d), 1)
+    assert lib.moe_workspace_size(ctypes.byref(d), 3) > lib.moe_workspace_size(ctypes.byref(d), 1)
+    assert lib.moe_workspace_size(ctypes.byref(d), 4) == 0
+    # a NULL amax array
+    args = [P(256)] * 19
+    args[7] = None                                                    # amax_x
+    s = lib.grouped_mlp_bwd_fp8_tensor(ctypes.byref(d), *args, 1 << 40, None)
+    assert s == 1 and b"amax" in lib.moe_last_error_message()
+    # transposes take multiples of 128
+    assert lib.moe_transpose_bf16(P(256), 1, 128, 100, P(256), None) == 2
+    assert lib.moe_transpose_bf16(None, 1, 128, 128, P(256), None) == 1
+    # the bf16 forward checks the optional saved_gu's alignment
+    s = lib.grouped_mlp_fwd_bf16(ctypes.byref(d), *([P(256)] * 7), P(8), P(256), 1 << 40, None)
+    assert s == 3
