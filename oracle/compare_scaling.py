@@ -49,37 +49,50 @@ def rel_fro(a, ref) -> float:
     return float(np.linalg.norm(np.asarray(a) - ref) / np.linalg.norm(ref))
 
 
+def _weights_bf16(w_gu, w_d):
+    """The BF16 path's weight operands: the bf16 master weights as they are (rounding bf16
+    values to bf16 changes nothing), the transposed ones as views -- no copies."""
+    return {"gu": w_gu, "d": w_d, "guT": np.swapaxes(w_gu, 1, 2), "dT": np.swapaxes(w_d, 1, 2)}
+
+
 def compare(x, logits, w_gu, w_d, k: int, dout=None) -> dict:
     """Errors of the three numerics against the exact forward (and, given dout, the
-    exact backward) on one input set."""
+    exact backward) on one input set.  One numerics at a time, keeping only its
+    errors, so the largest workloads fit in host memory."""
     idx, prob = route_topk(np.asarray(logits, dtype=np.float32), k)
     prob = prob.astype(np.float64)
     train = dout is not None
     exact = ef.forward(x, idx, prob, w_gu, w_d, ef.EXACT)
-    rows = {"mxfp8": ef.forward(x, idx, prob, w_gu, w_d, ef.MXFP8, wq=_weights_mx(w_gu, w_d, train)),
-            "fp8_per_tensor": pt.forward(x, idx, prob, w_gu, w_d),
-            "bf16_activations": ef.forward(x, idx, prob, w_gu, w_d, ef.BF16_PATH)}
+    ref_out, ref_a = exact["out"], exact["a"]
+    exb = ef.backward(exact, dout, ef.EXACT) if train else None
+    split = exact["perm"]["split_sizes"]
+    del exact
+    runs = {
+        "mxfp8": (lambda: ef.forward(x, idx, prob, w_gu, w_d, ef.MXFP8, wq=_weights_mx(w_gu, w_d, train)),
+                  lambda f: ef.backward(f, dout, ef.MXFP8)),
+        "fp8_per_tensor": (lambda: pt.forward(x, idx, prob, w_gu, w_d),
+                           lambda f: pt.backward(f, dout)),
+        "bf16_activations": (lambda: ef.forward(x, idx, prob, w_gu, w_d, ef.BF16_PATH, wq=_weights_bf16(w_gu, w_d)),
+                             lambda f: ef.backward(f, dout, ef.BF16_PATH)),
+    }
     out = {}
-    ref = exact["out"]
-    for name, f in rows.items():
-        tok = _token_rel(f["out"], ref)
-        out[name] = {"out_rel_fro": rel_fro(f["out"], ref),
+    for name, (fwd_fn, bwd_fn) in runs.items():
+        f = fwd_fn()
+        tok = _token_rel(f["out"], ref_out)
+        out[name] = {"out_rel_fro": rel_fro(f["out"], ref_out),
                      "out_token_rel_mean": float(np.mean(tok)),   # every token weighs the same
                      "out_token_rel_max": float(np.max(tok)),
-                     "a_rel_fro": rel_fro(f["a"], exact["a"])}   # a as it enters its quantizer
-    if train:
-        exb = ef.backward(exact, dout, ef.EXACT)
-        grads = {"mxfp8": ef.backward(rows["mxfp8"], dout, ef.MXFP8),
-                 "fp8_per_tensor": pt.backward(rows["fp8_per_tensor"], dout),
-                 "bf16_activations": ef.backward(rows["bf16_activations"], dout, ef.BF16_PATH)}
-        for name, g in grads.items():
+                     "a_rel_fro": rel_fro(f["a"], ref_a)}        # a as it enters its quantizer
+        if train:
+            g = bwd_fn(f)
             tok = _token_rel(g["dx"], exb["dx"])
             out[name].update({"dx_rel_fro": rel_fro(g["dx"], exb["dx"]),
                               "dx_token_rel_mean": float(np.mean(tok)),
                               "dw_gu_rel_fro": rel_fro(g["dw_gu"], exb["dw_gu"]),
                               "dw_d_rel_fro": rel_fro(g["dw_d"], exb["dw_d"]),
                               "dprob_rel_fro": rel_fro(g["dprob"], exb["dprob"])})
-    split = exact["perm"]["split_sizes"]
+            del g
+        del f
     out["loads"] = {"min": int(split.min()), "max": int(split.max()), "empty": int((split == 0).sum())}
     return out
 
@@ -120,20 +133,25 @@ def main():
     from moe_expert_ffn_03_gb300 import configs
     ap = argparse.ArgumentParser()
     ap.add_argument("--tokens-finegrained", type=int, default=4096)
+    ap.add_argument("--workloads", default="uneven,finegrained", help="comma-separated: uneven, finegrained")
     args = ap.parse_args()
+    chosen = set(args.workloads.split(","))
     variants = (("", lambda x: x),
                 ("  + outlier channels (x[:, ::128] * 100)", with_outlier_channels),
                 ("  + outlier tokens (x[::16] * 4096)", with_outlier_tokens))
-    for name, tokens in ((configs.UNEVEN, None), (configs.FINEGRAINED, args.tokens_finegrained)):
+    table = (("uneven", configs.UNEVEN, None), ("finegrained", configs.FINEGRAINED, args.tokens_finegrained))
+    for key, name, tokens in table:
+        if key not in chosen:
+            continue
         for label, make in variants:
             t0 = time.time()
             wl, x, logits, w_gu, w_d, dout = workload_inputs(configs.get(name), tokens)
             r = compare(make(x), logits, w_gu, w_d, wl.k, dout)
             print(f"{wl.name}{label}  (loads min {r['loads']['min']} max {r['loads']['max']} "
                   f"empty {r['loads']['empty']}; {time.time() - t0:.0f} s)")
-            for key in ("mxfp8", "fp8_per_tensor", "bf16_activations"):
-                v = r[key]
-                print(f"    {key:18s} out rel-Fro {v['out_rel_fro']:.3e}  per-token mean {v['out_token_rel_mean']:.3e}"
+            for num in ("mxfp8", "fp8_per_tensor", "bf16_activations"):
+                v = r[num]
+                print(f"    {num:18s} out rel-Fro {v['out_rel_fro']:.3e}  per-token mean {v['out_token_rel_mean']:.3e}"
                       f"  per-token max {v['out_token_rel_max']:.3e}  a rel-Fro {v['a_rel_fro']:.3e}")
                 print(f"    {'':18s} dx rel-Fro {v['dx_rel_fro']:.3e}  per-token mean {v['dx_token_rel_mean']:.3e}"
                       f"  dW_gu {v['dw_gu_rel_fro']:.3e}  dW_d {v['dw_d_rel_fro']:.3e}"
