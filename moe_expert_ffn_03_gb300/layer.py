@@ -24,11 +24,30 @@ LAUNCHES_PER_TRAINING_STEP = 20
 LAUNCHES_PER_FORWARD_STEP = 10
 
 
+class _Range:
+    """An NVTX range around one call when the layer asks for it (otherwise nothing)."""
+
+    def __init__(self, on: bool, name: str):
+        self.on, self.name = on, name
+
+    def __enter__(self):
+        if self.on:
+            torch.cuda.nvtx.range_push(self.name)
+
+    def __exit__(self, *exc):
+        if self.on:
+            torch.cuda.nvtx.range_pop()
+        return False
+
+
 class ExpertFFN:
     """Buffers of one layer for fixed sizes (T, H, I, E, k) on one device."""
 
-    def __init__(self, T, H, I, E, k, training=True, renormalize=True, device="cuda", bf16_training=False):
-        """bf16_training: also size the workspace for backward_bf16 (the bf16 training path)."""
+    def __init__(self, T, H, I, E, k, training=True, renormalize=True, device="cuda", bf16_training=False,
+                 nvtx=False):
+        """bf16_training: also size the workspace for backward_bf16 (the bf16 training path).
+        nvtx: mark every call with an NVTX range named after it (for profilers)."""
+        self.nvtx = nvtx
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
         self.training = training
         self.bf16_training = bool(training and bf16_training)
@@ -77,31 +96,35 @@ class ExpertFFN:
     def quantize_weights(self, w_gu, w_d, stream=None):
         """MX copies of the master weights: stacked tensors [E][2I][H] and [E][H][I], or
         lists of E per-expert tensors [2I][H] and [H][I]."""
-        E, H, I = self.E, self.H, self.I
-        if isinstance(w_gu, (list, tuple)):
-            t = self.training
-            B.mxfp8_quantize_experts(w_gu, 2 * I, H, self.wgu_q, self.wgu_s, self.wguT_q if t else None,
-                                     self.wguT_s if t else None, stream)
-            B.mxfp8_quantize_experts(w_d, H, I, self.wd_q, self.wd_s, self.wdT_q if t else None,
-                                     self.wdT_s if t else None, stream)
-            return
-        if self.training:
-            B.mxfp8_quantize_dual(w_gu, E, 2 * I, H, self.wgu_q, self.wgu_s, self.wguT_q, self.wguT_s, stream)
-            B.mxfp8_quantize_dual(w_d, E, H, I, self.wd_q, self.wd_s, self.wdT_q, self.wdT_s, stream)
-        else:
-            B.mxfp8_quantize(w_gu, E, 2 * I, H, 0, self.wgu_q, self.wgu_s, stream)
-            B.mxfp8_quantize(w_d, E, H, I, 0, self.wd_q, self.wd_s, stream)
+        with _Range(self.nvtx, "moe.quantize_weights"):
+            E, H, I = self.E, self.H, self.I
+            if isinstance(w_gu, (list, tuple)):
+                t = self.training
+                B.mxfp8_quantize_experts(w_gu, 2 * I, H, self.wgu_q, self.wgu_s, self.wguT_q if t else None,
+                                         self.wguT_s if t else None, stream)
+                B.mxfp8_quantize_experts(w_d, H, I, self.wd_q, self.wd_s, self.wdT_q if t else None,
+                                         self.wdT_s if t else None, stream)
+                return
+            if self.training:
+                B.mxfp8_quantize_dual(w_gu, E, 2 * I, H, self.wgu_q, self.wgu_s, self.wguT_q, self.wguT_s, stream)
+                B.mxfp8_quantize_dual(w_d, E, H, I, self.wd_q, self.wd_s, self.wdT_q, self.wdT_s, stream)
+            else:
+                B.mxfp8_quantize(w_gu, E, 2 * I, H, 0, self.wgu_q, self.wgu_s, stream)
+                B.mxfp8_quantize(w_d, E, H, I, 0, self.wd_q, self.wd_s, stream)
 
     def route(self, logits, x, stream=None):
-        B.moe_route_permute(self.d, logits, x, self.idx, self.prob, self.split_sizes, self.row_of, self.src_of,
-                            self.prob_perm, self.xq, self.xq_s, self.xq_col, self.xq_col_s, self.ws, stream)
+        with _Range(self.nvtx, "moe.route_permute"):
+            B.moe_route_permute(self.d, logits, x, self.idx, self.prob, self.split_sizes, self.row_of, self.src_of,
+                                self.prob_perm, self.xq, self.xq_s, self.xq_col, self.xq_col_s, self.ws, stream)
 
     def ffn_forward(self, stream=None):
-        B.grouped_mlp_fwd(self.d, self.xq, self.xq_s, self.split_sizes, self.prob_perm, self.wgu_q, self.wgu_s,
-                          self.wd_q, self.wd_s, self.y, self.saved_gu, self.aq_col, self.aq_col_s, self.ws, stream)
+        with _Range(self.nvtx, "moe.grouped_mlp_fwd"):
+            B.grouped_mlp_fwd(self.d, self.xq, self.xq_s, self.split_sizes, self.prob_perm, self.wgu_q, self.wgu_s,
+                              self.wd_q, self.wd_s, self.y, self.saved_gu, self.aq_col, self.aq_col_s, self.ws, stream)
 
     def combine_out(self, stream=None):
-        B.moe_unpermute_combine(self.d, self.y, self.row_of, None, self.out, stream)
+        with _Range(self.nvtx, "moe.combine"):
+            B.moe_unpermute_combine(self.d, self.y, self.row_of, None, self.out, stream)
 
     def forward(self, logits, x, stream=None):
         self.route(logits, x, stream)
@@ -110,12 +133,14 @@ class ExpertFFN:
         return self.out
 
     def ffn_backward(self, dout, stream=None):
-        B.grouped_mlp_bwd(self.d, dout, self.split_sizes, self.row_of, self.src_of, self.prob_perm, self.saved_gu,
-                          self.aq_col, self.aq_col_s, self.xq_col, self.xq_col_s, self.wguT_q, self.wguT_s,
-                          self.wdT_q, self.wdT_s, self.dx_perm, self.dwgu, self.dwd, self.dprob, self.ws, stream)
+        with _Range(self.nvtx, "moe.grouped_mlp_bwd"):
+            B.grouped_mlp_bwd(self.d, dout, self.split_sizes, self.row_of, self.src_of, self.prob_perm, self.saved_gu,
+                              self.aq_col, self.aq_col_s, self.xq_col, self.xq_col_s, self.wguT_q, self.wguT_s,
+                              self.wdT_q, self.wdT_s, self.dx_perm, self.dwgu, self.dwd, self.dprob, self.ws, stream)
 
     def combine_dx(self, stream=None):
-        B.moe_unpermute_combine(self.d, self.dx_perm, self.row_of, None, self.dx, stream)
+        with _Range(self.nvtx, "moe.combine_dx"):
+            B.moe_unpermute_combine(self.d, self.dx_perm, self.row_of, None, self.dx, stream)
 
     def backward(self, dout, stream=None):
         self.ffn_backward(dout, stream)

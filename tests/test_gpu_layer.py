@@ -197,3 +197,16 @@ def test_per_expert_weight_tensors_give_the_stacked_results():
         runs.append([t.clone() for t in (L.out, L.dx, L.dwgu, L.dwd, L.dprob)])
     for a, b in zip(*runs):
         assert torch.equal(a, b)
+
+
+def test_nvtx_ranges_change_nothing():
+    wl = configs.small(300, 256, 384, 6, 2, routing="biased", backward=True)
+    inp = {k: v.cuda() for k, v in synth.make_inputs(wl, 0).items()}
+    res = []
+    for nvtx in (False, True):
+        L = ExpertFFN(wl.T, wl.H, wl.I, wl.E, wl.k, training=True, nvtx=nvtx)
+        L.step(inp["w_gu"], inp["w_d"], inp["logits"], inp["x"], inp["dout"])
+        torch.cuda.synchronize()
+        res.append([t.clone() for t in (L.out, L.dx, L.dwgu, L.dwd, L.dprob)])
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
