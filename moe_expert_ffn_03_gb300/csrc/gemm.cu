@@ -34,6 +34,7 @@
 // TMEM and returns.
 #include <cuda.h>
 
+#include <atomic>
 #include <cstdio>
 
 #include "kernels.cuh"
@@ -929,12 +930,17 @@ bool encode_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, bool 
 
 template <int EPI>
 cudaError_t launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a, int grid, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Lay<EPI>::SMEM_BYTES);
+  // the shared-memory attribute is per device: set it once on each device this process uses
+  constexpr int kMaxDevices = 64;
+  static std::atomic<bool> attr_set[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices || !attr_set[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Lay<EPI>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    if (dev >= 0 && dev < kMaxDevices) attr_set[dev].store(true, std::memory_order_release);
   }
   grouped_gemm_kernel<EPI><<<grid, NUM_THREADS, Lay<EPI>::SMEM_BYTES, st>>>(ma, mb, a);
   return cudaGetLastError();
