@@ -8,27 +8,37 @@
 //   scaling are fused into the grouped MLP so no intermediate is stored in
 //   high precision.
 //
-// Design (one CTA per SM, persistent):
-//   warp 0      TMA producer: 128x128 A box + one or two 128x128 B boxes
-//               (128B swizzle) and the 512-byte scale atoms (bulk copies)
-//               per 128-deep K step into a 4-stage shared-memory ring.
-//   warp 18     scale factors: per stage, tcgen05.cp moves the scale atoms
-//               into that stage's TMEM columns, then commits to sf_ready.
-//   warp 1      TMEM allocator and MMA issuer: per stage, after sf_ready, four
-//               tcgen05.mma.kind::mxf8f6f4.block_scale (M=128, N=256 or 128,
-//               K=32) accumulate in TMEM (fp32, 256 columns); tcgen05.commit
-//               frees the stage and, after the last K step, hands the
-//               accumulator to the epilogue.  Kinds without scale factors
+// Design (persistent; CTA pairs of a 2-CTA cluster, one CTA per SM):
+//   Each pair computes a 256 x 256 output tile with tcgen05.mma.cta_group::2
+//   (M = 256): the even CTA of the cluster (the leader) holds rows 0..127 of
+//   the tile and the left 128 columns of B, the odd CTA (the peer) rows
+//   128..255 and the right 128 columns.  Each SM thus stages 32 KB of operands
+//   per 128-deep K step instead of 48 KB for the same tensor work, and the
+//   ring has 6 slots, filled and released two at a time.
+//   warp 0      (both CTAs) TMA producer: the CTA's 128x128 A box, its 128x128
+//               B box (128B swizzle) and, for MXFP8, the scale atoms of its A
+//               rows and of all 256 B rows; every copy signals the leader's
+//               full barrier of the stage (.cta_group::2), which the leader
+//               alone arms with both CTAs' byte count.
+//   warp 1      allocates TMEM (collectively with the peer); in the leader it
+//               issues, per stage, the scale-factor copies (tcgen05.cp, ordered
+//               before the MMAs that read them) and four tcgen05.mma (M=256,
+//               N=256, K=32); tcgen05.commit multicasts the stage release to both
+//               CTAs and, after the last K step, hands each CTA its half of the
+//               accumulator (fp32, 256 columns).  Kinds without scale factors
 //               (bf16, per-tensor E4M3) alternate two 256-column accumulators.
-//   warps 2..17 epilogue, four per TMEM lane quarter (32 rows), 64 accumulator
-//               columns each: tcgen05.ld into registers, release the
-//               accumulator at once (the next tile's MMAs start), then the
-//               fused epilogue math (bf16 store, ScaledSwiGLU + re-quantization
-//               along both axes, or SwiGLU backward + re-quantization).
-// Tiles: mode 0 walks the 128-row blocks of every expert segment (computed on
-// the device from split_sizes; empty experts get no tile) times the N tiles,
-// rasterised in groups of 8 row blocks; mode 1 (weight gradients) walks
-// expert x M tiles x N tiles with K = the expert's padded token range.
+//   warps 2..17 (both CTAs) epilogue, four per TMEM lane quarter (32 rows), 64
+//               accumulator columns each: tcgen05.ld into registers, release the
+//               accumulator at once (an arrival on the leader's barrier), then
+//               the fused epilogue math (bf16 store, ScaledSwiGLU +
+//               re-quantization along both axes, or SwiGLU backward +
+//               re-quantization).
+// Tiles: mode 0 walks pairs of 128-row blocks inside each expert segment
+// (computed on the device from split_sizes; empty experts get no tile; the
+// second block of an expert with an odd block count is computed and dropped)
+// times the N tiles, rasterised in groups of 8 pairs; mode 1 (weight
+// gradients) walks expert x 256-row M tiles x N tiles with K = the expert's
+// padded token range.
 // Every mbarrier wait is bounded; on expiry the CTA records
 // MOE_ERR_DEVICE_TIMEOUT, stops issuing, drains its copies and MMAs, frees
 // TMEM and returns.
@@ -42,22 +52,23 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128;
+constexpr int BM = 128, BN = 256, BK = 128;     // BM: rows per CTA; the pair's MMA has M = 2 * BM
+constexpr int MMA_M = 2 * BM;
 constexpr int A_TILE = BM * BK;                 // 16 KB of E4M3
-constexpr int B_HALF = 128 * BK;                // 16 KB: one 128-row box of B
+constexpr int B_HALF = 128 * BK;                // 16 KB: one 128-row box of B (this CTA's half of N)
 constexpr int SF_ATOM = 512;                    // 128 rows x 4 scale bytes
 constexpr int NUM_EPI_WARPS = 16;               // 4 per TMEM lane quarter
-constexpr int SF_WARP = 2 + NUM_EPI_WARPS;      // warp 18: scale-factor copies into TMEM
-constexpr int NUM_THREADS = 32 * (SF_WARP + 1);
+constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_ACC = 0;                  // accumulator: columns 0..255
 constexpr uint32_t TM_SF0 = 256, TM_SF_STRIDE = 12;  // per stage: SFA 4 columns + SFB 8 columns
-// Columns 320..447: per epilogue warp a 32-column parking place (lanes of its quarter)
+// Columns 384..511: per epilogue warp a 32-column parking place (lanes of its quarter)
 // for the second half of its accumulator columns in the SwiGLU-backward epilogue.
-constexpr uint32_t TM_STASH = 320;
+constexpr uint32_t TM_STASH = 384;
 constexpr int GROUP_M = 8;
 constexpr int SEG_INTS = 260;                   // per-expert prefix of 128-row blocks (E <= 256, plus the total)
 constexpr int kMaxSegE = 256;                   // mode-1 expert order (heaviest first) follows the prefix
+constexpr int SEG_PB = SEG_INTS + kMaxSegE;     // then the per-expert prefix of block pairs (mode 0)
 constexpr int TR_PITCH = 9;                     // floats per row of a warp's 32x8 transpose buffer
 constexpr int TR_WARP_FLOATS = 32 * TR_PITCH;
 
@@ -77,24 +88,31 @@ struct Ops {
   static constexpr int ACC_BUFS = (NOSF && !SWIGLU_BWD) ? 2 : 1;
 };
 
-// Shared-memory layout per epilogue kind (all use 256-column tiles today; a
-// 128-column tile would take one B box per stage and 6 stages).
+// Shared-memory layout (per CTA; both CTAs of a pair use the same offsets): six
+// slots, each one 128-deep K step of the CTA's A box, its B box and the scale
+// atoms (its A rows; the two 128-row blocks of B), then the barriers, the segment
+// tables and the epilogue warps' transpose buffers.  The slots are filled and
+// released two at a time (one barrier stage = 256 of K, 64 KB of operands):
+// measured on this GPU, what TMA delivers to an SM grows with the bytes behind
+// each barrier stage (about 35 B/clk with 32 KB stages, 50 with 64 KB), and the
+// pair needs 64 B/clk per SM to keep its MMAs busy.
 template <int EPI>
 struct Lay {
-  static constexpr int BNT = 256;
-  static constexpr int STG = (BNT == 256) ? 4 : 6;
-  static constexpr int B_T = BNT * BK;
-  static constexpr int SFB_T = (BNT / 128) * SF_ATOM;
+  static constexpr int STG = 6;                  // slots of one K step
+  static constexpr int PER = 2;                  // slots per barrier stage
+  static constexpr int NSTG = STG / PER;         // barrier stages
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STG * A_TILE;
-  static constexpr int OFF_SFA = OFF_B + STG * B_T;
-  static constexpr int OFF_SFB = OFF_SFA + STG * SF_ATOM;
-  static constexpr int OFF_BAR = OFF_SFB + STG * SFB_T;
-  // full[S], empty[S], sf_ready[S], tmem_full[2], tmem_empty[2], drain (MMA), drain (scale copies)
-  static constexpr int NUM_BARS = 3 * STG + 6;
+  static constexpr int OFF_SFA = OFF_B + STG * B_HALF;      // per slot: the atom of this CTA's A rows
+  static constexpr int OFF_SFB0 = OFF_SFA + STG * SF_ATOM;  // per slot: the atom of B rows 0..127
+  static constexpr int OFF_SFB1 = OFF_SFB0 + STG * SF_ATOM; // per slot: the atom of B rows 128..255
+  static constexpr int OFF_BAR = OFF_SFB1 + STG * SF_ATOM;
+  // full[NSTG] (leader: both CTAs' copies), empty[NSTG], tmem_full[2], tmem_empty[2] (leader:
+  // both CTAs' epilogue warps), drain (MMA)
+  static constexpr int NUM_BARS = 2 * NSTG + 5;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int OFF_SEG = OFF_MISC + 16;             // seg_mb[SEG_INTS], then order[kMaxSegE]
-  static constexpr int OFF_TR = OFF_SEG + (SEG_INTS + kMaxSegE) * 4;
+  static constexpr int OFF_SEG = OFF_MISC + 16;             // seg_mb[SEG_INTS], order[kMaxSegE], seg_pb[SEG_INTS]
+  static constexpr int OFF_TR = (OFF_SEG + (2 * SEG_INTS + kMaxSegE) * 4 + 15) & ~15;
   static constexpr int SMEM_USED = OFF_TR + NUM_EPI_WARPS * TR_WARP_FLOATS * 4;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 B
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -112,8 +130,24 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+// Cluster helpers.  A shared::cta address of this CTA is also its shared::cluster
+// address; mapa gives the address of the same offset in another CTA of the cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// arrive on an mbarrier anywhere in the cluster (release at cluster scope)
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -126,48 +160,51 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+// Tensor copy into this CTA's shared memory; completion is signalled on the
+// mbarrier at cluster address bar_c, which may sit in the pair's other CTA.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint32_t bar_c) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_c)
       : "memory");
-}
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
                "r"(ncols)
                : "memory");
 }
 __device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Arrives, once the pair's earlier tcgen05 operations are done, on the mbarrier at
+// this offset in both CTAs of the pair.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+      ::"r"(smem_u32(bar)), "h"(uint16_t(3))
+      : "memory");
 }
+// Each CTA of the pair copies the atom at this shared-memory offset into its own TMEM.
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 __device__ __forceinline__ void tc_mma_mxf8(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
       ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
       : "memory");
 }
@@ -237,7 +274,7 @@ __device__ __forceinline__ uint32_t idesc_mxf8(int N, int sf_id) {
          | (0u << 7) | (0u << 10)          // A, B format E4M3
          | (uint32_t(N >> 3) << 17)        // N / 8
          | (1u << 23)                      // scale format UE8M0
-         | (uint32_t(BM >> 4) << 24)       // M / 16
+         | (uint32_t(MMA_M >> 4) << 24)    // M / 16
          | (uint32_t(sf_id) << 29);        // A scale factor id
 }
 
@@ -246,21 +283,21 @@ __device__ __forceinline__ uint32_t idesc_bf16(int N) {
   return (1u << 4)                         // D format F32
          | (1u << 7) | (1u << 10)          // A, B format BF16
          | (uint32_t(N >> 3) << 17)        // N / 8
-         | (uint32_t(BM >> 4) << 24);      // M / 16
+         | (uint32_t(MMA_M >> 4) << 24);   // M / 16
 }
 // Instruction descriptor of kind::f8f6f4 without block scaling: E4M3 x E4M3 -> f32, both K-major.
 __device__ __forceinline__ uint32_t idesc_f8(int N) {
   return (1u << 4)                         // D format F32
          | (0u << 7) | (0u << 10)          // A, B format E4M3
          | (uint32_t(N >> 3) << 17)        // N / 8
-         | (uint32_t(BM >> 4) << 24);      // M / 16
+         | (uint32_t(MMA_M >> 4) << 24);   // M / 16
 }
 __device__ __forceinline__ void tc_mma_f8(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
       ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -269,47 +306,54 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d, uint64_t adesc, uint64_t
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
       ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
+// One CTA's view of a pair tile.
 struct Tile {
   int e;
   int nb;
   int k_tiles;
   int n0;
-  bool second;            // the second 128-row half of B (columns n0+128.. or the up half) is present
-  int64_t a_row;          // row of A
+  bool second;            // output columns n0+128.. of the tile exist (or the up half of a ScaledSwiGLU tile)
+  bool valid;             // this CTA's 128 rows belong to the tile (the peer's half can fall past the expert)
+  int64_t a_row;          // this CTA's first row of A
   int64_t k0;             // first K element
-  int64_t b_row0, b_row1; // rows of B for the two halves
-  int64_t out_row;        // output row of tile row 0 (mode 1: e*M + a_row)
+  int64_t b_row0, b_row1; // rows of B: the leader's half (columns 0..127) and the peer's (128..255)
+  int64_t out_row;        // output row of this CTA's row 0 (mode 1: e*M + a_row)
 };
 
-__device__ __forceinline__ int tile_count(const GemmArgs& a, const int* seg_mb) {
-  if (a.mode == 0) return seg_mb[a.E] * a.n_tiles;
-  return a.E * (a.M / BM) * a.n_tiles;
+__device__ __forceinline__ int tile_count(const GemmArgs& a, const int* seg) {
+  if (a.mode == 0) return seg[SEG_PB + a.E] * a.n_tiles;
+  return a.E * ((a.M + MMA_M - 1) / MMA_M) * a.n_tiles;
 }
 
+// seg: prefix of 128-row blocks per expert [0..E], the mode-1 expert order at
+// SEG_INTS, the prefix of block pairs per expert at SEG_PB.  rank: 0 (leader) or 1.
 template <int EPI>
-__device__ __forceinline__ void decode_tile(const GemmArgs& a, const int* seg_mb, int t, Tile& tl) {
+__device__ __forceinline__ void decode_tile(const GemmArgs& a, const int* seg, int t, int rank, Tile& tl) {
   if (a.mode == 0) {
-    const int total_mb = seg_mb[a.E];
+    const int* seg_pb = seg + SEG_PB;
+    const int total_pb = seg_pb[a.E];
     const int per_group = GROUP_M * a.n_tiles;
     const int group = t / per_group;
     const int first = group * GROUP_M;
-    const int gs = min(GROUP_M, total_mb - first);
+    const int gs = min(GROUP_M, total_pb - first);
     const int local = t - group * per_group;
-    const int mb = first + local % gs;
+    const int pb = first + local % gs;
     const int nb = local / gs;
-    int lo = 0, hi = a.E - 1;            // largest e with seg_mb[e] <= mb
+    int lo = 0, hi = a.E - 1;            // largest e with seg_pb[e] <= pb
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (seg_mb[mid] <= mb) lo = mid; else hi = mid - 1;
+      if (seg_pb[mid] <= pb) lo = mid; else hi = mid - 1;
     }
+    const int blk = 2 * (pb - seg_pb[lo]) + rank;    // 128-row block inside the expert's segment
     tl.e = lo;
     tl.nb = nb;
-    tl.a_row = int64_t(mb) * BM;
+    tl.valid = blk < seg[lo + 1] - seg[lo];
+    tl.a_row = int64_t(seg[lo] + blk) * BM;
     tl.k0 = 0;
     tl.k_tiles = a.K / Ops<EPI>::KSTEP;
     tl.out_row = tl.a_row;
@@ -325,20 +369,21 @@ __device__ __forceinline__ void decode_tile(const GemmArgs& a, const int* seg_mb
       tl.second = (tl.n0 + 128) < a.N;
     }
   } else {
-    // experts in order of decreasing token count (seg_mb is followed by that order), so the
-    // longest tiles are spread over the CTAs first and the short ones fill in at the end
-    const int m_tiles = a.M / BM;
+    // experts in order of decreasing token count (seg is followed by that order), so the
+    // longest tiles are spread over the pairs first and the short ones fill in at the end
+    const int m_tiles = (a.M + MMA_M - 1) / MMA_M;
     const int per_e = m_tiles * a.n_tiles;
     const int slot = t / per_e;
-    const int e = seg_mb[SEG_INTS + slot];
+    const int e = seg[SEG_INTS + slot];
     const int rem = t - slot * per_e;
     const int mb = rem / a.n_tiles;
     const int nb = rem - mb * a.n_tiles;
     tl.e = e;
     tl.nb = nb;
-    tl.a_row = int64_t(mb) * BM;
-    tl.k0 = int64_t(seg_mb[e]) * 128;
-    tl.k_tiles = (seg_mb[e + 1] - seg_mb[e]) * (128 / Ops<EPI>::KSTEP);
+    tl.a_row = int64_t(mb) * MMA_M + rank * BM;
+    tl.valid = tl.a_row < a.M;
+    tl.k0 = int64_t(seg[e]) * 128;
+    tl.k_tiles = (seg[e + 1] - seg[e]) * (128 / Ops<EPI>::KSTEP);
     tl.n0 = nb * BN;
     tl.b_row0 = tl.n0;
     tl.b_row1 = tl.n0 + 128;
@@ -347,28 +392,26 @@ __device__ __forceinline__ void decode_tile(const GemmArgs& a, const int* seg_mb
   }
 }
 
-// Global sources of one tile's K steps (TMA coordinates and scale atoms).
+// Global sources of one CTA's K steps: TMA coordinates of its A and B boxes and
+// the rows (in 256-byte units, two per atom) of the scale atoms it stages.
 struct TileSrc {
-  int a_row, b_row0, b_row1, k0, k_tiles;
-  bool second;
-  const uint8_t *sfa, *sfb0, *sfb1;
+  int a_row, b_row, k0, k_tiles;
+  int sfa_y, sfb0_y, sfb1_y;
 };
 
 template <int EPI>
-__device__ __forceinline__ void tile_src(const GemmArgs& a, const int* seg_mb, int t, TileSrc& ts) {
+__device__ __forceinline__ void tile_src(const GemmArgs& a, const int* seg, int t, int rank, TileSrc& ts) {
   Tile tl;
-  decode_tile<EPI>(a, seg_mb, t, tl);
+  decode_tile<EPI>(a, seg, t, rank, tl);
   const int64_t sfa_row_atoms = a.sfa_K / BK;
   const int64_t sfb_row_atoms = a.sfb_K / BK;
   ts.a_row = int(tl.a_row);
-  ts.b_row0 = int(tl.b_row0);
-  ts.b_row1 = int(tl.b_row1);
+  ts.b_row = int(rank == 0 ? tl.b_row0 : tl.b_row1);
   ts.k0 = int(tl.k0);
   ts.k_tiles = tl.k_tiles;
-  ts.second = tl.second;
-  ts.sfa = a.sfa + ((tl.a_row / BM) * sfa_row_atoms + tl.k0 / BK) * SF_ATOM;
-  ts.sfb0 = a.sfb + ((tl.b_row0 / 128) * sfb_row_atoms + tl.k0 / BK) * SF_ATOM;
-  ts.sfb1 = a.sfb + ((tl.b_row1 / 128) * sfb_row_atoms + tl.k0 / BK) * SF_ATOM;
+  ts.sfa_y = int(2 * ((tl.a_row / BM) * sfa_row_atoms + tl.k0 / BK));
+  ts.sfb0_y = int(2 * ((tl.b_row0 / 128) * sfb_row_atoms + tl.k0 / BK));
+  ts.sfb1_y = int(2 * ((tl.b_row1 / 128) * sfb_row_atoms + tl.k0 / BK));
 }
 
 // Bounded wait on an mbarrier phase.  Returns false when the CTA aborted or
@@ -482,11 +525,18 @@ __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + _
 // One epilogue warp on one tile.  The warp owns TMEM lane quarter q (32 rows) and
 // column group cg: 64 accumulator columns cg*64.. of an N=256 tile, or gate
 // columns cg*32.. and up columns 128+cg*32.. of a ScaledSwiGLU tile.  It pulls its
-// columns into registers, releases the accumulator (tmem_empty) and only then
-// runs the epilogue math, so the next tile's MMAs overlap it.
+// columns into registers, releases the accumulator (an arrival on the leader's
+// tmem_empty, at cluster address tmem_empty_c) and only then runs the epilogue
+// math, so the next tile's MMAs overlap it.  A CTA whose half of the pair tile
+// lies past the expert's rows (or past M) releases the accumulator and writes nothing.
 template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl, uint32_t tmem_row, int q, int cg,
-                                              int lane, uint64_t* tmem_empty, float* tr) {
+                                              int lane, uint32_t tmem_empty_c, float* tr) {
+  if (!tl.valid) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(tmem_empty_c);
+    return;
+  }
   const int64_t row = tl.out_row + q * 32 + lane;        // output / permuted row of this thread
   const int64_t row_blk0 = tl.out_row + q * 32;
   const int ncols = tl.second ? 256 : 128;                // valid accumulator columns
@@ -520,7 +570,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
   }
   tc_fence_before();
   __syncwarp();
-  if (lane == 0) mbar_arrive(tmem_empty);
+  if (lane == 0) mbar_arrive_cluster(tmem_empty_c);
 
   if (EPI == EPI_BF16 || EPI == EPI_B16_OUT || EPI == EPI_T8_OUT) {
     if (c0 >= ncols) return;
@@ -657,129 +707,154 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
 template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         const GemmArgs args) {
   using L = Lay<EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
-  uint64_t* empty = full + L::STG;
-  uint64_t* sf_ready = empty + L::STG;
-  uint64_t* tmem_full = sf_ready + L::STG;       // one per accumulator buffer
+  uint64_t* empty = full + L::NSTG;
+  uint64_t* tmem_full = empty + L::NSTG;         // one per accumulator buffer
   uint64_t* tmem_empty = tmem_full + 2;
   uint64_t* drain = tmem_empty + 2;
-  uint64_t* drain_sf = drain + 1;
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_s = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
-  int* seg_mb = reinterpret_cast<int*>(smem + L::OFF_SEG);
+  int* seg = reinterpret_cast<int*>(smem + L::OFF_SEG);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();       // 0: leader (issues the MMAs), 1: peer
+  const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < L::STG; ++s) {
-      mbar_init(&full[s], 1);
+    for (int s = 0; s < L::NSTG; ++s) {
+      mbar_init(&full[s], 1);                    // the leader expects both CTAs' bytes
       mbar_init(&empty[s], 1);
-      mbar_init(&sf_ready[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
-      mbar_init(&tmem_empty[b], NUM_EPI_WARPS);
+      mbar_init(&tmem_empty[b], 2 * NUM_EPI_WARPS);
     }
     mbar_init(drain, 1);
-    mbar_init(drain_sf, 1);
     *abort_s = 0;
-    int acc = 0;
+    int acc = 0, acc_pb = 0;
     for (int e = 0; e < args.E; ++e) {
-      seg_mb[e] = acc;
-      acc += (args.split_sizes[e] + 127) >> 7;
+      seg[e] = acc;
+      seg[SEG_PB + e] = acc_pb;
+      const int nblk = (args.split_sizes[e] + 127) >> 7;
+      acc += nblk;
+      acc_pb += (nblk + 1) >> 1;
     }
-    seg_mb[args.E] = acc;
+    seg[args.E] = acc;
+    seg[SEG_PB + args.E] = acc_pb;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (!Ops<EPI>::NOSF) {
+      prefetch_tmap(&tmSFA);
+      prefetch_tmap(&tmSFB);
+    }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_base_s, TMEM_COLS);
+    tmem_alloc(tmem_base_s, TMEM_COLS);          // collectively with the peer CTA
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();                                // the pair's barriers are initialised before any remote arrival
   tc_fence_after();
   if (args.mode == 1) {
     // rank of expert e: experts with more 128-token blocks, or as many and a lower id, come first
-    int* order = seg_mb + SEG_INTS;
+    int* order = seg + SEG_INTS;
     for (int e = threadIdx.x; e < args.E; e += blockDim.x) {
-      const int me = seg_mb[e + 1] - seg_mb[e];
-      int rank = 0;
+      const int me = seg[e + 1] - seg[e];
+      int rank_e = 0;
       for (int f = 0; f < args.E; ++f) {
-        const int other = seg_mb[f + 1] - seg_mb[f];
-        rank += (other > me) || (other == me && f < e);
+        const int other = seg[f + 1] - seg[f];
+        rank_e += (other > me) || (other == me && f < e);
       }
-      order[rank] = e;
+      order[rank_e] = e;
     }
     __syncthreads();
   }
   const uint32_t tmem = *tmem_base_s;
-  const int total = tile_count(args, seg_mb);
+  const int total = tile_count(args, seg);
   const uint64_t lim = args.wait_limit_ns != 0 ? args.wait_limit_ns : kWaitLimitNs;
   // the padded segments must fit the permuted capacity (rows in mode 0, K in mode 1)
-  if (int64_t(seg_mb[args.E]) * BM > args.cap) {
+  if (int64_t(seg[args.E]) * BM > args.cap) {
     if (threadIdx.x == 0) report_error(args.err, MOE_ERR_DEVICE_BOUNDS, SITE_GEMM_PRODUCER + 9);
   } else if (warp == 0) {
     if (lane == 0 && !args.selftest_no_loads) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producer (both CTAs) ----------------
+      const uint32_t full_c0 = mapa_shared(smem_u32(full), 0);   // the leader's full[0]
       int it = 0;
-      int last_round[L::STG];
+      bool issued_any = false;
+      int last_round[L::NSTG];
 #pragma unroll
-      for (int s = 0; s < L::STG; ++s) last_round[s] = -1;
+      for (int s = 0; s < L::NSTG; ++s) last_round[s] = -1;
       bool ok = true;
       TileSrc cur, nxt;
-      if (blockIdx.x < total) tile_src<EPI>(args, seg_mb, blockIdx.x, cur);
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        if (t + int(gridDim.x) < total) tile_src<EPI>(args, seg_mb, t + gridDim.x, nxt);
-        const uint32_t bytes = Ops<EPI>::NOSF ? A_TILE + (cur.second ? B_HALF * 2 : B_HALF)
-                                              : A_TILE + SF_ATOM * 2 + (cur.second ? (B_HALF * 2 + SF_ATOM) : B_HALF);
-        for (int kt = 0; kt < cur.k_tiles; ++kt, ++it) {
-          const int s = it % L::STG;
-          const int round = it / L::STG;
-          if (!wait_phase(&empty[s], (round & 1) ^ 1, abort_s, args.err, SITE_GEMM_PRODUCER, lim)) {
+      if (pair < total) tile_src<EPI>(args, seg, pair, rank, cur);
+      for (int t = pair; t < total && ok; t += num_pairs) {
+        if (t + num_pairs < total) tile_src<EPI>(args, seg, t + num_pairs, rank, nxt);
+        for (int kt0 = 0; kt0 < cur.k_tiles; kt0 += L::PER, ++it) {
+          const int st = it % L::NSTG;
+          const int round = it / L::NSTG;
+          const int nk = min(L::PER, cur.k_tiles - kt0);     // K steps in this stage (the last may be short)
+          if (!wait_phase(&empty[st], (round & 1) ^ 1, abort_s, args.err, SITE_GEMM_PRODUCER, lim)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], bytes);
-          last_round[s] = round;
-          const int kc = cur.k0 + kt * Ops<EPI>::KSTEP;
-          tma_load_2d(smem + L::OFF_A + s * A_TILE, &tmA, kc, cur.a_row, &full[s]);
-          tma_load_2d(smem + L::OFF_B + s * L::B_T, &tmB, kc, cur.b_row0, &full[s]);
-          if (cur.second) tma_load_2d(smem + L::OFF_B + s * L::B_T + B_HALF, &tmB, kc, cur.b_row1, &full[s]);
+          const uint32_t bar_c = full_c0 + uint32_t(st) * 8u;
+          // the leader expects both CTAs' bytes; the peer's copies complete on the same barrier.
+          // Scale boxes always carry two atoms (past the tile's K: unused).
+          const uint32_t bytes = uint32_t(nk) * (A_TILE + B_HALF) + (Ops<EPI>::NOSF ? 0u : 3u * L::PER * SF_ATOM);
+          if (rank == 0) mbar_arrive_expect_tx(&full[st], 2 * bytes);
+          last_round[st] = round;
+          issued_any = true;
+          for (int sub = 0; sub < nk; ++sub) {
+            const int slot = st * L::PER + sub;
+            const int kc = cur.k0 + (kt0 + sub) * Ops<EPI>::KSTEP;
+            tma_load_2d(smem + L::OFF_A + slot * A_TILE, &tmA, kc, cur.a_row, bar_c);
+            tma_load_2d(smem + L::OFF_B + slot * B_HALF, &tmB, kc, cur.b_row, bar_c);
+          }
           if (!Ops<EPI>::NOSF) {
-            bulk_load(smem + L::OFF_SFA + s * SF_ATOM, cur.sfa + kt * SF_ATOM, SF_ATOM, &full[s]);
-            bulk_load(smem + L::OFF_SFB + s * L::SFB_T, cur.sfb0 + kt * SF_ATOM, SF_ATOM, &full[s]);
-            if (cur.second) bulk_load(smem + L::OFF_SFB + s * L::SFB_T + SF_ATOM, cur.sfb1 + kt * SF_ATOM, SF_ATOM, &full[s]);
+            const int slot = st * L::PER;
+            tma_load_2d(smem + L::OFF_SFA + slot * SF_ATOM, &tmSFA, 0, cur.sfa_y + 2 * kt0, bar_c);
+            tma_load_2d(smem + L::OFF_SFB0 + slot * SF_ATOM, &tmSFB, 0, cur.sfb0_y + 2 * kt0, bar_c);
+            tma_load_2d(smem + L::OFF_SFB1 + slot * SF_ATOM, &tmSFB, 0, cur.sfb1_y + 2 * kt0, bar_c);
           }
         }
         cur = nxt;
       }
-      if (!ok) {
-        // let copies already issued land before the CTA exits
-        for (int s = 0; s < L::STG; ++s) {
-          if (last_round[s] < 0) continue;
+      if (!ok && issued_any) {
+        // let copies already issued land before the CTA exits: the leader watches the full
+        // barriers (which also count the peer's copies); the peer, whose copies signal the
+        // leader, gives them a fixed grace period
+        if (rank == 0) {
+          for (int s = 0; s < L::NSTG; ++s) {
+            if (last_round[s] < 0) continue;
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&full[s], last_round[s] & 1) && globaltimer_ns() - t0 < 20000000ull) {
+            }
+          }
+        } else {
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&full[s], last_round[s] & 1) && globaltimer_ns() - t0 < 20000000ull) {
+          while (globaltimer_ns() - t0 < 2000000ull) {
           }
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (leader) ----------------
       int it = 0, tcount = 0;
       bool ok = true, issued = false;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
+      for (int t = pair; t < total && ok; t += num_pairs, ++tcount) {
         Tile tl;
-        decode_tile<EPI>(args, seg_mb, t, tl);
+        decode_tile<EPI>(args, seg, t, 0, tl);
         // accumulator buffer of this tile and how often it was used before
         const int ab = Ops<EPI>::ACC_BUFS == 2 ? (tcount & 1) : 0;
         const int use = Ops<EPI>::ACC_BUFS == 2 ? (tcount >> 1) : tcount;
@@ -789,39 +864,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const int n = tl.second ? 256 : 128;
-        for (int kt = 0; kt < tl.k_tiles; ++kt, ++it) {
-          const int s = it % L::STG;
-          const int round = it / L::STG;
-          // the stage's operands have landed and its scale factors sit in TMEM
-          if (!wait_phase(&sf_ready[s], round & 1, abort_s, args.err, SITE_GEMM_MMA, lim)) {
+        for (int kt0 = 0; kt0 < tl.k_tiles; kt0 += L::PER, ++it) {
+          const int st = it % L::NSTG;
+          const int round = it / L::NSTG;
+          const int nk = min(L::PER, tl.k_tiles - kt0);
+          // both CTAs' operands (and scale atoms) of the stage have landed
+          if (!wait_phase(&full[st], round & 1, abort_s, args.err, SITE_GEMM_MMA, lim)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t tm_sfa = tmem + TM_SF0 + uint32_t(s) * TM_SF_STRIDE;
-          const uint32_t tm_sfb = tm_sfa + 4;
-          const uint64_t adesc = desc_sw128(smem_u32(smem + L::OFF_A + s * A_TILE));
-          const uint64_t bdesc = desc_sw128(smem_u32(smem + L::OFF_B + s * L::B_T));
+          for (int sub = 0; sub < nk; ++sub) {
+            const int slot = st * L::PER + sub;
+            const int kt = kt0 + sub;
+            const uint32_t tm_sfa = tmem + TM_SF0 + uint32_t(slot) * TM_SF_STRIDE;
+            const uint32_t tm_sfb = tm_sfa + 4;
+            if (!Ops<EPI>::NOSF) {
+              // issued by this thread ahead of the MMAs that read them: executed in order
+              tc_cp_sf(tm_sfa, desc_sf(smem_u32(smem + L::OFF_SFA + slot * SF_ATOM)));
+              tc_cp_sf(tm_sfb, desc_sf(smem_u32(smem + L::OFF_SFB0 + slot * SF_ATOM)));
+              tc_cp_sf(tm_sfb + 4, desc_sf(smem_u32(smem + L::OFF_SFB1 + slot * SF_ATOM)));
+            }
+            const uint64_t adesc = desc_sw128(smem_u32(smem + L::OFF_A + slot * A_TILE));
+            const uint64_t bdesc = desc_sw128(smem_u32(smem + L::OFF_B + slot * B_HALF));
 #pragma unroll
-          for (int kk = 0; kk < BK / 32; ++kk) {
-            // +32 bytes along K inside the 128-byte swizzle atom = +2 in the encoded start address
-            if (Ops<EPI>::B16) {
-              tc_mma_bf16(acc, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_bf16(n), (kt | kk) != 0);
-              continue;
+            for (int kk = 0; kk < BK / 32; ++kk) {
+              // +32 bytes along K inside the 128-byte swizzle atom = +2 in the encoded start address
+              if (Ops<EPI>::B16) {
+                tc_mma_bf16(acc, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_bf16(BN),
+                            (kt | kk) != 0);
+                continue;
+              }
+              if (Ops<EPI>::T8) {
+                tc_mma_f8(acc, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_f8(BN), (kt | kk) != 0);
+                continue;
+              }
+              tc_mma_mxf8(acc, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_mxf8(BN, kk), tm_sfa,
+                          tm_sfb, (kt | kk) != 0);
             }
-            if (Ops<EPI>::T8) {
-              tc_mma_f8(acc, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_f8(n), (kt | kk) != 0);
-              continue;
-            }
-            tc_mma_mxf8(acc, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_mxf8(n, kk), tm_sfa, tm_sfb,
-                        (kt | kk) != 0);
           }
           issued = true;
-          tc_commit(&empty[s]);
+          tc_commit(&empty[st]);                 // frees the stage in both CTAs
         }
         if (!ok) break;
-        tc_commit(&tmem_full[ab]);
+        tc_commit(&tmem_full[ab]);               // both halves of the accumulator are ready
       }
       if (!ok && issued) {
         tc_commit(drain);
@@ -830,53 +916,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
-  } else if (warp == SF_WARP) {
-    if (lane == 0) {
-      // ---------------- scale factors: shared memory -> TMEM ----------------
-      // Issued from their own thread, so the copies are not queued behind the
-      // MMA stream; each stage has its own TMEM columns.
-      int it = 0;
-      bool ok = true, issued = false;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        Tile tl;
-        decode_tile<EPI>(args, seg_mb, t, tl);
-        for (int kt = 0; kt < tl.k_tiles; ++kt, ++it) {
-          const int s = it % L::STG;
-          const int round = it / L::STG;
-          if (!wait_phase(&full[s], round & 1, abort_s, args.err, SITE_GEMM_MMA + 1, lim)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t tm_sfa = tmem + TM_SF0 + uint32_t(s) * TM_SF_STRIDE;
-          const uint32_t tm_sfb = tm_sfa + 4;
-          if (!Ops<EPI>::NOSF) {
-            tc_cp_sf(tm_sfa, desc_sf(smem_u32(smem + L::OFF_SFA + s * SF_ATOM)));
-            tc_cp_sf(tm_sfb, desc_sf(smem_u32(smem + L::OFF_SFB + s * L::SFB_T)));
-            if (tl.second) tc_cp_sf(tm_sfb + 4, desc_sf(smem_u32(smem + L::OFF_SFB + s * L::SFB_T + SF_ATOM)));
-          }
-          tc_commit(&sf_ready[s]);
-          issued = true;
-        }
-      }
-      if (!ok && issued) {
-        tc_commit(drain_sf);
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(drain_sf, 0) && globaltimer_ns() - t0 < 20000000ull) {
-        }
-      }
-    }
   } else {
-    // ---------------- epilogue warps 2..17 ----------------
+    // ---------------- epilogue warps 2..17 (both CTAs) ----------------
     const int q = warp & 3;                    // TMEM lane quarter this warp may access
     const int cg = (warp - 2) >> 2;            // column group 0..3
     const uint32_t tmem_row = tmem + (uint32_t(q * 32) << 16);
+    const uint32_t tmem_empty_c0 = mapa_shared(smem_u32(tmem_empty), 0);
     float* tr = reinterpret_cast<float*>(smem + L::OFF_TR) + (warp - 2) * TR_WARP_FLOATS;
     int tcount = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
+    for (int t = pair; t < total; t += num_pairs, ++tcount) {
       Tile tl;
-      decode_tile<EPI>(args, seg_mb, t, tl);
-      if (Ops<EPI>::SWIGLU_BWD) {
+      decode_tile<EPI>(args, seg, t, int(rank), tl);
+      if (Ops<EPI>::SWIGLU_BWD && tl.valid) {
         // pull this thread's saved g and u (128 B each) toward L2 while the MMAs run
         const __nv_bfloat16* grow = args.gu + (tl.out_row + q * 32 + lane) * (2 * int64_t(args.I)) + tl.n0 + cg * 64;
         asm volatile("prefetch.global.L2 [%0];" ::"l"(grow));
@@ -886,11 +937,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int use = Ops<EPI>::ACC_BUFS == 2 ? (tcount >> 1) : tcount;
       if (!wait_phase(&tmem_full[ab], use & 1, abort_s, args.err, SITE_GEMM_EPILOGUE, lim)) break;
       tc_fence_after();
-      epilogue_tile<EPI>(args, tl, tmem_row + uint32_t(ab) * 256u, q, cg, lane, &tmem_empty[ab], tr);
+      epilogue_tile<EPI>(args, tl, tmem_row + uint32_t(ab) * 256u, q, cg, lane, tmem_empty_c0 + uint32_t(ab) * 8u,
+                         tr);
     }
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();                                // no CTA leaves while the pair's MMAs or arrivals may touch it
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
@@ -928,8 +981,24 @@ bool encode_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, bool 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over n_atoms 512-byte scale atoms seen as [2 * n_atoms][256] bytes: one
+// {256, 4} box is two consecutive atoms (row 2i = atom i), the two K steps of a
+// barrier stage; no swizzle, so the atoms land in shared memory byte for byte.
+bool encode_sf_map(CUtensorMap* m, const void* base, int64_t n_atoms) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {256, cuuint64_t(2 * n_atoms)};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {256, 4};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int EPI>
-cudaError_t launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& a, int grid, cudaStream_t st) {
+cudaError_t launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msfa,
+                       const CUtensorMap& msfb, const GemmArgs& a, int grid, cudaStream_t st) {
   // the shared-memory attribute is per device: set it once on each device this process uses
   constexpr int kMaxDevices = 64;
   static std::atomic<bool> attr_set[kMaxDevices];
@@ -942,7 +1011,21 @@ cudaError_t launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, const GemmA
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) attr_set[dev].store(true, std::memory_order_release);
   }
-  grouped_gemm_kernel<EPI><<<grid, NUM_THREADS, Lay<EPI>::SMEM_BYTES, st>>>(ma, mb, a);
+  // CTA pairs: clusters of two along x
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = Lay<EPI>::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<EPI>, ma, mb, msfa, msfb, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -952,27 +1035,39 @@ cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64
                                 const void* B, int64_t b_rows, int64_t b_K, int64_t max_tiles, cudaStream_t st,
                                 char* msg, size_t msg_len) {
   if (max_tiles <= 0) return cudaSuccess;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, msfa, msfb;
   const bool b16 = (epi == EPI_B16_OUT || epi == EPI_B16_FWD_SWIGLU || epi == EPI_B16_BWD_SWIGLU);
+  const bool t8 = (epi == EPI_T8_OUT || epi == EPI_T8_FWD_SWIGLU || epi == EPI_T8_BWD_SWIGLU);
   if (!encode_map(&ma, A, a_rows, a_K, b16) || !encode_map(&mb, B, b_rows, b_K, b16)) {
     snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed (A %lld x %lld, B %lld x %lld)", (long long)a_rows,
              (long long)a_K, (long long)b_rows, (long long)b_K);
     return cudaErrorInvalidValue;
   }
+  if (b16 || t8) {
+    msfa = ma;                                   // no scale factors: never read
+    msfb = ma;
+  } else if (!encode_sf_map(&msfa, a.sfa, (a_rows / 128) * (a.sfa_K / BK)) ||
+             !encode_sf_map(&msfb, a.sfb, (b_rows / 128) * (a.sfb_K / BK))) {
+    snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed for the scale atoms (A %lld x %lld, B %lld x %lld)",
+             (long long)a_rows, (long long)a.sfa_K, (long long)b_rows, (long long)a.sfb_K);
+    return cudaErrorInvalidValue;
+  }
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = int(max_tiles < sms ? max_tiles : sms);
+  // persistent CTA pairs: at most one pair per two SMs, no more pairs than 128-row tiles
+  const int64_t pairs_max = sms / 2;
+  const int grid = 2 * int(max_tiles < pairs_max ? max_tiles : pairs_max);
   switch (epi) {
-    case EPI_BF16: return launch_epi<EPI_BF16>(ma, mb, a, grid, st);
-    case EPI_FWD_SWIGLU: return launch_epi<EPI_FWD_SWIGLU>(ma, mb, a, grid, st);
-    case EPI_BWD_SWIGLU: return launch_epi<EPI_BWD_SWIGLU>(ma, mb, a, grid, st);
-    case EPI_B16_OUT: return launch_epi<EPI_B16_OUT>(ma, mb, a, grid, st);
-    case EPI_B16_FWD_SWIGLU: return launch_epi<EPI_B16_FWD_SWIGLU>(ma, mb, a, grid, st);
-    case EPI_T8_OUT: return launch_epi<EPI_T8_OUT>(ma, mb, a, grid, st);
-    case EPI_T8_FWD_SWIGLU: return launch_epi<EPI_T8_FWD_SWIGLU>(ma, mb, a, grid, st);
-    case EPI_B16_BWD_SWIGLU: return launch_epi<EPI_B16_BWD_SWIGLU>(ma, mb, a, grid, st);
-    case EPI_T8_BWD_SWIGLU: return launch_epi<EPI_T8_BWD_SWIGLU>(ma, mb, a, grid, st);
+    case EPI_BF16: return launch_epi<EPI_BF16>(ma, mb, msfa, msfb, a, grid, st);
+    case EPI_FWD_SWIGLU: return launch_epi<EPI_FWD_SWIGLU>(ma, mb, msfa, msfb, a, grid, st);
+    case EPI_BWD_SWIGLU: return launch_epi<EPI_BWD_SWIGLU>(ma, mb, msfa, msfb, a, grid, st);
+    case EPI_B16_OUT: return launch_epi<EPI_B16_OUT>(ma, mb, msfa, msfb, a, grid, st);
+    case EPI_B16_FWD_SWIGLU: return launch_epi<EPI_B16_FWD_SWIGLU>(ma, mb, msfa, msfb, a, grid, st);
+    case EPI_T8_OUT: return launch_epi<EPI_T8_OUT>(ma, mb, msfa, msfb, a, grid, st);
+    case EPI_T8_FWD_SWIGLU: return launch_epi<EPI_T8_FWD_SWIGLU>(ma, mb, msfa, msfb, a, grid, st);
+    case EPI_B16_BWD_SWIGLU: return launch_epi<EPI_B16_BWD_SWIGLU>(ma, mb, msfa, msfb, a, grid, st);
+    case EPI_T8_BWD_SWIGLU: return launch_epi<EPI_T8_BWD_SWIGLU>(ma, mb, msfa, msfb, a, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
