@@ -96,10 +96,12 @@ struct Ops {
 // measured on this GPU, what TMA delivers to an SM grows with the bytes behind
 // each barrier stage (about 35 B/clk with 32 KB stages, 50 with 64 KB), and the
 // pair needs 64 B/clk per SM to keep its MMAs busy.
+constexpr int STAGE_STEPS = 2;                  // K steps (slots) per barrier stage
+
 template <int EPI>
 struct Lay {
   static constexpr int STG = 6;                  // slots of one K step
-  static constexpr int PER = 2;                  // slots per barrier stage
+  static constexpr int PER = STAGE_STEPS;        // slots per barrier stage
   static constexpr int NSTG = STG / PER;         // barrier stages
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STG * A_TILE;
@@ -117,6 +119,7 @@ struct Lay {
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 B
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(TM_SF0 + STG * TM_SF_STRIDE <= TM_STASH, "TMEM budget");
+  static_assert(STG % PER == 0, "slots come in whole barrier stages");
 };
 
 // ---- PTX wrappers -------------------------------------------------------------------
@@ -982,14 +985,14 @@ bool encode_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, bool 
 }
 
 // 2-D map over n_atoms 512-byte scale atoms seen as [2 * n_atoms][256] bytes: one
-// {256, 4} box is two consecutive atoms (row 2i = atom i), the two K steps of a
-// barrier stage; no swizzle, so the atoms land in shared memory byte for byte.
+// {256, 2 * STAGE_STEPS} box is the consecutive atoms of a barrier stage's K steps
+// (row 2i = atom i); no swizzle, so the atoms land in shared memory byte for byte.
 bool encode_sf_map(CUtensorMap* m, const void* base, int64_t n_atoms) {
   EncodeTiledFn fn = get_encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {256, cuuint64_t(2 * n_atoms)};
   cuuint64_t strides[1] = {256};
-  cuuint32_t box[2] = {256, 4};
+  cuuint32_t box[2] = {256, 2 * STAGE_STEPS};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
