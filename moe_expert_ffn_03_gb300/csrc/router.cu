@@ -9,7 +9,9 @@
 //   router_dlogits_kernel   one warp per token, straight-through top-k softmax;
 //   router_dx_kernel        dx[t] += sum_e dl[t][e] W_r[e] (bf16 in place);
 //   router_dw_partial/reduce dW_r = dl^T x over fixed token chunks, summed in
-//                           chunk order.
+//                           chunk order; each chunk's CTA stages 16-token
+//                           slices of dl and x in shared memory and keeps a
+//                           4x4 block of outputs per thread.
 #include "kernels.cuh"
 
 namespace moe {
@@ -147,43 +149,83 @@ __global__ void __launch_bounds__(256) router_dx_kernel(const float* __restrict_
   }
 }
 
-constexpr int RT_DW_CHUNKS = 8;
+// dW_r tiles: ET experts x (4096 / ET) hidden columns per CTA, 256 threads with a
+// 4 x 4 block each; tokens in slices of RT_DW_TS staged in shared memory.  The
+// number of token chunks depends on E and H only (it sizes the workspace): enough
+// CTAs to fill the GPU a few times over, between 8 and 64.
+constexpr int RT_DW_TS = 16;
 
-// partial[c][e][h] = sum over the tokens of chunk c of dl[t][e] * x[t][h]; CTA = 32
-// hidden columns x all experts of one token chunk.
-template <int EPT>
+__host__ __device__ inline int router_dw_et(int E) { return E <= 8 ? 8 : E <= 16 ? 16 : E <= 32 ? 32 : 64; }
+inline int router_dw_chunks(int E, int H) {
+  const int et = router_dw_et(E), ht = 4096 / et;
+  const int tiles = ((H + ht - 1) / ht) * ((E + et - 1) / et);
+  const int c = (600 + tiles - 1) / tiles;
+  return c < 8 ? 8 : c > 64 ? 64 : c;
+}
+
+// partial[c][e][h] = sum over the tokens of chunk c (ascending) of dl[t][e] * x[t][h].
+template <int ET>
 __global__ void __launch_bounds__(256) router_dw_partial_kernel(const float* __restrict__ dl,
                                                                 const __nv_bfloat16* __restrict__ x, int T, int H,
-                                                                int E, float* __restrict__ partial) {
-  const int h = blockIdx.x * 32 + (threadIdx.x & 31);
-  const int eg = threadIdx.x >> 5;
-  const int c = blockIdx.y;
-  const int per = (T + RT_DW_CHUNKS - 1) / RT_DW_CHUNKS;
-  const int ta = c * per, tb = min(T, ta + per);
-  float acc[EPT];
+                                                                int E, int chunks, float* __restrict__ partial) {
+  constexpr int HT = 4096 / ET;              // hidden columns of the tile
+  constexpr int TH = HT / 4;                 // threads along h (4 columns each)
+  __shared__ __align__(16) float dls[RT_DW_TS][ET];
+  __shared__ __align__(16) __nv_bfloat16 xs[RT_DW_TS][HT];
+  const int h0 = blockIdx.x * HT, e0 = blockIdx.y * ET, c = blockIdx.z;
+  const int hg = threadIdx.x % TH, eg = threadIdx.x / TH;   // columns h0+4hg.., experts e0+4eg..
+  const int per = (T + chunks - 1) / chunks;
+  const int ta = min(T, c * per), tb = min(T, ta + per);
+  float acc[4][4];
 #pragma unroll
-  for (int j = 0; j < EPT; ++j) acc[j] = 0.f;
-  for (int t = ta; t < tb; ++t) {
-    const float xv = __bfloat162float(x[int64_t(t) * H + h]);
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-      const int e = eg + 8 * j;
-      if (e < E) acc[j] += dl[int64_t(t) * E + e] * xv;
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int ts = ta; ts < tb; ts += RT_DW_TS) {
+    __syncthreads();
+    // dl slice: RT_DW_TS rows x ET floats (zero past T or E)
+    for (int i = threadIdx.x; i < RT_DW_TS * ET; i += 256) {
+      const int r = i / ET, e = i % ET;
+      const int t = ts + r;
+      dls[r][e] = (t < tb && e0 + e < E) ? dl[int64_t(t) * E + e0 + e] : 0.f;
+    }
+    // x slice: RT_DW_TS rows x HT bf16, 8 at a time (H is a multiple of 8)
+    for (int i = threadIdx.x; i < RT_DW_TS * (HT / 8); i += 256) {
+      const int r = i / (HT / 8), c8 = i % (HT / 8);
+      const int t = ts + r, h = h0 + c8 * 8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t < tb && h < H) v = *reinterpret_cast<const uint4*>(x + int64_t(t) * H + h);
+      *reinterpret_cast<uint4*>(&xs[r][c8 * 8]) = v;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int r = 0; r < RT_DW_TS; ++r) {
+      const float4 d = *reinterpret_cast<const float4*>(&dls[r][4 * eg]);
+      const uint2 xv = *reinterpret_cast<const uint2*>(&xs[r][4 * hg]);
+      const float xf[4] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y)};
+      const float df[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] += df[i] * xf[j];
     }
   }
 #pragma unroll
-  for (int j = 0; j < EPT; ++j) {
-    const int e = eg + 8 * j;
-    if (e < E) partial[(int64_t(c) * E + e) * H + h] = acc[j];
+  for (int i = 0; i < 4; ++i) {
+    const int e = e0 + 4 * eg + i;
+    const int h = h0 + 4 * hg;
+    if (e >= E || h >= H) continue;
+    *reinterpret_cast<float4*>(partial + (int64_t(c) * E + e) * H + h) =
+        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
   }
 }
 
 __global__ void __launch_bounds__(256) router_dw_reduce_kernel(const float* __restrict__ partial, int64_t n,
-                                                               float* __restrict__ dw) {
+                                                               int chunks, float* __restrict__ dw) {
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
   float s = 0.f;
-  for (int c = 0; c < RT_DW_CHUNKS; ++c) s += partial[int64_t(c) * n + i];
+  for (int c = 0; c < chunks; ++c) s += partial[int64_t(c) * n + i];
   dw[i] = s;
 }
 
@@ -210,13 +252,9 @@ template <int EPT>
 struct FwdK {
   static constexpr auto fn = router_fwd_kernel<EPT>;
 };
-template <int EPT>
-struct DwK {
-  static constexpr auto fn = router_dw_partial_kernel<EPT>;
-};
 }  // namespace
 
-size_t router_partial_bytes(int E, int H) { return size_t(RT_DW_CHUNKS) * E * H * sizeof(float); }
+size_t router_partial_bytes(int E, int H) { return size_t(router_dw_chunks(E, H)) * E * H * sizeof(float); }
 
 cudaError_t launch_router_fwd(const void* x, const void* w, int T, int H, int E, float* logits, cudaStream_t st) {
   const size_t smem = size_t(RT_HC) * RT_XP * sizeof(float) + size_t(E) * RT_HC * sizeof(__nv_bfloat16);
@@ -236,11 +274,20 @@ cudaError_t launch_router_bwd(const void* x, const void* w, const float* logits,
                                               static_cast<__nv_bfloat16*>(dx));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = dispatch_ept<DwK>(E, dim3(H / 32, RT_DW_CHUNKS), 0, st, static_cast<const float*>(dl),
-                        static_cast<const __nv_bfloat16*>(x), T, H, E, partial);
+  const int chunks = router_dw_chunks(E, H);
+  const int et = router_dw_et(E), ht = 4096 / et;
+  const dim3 grid(unsigned((H + ht - 1) / ht), unsigned((E + et - 1) / et), unsigned(chunks));
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  switch (et) {
+    case 8: router_dw_partial_kernel<8><<<grid, 256, 0, st>>>(dl, xb, T, H, E, chunks, partial); break;
+    case 16: router_dw_partial_kernel<16><<<grid, 256, 0, st>>>(dl, xb, T, H, E, chunks, partial); break;
+    case 32: router_dw_partial_kernel<32><<<grid, 256, 0, st>>>(dl, xb, T, H, E, chunks, partial); break;
+    default: router_dw_partial_kernel<64><<<grid, 256, 0, st>>>(dl, xb, T, H, E, chunks, partial); break;
+  }
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t n = int64_t(E) * H;
-  router_dw_reduce_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(partial, n, dw);
+  router_dw_reduce_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(partial, n, chunks, dw);
   return cudaGetLastError();
 }
 

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from helpers import assert_close
-from moe_expert_ffn_03_gb300 import build, configs, synth
+from moe_expert_ffn_03_gb300 import binding as B, build, configs, synth
 from moe_expert_ffn_03_gb300.layer import ExpertFFN
 from oracle import expert_ffn as ef
 from oracle import router as ro
@@ -71,3 +71,31 @@ def test_trainable_layer_with_router(T, H, I, E, k, renorm):
     assert_close(L.dlogits.cpu().numpy(), dl, "dlogits")
     assert_close(L.dw_r.cpu().numpy(), dw_r, "dW_r")
     assert_close(f64(L.dx), ro.add_to_bf16(bwd["dx"], dx_r), "dx (experts + router)")
+
+
+@pytest.mark.parametrize("renorm", [1, 0])
+@pytest.mark.parametrize("T,H,E,k", [(8192, 2048, 64, 6), (4096, 4096, 8, 2), (1000, 384, 256, 8), (70, 128, 4, 2)])
+def test_router_backward_direct(T, H, E, k, renorm):
+    """moe_router_bwd alone at the fine-grained and Mixtral hidden sizes (and ragged ones):
+    logits, routing and dprob are made on the host (seeded), so dlogits, the router's
+    dx term and dW_r are compared with the oracle on exactly the device's inputs."""
+    wl = configs.small(T, H, 128, E, k, backward=False)
+    inp = synth.make_inputs(wl, 0)
+    x, logits = inp["x"], inp["logits"]
+    w_r = synth.make_router_weight(wl, 0)
+    idx, prob = rt.route_topk(logits.numpy(), k, renormalize=bool(renorm))
+    dprob = np.random.default_rng(7).normal(0.0, 1e-2, size=(T, k)).astype(np.float32)
+    L = ExpertFFN(T, H, 128, E, k, training=True, renormalize=bool(renorm))
+    dev = lambda a, dt: torch.as_tensor(np.ascontiguousarray(a)).to(device="cuda", dtype=dt)
+    dlogits = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    dx = torch.zeros(T, H, dtype=torch.bfloat16, device="cuda")
+    dw_r = torch.empty(E, H, dtype=torch.float32, device="cuda")
+    B.moe_router_bwd(L.d, x.cuda(), w_r.cuda(), logits.cuda(), dev(idx, torch.int32), dev(prob, torch.float32),
+                     dev(dprob, torch.float32), dlogits, dx, dw_r, L.ws)
+    torch.cuda.synchronize()
+    assert L.device_error() == (0, 0)
+    dl = ro.router_backward(logits.numpy(), idx, prob, dprob, bool(renorm))
+    dx_r, dw_ref = ro.router_input_grads(dl, f64(x), f64(w_r))
+    assert_close(dlogits.cpu().numpy(), dl, "dlogits")
+    assert_close(dw_r.cpu().numpy(), dw_ref, "dW_r")
+    assert_close(f64(dx), ro.add_to_bf16(np.zeros((T, H)), dx_r), "router dx")
