@@ -417,13 +417,17 @@ moe_status moe_unpermute_combine(const moe_dims* d, const void* y_perm, const in
 
 /*
  * moe_router_fwd -- router logits of a linear router: logits[t][e] =
- * sum_h x[t][h] * w_r[e][h], f32 sums in ascending h (page
- * "英伟达开源MoE加速神器", section "三板斧": each token is routed to a few
- * experts; the pages give no router formula, a bias-free linear map is the
- * reading).
- *   x bf16 [T][H]; w_r bf16 [E][H]; logits out f32 [T][E].
+ * sum_h x[t][h] * w_r[e][h] (page "英伟达开源MoE加速神器", section "三板斧":
+ * each token is routed to a few experts; the pages give no router formula, a
+ * bias-free linear map is the reading).  Computed on the tensor cores: bf16
+ * products, f32 accumulation (the order of the partial sums is the MMA's).
+ *   x bf16 [T][H], 16-byte aligned; w_r bf16 [E][H], 16-byte aligned;
+ *   logits out f32 [T][E].
+ *   workspace: the layer's workspace (moe_workspace_size of any mode); its
+ *   error word records device-side failures (moe_get_device_error).
  */
-moe_status moe_router_fwd(const moe_dims* d, const void* x, const void* w_r, float* logits, moe_stream_t stream);
+moe_status moe_router_fwd(const moe_dims* d, const void* x, const void* w_r, float* logits, void* workspace,
+                          size_t workspace_bytes, moe_stream_t stream);
 
 /*
  * moe_router_bwd -- gradient of the router from dprob (grouped_mlp_bwd),

@@ -75,7 +75,7 @@ def lib() -> ctypes.CDLL:
             "moe_get_device_error": ([P, ctypes.POINTER(c_int32), ctypes.POINTER(c_int32), P], c_int32),
             "moe_clear_device_error": ([P, P], c_int32),
             "moe_route_permute_noalloc": ([D, P, P, P, P, P, P, P, P, P, P, P, P, P], c_int32),
-            "moe_router_fwd": ([D, P, P, P, P], c_int32),
+            "moe_router_fwd": ([D, P, P, P, P, c_size_t, P], c_int32),
             "moe_gather_rows": ([D, P, P, P, P, P, c_size_t, P], c_int32),
             "grouped_mlp_fwd_bf16": ([D, P, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
             "moe_transpose_bf16": ([P, c_int32, c_int32, c_int32, P, P], c_int32),
@@ -198,8 +198,9 @@ def grouped_mlp_bwd_bf16(d, dout, split_sizes, row_of, src_of, prob_perm, saved_
                                       workspace.numel() * workspace.element_size(), _st(stream)))
 
 
-def moe_router_fwd(d, x, w_r, logits, stream=None):
-    _check(lib().moe_router_fwd(ctypes.byref(d), _p(x), _p(w_r), _p(logits), _st(stream)))
+def moe_router_fwd(d, x, w_r, logits, workspace, stream=None):
+    _check(lib().moe_router_fwd(ctypes.byref(d), _p(x), _p(w_r), _p(logits), _p(workspace),
+                                workspace.numel() * workspace.element_size(), _st(stream)))
 
 
 def moe_router_bwd(d, x, w_r, logits, idx, prob, dprob, dlogits, dx, dw_r, workspace, stream=None):

@@ -1028,14 +1028,20 @@ moe_status moe_unpermute_combine(const moe_dims* d, const void* y_perm, const in
   return MOE_OK;
 }
 
-moe_status moe_router_fwd(const moe_dims* d, const void* x, const void* w_r, float* logits, moe_stream_t stream) {
+moe_status moe_router_fwd(const moe_dims* d, const void* x, const void* w_r, float* logits, void* workspace,
+                          size_t workspace_bytes, moe_stream_t stream) {
   g_msg[0] = 0;
   moe_status s = check_dims(d);
   if (s != MOE_OK) return s;
   REQUIRE_PTR(x);
   REQUIRE_PTR(w_r);
   REQUIRE_PTR(logits);
-  CUDA_TRY(launch_router_fwd(x, w_r, d->T, d->H, d->E, logits, static_cast<cudaStream_t>(stream)), "router fwd");
+  s = check_ws(d, workspace, workspace_bytes, false);
+  if (s != MOE_OK) return s;
+  const WsLayout w = ws_layout(d, false);
+  CUDA_TRY(launch_router_fwd(x, w_r, d->T, d->H, d->E, logits, at<int>(workspace, w.err),
+                             static_cast<cudaStream_t>(stream), g_msg, sizeof(g_msg)),
+           "router fwd");
   return MOE_OK;
 }
 

@@ -76,7 +76,8 @@ constexpr int TR_WARP_FLOATS = 32 * TR_PITCH;
 // Per-tensor E4M3 kinds: 128 K elements per stage, kind::f8f6f4 MMA, no block scales.
 template <int EPI>
 struct Ops {
-  static constexpr bool B16 = (EPI == EPI_B16_OUT || EPI == EPI_B16_FWD_SWIGLU || EPI == EPI_B16_BWD_SWIGLU);
+  static constexpr bool B16 = (EPI == EPI_B16_OUT || EPI == EPI_B16_FWD_SWIGLU || EPI == EPI_B16_BWD_SWIGLU ||
+                               EPI == EPI_B16_F32_OUT);
   static constexpr bool SWIGLU_BWD = (EPI == EPI_BWD_SWIGLU || EPI == EPI_B16_BWD_SWIGLU || EPI == EPI_T8_BWD_SWIGLU);
   static constexpr bool T8 = (EPI == EPI_T8_OUT || EPI == EPI_T8_FWD_SWIGLU || EPI == EPI_T8_BWD_SWIGLU);
   static constexpr bool NOSF = B16 || T8;         // no scale-factor loads or copies
@@ -575,6 +576,17 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
   __syncwarp();
   if (lane == 0) mbar_arrive_cluster(tmem_empty_c);
 
+  if (EPI == EPI_B16_F32_OUT) {
+    // f32 output [rows_limit][N]: rows past rows_limit and columns past N are not written
+    if (c0 >= ncols || row >= a.rows_limit) return;
+    float* orow = a.out_f32 + row * a.ldo;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const int64_t col = tl.n0 + c0 + i;
+      if (col < a.N) orow[col] = have ? __uint_as_float(r[i]) : 0.f;
+    }
+    return;
+  }
   if (EPI == EPI_BF16 || EPI == EPI_B16_OUT || EPI == EPI_T8_OUT) {
     if (c0 >= ncols) return;
     // per-tensor E4M3 operands: dequantize the accumulator with 1/(s_a s_b) of this expert
@@ -744,7 +756,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int e = 0; e < args.E; ++e) {
       seg[e] = acc;
       seg[SEG_PB + e] = acc_pb;
-      const int nblk = (args.split_sizes[e] + 127) >> 7;
+      const int rows_e = args.split_sizes != nullptr ? args.split_sizes[e] : int(args.rows_limit);
+      const int nblk = (rows_e + 127) >> 7;
       acc += nblk;
       acc_pb += (nblk + 1) >> 1;
     }
@@ -1039,7 +1052,8 @@ cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64
                                 char* msg, size_t msg_len) {
   if (max_tiles <= 0) return cudaSuccess;
   CUtensorMap ma, mb, msfa, msfb;
-  const bool b16 = (epi == EPI_B16_OUT || epi == EPI_B16_FWD_SWIGLU || epi == EPI_B16_BWD_SWIGLU);
+  const bool b16 = (epi == EPI_B16_OUT || epi == EPI_B16_FWD_SWIGLU || epi == EPI_B16_BWD_SWIGLU ||
+                    epi == EPI_B16_F32_OUT);
   const bool t8 = (epi == EPI_T8_OUT || epi == EPI_T8_FWD_SWIGLU || epi == EPI_T8_BWD_SWIGLU);
   if (!encode_map(&ma, A, a_rows, a_K, b16) || !encode_map(&mb, B, b_rows, b_K, b16)) {
     snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed (A %lld x %lld, B %lld x %lld)", (long long)a_rows,
@@ -1071,6 +1085,7 @@ cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64
     case EPI_T8_FWD_SWIGLU: return launch_epi<EPI_T8_FWD_SWIGLU>(ma, mb, msfa, msfb, a, grid, st);
     case EPI_B16_BWD_SWIGLU: return launch_epi<EPI_B16_BWD_SWIGLU>(ma, mb, msfa, msfb, a, grid, st);
     case EPI_T8_BWD_SWIGLU: return launch_epi<EPI_T8_BWD_SWIGLU>(ma, mb, msfa, msfb, a, grid, st);
+    case EPI_B16_F32_OUT: return launch_epi<EPI_B16_F32_OUT>(ma, mb, msfa, msfb, a, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -36,7 +36,8 @@ cudaError_t launch_quant_dual(const void* src, int batch, int rows, int cols, ui
 cudaError_t launch_quant_dual_experts(const ExpertSrc& src, int batch, int rows, int cols, uint8_t* codes,
                                       uint8_t* scales, uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st);
 size_t router_partial_bytes(int E, int H);
-cudaError_t launch_router_fwd(const void* x, const void* w, int T, int H, int E, float* logits, cudaStream_t st);
+cudaError_t launch_router_fwd(const void* x, const void* w, int T, int H, int E, float* logits, int* err,
+                              cudaStream_t st, char* msg, size_t msg_len);
 cudaError_t launch_router_bwd(const void* x, const void* w, const float* logits, const int* idx, const float* prob,
                               const float* dprob, int T, int H, int E, int k, int renorm, float* dl, void* dx,
                               float* dw, float* partial, int* err, cudaStream_t st);
@@ -99,6 +100,8 @@ enum Epilogue : int {
   EPI_B16_BWD_SWIGLU = 7,    // bf16 operands; SwiGLU backward writing bf16 dH to out [cap][2I] and out_t [2I][cap]
   EPI_T8_BWD_SWIGLU = 8,     // per-tensor E4M3 operands; SwiGLU backward writing bf16 dH to out [cap][2I]
                              // and raising every expert's amax of dH into amax_out
+  EPI_B16_F32_OUT = 9,       // bf16 operands; f32 out_f32 [rows_limit][N] (rows and columns past the ends
+                             // masked): the router logits
 };
 
 struct GemmArgs {
@@ -131,6 +134,8 @@ struct GemmArgs {
   const uint32_t* amax_a;    // T8 kinds: per-expert amax (float bits) of A's and B's tensors
   const uint32_t* amax_b;
   uint32_t* amax_out;        // EPI_T8_FWD_SWIGLU: per-expert amax of the bf16 `a` (raised, not set)
+  float* out_f32;            // EPI_B16_F32_OUT output, row stride ldo
+  int64_t rows_limit;        // mode 0 with split_sizes == nullptr: one segment of this many rows (E = 1)
   int* err;
   uint64_t wait_limit_ns;    // bound of every mbarrier wait (0: the default kWaitLimitNs)
   int selftest_no_loads;     // self-test only: the producer issues nothing, so the waits run out

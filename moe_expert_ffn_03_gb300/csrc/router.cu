@@ -2,166 +2,23 @@
 // top-k softmax (page "英伟达开源MoE加速神器", section "三板斧": tokens are
 // routed to a few experts; page "Efficient MoE Training for Biological
 // Foundation Models", section "MXFP8与融合MLP": the router probabilities scale
-// the SwiGLU output).  N = E is small (<= 256), so these are bandwidth-bound
-// CUDA-core kernels with fixed summation orders (deterministic results):
-//   router_fwd_narrow_kernel E <= 16: a GEMV per token, four tokens per warp, lane
-//                           partial sums over strided h chunks, fixed butterfly;
-//   router_fwd_kernel       E > 16: (4096/ET) tokens x ET experts per CTA, 4x4
-//                           outputs per thread, x and W_r slices in shared memory,
-//                           fp32 sums in ascending h;
+// the SwiGLU output).  The forward runs on the tensor cores; the backward
+// kernels run on the CUDA cores with fixed summation orders (deterministic
+// results):
+//   forward                 logits = x W_r^T on the tensor cores: the grouped GEMM
+//                           engine with bf16 operands, one segment of T rows,
+//                           N = E, f32 logits (rows and columns past T and E masked);
 //   router_dlogits_kernel   one warp per token, straight-through top-k softmax;
 //   router_dx_kernel        dx[t] += sum_e dl[t][e] W_r[e] (bf16 in place);
 //   router_dw_partial/reduce dW_r = dl^T x over fixed token chunks, summed in
 //                           chunk order; each chunk's CTA stages 16-token
 //                           slices of dl and x in shared memory and keeps a
 //                           4x4 block of outputs per thread.
-#include <algorithm>
-
 #include "kernels.cuh"
 
 namespace moe {
 
-// Forward tiles: (4096 / ET) tokens x ET experts per CTA, 256 threads with 4
-// tokens x 4 experts each; the hidden dimension in slices of RT_HS staged in
-// shared memory as fp32 (x transposed, token-contiguous), so every thread does 16
-// FMAs per pair of 16-byte shared loads.  Each logit is one fp32 FMA chain over
-// ascending h.
-constexpr int RT_HS = 16;
-
 __host__ __device__ inline int router_et(int E) { return E <= 8 ? 8 : E <= 16 ? 16 : E <= 32 ? 32 : 64; }
-
-template <int ET>
-__global__ void __launch_bounds__(256) router_fwd_kernel(const __nv_bfloat16* __restrict__ x,
-                                                         const __nv_bfloat16* __restrict__ w, int T, int H, int E,
-                                                         float* __restrict__ logits) {
-  constexpr int TT = 4096 / ET;              // tokens of the tile
-  constexpr int TE = ET / 4;                 // threads along e (4 experts each)
-  extern __shared__ __align__(16) float rsm[];
-  float* xs = rsm;                           // [RT_HS][TT]
-  float* ws = rsm + RT_HS * TT;              // [RT_HS][ET]
-  const int t0 = blockIdx.x * TT, e0 = blockIdx.y * ET;
-  const int te = threadIdx.x % TE, tt = threadIdx.x / TE;   // experts e0+4te.., tokens t0+4tt..
-  float acc[4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int h0 = 0; h0 < H; h0 += RT_HS) {
-    __syncthreads();
-    // x slice: TT tokens x RT_HS bf16 (two 16-byte loads per token), stored transposed
-    for (int i = threadIdx.x; i < TT * (RT_HS / 8); i += 256) {
-      const int r = i / (RT_HS / 8), c8 = i % (RT_HS / 8);
-      const int t = t0 + r;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t < T) v = *reinterpret_cast<const uint4*>(x + int64_t(t) * H + h0 + c8 * 8);
-      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        xs[(c8 * 8 + 2 * q) * TT + r] = bf16_lo(wv[q]);
-        xs[(c8 * 8 + 2 * q + 1) * TT + r] = bf16_hi(wv[q]);
-      }
-    }
-    // W_r slice: ET experts x RT_HS, stored transposed (expert-contiguous)
-    for (int i = threadIdx.x; i < ET * (RT_HS / 8); i += 256) {
-      const int e = i / (RT_HS / 8), c8 = i % (RT_HS / 8);
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (e0 + e < E) v = *reinterpret_cast<const uint4*>(w + int64_t(e0 + e) * H + h0 + c8 * 8);
-      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        ws[(c8 * 8 + 2 * q) * ET + e] = bf16_lo(wv[q]);
-        ws[(c8 * 8 + 2 * q + 1) * ET + e] = bf16_hi(wv[q]);
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int h = 0; h < RT_HS; ++h) {
-      const float4 xv = *reinterpret_cast<const float4*>(xs + h * TT + 4 * tt);
-      const float4 wv = *reinterpret_cast<const float4*>(ws + h * ET + 4 * te);
-      const float xf[4] = {xv.x, xv.y, xv.z, xv.w};
-      const float wf[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] += xf[i] * wf[j];
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + 4 * tt + i;
-    if (t >= T) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + 4 * te + j;
-      if (e < E) logits[int64_t(t) * E + e] = acc[i][j];
-    }
-  }
-}
-
-// Few experts (E <= EN <= 16): a GEMV per token, bound by reading x.  A warp takes 4
-// tokens at a time; lane l sums h chunks l, l+32, ... (8 values each, 16-byte loads
-// of x, W_r through the read-only cache) for all 4 tokens and EN experts, then a
-// fixed butterfly adds the 32 lanes' partial sums.
-template <int EN>
-__global__ void __launch_bounds__(256) router_fwd_narrow_kernel(const __nv_bfloat16* __restrict__ x,
-                                                                const __nv_bfloat16* __restrict__ w, int T, int H,
-                                                                int E, float* __restrict__ logits) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-  const int chunks = H / 8;
-  for (int64_t t0 = warp * 4; t0 < T; t0 += nwarps * 4) {
-    float acc[4][EN];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int e = 0; e < EN; ++e) acc[i][e] = 0.f;
-    for (int c = lane; c < chunks; c += 32) {
-      float xf[4][8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (t0 + i < T) v = *reinterpret_cast<const uint4*>(x + (t0 + i) * H + c * 8);
-        const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          xf[i][2 * q] = bf16_lo(vv[q]);
-          xf[i][2 * q + 1] = bf16_hi(vv[q]);
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < EN; ++e) {
-        if (e >= E) break;
-        const uint4 wv = __ldg(reinterpret_cast<const uint4*>(w + int64_t(e) * H + c * 8));
-        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float wq = (q & 1) ? bf16_hi(ww[q >> 1]) : bf16_lo(ww[q >> 1]);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) acc[i][e] += xf[i][q] * wq;
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int e = 0; e < EN; ++e)
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc[i][e] += __shfl_xor_sync(0xFFFFFFFFu, acc[i][e], off);
-    // every lane holds all sums: lane l writes output l (token l / EN, expert l % EN), and l + 32
-#pragma unroll
-    for (int o = lane; o < 4 * EN; o += 32) {
-      const int i = o / EN, e = o % EN;
-      float v = 0.f;
-#pragma unroll
-      for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-        for (int ee = 0; ee < EN; ++ee)
-          if (ii == i && ee == e) v = acc[ii][ee];
-      if (t0 + i < T && e < E) logits[(t0 + i) * E + e] = v;
-    }
-  }
-}
 
 // One warp per token.  renormalize: dl[e_j] = p_j (dp_j - sum_i p_i dp_i), 0 elsewhere;
 // plain softmax: dl[e] = s_e (g_e - sum_j p_j dp_j) with g the dprob scattered to idx.
@@ -322,37 +179,23 @@ __global__ void __launch_bounds__(256) router_dw_reduce_kernel(const float* __re
 
 size_t router_partial_bytes(int E, int H) { return size_t(router_dw_chunks(E, H)) * E * H * sizeof(float); }
 
-cudaError_t launch_router_fwd(const void* x, const void* w, int T, int H, int E, float* logits, cudaStream_t st) {
-  if (E <= 16) {
-    const int64_t tasks = (int64_t(T) + 3) / 4;               // 4 tokens per warp
-    const unsigned blocks = unsigned(std::min<int64_t>((tasks + 7) / 8, 8 * 152));
-    if (E <= 8)
-      router_fwd_narrow_kernel<8><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
-                                                          static_cast<const __nv_bfloat16*>(w), T, H, E, logits);
-    else
-      router_fwd_narrow_kernel<16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
-                                                           static_cast<const __nv_bfloat16*>(w), T, H, E, logits);
-    return cudaGetLastError();
-  }
-  const int et = router_et(E), tt = 4096 / et;
-  const dim3 grid(unsigned((T + tt - 1) / tt), unsigned((E + et - 1) / et));
-  const size_t smem = size_t(RT_HS) * (tt + et) * sizeof(float);
-  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w);
-  auto go = [&](auto kernel) {
-    if (smem > 48 * 1024) {
-      const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-      if (e != cudaSuccess) return e;
-    }
-    kernel<<<grid, 256, smem, st>>>(xb, wb, T, H, E, logits);
-    return cudaGetLastError();
-  };
-  switch (et) {
-    case 8: return go(router_fwd_kernel<8>);
-    case 16: return go(router_fwd_kernel<16>);
-    case 32: return go(router_fwd_kernel<32>);
-    default: return go(router_fwd_kernel<64>);
-  }
+cudaError_t launch_router_fwd(const void* x, const void* w, int T, int H, int E, float* logits, int* err,
+                              cudaStream_t st, char* msg, size_t msg_len) {
+  // one segment of T rows (E = 1 in the grouped engine's terms), N = the router's experts
+  GemmArgs g{};
+  g.mode = 0;
+  g.E = 1;
+  g.split_sizes = nullptr;
+  g.rows_limit = T;
+  g.K = H;
+  g.N = E;
+  g.n_tiles = (E + 255) / 256;
+  g.b_rows_per_expert = E;
+  g.cap = (int64_t(T) + 127) / 128 * 128;
+  g.out_f32 = logits;
+  g.ldo = E;
+  g.err = err;
+  return launch_grouped_gemm(EPI_B16_F32_OUT, g, x, T, H, w, E, H, (g.cap / 128) * g.n_tiles, st, msg, msg_len);
 }
 
 cudaError_t launch_router_bwd(const void* x, const void* w, const float* logits, const int* idx, const float* prob,

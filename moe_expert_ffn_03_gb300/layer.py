@@ -273,7 +273,7 @@ class ExpertFFN:
         """logits = x W_r^T into self.logits (allocated on first use)."""
         if not hasattr(self, "logits"):
             self.logits = torch.empty(self.T, self.E, dtype=torch.float32, device=self.ws.device)
-        B.moe_router_fwd(self.d, x, w_r, self.logits, stream)
+        B.moe_router_fwd(self.d, x, w_r, self.logits, self.ws, stream)
         return self.logits
 
     def router_backward(self, x, w_r, stream=None):
