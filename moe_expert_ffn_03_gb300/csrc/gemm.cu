@@ -15,11 +15,13 @@
 //   128..255 and the right 128 columns.  Each SM thus stages 32 KB of operands
 //   per 128-deep K step instead of 48 KB for the same tensor work, and the
 //   ring has 6 slots, filled and released two at a time.
-//   warp 0      (both CTAs) TMA producer: the CTA's 128x128 A box, its 128x128
-//               B box (128B swizzle) and, for MXFP8, the scale atoms of its A
-//               rows and of all 256 B rows; every copy signals the leader's
-//               full barrier of the stage (.cta_group::2), which the leader
-//               alone arms with both CTAs' byte count.
+//   warp 0      (both CTAs) TMA producer: per barrier stage (two 128-byte K
+//               steps) one 3-D box of the CTA's 128 A rows and one of its 128 B
+//               rows (128B swizzle; each lands as two K-step tiles) and, for
+//               MXFP8, the scale atoms of its A rows and of all 256 B rows;
+//               every copy signals the leader's full barrier of the stage
+//               (.cta_group::2), which the leader alone arms with both CTAs'
+//               byte count.
 //   warp 1      allocates TMEM (collectively with the peer); in the leader it
 //               issues, per stage, the scale-factor copies (tcgen05.cp, ordered
 //               before the MMAs that read them) and four tcgen05.mma (M=256,
@@ -171,6 +173,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
       " [%0], [%1, {%2, %3}], [%4];"
       ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_c)
+      : "memory");
+}
+// 3-D copy: {x in the 128-byte K atom, row, K atom}; a {.., 128, STAGE_STEPS} box lands
+// as 128-row SW128 tiles back to back, one per K step of a barrier stage.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint32_t bar_c) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_c)
       : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
@@ -818,26 +829,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int kt0 = 0; kt0 < cur.k_tiles; kt0 += L::PER, ++it) {
           const int st = it % L::NSTG;
           const int round = it / L::NSTG;
-          const int nk = min(L::PER, cur.k_tiles - kt0);     // K steps in this stage (the last may be short)
           if (!wait_phase(&empty[st], (round & 1) ^ 1, abort_s, args.err, SITE_GEMM_PRODUCER, lim)) {
             ok = false;
             break;
           }
           const uint32_t bar_c = full_c0 + uint32_t(st) * 8u;
-          // the leader expects both CTAs' bytes; the peer's copies complete on the same barrier.
-          // Scale boxes always carry two atoms (past the tile's K: unused).
-          const uint32_t bytes = uint32_t(nk) * (A_TILE + B_HALF) + (Ops<EPI>::NOSF ? 0u : 3u * L::PER * SF_ATOM);
+          // The leader expects both CTAs' bytes; the peer's copies complete on the same barrier.
+          // Every box carries the stage's full K: a short last stage (an odd number of K steps)
+          // loads one K step of operands and one scale atom per box that its MMAs do not read.
+          const uint32_t bytes = uint32_t(L::PER) * (A_TILE + B_HALF) + (Ops<EPI>::NOSF ? 0u : 3u * L::PER * SF_ATOM);
           if (rank == 0) mbar_arrive_expect_tx(&full[st], 2 * bytes);
           last_round[st] = round;
           issued_any = true;
-          for (int sub = 0; sub < nk; ++sub) {
-            const int slot = st * L::PER + sub;
-            const int kc = cur.k0 + (kt0 + sub) * Ops<EPI>::KSTEP;
-            tma_load_2d(smem + L::OFF_A + slot * A_TILE, &tmA, kc, cur.a_row, bar_c);
-            tma_load_2d(smem + L::OFF_B + slot * B_HALF, &tmB, kc, cur.b_row, bar_c);
-          }
+          const int slot = st * L::PER;
+          const int ka = cur.k0 / Ops<EPI>::KSTEP + kt0;        // first K atom of the stage
+          tma_load_3d(smem + L::OFF_A + slot * A_TILE, &tmA, 0, cur.a_row, ka, bar_c);
+          tma_load_3d(smem + L::OFF_B + slot * B_HALF, &tmB, 0, cur.b_row, ka, bar_c);
           if (!Ops<EPI>::NOSF) {
-            const int slot = st * L::PER;
             tma_load_2d(smem + L::OFF_SFA + slot * SF_ATOM, &tmSFA, 0, cur.sfa_y + 2 * kt0, bar_c);
             tma_load_2d(smem + L::OFF_SFB0 + slot * SF_ATOM, &tmSFB, 0, cur.sfb0_y + 2 * kt0, bar_c);
             tma_load_2d(smem + L::OFF_SFB1 + slot * SF_ATOM, &tmSFB, 0, cur.sfb1_y + 2 * kt0, bar_c);
@@ -982,19 +990,21 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2-D map over a row-major uint8 [rows][K] tensor, 128x128 boxes, 128-byte swizzle.
-bool encode_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, bool b16) {
+// 3-D map over a row-major [rows][K] tensor: {128 bytes of K, rows, K / 128-byte atoms}
+// with strides {row pitch, 128 bytes}; box {128 bytes, 128 rows, STAGE_STEPS atoms}.
+// One copy fetches a barrier stage's K steps of 128 rows: TMA delivery per SM grows
+// with the bytes per copy as well as per barrier stage.
+bool encode_map3(CUtensorMap* m, const void* base, int64_t rows, int64_t K, bool b16) {
   EncodeTiledFn fn = get_encode_fn();
   if (fn == nullptr) return false;
   const int64_t esize = b16 ? 2 : 1;
-  cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
-  cuuint64_t strides[1] = {cuuint64_t(K * esize)};
-  cuuint32_t box[2] = {cuuint32_t(BK / esize), 128};     // 128 bytes of K per row
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, b16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base),
-            dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  cuuint64_t dims[3] = {cuuint64_t(BK / esize), cuuint64_t(rows), cuuint64_t(K * esize / BK)};
+  cuuint64_t strides[2] = {cuuint64_t(K * esize), cuuint64_t(BK)};
+  cuuint32_t box[3] = {cuuint32_t(BK / esize), 128, cuuint32_t(STAGE_STEPS)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, b16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 2-D map over n_atoms 512-byte scale atoms seen as [2 * n_atoms][256] bytes: one
@@ -1055,7 +1065,7 @@ cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64
   const bool b16 = (epi == EPI_B16_OUT || epi == EPI_B16_FWD_SWIGLU || epi == EPI_B16_BWD_SWIGLU ||
                     epi == EPI_B16_F32_OUT);
   const bool t8 = (epi == EPI_T8_OUT || epi == EPI_T8_FWD_SWIGLU || epi == EPI_T8_BWD_SWIGLU);
-  if (!encode_map(&ma, A, a_rows, a_K, b16) || !encode_map(&mb, B, b_rows, b_K, b16)) {
+  if (!encode_map3(&ma, A, a_rows, a_K, b16) || !encode_map3(&mb, B, b_rows, b_K, b16)) {
     snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed (A %lld x %lld, B %lld x %lld)", (long long)a_rows,
              (long long)a_K, (long long)b_rows, (long long)b_K);
     return cudaErrorInvalidValue;
