@@ -131,3 +131,19 @@ def test_training_path_entry_points_check_arguments_on_the_host(lib):
     # the bf16 forward checks the optional saved_gu's alignment
     s = lib.grouped_mlp_fwd_bf16(ctypes.byref(d), *([P(256)] * 7), P(8), P(256), 1 << 40, None)
     assert s == 3
+
+
+def test_router_entry_points_check_arguments_on_the_host(lib):
+    P = ctypes.c_void_p
+    d = B.dims(64, 128, 128, 4, 2)
+    need = lib.moe_workspace_size(ctypes.byref(d), 0)
+    s = lib.moe_router_fwd(ctypes.byref(d), P(256), P(256), P(256), None, need, None)
+    assert s == 4                                                     # no workspace
+    s = lib.moe_router_fwd(ctypes.byref(d), P(256), P(256), P(256), P(256), need - 1, None)
+    assert s == 4                                                     # workspace too small
+    s = lib.moe_router_fwd(ctypes.byref(d), P(264), P(256), P(256), P(256), need, None)
+    assert s == 3 and b"x" in lib.moe_last_error_message()           # x not 16-byte aligned
+    s = lib.moe_router_fwd(ctypes.byref(d), None, P(256), P(256), P(256), need, None)
+    assert s == 1
+    s = lib.moe_router_bwd(ctypes.byref(d), *([P(256)] * 10), 16, None)
+    assert s == 4                                                     # workspace too small
