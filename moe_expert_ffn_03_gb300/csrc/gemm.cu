@@ -73,6 +73,10 @@ constexpr int kMaxSegE = 256;                   // mode-1 expert order (heaviest
 constexpr int SEG_PB = SEG_INTS + kMaxSegE;     // then the per-expert prefix of block pairs (mode 0)
 constexpr int TR_PITCH = 9;                     // floats per row of a warp's 32x8 transpose buffer
 constexpr int TR_WARP_FLOATS = 32 * TR_PITCH;
+// g,u staging of the SwiGLU backward: per lane (row) 32 g then 32 u values, eight
+// 16-byte chunks in a 128-byte row; chunk c of lane l sits at chunk c ^ (l & 7), so a
+// quarter warp reading one chunk index touches eight distinct bank groups.
+constexpr int GU_PITCH = 128;
 
 // bf16-operand kinds: 64 K elements per 128-byte stage row, kind::f16 MMA, no scales.
 // Per-tensor E4M3 kinds: 128 K elements per stage, kind::f8f6f4 MMA, no block scales.
@@ -103,7 +107,9 @@ constexpr int STAGE_STEPS = 2;                  // K steps (slots) per barrier s
 
 template <int EPI>
 struct Lay {
-  static constexpr int STG = 6;                  // slots of one K step
+  // The SwiGLU-backward kinds, bound by their epilogue, trade two slots for a per-warp
+  // staging buffer of the saved g,u (one half of the warp's columns, 32 rows).
+  static constexpr int STG = Ops<EPI>::SWIGLU_BWD ? 4 : 6;   // slots of one K step
   static constexpr int PER = STAGE_STEPS;        // slots per barrier stage
   static constexpr int NSTG = STG / PER;         // barrier stages
   static constexpr int OFF_A = 0;
@@ -118,7 +124,10 @@ struct Lay {
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_SEG = OFF_MISC + 16;             // seg_mb[SEG_INTS], order[kMaxSegE], seg_pb[SEG_INTS]
   static constexpr int OFF_TR = (OFF_SEG + (2 * SEG_INTS + kMaxSegE) * 4 + 15) & ~15;
-  static constexpr int SMEM_USED = OFF_TR + NUM_EPI_WARPS * TR_WARP_FLOATS * 4;
+  static constexpr int OFF_GU = OFF_TR + NUM_EPI_WARPS * TR_WARP_FLOATS * 4;
+  static constexpr int GU_WARP = Ops<EPI>::SWIGLU_BWD ? 32 * GU_PITCH : 0;
+  static constexpr int SMEM_USED = OFF_GU + NUM_EPI_WARPS * GU_WARP;
+  static_assert(OFF_GU % 16 == 0 && GU_PITCH % 16 == 0, "16-byte cp.async and vector reads of the g,u staging");
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 B
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(TM_SF0 + STG * TM_SF_STRIDE <= TM_STASH, "TMEM budget");
@@ -544,9 +553,20 @@ __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + _
 // tmem_empty, at cluster address tmem_empty_c) and only then runs the epilogue
 // math, so the next tile's MMAs overlap it.  A CTA whose half of the pair tile
 // lies past the expert's rows (or past M) releases the accumulator and writes nothing.
+// This lane's saved g and u (32 columns each from col) into its row of the warp's
+// staging buffer; completes with cp_async_wait_all.
+__device__ __forceinline__ void stage_gu(const GemmArgs& a, int64_t row, int64_t col, uint8_t* gu_s, int sw) {
+  const __nv_bfloat16* grow = a.gu + row * (2 * int64_t(a.I)) + col;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    cp_async16(gu_s + ((j ^ sw) << 4), grow + 8 * j, true);
+    cp_async16(gu_s + (((4 + j) ^ sw) << 4), grow + a.I + 8 * j, true);
+  }
+}
+
 template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl, uint32_t tmem_row, int q, int cg,
-                                              int lane, uint32_t tmem_empty_c, float* tr) {
+                                              int lane, uint32_t tmem_empty_c, float* tr, uint8_t* gu_s) {
   if (!tl.valid) {
     __syncwarp();
     if (lane == 0) mbar_arrive_cluster(tmem_empty_c);
@@ -671,7 +691,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
       const float alpha =
           Ops<EPI>::T8 ? __frcp_rn(t8_scale(a.amax_a[tl.e])) * __frcp_rn(t8_scale(a.amax_b[tl.e])) : 1.0f;
       uint32_t amax = 0;
-      const __nv_bfloat16* grow = a.gu + row * twoI;
       for (int h = 0; h < 2; ++h) {
         if (h == 1) {
           tmem_ld32_async(tmem_row + TM_STASH + cg * 32, r);
@@ -679,11 +698,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
         }
         const int64_t col = tl.n0 + c0 + 32 * h;
         float o[32];
+        cp_async_wait_all();                               // this half's g,u are in gu_s
         // dg = dA*p*u*silu'(g) and the row sum dp += dA*silu(g)*u
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint4 gw = *reinterpret_cast<const uint4*>(grow + col + 8 * j);
-          const uint4 uw = *reinterpret_cast<const uint4*>(grow + a.I + col + 8 * j);
+          const uint4 gw = *reinterpret_cast<const uint4*>(gu_s + ((j ^ (lane & 7)) << 4));
+          const uint4 uw = *reinterpret_cast<const uint4*>(gu_s + (((4 + j) ^ (lane & 7)) << 4));
           const uint32_t gs[4] = {gw.x, gw.y, gw.z, gw.w};
           const uint32_t us[4] = {uw.x, uw.y, uw.z, uw.w};
 #pragma unroll
@@ -701,6 +721,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
           }
         }
         const float* du = reinterpret_cast<const float*>(r);
+        if (h == 0) stage_gu(a, row, col + 32, gu_s, lane & 7);   // the second half, while this one is stored
         if (EPI == EPI_B16_BWD_SWIGLU) {
           store_bf16x32(a.out + row * twoI + col, o);
           store_col_bf16(o, a.out_t, row_blk0, col, a.cap, lane, tr);
@@ -947,23 +968,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem_row = tmem + (uint32_t(q * 32) << 16);
     const uint32_t tmem_empty_c0 = mapa_shared(smem_u32(tmem_empty), 0);
     float* tr = reinterpret_cast<float*>(smem + L::OFF_TR) + (warp - 2) * TR_WARP_FLOATS;
+    uint8_t* gu_s = smem + L::OFF_GU + (warp - 2) * L::GU_WARP + lane * GU_PITCH;
     int tcount = 0;
     for (int t = pair; t < total; t += num_pairs, ++tcount) {
       Tile tl;
       decode_tile<EPI>(args, seg, t, int(rank), tl);
-      if (Ops<EPI>::SWIGLU_BWD && tl.valid) {
-        // pull this thread's saved g and u (128 B each) toward L2 while the MMAs run
-        const __nv_bfloat16* grow = args.gu + (tl.out_row + q * 32 + lane) * (2 * int64_t(args.I)) + tl.n0 + cg * 64;
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(grow));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(grow + args.I));
+      if (Ops<EPI>::SWIGLU_BWD && tl.valid && cg * 64 < (tl.second ? 256 : 128)) {
+        // this lane's saved g and u of the first half land in shared memory while the MMAs run
+        stage_gu(args, tl.out_row + q * 32 + lane, tl.n0 + cg * 64, gu_s, lane & 7);
       }
       const int ab = Ops<EPI>::ACC_BUFS == 2 ? (tcount & 1) : 0;
       const int use = Ops<EPI>::ACC_BUFS == 2 ? (tcount >> 1) : tcount;
       if (!wait_phase(&tmem_full[ab], use & 1, abort_s, args.err, SITE_GEMM_EPILOGUE, lim)) break;
       tc_fence_after();
       epilogue_tile<EPI>(args, tl, tmem_row + uint32_t(ab) * 256u, q, cg, lane, tmem_empty_c0 + uint32_t(ab) * 8u,
-                         tr);
+                         tr, gu_s);
     }
+    if (Ops<EPI>::SWIGLU_BWD) cp_async_wait_all();   // nothing in flight when a wait gave up
   }
   tc_fence_before();
   __syncthreads();
