@@ -14,7 +14,8 @@
 //   the tile and the left 128 columns of B, the odd CTA (the peer) rows
 //   128..255 and the right 128 columns.  Each SM thus stages 32 KB of operands
 //   per 128-deep K step instead of 48 KB for the same tensor work, and the
-//   ring has 6 slots, filled and released two at a time.
+//   ring has 6 slots (4 for the SwiGLU-backward kinds), filled and released
+//   two at a time.
 //   warp 0      (both CTAs) TMA producer: per barrier stage (two 128-byte K
 //               steps) one 3-D box of the CTA's 128 A rows and one of its 128 B
 //               rows (128B swizzle; each lands as two K-step tiles) and, for
@@ -23,7 +24,7 @@
 //               (.cta_group::2), which the leader alone arms with both CTAs'
 //               byte count.
 //   warp 1      allocates TMEM (collectively with the peer); in the leader it
-//               issues, per stage, the scale-factor copies (tcgen05.cp, ordered
+//               issues, per K step, the scale-factor copies (tcgen05.cp, ordered
 //               before the MMAs that read them) and four tcgen05.mma (M=256,
 //               N=256, K=32); tcgen05.commit multicasts the stage release to both
 //               CTAs and, after the last K step, hands each CTA its half of the
@@ -34,7 +35,8 @@
 //               accumulator at once (an arrival on the leader's barrier), then
 //               the fused epilogue math (bf16 store, ScaledSwiGLU +
 //               re-quantization along both axes, or SwiGLU backward +
-//               re-quantization).
+//               re-quantization, its saved g,u staged in shared memory by
+//               cp.async ahead of use).
 // Tiles: mode 0 walks pairs of 128-row blocks inside each expert segment
 // (computed on the device from split_sizes; empty experts get no tile; the
 // second block of an expert with an odd block count is computed and dropped)
@@ -96,7 +98,8 @@ struct Ops {
 };
 
 // Shared-memory layout (per CTA; both CTAs of a pair use the same offsets): six
-// slots, each one 128-deep K step of the CTA's A box, its B box and the scale
+// slots (four for the SwiGLU-backward kinds, which stage g,u instead), each one
+// 128-deep K step of the CTA's A box, its B box and the scale
 // atoms (its A rows; the two 128-row blocks of B), then the barriers, the segment
 // tables and the epilogue warps' transpose buffers.  The slots are filled and
 // released two at a time (one barrier stage = 256 of K, 64 KB of operands):
