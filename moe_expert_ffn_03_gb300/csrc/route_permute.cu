@@ -20,8 +20,15 @@ namespace moe {
 constexpr int kMaxK = 8;
 constexpr int kMaxE = 256;
 
+// Total order of (logit, expert): larger logit first, ties to the lower expert id.
+// A NaN logit ranks below every number (-inf included) and NaNs tie among
+// themselves, so a row with fewer than k non-NaN logits still fills its k slots
+// with real experts (the NaN ones, lowest ids first).  +0 and -0 tie.
 __device__ __forceinline__ bool better(float va, int ea, float vb, int eb) {
-  return va > vb || (va == vb && ea < eb);
+  const bool na = va != va, nb = vb != vb;
+  if (na != nb) return nb;
+  if (!na && va != vb) return va > vb;
+  return ea < eb;
 }
 
 constexpr int RT_THREADS = 128;
@@ -43,7 +50,7 @@ __device__ __forceinline__ void topk_insert(float v, int e, float (&sv)[kMaxK], 
 
 __global__ void __launch_bounds__(RT_THREADS) route_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renorm,
-    int* __restrict__ idx, float* __restrict__ prob, uint32_t* __restrict__ masks, int G) {
+    int* __restrict__ idx, float* __restrict__ prob, uint32_t* __restrict__ masks, int G, int* err) {
   __shared__ uint32_t smask[RT_THREADS / 32][kMaxE];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int t = blockIdx.x * RT_THREADS + threadIdx.x;
@@ -56,7 +63,7 @@ __global__ void __launch_bounds__(RT_THREADS) route_topk_kernel(
     int se[kMaxK];
 #pragma unroll
     for (int s = 0; s < kMaxK; ++s) {
-      sv[s] = -INFINITY;
+      sv[s] = __int_as_float(0x7FFFFFFF);              // NaN with the largest id: below every real entry
       se[s] = 0x7FFFFFFF;
     }
     const float* row = logits + (int64_t)t * E;
@@ -85,6 +92,14 @@ __global__ void __launch_bounds__(RT_THREADS) route_topk_kernel(
 #pragma unroll
     for (int s = 0; s < kMaxK; ++s) {
       if (s < k) {
+        // k <= E, so the list holds k real experts; the check keeps a broken invariant
+        // from turning into a shared-memory access out of bounds
+        if (se[s] < 0 || se[s] >= E) {
+          report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_ROUTE);
+          idx[(int64_t)t * k + s] = -1;
+          prob[(int64_t)t * k + s] = 0.f;
+          continue;
+        }
         idx[(int64_t)t * k + s] = se[s];
         prob[(int64_t)t * k + s] = expf(sv[s] - m) / den;
         atomicOr(&smask[w][se[s]], 1u << lane);
@@ -160,6 +175,7 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
       const int e = idx[(int64_t)t * k + s];
       if (e < 0 || e >= E) {
         report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_PERMUTE + 1);
+        row_of[(int64_t)t * k + s] = -1;                // later kernels' row checks catch the slot
         continue;
       }
       const uint32_t msk = masks[(int64_t)e * G + g];
@@ -183,7 +199,7 @@ cudaError_t launch_route_permute(const float* logits, int T, int E, int k, int r
                                  float* prob_perm, int* err, cudaStream_t st) {
   const int G = (T + 31) / 32;
   route_topk_kernel<<<(G * 32 + RT_THREADS - 1) / RT_THREADS, RT_THREADS, 0, st>>>(logits, T, E, k, renorm, idx,
-                                                                                   prob, masks, G);
+                                                                                   prob, masks, G, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   permute_scan_kernel<<<E, 1024, 0, st>>>(masks, G, bases, split_sizes);

@@ -8,7 +8,11 @@ the SwiGLU output.
 
 Readings:
 * Top-k by logits (exact float comparisons), ties to the lower expert index,
-  slots in descending-logit order.
+  slots in descending-logit order.  +0 and -0 tie.  A NaN logit ranks below
+  every number (-inf included) and NaNs tie among themselves, so a row with
+  fewer than k non-NaN logits still selects k distinct experts; its
+  probabilities are then NaN (the pages say nothing about non-finite logits;
+  this is the plainest total order that keeps the selection well defined).
 * prob = softmax over the k selected logits (equivalently softmax over all E
   then renormalised over the top k).  ``renormalize=False`` keeps the plain
   softmax-over-E probabilities of the selected experts.
@@ -28,7 +32,11 @@ def route_topk(logits, k: int, renormalize: bool = True):
     """logits [T][E] float32 -> (idx int32 [T][k], prob float32 [T][k])."""
     l64 = np.asarray(logits, dtype=np.float32).astype(np.float64)
     T, E = l64.shape
-    order = np.argsort(-l64, axis=1, kind="stable")      # descending, ties -> lower index
+    nan = np.isnan(l64)
+    # sort keys, last one primary: NaN last, then descending logit, then ascending index
+    # (np.lexsort is stable, so equal keys keep the lower index first)
+    neg = np.where(nan, 0.0, -l64) + 0.0                 # + 0.0 turns -0 into +0: the two tie
+    order = np.stack([np.lexsort((neg[t], nan[t])) for t in range(T)]) if T else np.zeros((0, E), np.int64)
     idx = order[:, :k]
     sel = np.take_along_axis(l64, idx, axis=1)
     m = sel[:, :1]                                       # the largest logit

@@ -28,6 +28,55 @@ def test_topk_matches_brute_force_sort(T, E, k):
     assert list(idx[1]) == list(range(k))                    # all tied -> lowest indices
 
 
+def brute_topk_total_order(row, k):
+    """Pairwise comparison sort written out: a beats b when b is NaN and a is not, or
+    both are numbers and a > b, or they tie (both NaN, or equal numbers) and a has the
+    lower index."""
+    E = len(row)
+
+    def beats(a, b):
+        na, nb = np.isnan(row[a]), np.isnan(row[b])
+        if na != nb:
+            return nb
+        if not na and row[a] != row[b]:
+            return row[a] > row[b]
+        return a < b
+
+    chosen = []
+    rest = list(range(E))
+    for _ in range(k):
+        best = rest[0]
+        for c in rest[1:]:
+            if beats(c, best):
+                best = c
+        chosen.append(best)
+        rest.remove(best)
+    return chosen
+
+
+@pytest.mark.filterwarnings("ignore:invalid value encountered")
+def test_nan_logits_rank_last_and_the_row_still_fills():
+    nan, inf = np.float32(np.nan), np.float32(np.inf)
+    logits = np.array([
+        [nan, 1.0, nan, -2.0, 0.5, nan],          # fewer numbers (3) than k (4): one NaN expert joins
+        [nan, nan, nan, nan, nan, nan],           # all NaN: the lowest ids
+        [-inf, nan, -inf, 3.0, nan, -1.0],        # -inf still beats NaN
+        [0.0, -0.0, 0.0, -0.0, -1.0, nan],        # signed zeros tie: index order
+        [inf, 1.0, inf, nan, -inf, 2.0],
+    ], dtype=np.float32)
+    k = 4
+    idx, prob = rt.route_topk(logits, k)
+    for t in range(len(logits)):
+        assert list(idx[t]) == brute_topk_total_order(logits[t], k), t
+        assert len(set(idx[t])) == k
+    assert list(idx[0]) == [1, 4, 3, 0] and np.all(np.isnan(prob[0]))
+    assert list(idx[1]) == [0, 1, 2, 3]
+    assert list(idx[2]) == [3, 5, 0, 2]                      # -inf beats NaN; exp(-inf - 3) = 0
+    assert np.allclose(prob[2], [1 / (1 + np.exp(-4.0)), 1 - 1 / (1 + np.exp(-4.0)), 0, 0], rtol=1e-6)
+    assert list(idx[3]) == [0, 1, 2, 3]
+    assert np.allclose(prob[3], 0.25)
+
+
 def test_k_equals_E_is_plain_softmax():
     rng = np.random.default_rng(7)
     logits = rng.standard_normal((20, 6)).astype(np.float32)
