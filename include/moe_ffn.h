@@ -147,10 +147,13 @@ moe_status mxfp8_quantize_dual(const void* src, int32_t batch, int32_t rows, int
  * Foundation Models", section "GroupedLinear": tokens are collected per
  * expert, split_sizes counts them; page "英伟达开源MoE加速神器", section
  * "三板斧": each token is routed to a few experts).
- *   logits      f32 [T][E] (finite)
+ *   logits      f32 [T][E]
  *   x           bf16 [T][H]
  *   idx         out int32 [T][k]: top-k experts by logit, descending, ties to
- *               the lower expert index
+ *               the lower expert index (+0 and -0 tie).  A NaN logit ranks
+ *               below every number, -inf included, and NaNs tie among
+ *               themselves, so every row selects k distinct experts; a row
+ *               that selects a NaN logit gets NaN probabilities.
  *   prob        out f32 [T][k]: softmax of the selected logits (see renormalize)
  *   split_sizes out int32 [E]: tokens per expert (sum = T*k)
  *   row_of      out int32 [T][k]: permuted row of (token, slot); inside an
@@ -272,7 +275,6 @@ moe_status mxfp8_quantize_experts(const void* const* w, int32_t E, int32_t rows,
                                   uint8_t* scales, uint8_t* codes_t, uint8_t* scales_t, moe_stream_t stream);
 
 /*
- * Per-tensor FP8 with dynamic scaling/*
  * Per-tensor FP8 with dynamic scaling (page "英伟达开源MoE加速神器", section
  * "3. Transformer Engine：FP8 训练加速": the Hopper recipe scales every tensor by
  * its current range; page "Efficient MoE Training for Biological Foundation
@@ -461,6 +463,61 @@ moe_status moe_router_bwd(const moe_dims* d, const void* x, const void* w_r, con
 moe_status moe_selftest_wait_timeout(void* scratch, size_t scratch_bytes, int64_t limit_ns, int32_t* code,
                                      int32_t* site, moe_stream_t stream);
 
+/*
+ * moe_workspace_tensor -- where an intermediate tensor of the layer sits in a
+ * workspace of moe_workspace_size(d, training) bytes, for callers that want to
+ * inspect it (the tests compare these against the oracle).  The pages have no
+ * counterpart: these are the quantized operands the fused ops of page
+ * "Efficient MoE Training for Biological Foundation Models", section
+ * "MXFP8与融合MLP", keep internal.  *offset = byte offset from the workspace
+ * start (256-aligned), *bytes = size.  Layouts as documented for MX tensors:
+ *   MOE_WS_A_CODES / _SCALES        a = silu(g)*u*p, rows along I [CAP][I]
+ *                                   (written by grouped_mlp_fwd)
+ *   MOE_WS_DY_CODES / _SCALES       dY = dout gathered to rows, along H [CAP][H]
+ *   MOE_WS_DY_COL_CODES / _SCALES   dY along tokens, transposed [H][CAP]
+ *   MOE_WS_DH_CODES / _SCALES       dH = [dg | du], rows along 2I [CAP][2I]
+ *   MOE_WS_DH_COL_CODES / _SCALES   dH along tokens, transposed [2I][CAP]
+ * (the DY and DH tensors are written by grouped_mlp_bwd and exist only for
+ * training >= 1).  Contents are valid after the writing call completes and
+ * until the next call that writes the same workspace.  Host only.
+ */
+enum moe_ws_tensor {
+  MOE_WS_A_CODES = 0, MOE_WS_A_SCALES = 1,
+  MOE_WS_DY_CODES = 2, MOE_WS_DY_SCALES = 3, MOE_WS_DY_COL_CODES = 4, MOE_WS_DY_COL_SCALES = 5,
+  MOE_WS_DH_CODES = 6, MOE_WS_DH_SCALES = 7, MOE_WS_DH_COL_CODES = 8, MOE_WS_DH_COL_SCALES = 9
+};
+moe_status moe_workspace_tensor(const moe_dims* d, int32_t training, int32_t which, size_t* offset, size_t* bytes);
+
+/*
+ * moe_selftest_epilogue_quant -- runs the MX quantizers of the GEMM epilogues
+ * (the ones that write a after ScaledSwiGLU and dH after the SwiGLU backward;
+ * page "Efficient MoE Training for Biological Foundation Models", section
+ * "MXFP8与融合MLP": quantization is fused into the grouped MLP) on a caller's
+ * float32 tensor, so that their codes can be checked bit for bit on inputs with
+ * full 24-bit significands.  Each warp holds one 32x32 block the way an
+ * epilogue warp holds its accumulator columns (lane = row).
+ *   src      f32 [rows][cols] (rows, cols multiples of 128)
+ *   codes, scales      out MX [rows][cols], blocks of 32 along cols
+ *   codes_t, scales_t  out MX [cols][rows], blocks of 32 along rows
+ *                      (the tensor transposed, as the along-token copies)
+ */
+moe_status moe_selftest_epilogue_quant(const float* src, int32_t rows, int32_t cols, uint8_t* codes,
+                                       uint8_t* scales, uint8_t* codes_t, uint8_t* scales_t, moe_stream_t stream);
+
+/*
+ * moe_selftest_mma_issue -- the tensor pipe's MXFP8 issue ceiling for the GEMM's
+ * instruction mix, a measurement aid with no counterpart in the pages.  One
+ * launch of SMs/2 CTA pairs (one CTA per SM); in each pair one thread issues
+ * k_steps K steps, each three scale-factor copies (tcgen05.cp) and four
+ * tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale of M=256, N=256, K=32,
+ * on operands resident in shared memory (zeros), with no loads and no
+ * epilogue.  FLOPs of the launch = *pairs * k_steps * 2*256*256*128; time it
+ * with events on `stream`.  scratch >= 256 bytes, 256-byte aligned, zeroed by
+ * the caller: its first 8 bytes are a device error word (moe_get_device_error).
+ */
+moe_status moe_selftest_mma_issue(int32_t k_steps, void* scratch, size_t scratch_bytes, int32_t* pairs,
+                                  moe_stream_t stream);
+
 /* Read (and keep) the device error word of a workspace: *code is a
  * moe_status (MOE_OK if none), *site identifies the kernel and wait.
  * Synchronises `stream`. */
@@ -491,13 +548,16 @@ moe_status moe_clear_device_error(void* workspace, moe_stream_t stream);
  * nothing.
  *
  * The first call on each device looks up the array's device address with that
- * device current and caches it; make that first call before any stream
+ * device current and caches it with the id of the device's context; a call
+ * under a new context (after cudaDeviceReset) looks it up again.  Make the
+ * first call on a device, and the first after a reset, before any stream
  * capture.  All calls share the one array and each call rewrites it (only its
  * error word is cleared at the start of a call): calls whose kernels overlap on
  * the GPU -- different streams, or threads without ordering between them --
- * race and corrupt each other's permutation, so order them.  Index errors the
- * kernels detect are recorded in the array's own error word (not readable
- * through this interface) and the offending entries are skipped.
+ * race and corrupt each other's permutation, so order them.  The array's own
+ * error word cannot be read through this interface; instead a (token, slot)
+ * that the kernels had to skip is marked -1 in idx and row_of (no valid input
+ * produces one: every row selects k real experts, NaN logits included).
  */
 moe_status moe_route_permute_noalloc(const moe_dims* d, const float* logits, const void* x,
                                      int32_t* idx, float* prob, int32_t* split_sizes,

@@ -138,6 +138,8 @@ T* at(void* ws, size_t off) {
 }  // namespace
 
 char* moe::last_error_buffer() { return g_msg; }
+moe_status moe::check_layer_dims(const moe_dims* d) { return check_dims(d); }
+int64_t moe::rows_capacity(const moe_dims* d) { return capacity(d); }
 
 extern "C" {
 
@@ -1113,6 +1115,66 @@ moe_status moe_selftest_wait_timeout(void* scratch, size_t scratch_bytes, int64_
   CUDA_TRY(cudaStreamSynchronize(st), "synchronize");
   *code = h[0];
   *site = h[1];
+  return MOE_OK;
+}
+
+moe_status moe_workspace_tensor(const moe_dims* d, int32_t training, int32_t which, size_t* offset, size_t* bytes) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  if (offset == nullptr || bytes == nullptr) return fail(MOE_ERR_INVALID_ARG, "offset and bytes must be non-NULL");
+  if (training < 0 || training > 3) return fail(MOE_ERR_INVALID_ARG, "training=%d must be in 0..3", training);
+  const WsLayout w = ws_layout(d, training);
+  const size_t cap = size_t(capacity(d));
+  const size_t H = size_t(d->H), I = size_t(d->I);
+  size_t off = 0, n = 0;
+  switch (which) {
+    case MOE_WS_A_CODES: off = w.aq; n = cap * I; break;
+    case MOE_WS_A_SCALES: off = w.aq_s; n = cap * I / 32; break;
+    case MOE_WS_DY_CODES: off = w.dyq; n = cap * H; break;
+    case MOE_WS_DY_SCALES: off = w.dyq_s; n = cap * H / 32; break;
+    case MOE_WS_DY_COL_CODES: off = w.dyqc; n = H * cap; break;
+    case MOE_WS_DY_COL_SCALES: off = w.dyqc_s; n = H * cap / 32; break;
+    case MOE_WS_DH_CODES: off = w.dhq; n = cap * 2 * I; break;
+    case MOE_WS_DH_SCALES: off = w.dhq_s; n = cap * 2 * I / 32; break;
+    case MOE_WS_DH_COL_CODES: off = w.dhqc; n = 2 * I * cap; break;
+    case MOE_WS_DH_COL_SCALES: off = w.dhqc_s; n = 2 * I * cap / 32; break;
+    default: return fail(MOE_ERR_INVALID_ARG, "unknown workspace tensor %d", which);
+  }
+  if (which >= MOE_WS_DY_CODES && training == 0)
+    return fail(MOE_ERR_INVALID_ARG, "the backward tensors exist only in a training workspace (training >= 1)");
+  *offset = off;
+  *bytes = n;
+  return MOE_OK;
+}
+
+moe_status moe_selftest_epilogue_quant(const float* src, int32_t rows, int32_t cols, uint8_t* codes, uint8_t* scales,
+                                       uint8_t* codes_t, uint8_t* scales_t, moe_stream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE_PTR(src);
+  REQUIRE_PTR(codes);
+  REQUIRE_PTR(scales);
+  REQUIRE_PTR(codes_t);
+  REQUIRE_PTR(scales_t);
+  if (rows < 128 || cols < 128 || rows % 128 || cols % 128 || int64_t(rows) * cols > (int64_t(1) << 31))
+    return fail(MOE_ERR_UNSUPPORTED, "rows=%d cols=%d: need multiples of 128, rows*cols <= 2^31", rows, cols);
+  CUDA_TRY(launch_epilogue_quant_selftest(src, rows, cols, codes, scales, codes_t, scales_t,
+                                          static_cast<cudaStream_t>(stream)),
+           "epilogue quantizer self-test");
+  return MOE_OK;
+}
+
+moe_status moe_selftest_mma_issue(int32_t k_steps, void* scratch, size_t scratch_bytes, int32_t* pairs,
+                                  moe_stream_t stream) {
+  g_msg[0] = 0;
+  if (scratch == nullptr || pairs == nullptr) return fail(MOE_ERR_INVALID_ARG, "scratch and pairs must be non-NULL");
+  if ((reinterpret_cast<uintptr_t>(scratch) & 255u) != 0) return fail(MOE_ERR_ALIGNMENT, "scratch must be 256-byte aligned");
+  if (scratch_bytes < 256) return fail(MOE_ERR_WORKSPACE, "scratch needs 256 bytes");
+  if (k_steps < 1 || k_steps > (1 << 24)) return fail(MOE_ERR_INVALID_ARG, "k_steps=%d must be in 1..2^24", k_steps);
+  int p = 0;
+  CUDA_TRY(launch_mma_rate_selftest(k_steps, static_cast<int*>(scratch), &p, static_cast<cudaStream_t>(stream)),
+           "MMA issue self-test");
+  *pairs = p;
   return MOE_OK;
 }
 

@@ -9,6 +9,11 @@ namespace moe {
 // Per-thread text of the last host-side error, returned by moe_last_error_message().
 constexpr size_t kLastErrorBytes = 512;
 char* last_error_buffer();
+// The size checks every layer entry point applies (T, H, I, E, k, the row capacity);
+// on failure the message names the offending field.
+moe_status check_layer_dims(const moe_dims* d);
+// Rows of every permuted buffer for valid dims: roundup(T*k, 128) + 128*E.
+int64_t rows_capacity(const moe_dims* d);
 
 // Sources of a batch of bf16 [rows][cols] matrices: one stacked tensor, or one
 // pointer per matrix (each expert's own weight tensor), passed by value.
@@ -140,6 +145,18 @@ struct GemmArgs {
   uint64_t wait_limit_ns;    // bound of every mbarrier wait (0: the default kWaitLimitNs)
   int selftest_no_loads;     // self-test only: the producer issues nothing, so the waits run out
 };
+
+// The GEMM epilogues' MX quantizers (row-wise along cols, and along rows into the
+// transposed [cols][rows] tensor) applied to a caller's f32 [rows][cols] tensor
+// (rows, cols multiples of 128), one 32 x 32 block per warp as an epilogue warp
+// holds it.
+cudaError_t launch_epilogue_quant_selftest(const float* src, int rows, int cols, uint8_t* codes, uint8_t* scales,
+                                           uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st);
+
+// The MXFP8 MMA issue ceiling: one launch of SMs/2 CTA pairs, each issuing k_steps
+// K steps of the GEMM's MMAs (M=256, N=256, K=128 per step, with its scale copies)
+// on resident zero operands; *pairs = the pairs launched.  err: device error word.
+cudaError_t launch_mma_rate_selftest(int k_steps, int* err, int* pairs, cudaStream_t st);
 
 cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64_t a_rows, int64_t a_K,
                                 const void* B, int64_t b_rows, int64_t b_K, int64_t max_tiles, cudaStream_t st,

@@ -14,12 +14,17 @@
 // keeps it (kNoallocScratchBytes) until the process exits.  Host code cannot
 // use the array's name as a device address, so the first call on each device
 // asks the runtime for the address (cudaGetSymbolAddress, with that device
-// current) and remembers it; that first call should therefore come before any
-// stream capture.  Every call shares the same array: calls whose kernels
-// overlap on the GPU (different streams or host threads without ordering)
-// race on it.  Nothing here allocates.
-#include <atomic>
+// current) and remembers it together with the id of the device's current
+// context; a later call under another context (after cudaDeviceReset, which
+// unloads the module) looks the address up again.  That look-up happens on a
+// call, so the first call on a device (and the first after a reset) should
+// come before any stream capture.  Every call shares the same array: calls
+// whose kernels overlap on the GPU (different streams or host threads without
+// ordering) race on it.  Nothing here allocates.
+#include <cuda.h>
+
 #include <cstdio>
+#include <mutex>
 
 #include "kernels.cuh"
 
@@ -32,7 +37,39 @@ constexpr size_t kNoallocScratchBytes = kNoallocErrBytes + 2 * 4 * kNoallocMaxEx
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::atomic<unsigned char*> g_scratch_addr[kMaxDevices];
+struct ScratchSlot {
+  unsigned long long ctx_id;   // id of the context the address belongs to (0: none yet)
+  unsigned char* addr;
+};
+ScratchSlot g_slots[kMaxDevices];
+std::mutex g_slots_mutex;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Id of the calling thread's current context (the runtime's primary context of the
+// current device once the runtime has been used on it); 0 if it cannot be read.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 moe_status nfail(moe_status s, const char* what) {
   snprintf(moe::last_error_buffer(), moe::kLastErrorBytes, "%s", what);
@@ -41,14 +78,22 @@ moe_status nfail(moe_status s, const char* what) {
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Device address of the scratch array on the current device (set up once per device).
+// Device address of the scratch array on the current device, looked up once per device
+// and context.
 moe_status scratch_address(unsigned char** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return nfail(MOE_ERR_CUDA, cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return nfail(MOE_ERR_UNSUPPORTED, "device ordinal >= 64");
-  unsigned char* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
+  // make the runtime's primary context of this device current on this thread (it is the
+  // current device already; since CUDA 12 this also initialises the context), so that the
+  // context id below is the one the address belongs to
+  e = cudaSetDevice(dev);
+  if (e != cudaSuccess) return nfail(MOE_ERR_CUDA, cudaGetErrorString(e));
+  const unsigned long long ctx = current_context_id();
+  std::lock_guard<std::mutex> lock(g_slots_mutex);
+  ScratchSlot& slot = g_slots[dev];
+  if (slot.addr == nullptr || ctx == 0 || slot.ctx_id != ctx) {
     void* addr = nullptr;
     e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
     if (e != cudaSuccess || addr == nullptr) {
@@ -56,10 +101,10 @@ moe_status scratch_address(unsigned char** out) {
                cudaGetErrorString(e));
       return MOE_ERR_CUDA;
     }
-    p = static_cast<unsigned char*>(addr);
-    g_scratch_addr[dev].store(p, std::memory_order_release);
+    slot.addr = static_cast<unsigned char*>(addr);
+    slot.ctx_id = ctx;
   }
-  *out = p;
+  *out = slot.addr;
   return MOE_OK;
 }
 
@@ -70,10 +115,9 @@ extern "C" moe_status moe_route_permute_noalloc(const moe_dims* d, const float* 
                                                 int32_t* src_of, float* prob_perm, uint8_t* xq, uint8_t* xq_scale,
                                                 uint8_t* xq_col, uint8_t* xq_col_scale, moe_stream_t stream) {
   moe::last_error_buffer()[0] = 0;
-  if (d == nullptr) return nfail(MOE_ERR_INVALID_ARG, "dims is NULL");
-  if (d->T < 1 || d->H < 128 || d->H % 128 || d->I < 128 || d->I % 128 || d->E < 1 || d->E > 256 || d->k < 1 ||
-      d->k > 8 || d->k > d->E || d->H > 65536)
-    return nfail(MOE_ERR_UNSUPPORTED, "sizes outside the supported range (see moe_route_permute)");
+  // the checks of moe_route_permute (the message names the field), then the scratch limit
+  const moe_status dims_ok = moe::check_layer_dims(d);
+  if (dims_ok != MOE_OK) return dims_ok;
   const size_t groups = size_t(d->E) * size_t((d->T + 31) / 32);
   if (groups > kNoallocMaxExpertGroups) {
     snprintf(moe::last_error_buffer(), moe::kLastErrorBytes,
@@ -99,7 +143,7 @@ extern "C" moe_status moe_route_permute_noalloc(const moe_dims* d, const float* 
   int* bases = reinterpret_cast<int*>(base + kNoallocErrBytes + 4 * kNoallocMaxExpertGroups);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int64_t cap = ((int64_t(d->T) * d->k + 127) / 128) * 128 + 128 * int64_t(d->E);
+  const int64_t cap = moe::rows_capacity(d);
   // the masks and bases are fully rewritten by every call; only the error word starts at zero
   cudaError_t e = cudaMemsetAsync(err, 0, 8, st);
   if (e == cudaSuccess)
