@@ -21,8 +21,12 @@ EXPORTS = (
     "moe_selftest_wait_timeout", "moe_router_fwd", "moe_router_bwd", "moe_gather_rows", "grouped_mlp_fwd_bf16",
     "fp8_tensor_quantize", "moe_fp8_tensor_quantize_tokens", "grouped_mlp_fwd_fp8_tensor",
     "mxfp8_quantize_experts", "fp8_tensor_quantize_experts", "moe_transpose_bf16", "grouped_mlp_bwd_bf16",
-    "grouped_mlp_bwd_fp8_tensor",
+    "grouped_mlp_bwd_fp8_tensor", "moe_workspace_tensor", "moe_selftest_epilogue_quant", "moe_selftest_mma_issue",
 )
+
+# moe_ws_tensor ids (include/moe_ffn.h)
+WS_TENSORS = {"a_codes": 0, "a_scales": 1, "dy_codes": 2, "dy_scales": 3, "dy_col_codes": 4, "dy_col_scales": 5,
+              "dh_codes": 6, "dh_scales": 7, "dh_col_codes": 8, "dh_col_scales": 9}
 
 MOE_OK = 0
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
@@ -89,6 +93,10 @@ def lib() -> ctypes.CDLL:
             "fp8_tensor_quantize_experts": ([ctypes.POINTER(P), c_int32, c_int32, c_int32, P, P, P], c_int32),
             "moe_selftest_wait_timeout": ([P, c_size_t, ctypes.c_int64, ctypes.POINTER(c_int32),
                                            ctypes.POINTER(c_int32), P], c_int32),
+            "moe_workspace_tensor": ([D, c_int32, c_int32, ctypes.POINTER(c_size_t), ctypes.POINTER(c_size_t)],
+                                     c_int32),
+            "moe_selftest_epilogue_quant": ([P, c_int32, c_int32, P, P, P, P, P], c_int32),
+            "moe_selftest_mma_issue": ([c_int32, P, c_size_t, ctypes.POINTER(c_int32), P], c_int32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -214,6 +222,27 @@ def moe_selftest_wait_timeout(scratch, limit_ns, stream=None):
     _check(lib().moe_selftest_wait_timeout(_p(scratch), scratch.numel() * scratch.element_size(), int(limit_ns),
                                            ctypes.byref(code), ctypes.byref(site), _st(stream)))
     return int(code.value), int(site.value)
+
+
+def moe_workspace_tensor(d, training, which):
+    """(byte offset, bytes) of a named intermediate tensor inside a workspace."""
+    off, n = c_size_t(0), c_size_t(0)
+    _check(lib().moe_workspace_tensor(ctypes.byref(d), int(training), WS_TENSORS[which], ctypes.byref(off),
+                                      ctypes.byref(n)))
+    return int(off.value), int(n.value)
+
+
+def moe_selftest_epilogue_quant(src, rows, cols, codes, scales, codes_t, scales_t, stream=None):
+    _check(lib().moe_selftest_epilogue_quant(_p(src), rows, cols, _p(codes), _p(scales), _p(codes_t), _p(scales_t),
+                                             _st(stream)))
+
+
+def moe_selftest_mma_issue(k_steps, scratch, stream=None):
+    """Launches the MMA issue-rate self-test; returns the number of CTA pairs it used."""
+    pairs = c_int32(0)
+    _check(lib().moe_selftest_mma_issue(int(k_steps), _p(scratch), scratch.numel() * scratch.element_size(),
+                                        ctypes.byref(pairs), _st(stream)))
+    return int(pairs.value)
 
 
 def moe_clear_device_error(workspace, stream=None):

@@ -996,6 +996,93 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// ---- self-tests of the epilogue's parts ----------------------------------------------
+// The epilogue quantizers on caller data: warp w of a CTA takes the 32-row x 32-column
+// block (bx*4 + w) of an f32 [rows][cols] tensor, each lane one row's 32 values, exactly
+// as an epilogue warp holds them, and calls the epilogue's row-wise and along-token
+// quantizers on them.
+constexpr int EQ_WARPS = 4;
+__global__ void __launch_bounds__(32 * EQ_WARPS) epilogue_quant_selftest_kernel(
+    const float* __restrict__ src, int rows, int cols, uint8_t* codes, uint8_t* scales, uint8_t* codes_t,
+    uint8_t* scales_t) {
+  __shared__ float tr_all[EQ_WARPS * TR_WARP_FLOATS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t blk = int64_t(blockIdx.x) * EQ_WARPS + warp;
+  const int cb = cols / 32;
+  if (blk >= int64_t(rows / 32) * cb) return;                  // warp-uniform
+  const int64_t row_blk0 = (blk / cb) * 32;
+  const int64_t col = (blk % cb) * 32;
+  const int64_t row = row_blk0 + lane;
+  float v[32];
+  const float4* p = reinterpret_cast<const float4*>(src + row * cols + col);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 q = p[i];
+    v[4 * i + 0] = q.x;
+    v[4 * i + 1] = q.y;
+    v[4 * i + 2] = q.z;
+    v[4 * i + 3] = q.w;
+  }
+  quant_row_block(v, codes, scales, row, col, cols);
+  quant_col_block(v, codes_t, scales_t, row_blk0, col, rows, lane, tr_all + warp * TR_WARP_FLOATS);
+}
+
+// The MXFP8 tensor pipe's issue ceiling: CTA pairs (one CTA per SM) issue the GEMM's
+// MMAs -- per 128-deep K step three scale-factor copies and four
+// tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale of M=256, N=256, K=32 --
+// back to back on operands that stay in shared memory (zeros), with no loads and no
+// epilogue.  FLOPs per K step and pair: 2 * 256 * 256 * 128.
+constexpr int MR_THREADS = 64;
+constexpr int MR_OFF_A = 0, MR_OFF_B = A_TILE, MR_OFF_SF = A_TILE + B_HALF;
+constexpr int MR_OFF_BAR = MR_OFF_SF + 3 * SF_ATOM;
+constexpr int MR_SMEM = MR_OFF_BAR + 64 + 1024;
+__global__ void __launch_bounds__(MR_THREADS, 1) mma_rate_selftest_kernel(int k_steps, int* err, uint64_t limit_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* done = reinterpret_cast<uint64_t*>(smem + MR_OFF_BAR);
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + MR_OFF_BAR + 8);
+  volatile int* abort_s = reinterpret_cast<volatile int*>(smem + MR_OFF_BAR + 12);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  for (int i = threadIdx.x; i < MR_OFF_BAR / 16; i += MR_THREADS) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    mbar_init(done, 1);
+    *abort_s = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the zeros are visible to the tensor pipe
+  if (warp == 1) {
+    tmem_alloc(tmem_base_s, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_s;
+  if (warp == 0 && lane == 0 && rank == 0) {
+    const uint32_t tm_sfa = tmem + TM_SF0, tm_sfb = tm_sfa + 4;
+    const uint64_t adesc = desc_sw128(smem_u32(smem + MR_OFF_A));
+    const uint64_t bdesc = desc_sw128(smem_u32(smem + MR_OFF_B));
+    for (int kt = 0; kt < k_steps; ++kt) {
+      tc_cp_sf(tm_sfa, desc_sf(smem_u32(smem + MR_OFF_SF)));
+      tc_cp_sf(tm_sfb, desc_sf(smem_u32(smem + MR_OFF_SF + SF_ATOM)));
+      tc_cp_sf(tm_sfb + 4, desc_sf(smem_u32(smem + MR_OFF_SF + 2 * SF_ATOM)));
+#pragma unroll
+      for (int kk = 0; kk < BK / 32; ++kk)
+        tc_mma_mxf8(tmem + TM_ACC, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), idesc_mxf8(BN, kk), tm_sfa,
+                    tm_sfb, (kt | kk) != 0);
+    }
+    tc_commit(done);                               // arrives in both CTAs once every MMA is done
+  }
+  if (threadIdx.x == 0) wait_phase(done, 0, abort_s, err, SITE_GEMM_DRAIN + 5, limit_ns);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
 // ---- host side -----------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -1080,6 +1167,41 @@ cudaError_t launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
 }
 
 }  // namespace
+
+cudaError_t launch_epilogue_quant_selftest(const float* src, int rows, int cols, uint8_t* codes, uint8_t* scales,
+                                           uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st) {
+  const int64_t blocks = int64_t(rows / 32) * (cols / 32);
+  const int64_t grid = (blocks + EQ_WARPS - 1) / EQ_WARPS;
+  epilogue_quant_selftest_kernel<<<unsigned(grid), 32 * EQ_WARPS, 0, st>>>(src, rows, cols, codes, scales, codes_t,
+                                                                           scales_t);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mma_rate_selftest(int k_steps, int* err, int* pairs, cudaStream_t st) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(mma_rate_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MR_SMEM);
+  if (e != cudaSuccess) return e;
+  *pairs = sms / 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(2 * (sms / 2)));
+  cfg.blockDim = dim3(MR_THREADS);
+  cfg.dynamicSmemBytes = MR_SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, mma_rate_selftest_kernel, k_steps, err, kWaitLimitNs);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64_t a_rows, int64_t a_K,
                                 const void* B, int64_t b_rows, int64_t b_K, int64_t max_tiles, cudaStream_t st,

@@ -285,6 +285,13 @@ class ExpertFFN:
                          self.dw_r, self.ws, stream)
         return self.dx
 
+    def workspace_tensor(self, which: str) -> torch.Tensor:
+        """A uint8 view of a named intermediate tensor in this layer's workspace (binding.WS_TENSORS:
+        the MX codes and tile-layout scales of a, dY and dH; see moe_workspace_tensor)."""
+        training = 2 if self.bf16_training else int(self.training)
+        off, n = B.moe_workspace_tensor(self.d, training, which)
+        return self.ws[off:off + n]
+
     def device_error(self, stream=None):
         """(code, site) of the first device error recorded in any workspace of this layer."""
         for ws in (self.ws, getattr(self, "ws_t8", None)):

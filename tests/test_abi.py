@@ -147,3 +147,53 @@ def test_router_entry_points_check_arguments_on_the_host(lib):
     assert s == 1
     s = lib.moe_router_bwd(ctypes.byref(d), *([P(256)] * 10), 16, None)
     assert s == 4                                                     # workspace too small
+
+
+def test_workspace_tensor_offsets(lib):
+    """Named workspace tensors: sizes follow their documented shapes, they are 256-byte
+    aligned, disjoint and inside moe_workspace_size; backward tensors need a training
+    workspace."""
+    d = B.dims(300, 256, 384, 6, 2)
+    cap = B.moe_rows_capacity(d)
+    H, I = 256, 384
+    want = {"a_codes": cap * I, "a_scales": cap * I // 32, "dy_codes": cap * H, "dy_scales": cap * H // 32,
+            "dy_col_codes": H * cap, "dy_col_scales": H * cap // 32, "dh_codes": cap * 2 * I,
+            "dh_scales": cap * 2 * I // 32, "dh_col_codes": 2 * I * cap, "dh_col_scales": 2 * I * cap // 32}
+    for training in (1, 2, 3):
+        total = B.moe_workspace_size(d, training)
+        spans = []
+        for name, n in want.items():
+            off, got = B.moe_workspace_tensor(d, training, name)
+            assert got == n, name
+            assert off % 256 == 0 and off + n <= total, name
+            spans.append((off, off + n))
+        spans.sort()
+        assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:]))
+        assert spans[0][0] >= 256                       # the device error word comes first
+    off, n = B.moe_workspace_tensor(d, 0, "a_codes")
+    assert n == cap * I and off + n <= B.moe_workspace_size(d, 0)
+    with pytest.raises(B.MoeError):
+        B.moe_workspace_tensor(d, 0, "dy_codes")
+    off_c, size = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.moe_workspace_tensor(ctypes.byref(d), 1, 99, ctypes.byref(off_c), ctypes.byref(size)) == 1
+
+
+def test_selftest_entry_points_check_their_arguments(lib):
+    p = ctypes.c_void_p(256)
+    pairs = ctypes.c_int32(0)
+    assert lib.moe_selftest_mma_issue(0, p, 256, ctypes.byref(pairs), None) == 1          # k_steps < 1
+    assert lib.moe_selftest_mma_issue(10, ctypes.c_void_p(16), 256, ctypes.byref(pairs), None) == 3
+    assert lib.moe_selftest_mma_issue(10, p, 64, ctypes.byref(pairs), None) == 4          # scratch too small
+    assert lib.moe_selftest_epilogue_quant(p, 128, 100, p, p, p, p, None) == 2           # cols % 128
+    assert lib.moe_selftest_epilogue_quant(None, 128, 128, p, p, p, p, None) == 1
+
+
+def test_noalloc_names_the_bad_field(lib):
+    """The workspace-free routing call applies moe_route_permute's own size checks."""
+    p = ctypes.c_void_p(256)
+    d = B.dims(64, 128, 128, 4, 5)                   # k > E
+    assert lib.moe_route_permute_noalloc(ctypes.byref(d), *([p] * 12), None) == 2
+    assert b"k=5" in lib.moe_last_error_message()
+    d = B.dims(64, 100, 128, 4, 2)                   # H not a multiple of 128
+    assert lib.moe_route_permute_noalloc(ctypes.byref(d), *([p] * 12), None) == 2
+    assert b"H=100" in lib.moe_last_error_message()

@@ -3,9 +3,12 @@
 The whole layer runs on the GPU; the oracle then recomputes, one by one,
 sampled outputs it can afford on the host: complete routing and permutation
 (bit-exact), the MX codes of x (bit-exact), whole rows of y / out / dx /
-dprob for sampled tokens, and sampled entries of dW_gu and dW_d (each a
-full reduction over an expert's tokens).  The per-row and per-column pieces
-call the oracle's own primitives in the order its per-expert loop uses them.
+dprob for sampled tokens, and one entry of dW_gu and of dW_d in every
+256 x 256 output tile of the busiest expert, of an expert whose token range
+is an odd number of 128-row blocks, and (fine-grained) of the lightest and an
+empty expert -- each entry a full reduction over the expert's tokens.  The
+per-row and per-column pieces call the oracle's own primitives in the order
+its per-expert loop uses them.
 """
 import numpy as np
 import pytest
@@ -141,8 +144,12 @@ def check_rows(wl, L, cpu, idx, prob, perm, tokens, training):
         check_sample(got_dp, ref_dp, "dprob")
 
 
-def check_wgrad_entries(wl, L, cpu, prob, perm, experts, rng, n=4):
-    """Sampled dW_d[e][h][i] and dW_gu[e][j][h]: full token reductions per expert."""
+def check_wgrad_tiles(wl, L, cpu, prob, perm, experts, rng):
+    """One entry of dW_d[e] ([H][I]) and one of dW_gu[e] ([2I][H]) in EVERY 256 x 256 output
+    tile of each listed expert, each a full reduction over the expert's tokens, recomputed
+    with the oracle's primitives in its per-expert order (the columns of a and dH that the
+    sampled entries need are computed as batched matmuls of the same operands).  An expert
+    without tokens must have all-zero gradients."""
     cache = ExpertCache(cpu["w_gu"], cpu["w_d"])
     offs, split, src = perm["offsets_pad"], perm["split_sizes"], perm["src_of"]
     prob_perm = np.zeros(perm["rows"])
@@ -158,26 +165,49 @@ def check_wgrad_entries(wl, L, cpu, prob, perm, experts, rng, n=4):
         toks = src[offs[e]:offs[e] + m]
         xq_rows = ef.q_rowwise(cpu["x"][toks].float().numpy().astype(np.float64), ef.MXFP8)
         dyq_rows = ef.q_rowwise(cpu["dout"][toks].float().numpy().astype(np.float64), ef.MXFP8)
-        p = prob_perm[offs[e]:offs[e] + m][:, None]
-        hs = rng.choice(H, size=n, replace=False)
-        cols_i = rng.choice(I, size=n, replace=False)
-        for h, i in zip(hs, cols_i):
-            g = xq_rows @ q["gu"][i]
-            u = xq_rows @ q["gu"][I + i]
-            a = mx.fp32(ef.silu(g) * u * p[:, 0])
-            dy = cpu["dout"][toks, h].float().numpy().astype(np.float64)
-            ref_d.append(float(ef.q_tokens(dy[:, None], ef.MXFP8)[:, 0] @ ef.q_tokens(a[:, None], ef.MXFP8)[:, 0]))
-            got_d.append(float(L.dwd[e, h, i]))
-            # dW_gu rows j = i (gate) and I + i (up) at column h
-            dA = dyq_rows @ q["dT"][i]
-            dg, du, _ = ef.swiglu_backward(dA[:, None], mx.bf16(g)[:, None], mx.bf16(u)[:, None], p[:, 0])
-            xc = cpu["x"][toks, h].float().numpy().astype(np.float64)
-            xcq = ef.q_tokens(xc[:, None], ef.MXFP8)[:, 0]
-            for jj, col in ((i, dg), (I + i, du)):
-                ref_g.append(float(ef.q_tokens(mx.fp32(col), ef.MXFP8)[:, 0] @ xcq))
-                got_g.append(float(L.dwgu[e, jj, h]))
-    check_sample(got_d, ref_d, "dW_d entries")
-    check_sample(got_g, ref_g, "dW_gu entries")
+        p = prob_perm[offs[e]:offs[e] + m]
+        # dW_d tiles (hb, ib): entry (h, i); dW_gu tiles (jb, hb): entry (j, h), j < I gate, j >= I up
+        def pick(n, blk):                                 # an index inside 256-block blk of range(n)
+            return blk * 256 + int(rng.integers(min(256, n - blk * 256)))
+
+        d_ent = [(pick(H, hb), pick(I, ib)) for hb in range(-(-H // 256)) for ib in range(-(-I // 256))]
+        g_ent = [(pick(2 * I, jb), pick(H, hb)) for jb in range(-(-2 * I // 256)) for hb in range(-(-H // 256))]
+        cols = sorted(set(i for _, i in d_ent) | set(j % I for j, _ in g_ent))
+        ci = {c: n for n, c in enumerate(cols)}
+        cols = np.array(cols)
+        g = xq_rows @ q["gu"][cols].T                     # [m][n] gate columns
+        u = xq_rows @ q["gu"][I + cols].T                 # [m][n] up columns
+        a = mx.fp32(ef.silu(g) * u * p[:, None])          # the quantizer input of a
+        a_tok = ef.q_tokens(a, ef.MXFP8)
+        dA = dyq_rows @ q["dT"][cols].T                   # [m][n]
+        dg, du, _ = ef.swiglu_backward(dA, mx.bf16(g), mx.bf16(u), p)
+        dg_tok = ef.q_tokens(mx.fp32(dg), ef.MXFP8)
+        du_tok = ef.q_tokens(mx.fp32(du), ef.MXFP8)
+        h_d = np.array([h for h, _ in d_ent])
+        dy_tok = ef.q_tokens(cpu["dout"][toks][:, h_d].float().numpy().astype(np.float64), ef.MXFP8)
+        h_g = np.array([h for _, h in g_ent])
+        x_tok = ef.q_tokens(cpu["x"][toks][:, h_g].float().numpy().astype(np.float64), ef.MXFP8)
+        dwd_e = L.dwd[e].float().cpu().numpy()
+        dwgu_e = L.dwgu[e].float().cpu().numpy()
+        for n, (h, i) in enumerate(d_ent):
+            ref_d.append(float(dy_tok[:, n] @ a_tok[:, ci[i]]))
+            got_d.append(float(dwd_e[h, i]))
+        for n, (j, h) in enumerate(g_ent):
+            col = (dg_tok if j < I else du_tok)[:, ci[j % I]]
+            ref_g.append(float(col @ x_tok[:, n]))
+            got_g.append(float(dwgu_e[j, h]))
+    check_sample(got_d, ref_d, "dW_d entries (one per 256 x 256 tile)")
+    check_sample(got_g, ref_g, "dW_gu entries (one per 256 x 256 tile)")
+
+
+def odd_block_expert(split, exclude):
+    """An expert (other than `exclude`) whose padded token range is an odd number of
+    128-row blocks: its weight-gradient tiles end in a short barrier stage."""
+    for e in np.argsort(-split, kind="stable"):
+        nb = -(-int(split[e]) // 128)
+        if int(e) not in exclude and nb % 2 == 1:
+            return [int(e)]
+    return []
 
 
 def test_mixtral_fwd_bwd_full_size():
@@ -185,9 +215,11 @@ def test_mixtral_fwd_bwd_full_size():
     idx, prob, perm = check_routing_and_codes(wl, L, cpu)
     rng = np.random.default_rng(0)
     experts = sorted(set(int(e) for e in idx[0]))
-    toks = sample_tokens(idx, experts, 4, rng)
+    toks = sample_tokens(idx, experts, 12, rng)
     check_rows(wl, L, cpu, idx, prob, perm, toks, True)
-    check_wgrad_entries(wl, L, cpu, prob, perm, experts[:1], rng, n=3)
+    split = perm["split_sizes"]
+    busiest = int(np.argmax(split))
+    check_wgrad_tiles(wl, L, cpu, prob, perm, [busiest] + odd_block_expert(split, {busiest}), rng)
 
 
 def test_mixtral_forward_full_size():
@@ -195,7 +227,7 @@ def test_mixtral_forward_full_size():
     idx, prob, perm = check_routing_and_codes(wl, L, cpu)
     rng = np.random.default_rng(1)
     experts = sorted(set(int(e) for e in idx[-1]))
-    check_rows(wl, L, cpu, idx, prob, perm, sample_tokens(idx, experts, 4, rng), False)
+    check_rows(wl, L, cpu, idx, prob, perm, sample_tokens(idx, experts, 12, rng), False)
 
 
 def test_finegrained_fwd_bwd_full_size():
@@ -209,4 +241,5 @@ def test_finegrained_fwd_bwd_full_size():
     busiest = int(np.argmax(split))
     empty = int(np.nonzero(split == 0)[0][0])
     light = int(np.nonzero(split > 0)[0][np.argmin(split[split > 0])])
-    check_wgrad_entries(wl, L, cpu, prob, perm, [busiest, light, empty], rng, n=4)
+    chosen = [busiest, light, empty]
+    check_wgrad_tiles(wl, L, cpu, prob, perm, chosen + odd_block_expert(split, set(chosen)), rng)

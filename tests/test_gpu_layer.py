@@ -1,9 +1,12 @@
 """GPU expert-FFN layer vs the oracle on the same seeded inputs.
 
 Bit-exact: routing indices, split_sizes, the permutation, the MX codes and
-scales of x (both axes).  Floats (y, saved g/u, a after quantization along
-tokens, out, dx, dW_gu, dW_d, dprob): relative Frobenius error <= 5e-3 and
-max abs error <= 2e-2 * max|ref|.
+scales of x and of dOut (both axes each).  Floats (y, saved g/u, a after
+quantization along rows and along tokens, dH after quantization along rows
+and along tokens, out, dx, dW_gu, dW_d, dprob): relative Frobenius error
+<= 5e-3 and max abs error <= 2e-2 * max|ref|.  Device buffers are sliced to
+the padded row count on the device before they reach numpy, and numpy
+RuntimeWarnings (a NaN or an overflow in a cast) fail the test.
 """
 import numpy as np
 import pytest
@@ -16,7 +19,7 @@ from oracle import expert_ffn as ef
 from oracle import mxfp8 as mx
 from oracle import routing as rt
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.filterwarnings("error::RuntimeWarning")]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -26,6 +29,41 @@ def _lib():
 
 def f64(t):
     return t.float().cpu().numpy().astype(np.float64)
+
+
+def check_mx_codes(codes, scales, codes_t, scales_t, ref, cap, rows, name):
+    """Codes and scales of a [cap][K] row-wise MX tensor (and, when given, of its
+    along-token copy [K][cap]) equal the oracle quantizer's on ref [rows][K]."""
+    K = ref.shape[1]
+    ref_c, ref_s = mx.quantize_blocks(ref, axis=1)
+    assert np.array_equal(codes.view(cap, K)[:rows].cpu().numpy(), ref_c), f"{name} row codes"
+    assert np.array_equal(untile_scales(scales.cpu().numpy(), cap, K)[:rows], ref_s), f"{name} row scales"
+    if codes_t is not None:
+        # segments start on 128-row boundaries and are zero-padded: blocks of 32 rows of the
+        # whole padded tensor are the blocks along tokens inside every segment
+        ref_c, ref_s = mx.quantize_blocks(ref, axis=0)
+        assert np.array_equal(codes_t.view(K, cap)[:, :rows].cpu().numpy(), ref_c.T), f"{name} token codes"
+        assert np.array_equal(untile_scales(scales_t.cpu().numpy(), K, cap)[:, :rows // 32], ref_s.T), \
+            f"{name} token scales"
+
+
+def dequant_rows(codes, scales, cap, K, rows):
+    return mx.dequantize_blocks(codes.view(cap, K)[:rows].cpu().numpy(),
+                                untile_scales(scales.cpu().numpy(), cap, K)[:rows], axis=1)
+
+
+def dequant_cols(codes_t, scales_t, cap, K, rows):
+    """The along-token MX copy [K][cap], dequantized and transposed back to [rows][K]."""
+    return mx.dequantize_blocks(codes_t.view(K, cap)[:, :rows].cpu().numpy(),
+                                untile_scales(scales_t.cpu().numpy(), K, cap)[:, :rows // 32], axis=1).T
+
+
+def q_tokens_segments(v, offs, split):
+    out = np.zeros_like(v)
+    for e in range(len(split)):
+        sl = slice(offs[e], offs[e] + split[e])
+        out[sl] = ef.q_tokens(v[sl], ef.MXFP8)
+    return out
 
 
 def run_gpu(wl, inp, training):
@@ -58,32 +96,35 @@ def check_layer(wl, inp, training, report=None):
     assert np.allclose(L.prob.cpu().numpy(), prob, rtol=2e-6, atol=1e-7)
     assert np.array_equal(L.split_sizes.cpu().numpy(), perm["split_sizes"])
     assert np.array_equal(L.row_of.cpu().numpy(), perm["row_of"])
-    assert np.array_equal(L.src_of.cpu().numpy()[:rows], perm["src_of"])
-    assert np.allclose(L.prob_perm.cpu().numpy()[:rows], fwd["prob_perm"], rtol=2e-6, atol=1e-7)
+    assert np.array_equal(L.src_of[:rows].cpu().numpy(), perm["src_of"])
+    assert np.allclose(L.prob_perm[:rows].cpu().numpy(), fwd["prob_perm"], rtol=2e-6, atol=1e-7)
     # ---- bit-exact MX codes/scales of x ----
-    ref_c, ref_s = mx.quantize_blocks(fwd["x_perm"], axis=1)
-    assert np.array_equal(L.xq.cpu().numpy()[:rows], ref_c)
-    assert np.array_equal(untile_scales(L.xq_s.cpu().numpy(), L.cap, wl.H)[:rows], ref_s)
-    if training:
-        ref_c, ref_s = mx.quantize_blocks(fwd["x_perm"], axis=0)
-        assert np.array_equal(L.xq_col.cpu().numpy()[:, :rows], ref_c.T)
-        assert np.array_equal(untile_scales(L.xq_col_s.cpu().numpy(), wl.H, L.cap)[:, :rows // 32], ref_s.T)
+    check_mx_codes(L.xq, L.xq_s, L.xq_col if training else None, L.xq_col_s if training else None,
+                   fwd["x_perm"], L.cap, rows, "x")
     # ---- forward floats ----
-    assert_close(f64(L.y)[:rows], fwd["y"], "y")
+    assert_close(f64(L.y[:rows]), fwd["y"], "y")
     assert_close(f64(L.out), fwd["out"], "out")
+    a_rows = dequant_rows(L.workspace_tensor("a_codes"), L.workspace_tensor("a_scales"), L.cap, wl.I, rows)
+    assert_close(a_rows, ef.q_rowwise(fwd["a"], ef.MXFP8), "a quantized along rows")
     res = {"out_rel": rel_frob(f64(L.out), fwd["out"])}
     if training:
-        gu = f64(L.saved_gu)[:rows]
+        gu = f64(L.saved_gu[:rows])
         assert_close(gu[:, :wl.I], fwd["g"], "g")
         assert_close(gu[:, wl.I:], fwd["u"], "u")
-        aq_col = mx.dequantize_blocks(L.aq_col.cpu().numpy()[:, :rows],
-                                      untile_scales(L.aq_col_s.cpu().numpy(), wl.I, L.cap)[:, :rows // 32], axis=1)
-        ref_aq_col = np.zeros((rows, wl.I))
         offs, split = perm["offsets_pad"], perm["split_sizes"]
-        for e in range(wl.E):
-            sl = slice(offs[e], offs[e] + split[e])
-            ref_aq_col[sl] = ef.q_tokens(fwd["a"][sl], ef.MXFP8)
-        assert_close(aq_col.T, ref_aq_col, "a quantized along tokens")
+        aq_col = dequant_cols(L.aq_col, L.aq_col_s, L.cap, wl.I, rows)
+        assert_close(aq_col, q_tokens_segments(fwd["a"], offs, split), "a quantized along tokens")
+        # ---- bit-exact MX codes/scales of dOut gathered to rows (both axes) ----
+        check_mx_codes(L.workspace_tensor("dy_codes"), L.workspace_tensor("dy_scales"),
+                       L.workspace_tensor("dy_col_codes"), L.workspace_tensor("dy_col_scales"),
+                       bwd["dy_perm"], L.cap, rows, "dY")
+        # ---- dH = [dg | du] after its quantizers (inputs differ by accumulation order: tolerance) ----
+        dh_rows = dequant_rows(L.workspace_tensor("dh_codes"), L.workspace_tensor("dh_scales"), L.cap, 2 * wl.I,
+                               rows)
+        assert_close(dh_rows, ef.q_rowwise(bwd["dH"], ef.MXFP8), "dH quantized along rows")
+        dh_col = dequant_cols(L.workspace_tensor("dh_col_codes"), L.workspace_tensor("dh_col_scales"), L.cap,
+                              2 * wl.I, rows)
+        assert_close(dh_col, q_tokens_segments(bwd["dH"], offs, split), "dH quantized along tokens")
         assert_close(f64(L.dx), bwd["dx"], "dx")
         assert_close(f64(L.dwgu), bwd["dw_gu"], "dW_gu")
         assert_close(f64(L.dwd), bwd["dw_d"], "dW_d")
@@ -210,3 +251,36 @@ def test_nvtx_ranges_change_nothing():
         res.append([t.clone() for t in (L.out, L.dx, L.dwgu, L.dwd, L.dprob)])
     for a, b in zip(*res):
         assert torch.equal(a, b)
+
+
+@pytest.mark.filterwarnings("ignore:invalid value encountered")
+@pytest.mark.parametrize("k", [2, 6])
+def test_nan_logits_route_like_the_oracle(k):
+    """NaN logits rank below every number (-inf included): rows with fewer numbers than k
+    still select k distinct experts, identical to the oracle's choice; the permutation stays
+    bit-exact; probabilities match, NaN where the oracle has NaN."""
+    T, E = 300, 6
+    wl = configs.small(T, 128, 128, E, k, backward=False)
+    inp = synth.make_inputs(wl, 0)
+    logits = inp["logits"].clone()
+    rng = np.random.default_rng(5)
+    logits[rng.choice(T, 40, replace=False), 2] = float("nan")               # one NaN
+    rows = rng.choice(T, 20, replace=False)
+    logits[rows[:10], :E - 1] = float("nan")                                 # one number left
+    logits[rows[10:], :] = float("nan")                                      # all NaN
+    logits[rows[10:15], 3] = float("-inf")                                   # -inf beats NaN
+    logits[rng.choice(T, 10, replace=False), 4] = float("inf")
+    L = ExpertFFN(wl.T, wl.H, wl.I, wl.E, wl.k, training=False)
+    L.route(logits.cuda(), inp["x"].cuda())
+    torch.cuda.synchronize()
+    assert L.device_error() == (0, 0)
+    idx, prob = rt.route_topk(logits.numpy(), k)
+    assert np.array_equal(L.idx.cpu().numpy(), idx)
+    got = L.prob.cpu().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(prob))
+    fin = ~np.isnan(prob)
+    assert np.allclose(got[fin], prob[fin], rtol=2e-6, atol=1e-7)
+    perm = rt.permute(idx, E)
+    assert np.array_equal(L.split_sizes.cpu().numpy(), perm["split_sizes"])
+    assert np.array_equal(L.row_of.cpu().numpy(), perm["row_of"])
+    assert np.array_equal(L.src_of[:perm["rows"]].cpu().numpy(), perm["src_of"])

@@ -45,11 +45,27 @@ class OracleLayer:
 
 
 def test_sampled_checks_agree_with_full_oracle():
-    wl = configs.small(400, 128, 256, 6, 2, routing="biased", backward=True)
+    wl = configs.small(400, 384, 384, 6, 2, routing="biased", backward=True)   # partial 256-tiles on both axes
     inp = synth.make_inputs(wl, 0)
     L = OracleLayer(wl, inp)
     idx, prob, perm = fs.check_routing_and_codes(wl, L, inp)
     rng = np.random.default_rng(0)
     experts = sorted(set(int(e) for e in idx[0]))
     fs.check_rows(wl, L, inp, idx, prob, perm, fs.sample_tokens(idx, experts, 5, rng), True)
-    fs.check_wgrad_entries(wl, L, inp, prob, perm, list(range(wl.E)), rng, n=4)
+    split = perm["split_sizes"]
+    assert fs.odd_block_expert(split, set()), "the workload should hold an odd-block expert"
+    fs.check_wgrad_tiles(wl, L, inp, prob, perm, list(range(wl.E)), rng)
+
+
+def test_sampled_wgrad_check_catches_a_wrong_tile():
+    """A single wrong dW entry in one 256 x 256 tile fails the per-tile check."""
+    import pytest
+    wl = configs.small(300, 384, 384, 4, 2, routing="biased", backward=True)
+    inp = synth.make_inputs(wl, 0)
+    L = OracleLayer(wl, inp)
+    idx, prob, perm = fs.check_routing_and_codes(wl, L, inp)
+    e = int(np.argmax(perm["split_sizes"]))
+    # corrupt the whole last (partial) tile of dW_gu[e]: whichever entry the check samples
+    L.dwgu[e, 512:, 256:] = -L.dwgu[e, 512:, 256:] * 3
+    with pytest.raises(AssertionError):
+        fs.check_wgrad_tiles(wl, L, inp, prob, perm, [e], np.random.default_rng(0))

@@ -5,11 +5,14 @@ of moe_route_permute on the same inputs, on consecutive calls sharing that
 array.  This file is collected last on purpose."""
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
 from moe_expert_ffn_03_gb300 import binding as B
 from moe_expert_ffn_03_gb300 import build, configs, synth
+from oracle import mxfp8 as mx
+from oracle import routing as rt
 
 pytestmark = pytest.mark.gpu
 
@@ -50,6 +53,22 @@ def run_both(wl, seed):
             assert torch.allclose(a, b, rtol=0, atol=0), k
         else:
             assert torch.equal(a, b), k
+    # and directly against the oracle: routing, permutation and x codes bit-exact
+    idx, prob = rt.route_topk(inp["logits"].cpu().numpy(), wl.k)
+    perm = rt.permute(idx, wl.E)
+    assert np.array_equal(got["idx"].cpu().numpy(), idx)
+    assert np.allclose(got["prob"].cpu().numpy(), prob, rtol=2e-6, atol=1e-7)
+    assert np.array_equal(got["split_sizes"].cpu().numpy(), perm["split_sizes"])
+    assert np.array_equal(got["row_of"].cpu().numpy(), perm["row_of"])
+    assert np.array_equal(got["src_of"][:rows].cpu().numpy(), perm["src_of"])
+    x = inp["x"].float().cpu().numpy().astype(np.float64)
+    x_perm = np.zeros((rows, wl.H))
+    valid = perm["src_of"] >= 0
+    x_perm[valid] = x[perm["src_of"][valid]]
+    ref_c, _ = mx.quantize_blocks(x_perm, axis=1)
+    assert np.array_equal(got["xq"][:rows].cpu().numpy(), ref_c)
+    ref_c, _ = mx.quantize_blocks(x_perm, axis=0)
+    assert np.array_equal(got["xq_col"][:, :rows].cpu().numpy(), ref_c.T)
     return ref
 
 
