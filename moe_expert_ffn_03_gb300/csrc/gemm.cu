@@ -1035,7 +1035,10 @@ __global__ void __launch_bounds__(32 * EQ_WARPS) epilogue_quant_selftest_kernel(
 constexpr int MR_THREADS = 64;
 constexpr int MR_OFF_A = 0, MR_OFF_B = A_TILE, MR_OFF_SF = A_TILE + B_HALF;
 constexpr int MR_OFF_BAR = MR_OFF_SF + 3 * SF_ATOM;
-constexpr int MR_SMEM = MR_OFF_BAR + 64 + 1024;
+constexpr int MR_SMEM_USED = MR_OFF_BAR + 64 + 1024;
+// requested so that a second CTA never fits on an SM: one CTA (and one TMEM allocation) per SM
+constexpr int MR_SMEM = 160 * 1024;
+static_assert(MR_SMEM_USED <= MR_SMEM, "self-test shared memory");
 __global__ void __launch_bounds__(MR_THREADS, 1) mma_rate_selftest_kernel(int k_steps, int* err, uint64_t limit_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
