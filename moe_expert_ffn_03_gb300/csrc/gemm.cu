@@ -69,6 +69,10 @@ constexpr uint32_t TM_SF0 = 256, TM_SF_STRIDE = 12;  // per stage: SFA 4 columns
 // Columns 384..511: per epilogue warp a 32-column parking place (lanes of its quarter)
 // for the second half of its accumulator columns in the SwiGLU-backward epilogue.
 constexpr uint32_t TM_STASH = 384;
+// MXFP8 SwiGLU backward (four slots, so its scale columns end at 304): per epilogue warp
+// 48 columns 304 + 48*cg .. (lanes of its quarter) hold columns 16..63 of its dA; columns
+// 0..15 stay in registers.
+constexpr uint32_t TM_DA_STASH = 304, TM_DA_STASH_W = 48;
 constexpr int GROUP_M = 8;
 constexpr int SEG_INTS = 260;                   // per-expert prefix of 128-row blocks (E <= 256, plus the total)
 constexpr int kMaxSegE = 256;                   // mode-1 expert order (heaviest first) follows the prefix
@@ -134,6 +138,9 @@ struct Lay {
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 B
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(TM_SF0 + STG * TM_SF_STRIDE <= TM_STASH, "TMEM budget");
+  static_assert(EPI != EPI_BWD_SWIGLU ||
+                    (TM_SF0 + STG * TM_SF_STRIDE <= TM_DA_STASH && TM_DA_STASH + 4 * TM_DA_STASH_W <= TMEM_COLS),
+                "TMEM budget of the dA stash");
   static_assert(STG % PER == 0, "slots come in whole barrier stages");
 };
 
@@ -247,6 +254,32 @@ __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t* r) {
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
+      : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns (valid after tmem_wait_ld).
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+// 32 lanes x 8 consecutive 32-bit columns (valid after tmem_wait_ld).
+__device__ __forceinline__ void tmem_ld8_async(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns from registers into TMEM.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 // 32 lanes x 32 consecutive 32-bit columns from registers into TMEM.
@@ -470,55 +503,146 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, const float* v) 
                        pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
 }
 
+// ---- MX quantization pieces of the epilogues --------------------------------------
+// Block maximum of |v| raised by two values, as a float: non-negative floats order like
+// their bits, so this is the integer maximum of the |v| bit patterns for finite values;
+// max.NaN propagates a NaN, and a NaN or Inf maximum has exponent field 255, which
+// mx_scale_code turns into the NaN scale -- the same code as the integer form gives.
+__device__ __forceinline__ float amax_raise(float m, float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(m), "f"(fabsf(a)), "f"(fabsf(b)));
+  return r;
+}
+
+// Eight values of a block whose scale code c is known -> eight E4M3 codes (two words,
+// value 0 in the low byte of the first): v * 2^(127 - c) rounded to nearest even, or the
+// NaN codes when c is the NaN scale.
+__device__ __forceinline__ uint2 mx_encode8(const float* v, uint32_t c) {
+  if (c == 255u) return make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  const float m = mx_inv_scale(c);
+  const float2 m2 = make_float2(m, m);
+  const float2 a = __fmul2_rn(make_float2(v[0], v[1]), m2), b = __fmul2_rn(make_float2(v[2], v[3]), m2);
+  const float2 e = __fmul2_rn(make_float2(v[4], v[5]), m2), f = __fmul2_rn(make_float2(v[6], v[7]), m2);
+  return make_uint2(cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(b.x, b.y) << 16),
+                    cvt_e4m3x2(e.x, e.y) | (cvt_e4m3x2(f.x, f.y) << 16));
+}
+
+// One 32-byte store per lane (256-bit): a 32-column block of one row's codes.
+__device__ __forceinline__ void st_global_v8(uint8_t* p, const uint32_t* q) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(q[0]), "r"(q[1]), "r"(q[2]),
+               "r"(q[3]), "r"(q[4]), "r"(q[5]), "r"(q[6]), "r"(q[7]) : "memory");
+}
+// Keeps a pointer opaque to the compiler, so that an unrolled loop advances it step by step
+// instead of holding every step's precomputed address in registers.
+__device__ __forceinline__ void opaque(uint8_t*& p) { asm volatile("" : "+l"(p)); }
+
+// Row-wise codes of eight columns with known scale code c: 8 bytes at p.
+__device__ __forceinline__ void store_row8(const float* v, uint32_t c, uint8_t* p) {
+  *reinterpret_cast<uint2*>(p) = mx_encode8(v, c);
+}
+
+// Along-token quantization: where lane (c = lane/4, g = lane%4) of a warp whose 32 lanes
+// are the rows row_blk0.. writes the codes of column col + c (rows 8g..8g+7 of its block)
+// and that column's scale, in the transposed [cols][cap] tensor.  The next eight columns
+// (the next round) are 8*cap bytes further for the codes and 128 bytes further for the
+// scale: col is a multiple of 32, so the rounds stay inside one 32-row group of the scale
+// atom.
+struct ColDst {
+  uint8_t* codes;
+  uint8_t* scales;
+};
+__device__ __forceinline__ ColDst col_dst(uint8_t* codes_t, uint8_t* scales_t, int64_t row_blk0, int64_t col,
+                                          int64_t cap, int lane) {
+  const int64_t crow = col + (lane >> 2);
+  return ColDst{codes_t + crow * cap + row_blk0 + 8 * (lane & 3), scales_t + sf_offset(crow, row_blk0 >> 5, cap)};
+}
+
+// One round of the along-token quantizer: eight columns of the warp's 32 consecutive
+// permuted rows (one MX block along tokens; lane = row, v = this lane's eight values).
+// The eight columns go through the warp's shared-memory buffer (32 rows x 9 floats,
+// conflict-free both ways): lane (c = lane/4, g = lane%4) then holds rows 8g..8g+7 of
+// column c, takes the block maximum with two shuffles and stores its 8 codes as one
+// 8-byte word at dst.codes; the g == 0 lane stores the column's scale at dst.scales.
+__device__ __forceinline__ void quant_col_round(const float* v, ColDst dst, int lane, float* tr) {
+  const int c = lane >> 2, g = lane & 3;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) tr[lane * TR_PITCH + t] = v[t];
+  __syncwarp();
+  float w[8];
+  float amax = 0.f;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) w[t] = tr[(8 * g + t) * TR_PITCH + c];
+  __syncwarp();
+#pragma unroll
+  for (int t = 0; t < 8; t += 2) amax = amax_raise(amax, w[t], w[t + 1]);
+  uint32_t ab = __float_as_uint(amax);
+  ab = max(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 1));
+  ab = max(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 2));
+  const uint32_t sc = mx_scale_code(ab);
+  *reinterpret_cast<uint2*>(dst.codes) = mx_encode8(w, sc);
+  if (g == 0) *dst.scales = uint8_t(sc);
+}
+__device__ __forceinline__ void next_round(ColDst& d, int64_t cap) {
+  d.codes += 8 * cap;
+  d.scales += 128;
+  opaque(d.codes);
+  opaque(d.scales);
+}
+
 // 32 values of one column block (this thread's row) quantized rowwise; the scale
 // of (row, block) goes to the tile layout with row length K.
 __device__ __forceinline__ void quant_row_block(const float* v, uint8_t* codes, uint8_t* scales, int64_t row,
                                                 int64_t col, int64_t K) {
-  uint32_t q[8];
-  const uint32_t c = mx_quant32(v, q);
-  store_codes32(codes + row * K + col, q);
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) amax = amax_raise(amax, v[i], v[i + 1]);
+  const uint32_t c = mx_scale_code(__float_as_uint(amax));
+  uint8_t* p = codes + row * K + col;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) store_row8(v + 8 * j, c, p + 8 * j);
   scales[sf_offset(row, col >> 5, K)] = uint8_t(c);
 }
 
-// The same 32 columns quantized along tokens.  The warp's 32 lanes are 32
-// consecutive permuted rows (one MX block along tokens); column col+i becomes
-// row col+i of the transposed [cols][cap] tensor.  Eight columns at a time go
-// through the warp's shared-memory buffer (32 rows x 9 floats, conflict-free
-// both ways): lane (c = lane/4, g = lane%4) then holds rows 8g..8g+7 of column c,
-// takes the block amax with two shuffles and stores its 8 codes as one 8-byte
-// word; the g == 0 lane stores the column's scale.
+// The same 32 columns quantized along tokens: four rounds of eight columns.
 __device__ __forceinline__ void quant_col_block(const float* v, uint8_t* codes_t, uint8_t* scales_t,
                                                 int64_t row_blk0, int64_t col, int64_t cap, int lane,
                                                 float* tr) {
-  const int c = lane >> 2, g = lane & 3;
+  ColDst d = col_dst(codes_t, scales_t, row_blk0, col, cap, lane);
 #pragma unroll
   for (int rnd = 0; rnd < 4; ++rnd) {
-#pragma unroll
-    for (int t = 0; t < 8; ++t) tr[lane * TR_PITCH + t] = v[8 * rnd + t];
-    __syncwarp();
-    float w[8];
-    uint32_t amax = 0;
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      w[t] = tr[(8 * g + t) * TR_PITCH + c];
-      amax = max(amax, abs_bits(w[t]));
-    }
-    __syncwarp();
-    amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-    amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-    const uint32_t sc = mx_scale_code(amax);
-    uint32_t lo, hi;
-    if (sc == 255u) {
-      lo = hi = 0x7F7F7F7Fu;
-    } else {
-      const float m = mx_inv_scale(sc);
-      lo = cvt_e4m3x2(w[0] * m, w[1] * m) | (cvt_e4m3x2(w[2] * m, w[3] * m) << 16);
-      hi = cvt_e4m3x2(w[4] * m, w[5] * m) | (cvt_e4m3x2(w[6] * m, w[7] * m) << 16);
-    }
-    const int64_t crow = col + 8 * rnd + c;               // row of the transposed tensor
-    *reinterpret_cast<uint2*>(codes_t + crow * cap + row_blk0 + 8 * g) = make_uint2(lo, hi);
-    if (g == 0) scales_t[sf_offset(crow, row_blk0 >> 5, cap)] = uint8_t(sc);
+    quant_col_round(v + 8 * rnd, d, lane, tr);
+    next_round(d, cap);
   }
+}
+
+// ScaledSwiGLU backward of two columns of one row (a = silu(g)*u*p): with s = sigmoid(g)
+// and dp = dA*p,
+//   dg = dp*u*s*(1 + g*(1 - s)),  du = dp*g*s,  and sg*u = g*s*u for the row sum of dA*silu(g)*u.
+// Packed float32x2 arithmetic; exp and the reciprocal are the hardware approximations
+// (about 2 ulp; the results feed E4M3 quantizers with 3 mantissa bits).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void swiglu_bwd2(float2 d, float2 g, float2 u, float2 p2, float2& dg, float2& du,
+                                            float2& sgu) {
+  const float2 one = make_float2(1.f, 1.f);
+  const float2 t = __fmul2_rn(g, make_float2(-1.4426950408889634f, -1.4426950408889634f));   // -g log2(e)
+  const float2 den = __fadd2_rn(one, make_float2(ex2_approx(t.x), ex2_approx(t.y)));          // 1 + e^-g
+  const float2 s = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+  const float2 sg = __fmul2_rn(g, s);
+  const float2 oms = __ffma2_rn(s, make_float2(-1.f, -1.f), one);                              // 1 - s
+  const float2 dsilu = __fmul2_rn(s, __ffma2_rn(g, oms, one));
+  const float2 dpa = __fmul2_rn(d, p2);
+  dg = __fmul2_rn(__fmul2_rn(dpa, u), dsilu);
+  du = __fmul2_rn(dpa, sg);
+  sgu = __fmul2_rn(sg, u);
 }
 
 // SiLU with the fast divide (__fdividef, about 2 ulp): the result feeds an E4M3
@@ -567,6 +691,49 @@ __device__ __forceinline__ void stage_gu(const GemmArgs& a, int64_t row, int64_t
   }
 }
 
+// dA of chunk j of half h of an epilogue warp's 64 columns: columns 0..15 are in registers
+// r, columns 16..63 in the warp's TMEM stash.
+__device__ __forceinline__ void da_chunk(const uint32_t* r, uint32_t stash, int h, int j, uint32_t* d) {
+  if (h == 0 && j < 2) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = r[8 * j + i];
+  } else {
+    tmem_ld8_async(stash + uint32_t(8 * (4 * h + j - 2)), d);
+    tmem_wait_ld<8>(d);
+  }
+}
+
+// Chunk j (columns 8j..8j+7 of the half starting at col) of this lane's g and u into its
+// row of the staging buffer; completes with cp_async_wait_all.
+__device__ __forceinline__ void stage_gu_chunk(const GemmArgs& a, int64_t row, int64_t col, uint8_t* gu_s, int sw,
+                                               int j) {
+  const __nv_bfloat16* grow = a.gu + row * (2 * int64_t(a.I)) + col;
+  cp_async16(gu_s + ((j ^ sw) << 4), grow + 8 * j, true);
+  cp_async16(gu_s + (((4 + j) ^ sw) << 4), grow + a.I + 8 * j, true);
+}
+
+// dg and du of chunk j (eight columns) of this lane's row from its dA (d[0..7]), its
+// staged g,u and p; with dp2 != nullptr the chunk's dA*silu(g)*u is added to the pair sum.
+__device__ __forceinline__ void swiglu_bwd_chunk(const uint32_t* d, const uint8_t* gu_s, int j, int lane,
+                                                 float2 p2, float* vg, float* vu, float2* dp2) {
+  const uint4 gw = *reinterpret_cast<const uint4*>(gu_s + ((j ^ (lane & 7)) << 4));
+  const uint4 uw = *reinterpret_cast<const uint4*>(gu_s + (((4 + j) ^ (lane & 7)) << 4));
+  const uint32_t gs[4] = {gw.x, gw.y, gw.z, gw.w};
+  const uint32_t us[4] = {uw.x, uw.y, uw.z, uw.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    float2 dg, du, sgu;
+    const float2 dd = make_float2(__uint_as_float(d[2 * t]), __uint_as_float(d[2 * t + 1]));
+    swiglu_bwd2(dd, make_float2(bf16_lo(gs[t]), bf16_hi(gs[t])), make_float2(bf16_lo(us[t]), bf16_hi(us[t])), p2,
+                dg, du, sgu);
+    if (dp2 != nullptr) *dp2 = __ffma2_rn(dd, sgu, *dp2);
+    vg[2 * t] = dg.x;
+    vg[2 * t + 1] = dg.y;
+    vu[2 * t] = du.x;
+    vu[2 * t + 1] = du.y;
+  }
+}
+
 template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl, uint32_t tmem_row, int q, int cg,
                                               int lane, uint32_t tmem_empty_c, float* tr, uint8_t* gu_s) {
@@ -586,6 +753,22 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     tmem_ld32_async(tmem_row + TM_ACC + cg * 32, r);
     tmem_ld32_async(tmem_row + TM_ACC + 128 + cg * 32, r + 32);
     tmem_wait_ld<64>(r);
+  } else if (EPI == EPI_BWD_SWIGLU) {
+    // columns 16..63 of this warp's dA go to its TMEM stash (three rounds of 16), columns
+    // 0..15 stay in registers; then the accumulator is free for the next tile
+    have = c0 < ncols;
+    if (have) {
+      const uint32_t stash = tmem_row + TM_DA_STASH + uint32_t(cg) * TM_DA_STASH_W;
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        tmem_ld16_async(tmem_row + TM_ACC + c0 + 16 + 16 * k, r);
+        tmem_wait_ld<16>(r);
+        tmem_st16(stash + 16 * k, r);
+      }
+      tmem_ld16_async(tmem_row + TM_ACC + c0, r);
+      tmem_wait_ld<16>(r);
+      tmem_wait_st();
+    }
   } else if (Ops<EPI>::SWIGLU_BWD) {
     // 64 columns do not fit the register budget next to the SwiGLU-backward math:
     // park the second 32 in this warp's spare TMEM columns, then free the accumulator
@@ -685,7 +868,71 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     for (int i = 0; i < 32; ++i) f[i] = silu_f(f[i]) * f[32 + i] * p;
     quant_row_block(f, a.q_row, a.q_row_s, row, col, a.q_row_K);
     if (a.q_col != nullptr) quant_col_block(f, a.q_col, a.q_col_s, row_blk0, col, a.cap, lane, tr);
-  } else {  // SwiGLU backward (MX or bf16 dH): this warp's 64 columns of dA, as two halves of 32
+  } else if (EPI == EPI_BWD_SWIGLU) {
+    // MXFP8 SwiGLU backward: this warp's 64 columns of dA, as two halves of 32, each in two
+    // passes over four chunks of eight columns.  Pass A computes dg and du (packed pairs),
+    // runs the along-token quantizer rounds of the chunk (their blocks run over the warp's
+    // 32 rows, so a chunk's eight columns are complete), raises the row-block maxima and
+    // sums dp.  Pass B recomputes the same dg and du (the same instructions on the same
+    // inputs: bit-identical) and writes their row-wise codes with the scales pass A found.
+    // A chunk's dA comes from registers (columns 0..15) or from the TMEM stash; only one
+    // chunk is live at a time, which keeps the epilogue within its registers.  Pass B
+    // refills each chunk's g,u slot with the next half's as it frees it.
+    float2 dp2 = make_float2(0.f, 0.f);
+    if (have) {
+      const float p = a.prob_perm[row];
+      const float2 p2 = make_float2(p, p);
+      const int64_t twoI = 2 * int64_t(a.I);
+      const uint32_t stash = tmem_row + TM_DA_STASH + uint32_t(cg) * TM_DA_STASH_W;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const int64_t col = tl.n0 + c0 + 32 * h;
+        cp_async_wait_all();                               // this half's g,u are in gu_s
+        float amax_g = 0.f, amax_u = 0.f;
+        ColDst dst_g = col_dst(a.q_col, a.q_col_s, row_blk0, col, a.cap, lane);
+        ColDst dst_u = col_dst(a.q_col, a.q_col_s, row_blk0, a.I + col, a.cap, lane);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t d[8];
+          da_chunk(r, stash, h, j, d);
+          float vg[8], vu[8];
+          swiglu_bwd_chunk(d, gu_s, j, lane, p2, vg, vu, &dp2);
+#pragma unroll
+          for (int t = 0; t < 8; t += 2) {
+            amax_g = amax_raise(amax_g, vg[t], vg[t + 1]);
+            amax_u = amax_raise(amax_u, vu[t], vu[t + 1]);
+          }
+          quant_col_round(vg, dst_g, lane, tr);
+          quant_col_round(vu, dst_u, lane, tr);
+          next_round(dst_g, a.cap);
+          next_round(dst_u, a.cap);
+        }
+        const uint32_t c_g = mx_scale_code(__float_as_uint(amax_g));
+        const uint32_t c_u = mx_scale_code(__float_as_uint(amax_u));
+        uint8_t* row_g = a.q_row + row * twoI + col;
+        uint8_t* row_u = row_g + a.I;
+        uint32_t qg[8], qu[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t d[8];
+          da_chunk(r, stash, h, j, d);
+          float vg[8], vu[8];
+          swiglu_bwd_chunk(d, gu_s, j, lane, p2, vg, vu, nullptr);
+          if (h == 0) stage_gu_chunk(a, row, col + 32, gu_s, lane & 7, j);   // the next half's chunk j
+          const uint2 eg = mx_encode8(vg, c_g), eu = mx_encode8(vu, c_u);
+          qg[2 * j] = eg.x;
+          qg[2 * j + 1] = eg.y;
+          qu[2 * j] = eu.x;
+          qu[2 * j + 1] = eu.y;
+        }
+        st_global_v8(row_g, qg);
+        st_global_v8(row_u, qu);
+        a.q_row_s[sf_offset(row, col >> 5, twoI)] = uint8_t(c_g);
+        a.q_row_s[sf_offset(row, (a.I + col) >> 5, twoI)] = uint8_t(c_u);
+      }
+    }
+    a.dp_part[(int64_t(tl.nb) * 4 + cg) * a.cap + row] = dp2.x + dp2.y;
+  } else {  // SwiGLU backward with bf16 dH (bf16 and per-tensor operands): 64 columns as two halves of 32
     float dp = 0.f;
     if (have) {
       const float p = a.prob_perm[row];
@@ -730,17 +977,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
           store_col_bf16(o, a.out_t, row_blk0, col, a.cap, lane, tr);
           store_bf16x32(a.out + row * twoI + a.I + col, du);
           store_col_bf16(du, a.out_t, row_blk0, a.I + col, a.cap, lane, tr);
-        } else if (EPI == EPI_T8_BWD_SWIGLU) {
-          // bf16 dH rows; its per-tensor codes (both orientations) come after the amax
+        } else {
+          // per-tensor operands: bf16 dH rows; its codes (both orientations) come after the amax
           store_bf16x32(a.out + row * twoI + col, o);
           store_bf16x32(a.out + row * twoI + a.I + col, du);
 #pragma unroll
           for (int i = 0; i < 32; ++i) amax = max(amax, max(abs_bits(o[i]), abs_bits(du[i])));
-        } else {
-          quant_row_block(o, a.q_row, a.q_row_s, row, col, twoI);
-          quant_col_block(o, a.q_col, a.q_col_s, row_blk0, col, a.cap, lane, tr);
-          quant_row_block(du, a.q_row, a.q_row_s, row, a.I + col, twoI);
-          quant_col_block(du, a.q_col, a.q_col_s, row_blk0, a.I + col, a.cap, lane, tr);
         }
       }
       if (EPI == EPI_T8_BWD_SWIGLU) {

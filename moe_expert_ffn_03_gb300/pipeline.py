@@ -2,10 +2,12 @@
 
 A step's inputs (x, logits and, for training, dout) arrive from pinned host
 buffers and its results (out and, for training, dx) go back to pinned host
-buffers.  The copies run on their own stream while the kernels run on the
-compute stream:
+buffers.  The copies run on two streams of their own, one per direction (the
+GPU has separate copy engines for each), while the kernels run on the compute
+stream:
 
-  copy stream     H2D inputs[i+1] -> slot (i+1)%2      D2H out[i]     D2H dx[i]
+  input stream    H2D inputs[i+1] -> slot (i+1)%2
+  output stream                                        D2H out[i]     D2H dx[i]
   compute stream  step i on slot i%2 ............ combine_out ..... combine_dx
 
 * Two device slots hold the inputs, so the next step's inputs land while this
@@ -29,7 +31,8 @@ class HostPipeline:
         self.train = layer.training
         dev = layer.ws.device
         self.compute = stream if stream is not None else torch.cuda.current_stream(dev)
-        self.copy = torch.cuda.Stream(dev)
+        self.copy_in = torch.cuda.Stream(dev)
+        self.copy_out = torch.cuda.Stream(dev)
         T, H, E = layer.T, layer.H, layer.E
         names = ("x", "logits", "dout") if self.train else ("x", "logits")
         shapes = {"x": ((T, H), torch.bfloat16), "logits": ((T, E), torch.float32),
@@ -45,24 +48,25 @@ class HostPipeline:
         self._first = True
 
     def _h2d(self, slot: int, host: dict, wait_release: bool):
-        with torch.cuda.stream(self.copy):
+        with torch.cuda.stream(self.copy_in):
             if wait_release:
-                self.copy.wait_event(self.released[slot])
+                self.copy_in.wait_event(self.released[slot])
             for n in self.names:
                 self.slots[slot][n].copy_(host[n], non_blocking=True)
-            self.landed[slot].record(self.copy)
+            self.landed[slot].record(self.copy_in)
 
     def run(self, host_inputs: list, host_outputs: list, after: torch.cuda.Event | None = None):
         """One step per entry of host_inputs (dicts of pinned tensors named x, logits[,
         dout]); step i's out (and dx) are copied into host_outputs[i] (dicts of pinned
-        tensors named out[, dx]).  The copy stream first waits for `after` if given.
+        tensors named out[, dx]).  Both copy streams first wait for `after` if given.
         Returns without waiting; synchronize (or join()) before reading the results."""
         n = len(host_inputs)
         if n == 0:
             return
         L, st = self.L, self.compute
         if after is not None:
-            self.copy.wait_event(after)
+            self.copy_in.wait_event(after)
+            self.copy_out.wait_event(after)
         self._h2d(0, host_inputs[0], wait_release=not self._first)
         for i in range(n):
             s = i % 2
@@ -86,18 +90,19 @@ class HostPipeline:
                 self.dx_done.record(st)
             else:
                 self.released[s].record(st)
-            with torch.cuda.stream(self.copy):
-                self.copy.wait_event(self.out_done)
+            with torch.cuda.stream(self.copy_out):
+                self.copy_out.wait_event(self.out_done)
                 host_outputs[i]["out"].copy_(L.out, non_blocking=True)
-                self.out_copied.record(self.copy)
+                self.out_copied.record(self.copy_out)
                 if self.train:
-                    self.copy.wait_event(self.dx_done)
+                    self.copy_out.wait_event(self.dx_done)
                     host_outputs[i]["dx"].copy_(L.dx, non_blocking=True)
-                    self.dx_copied.record(self.copy)
+                    self.dx_copied.record(self.copy_out)
         self._first = False
 
     def join(self):
         """Make the compute stream wait for every copy issued so far."""
-        e = torch.cuda.Event()
-        e.record(self.copy)
-        self.compute.wait_event(e)
+        for st in (self.copy_in, self.copy_out):
+            e = torch.cuda.Event()
+            e.record(st)
+            self.compute.wait_event(e)

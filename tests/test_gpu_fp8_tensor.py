@@ -17,7 +17,7 @@ from oracle import fp8_tensor as pt
 from oracle import mxfp8 as mx
 from oracle import routing as rt
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.filterwarnings("error::RuntimeWarning")]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -95,7 +95,7 @@ def test_fp8_tensor_forward_matches_oracle(name_or_dims):
     assert np.array_equal(L.t8_xq.cpu().numpy()[:rows], fwd["xq_codes"])
 
     # the activation and what follows: float tolerance
-    assert_close(f64(L.t8_a)[:rows], fwd["a"], "a (bf16)")
+    assert_close(f64(L.t8_a[:rows]), fwd["a"], "a (bf16)")
     s_a = np.array([pt.tensor_scale(v) for v in L.t8_amax_a.cpu().tolist()])
     assert np.allclose(s_a[used], fwd["s_a"][used], rtol=2e-2)
     offs = perm["offsets_pad"]
@@ -107,7 +107,7 @@ def test_fp8_tensor_forward_matches_oracle(name_or_dims):
         aq_dev[sl] = pt.dequantize_tensor(codes[sl], s_a[e])
         aq_ref[sl] = pt.dequantize_tensor(fwd["aq_codes"][sl], fwd["s_a"][e])
     assert_close(aq_dev, aq_ref, "a after per-tensor quantization")
-    assert_close(f64(L.t8_y)[:rows], fwd["y"], "y")
+    assert_close(f64(L.t8_y[:rows]), fwd["y"], "y")
     assert_close(f64(out), fwd["out"], "out")
 
 
@@ -155,8 +155,8 @@ def test_fp8_tensor_training_step_matches_oracle(name_or_dims):
     fwd = pt.forward(f64(inp["x"]), idx, prob.astype(np.float64), f64(inp["w_gu"]), f64(inp["w_d"]))
     bwd = pt.backward(fwd, f64(inp["dout"]))
     rows, I = fwd["perm"]["rows"], wl.I
-    assert_close(f64(L.saved_gu)[:rows, :I], fwd["g"], "g")
-    assert_close(f64(L.saved_gu)[:rows, I:], fwd["u"], "u")
+    assert_close(f64(L.saved_gu[:rows, :I]), fwd["g"], "g")
+    assert_close(f64(L.saved_gu[:rows, I:]), fwd["u"], "u")
     assert_close(f64(dx), bwd["dx"], "dx")
     assert_close(f64(L.t8_dwgu), bwd["dw_gu"], "dW_gu")
     assert_close(f64(L.t8_dwd), bwd["dw_d"], "dW_d")

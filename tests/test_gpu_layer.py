@@ -253,7 +253,6 @@ def test_nvtx_ranges_change_nothing():
         assert torch.equal(a, b)
 
 
-@pytest.mark.filterwarnings("ignore:invalid value encountered")
 @pytest.mark.parametrize("k", [2, 6])
 def test_nan_logits_route_like_the_oracle(k):
     """NaN logits rank below every number (-inf included): rows with fewer numbers than k
@@ -274,7 +273,8 @@ def test_nan_logits_route_like_the_oracle(k):
     L.route(logits.cuda(), inp["x"].cuda())
     torch.cuda.synchronize()
     assert L.device_error() == (0, 0)
-    idx, prob = rt.route_topk(logits.numpy(), k)
+    with np.errstate(invalid="ignore"):                                  # NaN - NaN in the oracle's softmax
+        idx, prob = rt.route_topk(logits.numpy(), k)
     assert np.array_equal(L.idx.cpu().numpy(), idx)
     got = L.prob.cpu().numpy()
     assert np.array_equal(np.isnan(got), np.isnan(prob))
