@@ -455,6 +455,7 @@ __device__ __forceinline__ void decode_tile(const GemmArgs& a, const int* seg, i
 // Global sources of one CTA's K steps: TMA coordinates of its A and B boxes and
 // the rows (in 256-byte units, two per atom) of the scale atoms it stages.
 struct TileSrc {
+  int e;
   int a_row, b_row, k0, k_tiles;
   int sfa_y, sfb0_y, sfb1_y;
 };
@@ -465,6 +466,7 @@ __device__ __forceinline__ void tile_src(const GemmArgs& a, const int* seg, int 
   decode_tile<EPI>(a, seg, t, rank, tl);
   const int64_t sfa_row_atoms = a.sfa_K / BK;
   const int64_t sfb_row_atoms = a.sfb_K / BK;
+  ts.e = tl.e;
   ts.a_row = int(tl.a_row);
   ts.b_row = int(rank == 0 ? tl.b_row0 : tl.b_row1);
   ts.k0 = int(tl.k0);
@@ -996,11 +998,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
   }
 }
 
-template <int EPI>
+// B operand maps: one stacked tensor (tmB), or with PE one map per expert (each expert's
+// own weight tensor; the tile decode then gives B rows inside the expert's matrix, since
+// b_rows_per_expert is 0).
+template <int N>
+struct BMaps {
+  CUtensorMap m[N];
+};
+constexpr int kMaxMapExperts = 128;
+
+template <int EPI, bool PE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                        const GemmArgs args) {
+                        const __grid_constant__ BMaps<PE ? kMaxMapExperts : 1> bmaps, const GemmArgs args) {
   using L = Lay<EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1092,6 +1103,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (pair < total) tile_src<EPI>(args, seg, pair, rank, cur);
       for (int t = pair; t < total && ok; t += num_pairs) {
         if (t + num_pairs < total) tile_src<EPI>(args, seg, t + num_pairs, rank, nxt);
+        if (PE) prefetch_tmap(&bmaps.m[cur.e]);
         for (int kt0 = 0; kt0 < cur.k_tiles; kt0 += L::PER, ++it) {
           const int st = it % L::NSTG;
           const int round = it / L::NSTG;
@@ -1110,7 +1122,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int slot = st * L::PER;
           const int ka = cur.k0 / Ops<EPI>::KSTEP + kt0;        // first K atom of the stage
           tma_load_3d(smem + L::OFF_A + slot * A_TILE, &tmA, 0, cur.a_row, ka, bar_c);
-          tma_load_3d(smem + L::OFF_B + slot * B_HALF, &tmB, 0, cur.b_row, ka, bar_c);
+          tma_load_3d(smem + L::OFF_B + slot * B_HALF, PE ? &bmaps.m[cur.e] : &tmB, 0, cur.b_row, ka, bar_c);
           if (!Ops<EPI>::NOSF) {
             tma_load_2d(smem + L::OFF_SFA + slot * SF_ATOM, &tmSFA, 0, cur.sfa_y + 2 * kt0, bar_c);
             tma_load_2d(smem + L::OFF_SFB0 + slot * SF_ATOM, &tmSFB, 0, cur.sfb0_y + 2 * kt0, bar_c);
@@ -1378,9 +1390,10 @@ bool encode_sf_map(CUtensorMap* m, const void* base, int64_t n_atoms) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int EPI>
+template <int EPI, bool PE>
 cudaError_t launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msfa,
-                       const CUtensorMap& msfb, const GemmArgs& a, int grid, cudaStream_t st) {
+                       const CUtensorMap& msfb, const BMaps<PE ? kMaxMapExperts : 1>& bmaps, const GemmArgs& a,
+                       int grid, cudaStream_t st) {
   // the shared-memory attribute is per device: set it once on each device this process uses
   constexpr int kMaxDevices = 64;
   static std::atomic<bool> attr_set[kMaxDevices];
@@ -1388,7 +1401,7 @@ cudaError_t launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices || !attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, PE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Lay<EPI>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) attr_set[dev].store(true, std::memory_order_release);
@@ -1406,9 +1419,22 @@ cudaError_t launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<EPI>, ma, mb, msfa, msfb, a);
+  e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<EPI, PE>, ma, mb, msfa, msfb, bmaps, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <int EPI>
+cudaError_t launch_kind(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msfa,
+                        const CUtensorMap& msfb, const BMaps<kMaxMapExperts>* pe_maps, const GemmArgs& a, int grid,
+                        cudaStream_t st) {
+  // one B map per expert: the bf16 forward kinds (they read the master weights as they are)
+  if constexpr (EPI == EPI_B16_OUT || EPI == EPI_B16_FWD_SWIGLU) {
+    if (pe_maps != nullptr) return launch_epi<EPI, true>(ma, mb, msfa, msfb, *pe_maps, a, grid, st);
+  }
+  if (pe_maps != nullptr) return cudaErrorInvalidValue;
+  const BMaps<1> none{mb};
+  return launch_epi<EPI, false>(ma, mb, msfa, msfb, none, a, grid, st);
 }
 
 }  // namespace
@@ -1450,8 +1476,25 @@ cudaError_t launch_mma_rate_selftest(int k_steps, int* err, int* pairs, cudaStre
 
 cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64_t a_rows, int64_t a_K,
                                 const void* B, int64_t b_rows, int64_t b_K, int64_t max_tiles, cudaStream_t st,
-                                char* msg, size_t msg_len) {
+                                char* msg, size_t msg_len, const void* const* b_experts) {
   if (max_tiles <= 0) return cudaSuccess;
+  // one B map per expert: b_experts[e] is expert e's [b_rows][b_K] matrix
+  static thread_local BMaps<kMaxMapExperts> pe_maps;
+  if (b_experts != nullptr) {
+    if (a.E > kMaxMapExperts || a.b_rows_per_expert != 0) {
+      snprintf(msg, msg_len, "per-expert weight tensors: E=%d must be <= %d", a.E, kMaxMapExperts);
+      return cudaErrorInvalidValue;
+    }
+    const bool b16e = (epi == EPI_B16_OUT || epi == EPI_B16_FWD_SWIGLU);
+    for (int e = 0; e < a.E; ++e) {
+      if (!encode_map3(&pe_maps.m[e], b_experts[e], b_rows, b_K, b16e)) {
+        snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed for expert %d's weight (%lld x %lld)", e,
+                 (long long)b_rows, (long long)b_K);
+        return cudaErrorInvalidValue;
+      }
+    }
+    for (int e = a.E; e < kMaxMapExperts; ++e) pe_maps.m[e] = pe_maps.m[0];
+  }
   CUtensorMap ma, mb, msfa, msfb;
   const bool b16 = (epi == EPI_B16_OUT || epi == EPI_B16_FWD_SWIGLU || epi == EPI_B16_BWD_SWIGLU ||
                     epi == EPI_B16_F32_OUT);
@@ -1477,16 +1520,16 @@ cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64
   const int64_t pairs_max = sms / 2;
   const int grid = 2 * int(max_tiles < pairs_max ? max_tiles : pairs_max);
   switch (epi) {
-    case EPI_BF16: return launch_epi<EPI_BF16>(ma, mb, msfa, msfb, a, grid, st);
-    case EPI_FWD_SWIGLU: return launch_epi<EPI_FWD_SWIGLU>(ma, mb, msfa, msfb, a, grid, st);
-    case EPI_BWD_SWIGLU: return launch_epi<EPI_BWD_SWIGLU>(ma, mb, msfa, msfb, a, grid, st);
-    case EPI_B16_OUT: return launch_epi<EPI_B16_OUT>(ma, mb, msfa, msfb, a, grid, st);
-    case EPI_B16_FWD_SWIGLU: return launch_epi<EPI_B16_FWD_SWIGLU>(ma, mb, msfa, msfb, a, grid, st);
-    case EPI_T8_OUT: return launch_epi<EPI_T8_OUT>(ma, mb, msfa, msfb, a, grid, st);
-    case EPI_T8_FWD_SWIGLU: return launch_epi<EPI_T8_FWD_SWIGLU>(ma, mb, msfa, msfb, a, grid, st);
-    case EPI_B16_BWD_SWIGLU: return launch_epi<EPI_B16_BWD_SWIGLU>(ma, mb, msfa, msfb, a, grid, st);
-    case EPI_T8_BWD_SWIGLU: return launch_epi<EPI_T8_BWD_SWIGLU>(ma, mb, msfa, msfb, a, grid, st);
-    case EPI_B16_F32_OUT: return launch_epi<EPI_B16_F32_OUT>(ma, mb, msfa, msfb, a, grid, st);
+    case EPI_BF16: return launch_kind<EPI_BF16>(ma, mb, msfa, msfb, b_experts != nullptr ? &pe_maps : nullptr, a, grid, st);
+    case EPI_FWD_SWIGLU: return launch_kind<EPI_FWD_SWIGLU>(ma, mb, msfa, msfb, b_experts != nullptr ? &pe_maps : nullptr, a, grid, st);
+    case EPI_BWD_SWIGLU: return launch_kind<EPI_BWD_SWIGLU>(ma, mb, msfa, msfb, b_experts != nullptr ? &pe_maps : nullptr, a, grid, st);
+    case EPI_B16_OUT: return launch_kind<EPI_B16_OUT>(ma, mb, msfa, msfb, b_experts != nullptr ? &pe_maps : nullptr, a, grid, st);
+    case EPI_B16_FWD_SWIGLU: return launch_kind<EPI_B16_FWD_SWIGLU>(ma, mb, msfa, msfb, b_experts != nullptr ? &pe_maps : nullptr, a, grid, st);
+    case EPI_T8_OUT: return launch_kind<EPI_T8_OUT>(ma, mb, msfa, msfb, b_experts != nullptr ? &pe_maps : nullptr, a, grid, st);
+    case EPI_T8_FWD_SWIGLU: return launch_kind<EPI_T8_FWD_SWIGLU>(ma, mb, msfa, msfb, b_experts != nullptr ? &pe_maps : nullptr, a, grid, st);
+    case EPI_B16_BWD_SWIGLU: return launch_kind<EPI_B16_BWD_SWIGLU>(ma, mb, msfa, msfb, b_experts != nullptr ? &pe_maps : nullptr, a, grid, st);
+    case EPI_T8_BWD_SWIGLU: return launch_kind<EPI_T8_BWD_SWIGLU>(ma, mb, msfa, msfb, b_experts != nullptr ? &pe_maps : nullptr, a, grid, st);
+    case EPI_B16_F32_OUT: return launch_kind<EPI_B16_F32_OUT>(ma, mb, msfa, msfb, b_experts != nullptr ? &pe_maps : nullptr, a, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -20,8 +20,11 @@ namespace {
 constexpr int TT = 128;                 // tile edge
 constexpr int TP = TT + 8;              // bf16 per shared row (16 B pad)
 
+// S: StackedSrc (one tensor of batch matrices; with src_map its matrix 0 is the gather
+// source) or ExpertSrc (one pointer per matrix: each expert's own weight tensor).
+template <typename S>
 __global__ void __launch_bounds__(256, 6) transpose_bf16_kernel(
-    const __nv_bfloat16* __restrict__ src, const int* __restrict__ src_map, int64_t n_src_rows, int rows, int cols,
+    S src, const int* __restrict__ src_map, int64_t n_src_rows, int rows, int cols,
     const int* __restrict__ split_sizes, int E, __nv_bfloat16* __restrict__ out, int* err) {
   __shared__ __align__(16) __nv_bfloat16 tile[TT * TP];
   __shared__ int s_rows_used;
@@ -45,6 +48,7 @@ __global__ void __launch_bounds__(256, 6) transpose_bf16_kernel(
     __syncthreads();
     if (row0 >= s_rows_used) return;                  // rows past the padded segments
   }
+  const __nv_bfloat16* mat = src.mat(src_map != nullptr ? 0 : batch);
 #pragma unroll
   for (int it = 0; it < TT / 16; ++it) {
     const int r = rbase + 16 * it;
@@ -56,10 +60,10 @@ __global__ void __launch_bounds__(256, 6) transpose_bf16_kernel(
         s = -1;
       }
     } else {
-      s = batch * rows + row0 + r;
+      s = row0 + r;
     }
     const bool valid = s >= 0;
-    cp_async16(&tile[r * TP + c16 * 8], valid ? static_cast<const void*>(src + s * cols + col0 + c16 * 8) : src,
+    cp_async16(&tile[r * TP + c16 * 8], valid ? static_cast<const void*>(mat + s * cols + col0 + c16 * 8) : mat,
                valid);
   }
   cp_async_wait_all();
@@ -142,8 +146,17 @@ cudaError_t launch_transpose_u8(const uint8_t* src, int batch, int rows, int col
 cudaError_t launch_transpose_bf16(const void* src, const int* src_map, int64_t n_src_rows, int batch, int rows,
                                   int cols, const int* split_sizes, int E, void* out, int* err, cudaStream_t st) {
   dim3 grid(rows / TT, cols / TT, batch);
-  transpose_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), src_map, n_src_rows, rows,
-                                              cols, split_sizes, E, static_cast<__nv_bfloat16*>(out), err);
+  const StackedSrc s{static_cast<const __nv_bfloat16*>(src), int64_t(rows) * cols};
+  transpose_bf16_kernel<<<grid, 256, 0, st>>>(s, src_map, n_src_rows, rows, cols, split_sizes, E,
+                                              static_cast<__nv_bfloat16*>(out), err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_bf16_experts(const ExpertSrc& src, int batch, int rows, int cols, void* out,
+                                          cudaStream_t st) {
+  dim3 grid(rows / TT, cols / TT, batch);
+  transpose_bf16_kernel<<<grid, 256, 0, st>>>(src, nullptr, 0, rows, cols, nullptr, 0,
+                                              static_cast<__nv_bfloat16*>(out), nullptr);
   return cudaGetLastError();
 }
 

@@ -172,7 +172,8 @@ class ExpertFFN:
 
     # ---- bf16 forward (no quantization), on the routing of route() ----------------------
     def forward_bf16(self, x, w_gu, w_d, stream=None):
-        """After route(): gather x rows, bf16 grouped gate_up + ScaledSwiGLU + down, combine."""
+        """After route(): gather x rows, bf16 grouped gate_up + ScaledSwiGLU + down, combine.
+        w_gu, w_d: stacked [E][2I][H], [E][H][I], or lists of E per-expert tensors."""
         if not hasattr(self, "x_perm"):
             dev = self.ws.device
             self.x_perm = torch.empty(self.cap, self.H, dtype=torch.bfloat16, device=dev)
@@ -180,18 +181,28 @@ class ExpertFFN:
             self.y_b16 = torch.empty(self.cap, self.H, dtype=torch.bfloat16, device=dev)
             self.out_b16 = torch.empty(self.T, self.H, dtype=torch.bfloat16, device=dev)
         B.moe_gather_rows(self.d, x, self.row_of, self.split_sizes, self.x_perm, self.ws, stream)
-        B.grouped_mlp_fwd_bf16(self.d, self.x_perm, self.split_sizes, self.prob_perm, w_gu, w_d, self.a_perm,
-                               self.y_b16, self.ws, self.saved_gu if self.bf16_training else None, stream)
+        saved = self.saved_gu if self.bf16_training else None
+        if isinstance(w_gu, (list, tuple)):                 # one weight tensor per expert
+            B.grouped_mlp_fwd_bf16_experts(self.d, self.x_perm, self.split_sizes, self.prob_perm, w_gu, w_d,
+                                           self.a_perm, self.y_b16, self.ws, saved, stream)
+        else:
+            B.grouped_mlp_fwd_bf16(self.d, self.x_perm, self.split_sizes, self.prob_perm, w_gu, w_d, self.a_perm,
+                                   self.y_b16, self.ws, saved, stream)
         B.moe_unpermute_combine(self.d, self.y_b16, self.row_of, None, self.out_b16, stream)
         return self.out_b16
 
     # ---- bf16 training path: transposed weights once per step, then the backward ------------
     def transpose_weights_bf16(self, w_gu, w_d, stream=None):
-        """W_gu^T [E][H][2I] and W_d^T [E][I][H] for backward_bf16 (once per step)."""
+        """W_gu^T [E][H][2I] and W_d^T [E][I][H] for backward_bf16 (once per step); the weights
+        stacked or as lists of per-expert tensors."""
         if not hasattr(self, "wguT16"):
             dev = self.ws.device
             self.wguT16 = torch.empty(self.E, self.H, 2 * self.I, dtype=torch.bfloat16, device=dev)
             self.wdT16 = torch.empty(self.E, self.I, self.H, dtype=torch.bfloat16, device=dev)
+        if isinstance(w_gu, (list, tuple)):                 # one weight tensor per expert
+            B.moe_transpose_bf16_experts(w_gu, 2 * self.I, self.H, self.wguT16, stream)
+            B.moe_transpose_bf16_experts(w_d, self.H, self.I, self.wdT16, stream)
+            return
         B.moe_transpose_bf16(w_gu, self.E, 2 * self.I, self.H, self.wguT16, stream)
         B.moe_transpose_bf16(w_d, self.E, self.H, self.I, self.wdT16, stream)
 

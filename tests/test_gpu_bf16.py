@@ -84,3 +84,38 @@ def test_transpose_bf16_is_exact():
     B.moe_transpose_bf16(w, 3, 256, 384, out)
     torch.cuda.synchronize()
     assert torch.equal(out, w.transpose(1, 2))
+
+
+@pytest.mark.parametrize("dims", [(500, 256, 384, 6, 2, "biased"), (300, 128, 256, 64, 6, "biased"),
+                                  (200, 384, 128, 3, 2, "normal")])
+def test_bf16_per_expert_weight_tensors_equal_stacked(dims):
+    """One weight tensor per expert (the pages' weight0, weight1, ...): the forward reads each
+    expert's own tensor through its own TMA descriptor, the transposes read one pointer per
+    expert; the training step is bit-identical to the stacked weights'."""
+    wl = configs.small(*dims[:5], routing=dims[5])
+    inp = {k: v.cuda() for k, v in synth.make_inputs(wl, 0, with_grad=True).items()}
+    res = []
+    for as_list in (False, True):
+        L = ExpertFFN(wl.T, wl.H, wl.I, wl.E, wl.k, training=True, bf16_training=True)
+        w_gu = [w.clone() for w in inp["w_gu"]] if as_list else inp["w_gu"]
+        w_d = [w.clone() for w in inp["w_d"]] if as_list else inp["w_d"]
+        L.route(inp["logits"], inp["x"])
+        L.forward_bf16(inp["x"], w_gu, w_d)
+        L.transpose_weights_bf16(w_gu, w_d)
+        L.backward_bf16(inp["dout"])
+        torch.cuda.synchronize()
+        assert L.device_error() == (0, 0)
+        rows = L.padded_rows()                                    # a_perm rows past the segments are unwritten
+        res.append([t.clone() for t in (L.out_b16, L.a_perm[:rows], L.dx16, L.dwgu16, L.dwd16, L.dprob16, L.wguT16,
+                                        L.wdT16)])
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
+
+
+def test_bf16_per_expert_host_checks():
+    from moe_expert_ffn_03_gb300 import binding as B
+    wl = configs.small(64, 128, 128, 129, 2)                       # E above the per-expert map limit
+    L = ExpertFFN(wl.T, wl.H, wl.I, wl.E, wl.k, training=False)
+    w = [torch.zeros(256, 128, dtype=torch.bfloat16, device="cuda")] * wl.E
+    with pytest.raises(B.MoeError):
+        B.grouped_mlp_fwd_bf16_experts(L.d, L.xq, L.split_sizes, L.prob_perm, w, w, L.y, L.y, L.ws)
