@@ -175,6 +175,67 @@ moe_status moe_route_permute(const moe_dims* d, const float* logits, const void*
                              void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * moe_route -- the routing and permutation of moe_route_permute without the
+ * gather and quantization of x: idx, prob, split_sizes, row_of, src_of and
+ * prob_perm exactly as moe_route_permute writes them.  An expert-parallel
+ * rank (moe_ep_pack) needs only these on the tokens' side.  workspace as for
+ * moe_route_permute with training = 0.
+ */
+moe_status moe_route(const moe_dims* d, const float* logits, int32_t* idx, float* prob, int32_t* split_sizes,
+                     int32_t* row_of, int32_t* src_of, float* prob_perm, void* workspace, size_t workspace_bytes,
+                     moe_stream_t stream);
+
+/*
+ * moe_permute -- moe_route_permute for rows whose experts are already known
+ * (page "Efficient MoE Training for Biological Foundation Models", section
+ * "GroupedLinear": the grouped call receives the tokens collected per expert
+ * together with split_sizes).  idx int32 [T][k] holds expert ids in 0..E-1 and
+ * prob f32 [T][k] their probabilities; the stable expert-major permutation
+ * (ascending row inside each segment, segments padded to 128 rows), the MX
+ * codes of x rows and, optionally, of x along tokens are those moe_route_permute
+ * produces for the same idx.  An expert-parallel rank calls it on the rows it
+ * received (k = 1, idx = their local expert ids).  An id outside 0..E-1 is
+ * recorded in the workspace error word and its slot skipped (row_of -1).
+ * Arguments otherwise as moe_route_permute.
+ */
+moe_status moe_permute(const moe_dims* d, const int32_t* idx, const float* prob, const void* x, int32_t* split_sizes,
+                       int32_t* row_of, int32_t* src_of, float* prob_perm, uint8_t* xq, uint8_t* xq_scale,
+                       uint8_t* xq_col, uint8_t* xq_col_scale, void* workspace, size_t workspace_bytes,
+                       moe_stream_t stream);
+
+/*
+ * moe_ep_pack -- the send side of the expert-parallel dispatch (page
+ * "英伟达开源MoE加速神器：一行代码，微调快3.7倍", section "三板斧": experts are
+ * spread over the GPUs and an All-to-All takes each token to its expert's GPU).
+ * The E experts are laid out over `world` ranks in contiguous blocks (rank r owns
+ * experts r*E/world .. (r+1)*E/world - 1; world divides E).  From the routing of
+ * moe_route (idx, prob, row_of, split_sizes of this rank's T tokens) it writes the
+ * T*k rows densely in expert-major order, which groups them by destination rank:
+ *   send_x     out bf16 [T*k][H]: row pos of (t, j) = x[t], where pos = the number
+ *              of rows of experts before idx[t][j] plus the row's rank inside its
+ *              expert (ascending token order)
+ *   send_prob  out f32 [T*k]: prob[t][j] at pos
+ *   send_eid   out int32 [T*k]: idx[t][j] modulo E/world (the destination's local id)
+ *   pos_of     out int32 [T][k]: pos of every (t, j) (the combine's row map)
+ *   rank_counts out int32 [world]: rows for each destination rank (the split sizes
+ *              of the All-to-All)
+ * workspace as for moe_route (its error word records inconsistent inputs).
+ */
+moe_status moe_ep_pack(const moe_dims* d, int32_t world, const void* x, const int32_t* idx, const float* prob,
+                       const int32_t* row_of, const int32_t* split_sizes, void* send_x, float* send_prob,
+                       int32_t* send_eid, int32_t* pos_of, int32_t* rank_counts, void* workspace,
+                       size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * moe_gather_f32 -- out[i] = src[map[i]] for i < n (f32); a map entry outside
+ * 0..n_src-1 gives 0 and is recorded in the error word at `workspace` (any
+ * layer workspace).  The expert-parallel combine takes the returned dprob rows
+ * back to [T][k] with it (map = pos_of).
+ */
+moe_status moe_gather_f32(const float* src, int64_t n_src, const int32_t* map, int64_t n, float* out,
+                          void* workspace, moe_stream_t stream);
+
+/*
  * grouped_mlp_fwd -- grouped gate_up GEMM + ScaledSwiGLU + grouped down GEMM
  * (page "Efficient MoE Training for Biological Foundation Models", sections
  * "GroupedLinear" and "MXFP8与融合MLP").  One launch per GEMM covers every
@@ -234,6 +295,35 @@ moe_status grouped_mlp_fwd_bf16(const moe_dims* d, const void* x_perm, const int
  */
 moe_status moe_transpose_bf16(const void* src, int32_t batch, int32_t rows, int32_t cols, void* dst,
                               moe_stream_t stream);
+
+/*
+ * moe_transpose_bf16_experts -- moe_transpose_bf16 for weights held as one
+ * tensor per expert (page "Efficient MoE Training for Biological Foundation
+ * Models", section "GroupedLinear": every expert keeps its own weight, weight0,
+ * weight1, ...).  src is a HOST array of E device pointers, each to a bf16
+ * [rows][cols] matrix (16-byte aligned; read during the call only); dst is the
+ * stacked transposed tensor [E][cols][rows] that grouped_mlp_bwd_bf16 reads.
+ * rows, cols multiples of 128; 1 <= E <= 256.
+ */
+moe_status moe_transpose_bf16_experts(const void* const* src, int32_t E, int32_t rows, int32_t cols, void* dst,
+                                      moe_stream_t stream);
+
+/*
+ * grouped_mlp_fwd_bf16_experts -- grouped_mlp_fwd_bf16 on one weight tensor per
+ * expert (page "Efficient MoE Training for Biological Foundation Models",
+ * section "GroupedLinear": GroupedLinear keeps weight0, weight1, ... and the
+ * grouped call applies each expert's own matrix to its split of the tokens).
+ * w_gu and w_d are HOST arrays of E device pointers (read during the call):
+ * w_gu[e] bf16 [2I][H] (rows 0..I-1 gate, I..2I-1 up), w_d[e] bf16 [H][I], each
+ * 16-byte aligned.  The GEMMs read each expert's tensor where it is, through one
+ * TMA descriptor per expert; results are bit-identical to grouped_mlp_fwd_bf16
+ * on the same weights stacked.  E <= 128 (MOE_ERR_UNSUPPORTED above).  Other
+ * arguments, outputs and errors as grouped_mlp_fwd_bf16.
+ */
+moe_status grouped_mlp_fwd_bf16_experts(const moe_dims* d, const void* x_perm, const int32_t* split_sizes,
+                                        const float* prob_perm, const void* const* w_gu, const void* const* w_d,
+                                        void* a_perm, void* y, void* saved_gu, void* workspace,
+                                        size_t workspace_bytes, moe_stream_t stream);
 
 /*
  * grouped_mlp_bwd_bf16 -- backward of grouped_mlp_fwd_bf16 (no quantization;

@@ -22,6 +22,8 @@ EXPORTS = (
     "fp8_tensor_quantize", "moe_fp8_tensor_quantize_tokens", "grouped_mlp_fwd_fp8_tensor",
     "mxfp8_quantize_experts", "fp8_tensor_quantize_experts", "moe_transpose_bf16", "grouped_mlp_bwd_bf16",
     "grouped_mlp_bwd_fp8_tensor", "moe_workspace_tensor", "moe_selftest_epilogue_quant", "moe_selftest_mma_issue",
+    "moe_transpose_bf16_experts", "grouped_mlp_fwd_bf16_experts", "moe_route", "moe_permute", "moe_ep_pack",
+    "moe_gather_f32",
 )
 
 # moe_ws_tensor ids (include/moe_ffn.h)
@@ -97,6 +99,13 @@ def lib() -> ctypes.CDLL:
                                      c_int32),
             "moe_selftest_epilogue_quant": ([P, c_int32, c_int32, P, P, P, P, P], c_int32),
             "moe_selftest_mma_issue": ([c_int32, P, c_size_t, ctypes.POINTER(c_int32), P], c_int32),
+            "moe_transpose_bf16_experts": ([ctypes.POINTER(P), c_int32, c_int32, c_int32, P, P], c_int32),
+            "moe_route": ([D, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
+            "moe_permute": ([D] + [P] * 12 + [c_size_t, P], c_int32),
+            "moe_ep_pack": ([D, c_int32] + [P] * 11 + [c_size_t, P], c_int32),
+            "moe_gather_f32": ([P, ctypes.c_int64, P, ctypes.c_int64, P, P, P], c_int32),
+            "grouped_mlp_fwd_bf16_experts": ([D, P, P, P, ctypes.POINTER(P), ctypes.POINTER(P), P, P, P, P, c_size_t,
+                                              P], c_int32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -284,6 +293,45 @@ def _ptr_array(tensors):
 def mxfp8_quantize_experts(w_list, rows, cols, codes, scales, codes_t=None, scales_t=None, stream=None):
     _check(lib().mxfp8_quantize_experts(_ptr_array(w_list), len(w_list), rows, cols, _p(codes), _p(scales),
                                         _p(codes_t), _p(scales_t), _st(stream)))
+
+
+def _wsb(workspace):
+    return workspace.numel() * workspace.element_size()
+
+
+def moe_route(d, logits, idx, prob, split_sizes, row_of, src_of, prob_perm, workspace, stream=None):
+    _check(lib().moe_route(ctypes.byref(d), _p(logits), _p(idx), _p(prob), _p(split_sizes), _p(row_of), _p(src_of),
+                           _p(prob_perm), _p(workspace), _wsb(workspace), _st(stream)))
+
+
+def moe_permute(d, idx, prob, x, split_sizes, row_of, src_of, prob_perm, xq, xq_scale, xq_col, xq_col_scale,
+                workspace, stream=None):
+    _check(lib().moe_permute(ctypes.byref(d), _p(idx), _p(prob), _p(x), _p(split_sizes), _p(row_of), _p(src_of),
+                             _p(prob_perm), _p(xq), _p(xq_scale), _p(xq_col), _p(xq_col_scale), _p(workspace),
+                             _wsb(workspace), _st(stream)))
+
+
+def moe_ep_pack(d, world, x, idx, prob, row_of, split_sizes, send_x, send_prob, send_eid, pos_of, rank_counts,
+                workspace, stream=None):
+    _check(lib().moe_ep_pack(ctypes.byref(d), int(world), _p(x), _p(idx), _p(prob), _p(row_of), _p(split_sizes),
+                             _p(send_x), _p(send_prob), _p(send_eid), _p(pos_of), _p(rank_counts), _p(workspace),
+                             _wsb(workspace), _st(stream)))
+
+
+def moe_gather_f32(src, map_, n, out, workspace, stream=None):
+    _check(lib().moe_gather_f32(_p(src), src.numel(), _p(map_), int(n), _p(out), _p(workspace), _st(stream)))
+
+
+def moe_transpose_bf16_experts(w_list, rows, cols, dst, stream=None):
+    _check(lib().moe_transpose_bf16_experts(_ptr_array(w_list), len(w_list), rows, cols, _p(dst), _st(stream)))
+
+
+def grouped_mlp_fwd_bf16_experts(d, x_perm, split_sizes, prob_perm, w_gu_list, w_d_list, a_perm, y, workspace,
+                                 saved_gu=None, stream=None):
+    _check(lib().grouped_mlp_fwd_bf16_experts(ctypes.byref(d), _p(x_perm), _p(split_sizes), _p(prob_perm),
+                                              _ptr_array(w_gu_list), _ptr_array(w_d_list), _p(a_perm), _p(y),
+                                              _p(saved_gu), _p(workspace), workspace.numel() * workspace.element_size(),
+                                              _st(stream)))
 
 
 def fp8_tensor_quantize_experts(w_list, rows, cols, codes, amax, stream=None):

@@ -316,6 +316,112 @@ moe_status moe_route_permute(const moe_dims* d, const float* logits, const void*
   return MOE_OK;
 }
 
+moe_status moe_route(const moe_dims* d, const float* logits, int32_t* idx, float* prob, int32_t* split_sizes,
+                     int32_t* row_of, int32_t* src_of, float* prob_perm, void* workspace, size_t workspace_bytes,
+                     moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  REQUIRE_PTR(logits);
+  REQUIRE_PTR(idx);
+  REQUIRE_PTR(prob);
+  REQUIRE_PTR(split_sizes);
+  REQUIRE_PTR(row_of);
+  REQUIRE_PTR(src_of);
+  REQUIRE_PTR(prob_perm);
+  s = check_ws(d, workspace, workspace_bytes, false);
+  if (s != MOE_OK) return s;
+  const WsLayout w = ws_layout(d, false);
+  CUDA_TRY(launch_route_permute(logits, d->T, d->E, d->k, d->renormalize, idx, prob, at<uint32_t>(workspace, w.masks),
+                                at<int>(workspace, w.bases), split_sizes, row_of, src_of, prob_perm,
+                                at<int>(workspace, w.err), static_cast<cudaStream_t>(stream)),
+           "route");
+  return MOE_OK;
+}
+
+moe_status moe_permute(const moe_dims* d, const int32_t* idx, const float* prob, const void* x, int32_t* split_sizes,
+                       int32_t* row_of, int32_t* src_of, float* prob_perm, uint8_t* xq, uint8_t* xq_scale,
+                       uint8_t* xq_col, uint8_t* xq_col_scale, void* workspace, size_t workspace_bytes,
+                       moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  REQUIRE_PTR(idx);
+  REQUIRE_PTR(prob);
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(split_sizes);
+  REQUIRE_PTR(row_of);
+  REQUIRE_PTR(src_of);
+  REQUIRE_PTR(prob_perm);
+  REQUIRE_PTR(xq);
+  REQUIRE_PTR(xq_scale);
+  if ((xq_col == nullptr) != (xq_col_scale == nullptr))
+    return fail(MOE_ERR_INVALID_ARG, "xq_col and xq_col_scale must both be set or both be NULL");
+  if (xq_col != nullptr) {
+    REQUIRE_PTR(xq_col);
+    REQUIRE_PTR(xq_col_scale);
+  }
+  s = check_ws(d, workspace, workspace_bytes, false);
+  if (s != MOE_OK) return s;
+  const WsLayout w = ws_layout(d, false);
+  int* err = at<int>(workspace, w.err);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t cap = capacity(d);
+  CUDA_TRY(launch_permute_from_idx(idx, prob, d->T, d->E, d->k, at<uint32_t>(workspace, w.masks),
+                                   at<int>(workspace, w.bases), split_sizes, row_of, src_of, prob_perm, err, st),
+           "permute");
+  CUDA_TRY(launch_quant_rowwise(x, d->T, d->H, row_of, d->k, cap, xq, xq_scale, err, st), "gather_quant_rowwise");
+  CUDA_TRY(launch_fill_pad_rows(split_sizes, d->E, d->H, xq, xq_scale, st), "fill_pad_rows");
+  if (xq_col != nullptr)
+    CUDA_TRY(launch_quant_colwise(x, src_of, d->T, 1, int(cap), d->H, split_sizes, d->E, xq_col, xq_col_scale, err,
+                                  st),
+             "gather_quant_colwise");
+  return MOE_OK;
+}
+
+moe_status moe_ep_pack(const moe_dims* d, int32_t world, const void* x, const int32_t* idx, const float* prob,
+                       const int32_t* row_of, const int32_t* split_sizes, void* send_x, float* send_prob,
+                       int32_t* send_eid, int32_t* pos_of, int32_t* rank_counts, void* workspace,
+                       size_t workspace_bytes, moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  if (world < 1 || world > d->E || d->E % world != 0)
+    return fail(MOE_ERR_UNSUPPORTED, "world=%d must divide E=%d", world, d->E);
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(idx);
+  REQUIRE_PTR(prob);
+  REQUIRE_PTR(row_of);
+  REQUIRE_PTR(split_sizes);
+  REQUIRE_PTR(send_x);
+  REQUIRE_PTR(send_prob);
+  REQUIRE_PTR(send_eid);
+  REQUIRE_PTR(pos_of);
+  REQUIRE_PTR(rank_counts);
+  s = check_ws(d, workspace, workspace_bytes, false);
+  if (s != MOE_OK) return s;
+  const WsLayout w = ws_layout(d, false);
+  CUDA_TRY(launch_ep_pack(x, idx, prob, row_of, split_sizes, d->T, d->H, d->E, d->k, world, send_x, send_prob,
+                          send_eid, pos_of, rank_counts, at<int>(workspace, w.err), static_cast<cudaStream_t>(stream)),
+           "expert-parallel pack");
+  return MOE_OK;
+}
+
+moe_status moe_gather_f32(const float* src, int64_t n_src, const int32_t* map, int64_t n, float* out,
+                          void* workspace, moe_stream_t stream) {
+  g_msg[0] = 0;
+  if (n < 0 || n_src < 0) return fail(MOE_ERR_INVALID_ARG, "negative size");
+  if (n == 0) return MOE_OK;
+  if (src == nullptr || map == nullptr || out == nullptr || workspace == nullptr)
+    return fail(MOE_ERR_INVALID_ARG, "src, map, out and workspace must be non-NULL");
+  if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(map)) & 3u)
+    return fail(MOE_ERR_ALIGNMENT, "src, map and out must be 4-byte aligned");
+  CUDA_TRY(launch_gather_f32(src, n_src, map, n, out, static_cast<int*>(workspace),
+                             static_cast<cudaStream_t>(stream)),
+           "gather f32");
+  return MOE_OK;
+}
+
 moe_status grouped_mlp_fwd(const moe_dims* d, const uint8_t* xq, const uint8_t* xq_scale, const int32_t* split_sizes,
                            const float* prob_perm, const uint8_t* wgu_q, const uint8_t* wgu_s, const uint8_t* wd_q,
                            const uint8_t* wd_s, void* y, void* saved_gu, uint8_t* aq_col, uint8_t* aq_col_scale,
@@ -598,6 +704,84 @@ moe_status moe_transpose_bf16(const void* src, int32_t batch, int32_t rows, int3
   CUDA_TRY(launch_transpose_bf16(src, nullptr, int64_t(batch) * rows, batch, rows, cols, nullptr, 0, dst, nullptr,
                                  static_cast<cudaStream_t>(stream)),
            "transpose");
+  return MOE_OK;
+}
+
+moe_status moe_transpose_bf16_experts(const void* const* src, int32_t E, int32_t rows, int32_t cols, void* dst,
+                                      moe_stream_t stream) {
+  g_msg[0] = 0;
+  REQUIRE_PTR(dst);
+  if (rows < 128 || cols < 128 || rows % 128 || cols % 128)
+    return fail(MOE_ERR_UNSUPPORTED, "rows=%d cols=%d: need multiples of 128", rows, cols);
+  if (int64_t(E) * rows > (int64_t(1) << 31) || int64_t(E) * cols > (int64_t(1) << 31))
+    return fail(MOE_ERR_UNSUPPORTED, "tensor too large");
+  ExpertSrc tbl;
+  moe_status s = expert_table(src, E, &tbl);
+  if (s != MOE_OK) return s;
+  CUDA_TRY(launch_transpose_bf16_experts(tbl, E, rows, cols, dst, static_cast<cudaStream_t>(stream)),
+           "transpose (per-expert pointers)");
+  return MOE_OK;
+}
+
+moe_status grouped_mlp_fwd_bf16_experts(const moe_dims* d, const void* x_perm, const int32_t* split_sizes,
+                                        const float* prob_perm, const void* const* w_gu, const void* const* w_d,
+                                        void* a_perm, void* y, void* saved_gu, void* workspace,
+                                        size_t workspace_bytes, moe_stream_t stream) {
+  g_msg[0] = 0;
+  moe_status s = check_dims(d);
+  if (s != MOE_OK) return s;
+  REQUIRE_PTR(x_perm);
+  REQUIRE_PTR(split_sizes);
+  REQUIRE_PTR(prob_perm);
+  REQUIRE_PTR(a_perm);
+  REQUIRE_PTR(y);
+  if (saved_gu != nullptr) REQUIRE_PTR(saved_gu);
+  if (d->E > 128) return fail(MOE_ERR_UNSUPPORTED, "E=%d: per-expert weight tensors take E <= 128", d->E);
+  ExpertSrc tgu, td;                               // checks the pointer arrays (NULL, alignment)
+  s = expert_table(w_gu, d->E, &tgu);
+  if (s != MOE_OK) return s;
+  s = expert_table(w_d, d->E, &td);
+  if (s != MOE_OK) return s;
+  s = check_ws(d, workspace, workspace_bytes, false);
+  if (s != MOE_OK) return s;
+  const WsLayout w = ws_layout(d, false);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t cap = capacity(d);
+  const int H = d->H, I = d->I, E = d->E;
+  GemmArgs g1{};
+  g1.mode = 0;
+  g1.E = E;
+  g1.split_sizes = split_sizes;
+  g1.K = H;
+  g1.N = I;
+  g1.n_tiles = I / 128;
+  g1.b_rows_per_expert = 0;                        // B rows inside each expert's own tensor
+  g1.cap = cap;
+  g1.prob_perm = prob_perm;
+  g1.out = static_cast<__nv_bfloat16*>(a_perm);
+  g1.ldo = I;
+  g1.gu = static_cast<__nv_bfloat16*>(saved_gu);
+  g1.I = I;
+  g1.err = at<int>(workspace, w.err);
+  CUDA_TRY(launch_grouped_gemm(EPI_B16_FWD_SWIGLU, g1, x_perm, cap, H, w_gu[0], 2 * int64_t(I), H,
+                               (cap / 128) * g1.n_tiles, st, g_msg, sizeof(g_msg), w_gu),
+           "bf16 grouped gate_up GEMM (per-expert weights)");
+  GemmArgs g2{};
+  g2.mode = 0;
+  g2.E = E;
+  g2.split_sizes = split_sizes;
+  g2.K = I;
+  g2.N = H;
+  g2.n_tiles = (H + 255) / 256;
+  g2.b_rows_per_expert = 0;
+  g2.cap = cap;
+  g2.out = static_cast<__nv_bfloat16*>(y);
+  g2.ldo = H;
+  g2.I = I;
+  g2.err = g1.err;
+  CUDA_TRY(launch_grouped_gemm(EPI_B16_OUT, g2, a_perm, cap, I, w_d[0], H, I, (cap / 128) * g2.n_tiles, st, g_msg,
+                               sizeof(g_msg), w_d),
+           "bf16 grouped down GEMM (per-expert weights)");
   return MOE_OK;
 }
 

@@ -49,6 +49,16 @@ cudaError_t launch_router_bwd(const void* x, const void* w, const float* logits,
 cudaError_t launch_route_permute(const float* logits, int T, int E, int k, int renorm, int* idx, float* prob,
                                  uint32_t* masks, int* bases, int* split_sizes, int* row_of, int* src_of,
                                  float* prob_perm, int* err, cudaStream_t st);
+// The permutation of moe_route_permute for given expert ids idx [T][k] and probabilities.
+cudaError_t launch_permute_from_idx(const int* idx, const float* prob, int T, int E, int k, uint32_t* masks,
+                                    int* bases, int* split_sizes, int* row_of, int* src_of, float* prob_perm,
+                                    int* err, cudaStream_t st);
+// Expert parallelism: pack the (token, slot) rows of x by destination rank (see expert_parallel.cu).
+cudaError_t launch_ep_pack(const void* x, const int* idx, const float* prob, const int* row_of,
+                           const int* split_sizes, int T, int H, int E, int k, int G, void* send_x, float* send_prob,
+                           int* send_eid, int* pos_of, int* rank_counts, int* err, cudaStream_t st);
+cudaError_t launch_gather_f32(const float* src, int64_t n_src, const int* map, int64_t n, float* out, int* err,
+                              cudaStream_t st);
 cudaError_t launch_gather_rows(const void* x, const int* row_of, const int* split_sizes, int T, int k, int H, int E,
                                int64_t cap, void* x_perm, int* err, cudaStream_t st);
 cudaError_t launch_combine(const void* y, const int* row_of, const float* prob, int T, int k, int H, int64_t cap,
@@ -73,6 +83,9 @@ cudaError_t launch_t8_quant_segments(const void* src, const int* split_sizes, in
 // segments are skipped.
 cudaError_t launch_transpose_bf16(const void* src, const int* src_map, int64_t n_src_rows, int batch, int rows,
                                   int cols, const int* split_sizes, int E, void* out, int* err, cudaStream_t st);
+// the same for one bf16 [rows][cols] matrix per expert (src.p[b]), out stacked [batch][cols][rows]
+cudaError_t launch_transpose_bf16_experts(const ExpertSrc& src, int batch, int rows, int cols, void* out,
+                                          cudaStream_t st);
 // out[b*cols + c][r] = src[b][r][c] for uint8 [batch][rows][cols] (multiples of 128);
 // with split_sizes, row tiles past the padded segments are skipped.
 cudaError_t launch_transpose_u8(const uint8_t* src, int batch, int rows, int cols, const int* split_sizes, int E,
@@ -158,8 +171,10 @@ cudaError_t launch_epilogue_quant_selftest(const float* src, int rows, int cols,
 // on resident zero operands; *pairs = the pairs launched.  err: device error word.
 cudaError_t launch_mma_rate_selftest(int k_steps, int* err, int* pairs, cudaStream_t st);
 
+// b_experts (host array of E pointers, E <= 128; the bf16 forward kinds only): B is one
+// [b_rows][b_K] matrix per expert instead of the stacked tensor B (then a.b_rows_per_expert = 0).
 cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64_t a_rows, int64_t a_K,
                                 const void* B, int64_t b_rows, int64_t b_K, int64_t max_tiles, cudaStream_t st,
-                                char* msg, size_t msg_len);
+                                char* msg, size_t msg_len, const void* const* b_experts = nullptr);
 
 }  // namespace moe

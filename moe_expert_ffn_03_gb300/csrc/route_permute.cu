@@ -194,6 +194,48 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
   }
 }
 
+// Ballot masks of given expert ids (the routing-free permutation): warp w of a CTA takes
+// the 32-token group g; bit l of mask[e][g] = token g*32+l has a slot with expert e.
+// An id outside 0..E-1 is recorded and its slot skipped (the scatter marks it -1).
+__global__ void __launch_bounds__(RT_THREADS) idx_masks_kernel(const int* __restrict__ idx, int T, int E, int k,
+                                                               uint32_t* __restrict__ masks, int G, int* err) {
+  __shared__ uint32_t smask[RT_THREADS / 32][kMaxE];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int t = blockIdx.x * RT_THREADS + threadIdx.x;
+  const int g = t >> 5;
+  if (g >= G) return;                                  // warp-uniform
+  for (int e = lane; e < E; e += 32) smask[w][e] = 0u;
+  __syncwarp();
+  if (t < T) {
+    for (int s = 0; s < k; ++s) {
+      const int e = idx[(int64_t)t * k + s];
+      if (e < 0 || e >= E) {
+        report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_ROUTE + 1);
+        continue;
+      }
+      atomicOr(&smask[w][e], 1u << lane);
+    }
+  }
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) masks[(int64_t)e * G + g] = smask[w][e];
+}
+
+cudaError_t launch_permute_from_idx(const int* idx, const float* prob, int T, int E, int k, uint32_t* masks,
+                                    int* bases, int* split_sizes, int* row_of, int* src_of, float* prob_perm,
+                                    int* err, cudaStream_t st) {
+  const int G = (T + 31) / 32;
+  idx_masks_kernel<<<(G * 32 + RT_THREADS - 1) / RT_THREADS, RT_THREADS, 0, st>>>(idx, T, E, k, masks, G, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  permute_scan_kernel<<<E, 1024, 0, st>>>(masks, G, bases, split_sizes);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int token_blocks = (T + 255) / 256;
+  permute_scatter_kernel<<<token_blocks + E, 256, 0, st>>>(idx, prob, T, k, E, G, masks, bases, split_sizes,
+                                                           row_of, src_of, prob_perm, token_blocks, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_route_permute(const float* logits, int T, int E, int k, int renorm, int* idx, float* prob,
                                  uint32_t* masks, int* bases, int* split_sizes, int* row_of, int* src_of,
                                  float* prob_perm, int* err, cudaStream_t st) {
