@@ -587,7 +587,8 @@ moe_status moe_workspace_tensor(const moe_dims* d, int32_t training, int32_t whi
  * full 24-bit significands.  Each warp holds one 32x32 block the way an
  * epilogue warp holds its accumulator columns (lane = row).
  *   src      f32 [rows][cols] (rows, cols multiples of 128)
- *   codes, scales      out MX [rows][cols], blocks of 32 along cols
+ *   codes, scales      out MX [rows][cols], blocks of 32 along cols (codes
+ *                      32-byte aligned: each row block is one 256-bit store)
  *   codes_t, scales_t  out MX [cols][rows], blocks of 32 along rows
  *                      (the tensor transposed, as the along-token copies)
  */

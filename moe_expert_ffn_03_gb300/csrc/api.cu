@@ -1340,6 +1340,7 @@ moe_status moe_selftest_epilogue_quant(const float* src, int32_t rows, int32_t c
   REQUIRE_PTR(scales);
   REQUIRE_PTR(codes_t);
   REQUIRE_PTR(scales_t);
+  if (reinterpret_cast<uintptr_t>(codes) & 31u) return fail(MOE_ERR_ALIGNMENT, "codes must be 32-byte aligned");
   if (rows < 128 || cols < 128 || rows % 128 || cols % 128 || int64_t(rows) * cols > (int64_t(1) << 31))
     return fail(MOE_ERR_UNSUPPORTED, "rows=%d cols=%d: need multiples of 128, rows*cols <= 2^31", rows, cols);
   CUDA_TRY(launch_epilogue_quant_selftest(src, rows, cols, codes, scales, codes_t, scales_t,

@@ -497,12 +497,29 @@ __device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile
 }
 
 // ---- epilogues ---------------------------------------------------------------------
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, const float* v) {
-  uint4* p4 = reinterpret_cast<uint4*>(p);
+// One 32-byte store per lane (256-bit, 32-byte aligned p): a row's 32 codes, or 16 bf16.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* q) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(q[0]), "r"(q[1]), "r"(q[2]),
+               "r"(q[3]), "r"(q[4]), "r"(q[5]), "r"(q[6]), "r"(q[7]) : "memory");
+}
+
+// 32 floats of one row as bf16 (64 bytes at p): two 256-bit stores when the output's base
+// pointers are 32-byte aligned (v8, set by the host; the offsets are multiples of 64
+// bytes), else four 16-byte stores.
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, const float* v, bool v8) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    p4[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                       pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+  for (int h = 0; h < 2; ++h) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[16 * h + 2 * i], v[16 * h + 2 * i + 1]);
+    if (v8) {
+      st_global_v8(p + 16 * h, w);
+    } else {
+      uint4* p4 = reinterpret_cast<uint4*>(p + 16 * h);
+      p4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      p4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+  }
 }
 
 // ---- MX quantization pieces of the epilogues --------------------------------------
@@ -529,11 +546,6 @@ __device__ __forceinline__ uint2 mx_encode8(const float* v, uint32_t c) {
                     cvt_e4m3x2(e.x, e.y) | (cvt_e4m3x2(f.x, f.y) << 16));
 }
 
-// One 32-byte store per lane (256-bit): a 32-column block of one row's codes.
-__device__ __forceinline__ void st_global_v8(uint8_t* p, const uint32_t* q) {
-  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(q[0]), "r"(q[1]), "r"(q[2]),
-               "r"(q[3]), "r"(q[4]), "r"(q[5]), "r"(q[6]), "r"(q[7]) : "memory");
-}
 // Keeps a pointer opaque to the compiler, so that an unrolled loop advances it step by step
 // instead of holding every step's precomputed address in registers.
 __device__ __forceinline__ void opaque(uint8_t*& p) { asm volatile("" : "+l"(p)); }
@@ -599,9 +611,14 @@ __device__ __forceinline__ void quant_row_block(const float* v, uint8_t* codes, 
 #pragma unroll
   for (int i = 0; i < 32; i += 2) amax = amax_raise(amax, v[i], v[i + 1]);
   const uint32_t c = mx_scale_code(__float_as_uint(amax));
-  uint8_t* p = codes + row * K + col;
+  uint32_t q[8];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) store_row8(v + 8 * j, c, p + 8 * j);
+  for (int j = 0; j < 4; ++j) {
+    const uint2 e = mx_encode8(v + 8 * j, c);
+    q[2 * j] = e.x;
+    q[2 * j + 1] = e.y;
+  }
+  st_global_v8(codes + row * K + col, q);
   scales[sf_offset(row, col >> 5, K)] = uint8_t(c);
 }
 
@@ -631,6 +648,14 @@ __device__ __forceinline__ float rcp_approx(float x) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
+}
+// ScaledSwiGLU of two columns: a = silu(g) * u * p with silu(g) = g / (1 + e^-g), the
+// quotient as g times the approximate reciprocal (the result feeds an E4M3 quantizer).
+__device__ __forceinline__ float2 scaled_swiglu2(float2 g, float2 u, float2 p2) {
+  const float2 t = __fmul2_rn(g, make_float2(-1.4426950408889634f, -1.4426950408889634f));   // -g log2(e)
+  const float2 den = __fadd2_rn(make_float2(1.f, 1.f), make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+  const float2 sg = __fmul2_rn(g, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+  return __fmul2_rn(__fmul2_rn(sg, u), p2);
 }
 __device__ __forceinline__ void swiglu_bwd2(float2 d, float2 g, float2 u, float2 p2, float2& dg, float2& du,
                                             float2& sgu) {
@@ -817,7 +842,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
       float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = have ? __uint_as_float(r[32 * h + i]) * alpha : 0.f;
-      store_bf16x32(orow + 32 * h, v);
+      store_bf16x32(orow + 32 * h, v, a.out_v8);
     }
   } else if (EPI == EPI_T8_FWD_SWIGLU) {
     // per-tensor path: a = silu(g)*u*p stored as bf16 [cap][I] in out; the expert's amax of
@@ -831,8 +856,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     for (int i = 0; i < 64; ++i) f[i] *= alpha;            // g | u
     if (a.gu != nullptr) {                                   // saved for the per-tensor backward
       const int64_t twoI = 2 * int64_t(a.I);
-      store_bf16x32(a.gu + row * twoI + col, f);
-      store_bf16x32(a.gu + row * twoI + a.I + col, f + 32);
+      store_bf16x32(a.gu + row * twoI + col, f, a.out_v8);
+      store_bf16x32(a.gu + row * twoI + a.I + col, f + 32, a.out_v8);
     }
     uint32_t amax = 0;
 #pragma unroll
@@ -840,7 +865,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
       f[i] = silu_f(f[i]) * f[32 + i] * p;
       amax = max(amax, abs_bits(f[i]));
     }
-    store_bf16x32(a.out + row * a.ldo + col, f);
+    store_bf16x32(a.out + row * a.ldo + col, f, a.out_v8);
     amax = __float_as_uint(__bfloat162float(__float2bfloat16_rn(__uint_as_float(amax))));
     amax = __reduce_max_sync(0xFFFFFFFFu, amax);
     if (lane == 0 && amax != 0u) atomicMax(a.amax_out + tl.e, amax);
@@ -851,23 +876,28 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     float* f = reinterpret_cast<float*>(r);
     if (a.gu != nullptr) {
       const int64_t twoI = 2 * int64_t(a.I);
-      store_bf16x32(a.gu + row * twoI + col, f);
-      store_bf16x32(a.gu + row * twoI + a.I + col, f + 32);
+      store_bf16x32(a.gu + row * twoI + col, f, a.out_v8);
+      store_bf16x32(a.gu + row * twoI + a.I + col, f + 32, a.out_v8);
     }
 #pragma unroll
     for (int i = 0; i < 32; ++i) f[i] = silu_f(f[i]) * f[32 + i] * p;
-    store_bf16x32(a.out + row * a.ldo + col, f);
+    store_bf16x32(a.out + row * a.ldo + col, f, a.out_v8);
   } else if (EPI == EPI_FWD_SWIGLU) {
     const float p = a.prob_perm[row];
     const int64_t twoI = 2 * int64_t(a.I);
     const int64_t col = tl.n0 + cg * 32;                  // column inside I
     float* f = reinterpret_cast<float*>(r);
     if (a.gu != nullptr) {
-      store_bf16x32(a.gu + row * twoI + col, f);
-      store_bf16x32(a.gu + row * twoI + a.I + col, f + 32);
+      store_bf16x32(a.gu + row * twoI + col, f, a.out_v8);
+      store_bf16x32(a.gu + row * twoI + a.I + col, f + 32, a.out_v8);
     }
+    const float2 p2 = make_float2(p, p);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) f[i] = silu_f(f[i]) * f[32 + i] * p;
+    for (int i = 0; i < 32; i += 2) {
+      const float2 av = scaled_swiglu2(make_float2(f[i], f[i + 1]), make_float2(f[32 + i], f[33 + i]), p2);
+      f[i] = av.x;
+      f[i + 1] = av.y;
+    }
     quant_row_block(f, a.q_row, a.q_row_s, row, col, a.q_row_K);
     if (a.q_col != nullptr) quant_col_block(f, a.q_col, a.q_col_s, row_blk0, col, a.cap, lane, tr);
   } else if (EPI == EPI_BWD_SWIGLU) {
@@ -975,14 +1005,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
         const float* du = reinterpret_cast<const float*>(r);
         if (h == 0) stage_gu(a, row, col + 32, gu_s, lane & 7);   // the second half, while this one is stored
         if (EPI == EPI_B16_BWD_SWIGLU) {
-          store_bf16x32(a.out + row * twoI + col, o);
+          store_bf16x32(a.out + row * twoI + col, o, a.out_v8);
           store_col_bf16(o, a.out_t, row_blk0, col, a.cap, lane, tr);
-          store_bf16x32(a.out + row * twoI + a.I + col, du);
+          store_bf16x32(a.out + row * twoI + a.I + col, du, a.out_v8);
           store_col_bf16(du, a.out_t, row_blk0, a.I + col, a.cap, lane, tr);
         } else {
           // per-tensor operands: bf16 dH rows; its codes (both orientations) come after the amax
-          store_bf16x32(a.out + row * twoI + col, o);
-          store_bf16x32(a.out + row * twoI + a.I + col, du);
+          store_bf16x32(a.out + row * twoI + col, o, a.out_v8);
+          store_bf16x32(a.out + row * twoI + a.I + col, du, a.out_v8);
 #pragma unroll
           for (int i = 0; i < 32; ++i) amax = max(amax, max(abs_bits(o[i]), abs_bits(du[i])));
         }
@@ -1474,10 +1504,13 @@ cudaError_t launch_mma_rate_selftest(int k_steps, int* err, int* pairs, cudaStre
   return cudaGetLastError();
 }
 
-cudaError_t launch_grouped_gemm(int epi, const GemmArgs& a, const void* A, int64_t a_rows, int64_t a_K,
+cudaError_t launch_grouped_gemm(int epi, const GemmArgs& args, const void* A, int64_t a_rows, int64_t a_K,
                                 const void* B, int64_t b_rows, int64_t b_K, int64_t max_tiles, cudaStream_t st,
                                 char* msg, size_t msg_len, const void* const* b_experts) {
   if (max_tiles <= 0) return cudaSuccess;
+  GemmArgs a = args;
+  const auto al32 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; };
+  a.out_v8 = al32(a.out) && al32(a.out_t) && al32(a.gu);
   // one B map per expert: b_experts[e] is expert e's [b_rows][b_K] matrix
   static thread_local BMaps<kMaxMapExperts> pe_maps;
   if (b_experts != nullptr) {

@@ -155,6 +155,7 @@ struct GemmArgs {
   float* out_f32;            // EPI_B16_F32_OUT output, row stride ldo
   int64_t rows_limit;        // mode 0 with split_sizes == nullptr: one segment of this many rows (E = 1)
   int* err;
+  bool out_v8;               // set by launch_grouped_gemm: out, out_t and gu are 32-byte aligned (256-bit stores)
   uint64_t wait_limit_ns;    // bound of every mbarrier wait (0: the default kWaitLimitNs)
   int selftest_no_loads;     // self-test only: the producer issues nothing, so the waits run out
 };

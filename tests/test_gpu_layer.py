@@ -284,3 +284,23 @@ def test_nan_logits_route_like_the_oracle(k):
     assert np.array_equal(L.split_sizes.cpu().numpy(), perm["split_sizes"])
     assert np.array_equal(L.row_of.cpu().numpy(), perm["row_of"])
     assert np.array_equal(L.src_of[:perm["rows"]].cpu().numpy(), perm["src_of"])
+
+
+def test_outputs_at_16_byte_offsets_give_the_same_results():
+    """The GEMM epilogues store 32 bytes per lane when the output pointers are 32-byte aligned
+    and 16 bytes otherwise; y and saved g,u at a 16-byte (not 32-byte) offset give the same
+    values as 256-byte aligned ones."""
+    from moe_expert_ffn_03_gb300 import binding as B
+    wl = configs.small(300, 256, 384, 6, 2, routing="biased", backward=True)
+    inp = {k: v.cuda() for k, v in synth.make_inputs(wl, 0).items()}
+    L = run_gpu(wl, inp, True)
+    cap = L.cap
+    y_off = torch.empty(cap * wl.H + 8, dtype=torch.bfloat16, device="cuda")[8:].view(cap, wl.H)
+    gu_off = torch.empty(cap * 2 * wl.I + 8, dtype=torch.bfloat16, device="cuda")[8:].view(cap, 2 * wl.I)
+    assert y_off.data_ptr() % 32 == 16 and gu_off.data_ptr() % 32 == 16
+    B.grouped_mlp_fwd(L.d, L.xq, L.xq_s, L.split_sizes, L.prob_perm, L.wgu_q, L.wgu_s, L.wd_q, L.wd_s, y_off, gu_off,
+                      L.aq_col, L.aq_col_s, L.ws)
+    torch.cuda.synchronize()
+    rows = L.padded_rows()
+    assert torch.equal(y_off[:rows], L.y[:rows])
+    assert torch.equal(gu_off[:rows], L.saved_gu[:rows])
