@@ -7,6 +7,9 @@
 
 namespace moe {
 
+// V8: y and out 32-byte aligned, 16 bf16 per lane and step with 256-bit loads and stores;
+// otherwise 8 with 16-byte ones.
+template <bool V8>
 __global__ void __launch_bounds__(256) combine_kernel(
     const __nv_bfloat16* __restrict__ y, const int* __restrict__ row_of, const float* __restrict__ prob,
     int T, int k, int H, int64_t cap, __nv_bfloat16* __restrict__ out, int* err) {
@@ -28,27 +31,36 @@ __global__ void __launch_bounds__(256) combine_kernel(
       }
     }
   }
-  const int nvec = H >> 3;                            // 8 bf16 per 16-byte vector
+  constexpr int W = V8 ? 8 : 4;                      // 32-bit words (two bf16 each) per lane and step
+  const int nvec = H / (2 * W);
   for (int c = lane; c < nvec; c += 32) {
-    float acc[8];
+    float acc[2 * W];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int i = 0; i < 2 * W; ++i) acc[i] = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (j < k) {
-        const uint4 w = reinterpret_cast<const uint4*>(y + int64_t(rows[j]) * H)[c];
-        acc[0] += p[j] * bf16_lo(w.x); acc[1] += p[j] * bf16_hi(w.x);
-        acc[2] += p[j] * bf16_lo(w.y); acc[3] += p[j] * bf16_hi(w.y);
-        acc[4] += p[j] * bf16_lo(w.z); acc[5] += p[j] * bf16_hi(w.z);
-        acc[6] += p[j] * bf16_lo(w.w); acc[7] += p[j] * bf16_hi(w.w);
+        uint32_t w[W];
+        const __nv_bfloat16* src = y + int64_t(rows[j]) * H + int64_t(c) * 2 * W;
+        if (V8) {
+          ld_global_v8(src, w);
+        } else {
+          const uint4 v = *reinterpret_cast<const uint4*>(src);
+          w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+        }
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+          acc[2 * i] += p[j] * bf16_lo(w[i]);
+          acc[2 * i + 1] += p[j] * bf16_hi(w[i]);
+        }
       }
     }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    reinterpret_cast<uint4*>(out + t * H)[c] = o;
+    uint32_t o[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) o[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+    __nv_bfloat16* dst = out + t * H + int64_t(c) * 2 * W;
+    if (V8) st_global_v8(dst, o);
+    else *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -120,8 +132,13 @@ cudaError_t launch_gather_rows(const void* x, const int* row_of, const int* spli
 cudaError_t launch_combine(const void* y, const int* row_of, const float* prob, int T, int k, int H, int64_t cap,
                            void* out, int* err, cudaStream_t st) {
   const int64_t threads = int64_t(T) * 32;
-  combine_kernel<<<unsigned((threads + 255) / 256), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(y), row_of, prob, T, k, H, cap, static_cast<__nv_bfloat16*>(out), err);
+  const unsigned grid = unsigned((threads + 255) / 256);
+  const __nv_bfloat16* yb = static_cast<const __nv_bfloat16*>(y);
+  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out);
+  if (aligned32(y) && aligned32(out) && H % 16 == 0)
+    combine_kernel<true><<<grid, 256, 0, st>>>(yb, row_of, prob, T, k, H, cap, ob, err);
+  else
+    combine_kernel<false><<<grid, 256, 0, st>>>(yb, row_of, prob, T, k, H, cap, ob, err);
   return cudaGetLastError();
 }
 

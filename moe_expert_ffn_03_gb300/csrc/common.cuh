@@ -155,7 +155,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ void store_codes32(uint8_t* p, const uint32_t (&q)[8]) {
+// 32 bytes at p from 8 words in one 256-bit store (p 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* q) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(q[0]), "r"(q[1]), "r"(q[2]),
+               "r"(q[3]), "r"(q[4]), "r"(q[5]), "r"(q[6]), "r"(q[7]) : "memory");
+}
+// 32 bytes at p into 8 words in one 256-bit load (p 32-byte aligned).
+__device__ __forceinline__ void ld_global_v8(const void* p, uint32_t* q) {
+  asm volatile("ld.global.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7])
+               : "l"(p));
+}
+__host__ __device__ __forceinline__ bool aligned32(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 31u) == 0;
+}
+
+// 32 codes at p (32-byte offset inside its tensor): one 256-bit store when the tensor's base
+// is 32-byte aligned (v8), else two 16-byte stores.
+__device__ __forceinline__ void store_codes32(uint8_t* p, const uint32_t (&q)[8], bool v8) {
+  if (v8) {
+    st_global_v8(p, q);
+    return;
+  }
   uint4* p4 = reinterpret_cast<uint4*>(p);
   p4[0] = make_uint4(q[0], q[1], q[2], q[3]);
   p4[1] = make_uint4(q[4], q[5], q[6], q[7]);

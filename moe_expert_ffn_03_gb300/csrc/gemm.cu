@@ -497,12 +497,6 @@ __device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile
 }
 
 // ---- epilogues ---------------------------------------------------------------------
-// One 32-byte store per lane (256-bit, 32-byte aligned p): a row's 32 codes, or 16 bf16.
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* q) {
-  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(q[0]), "r"(q[1]), "r"(q[2]),
-               "r"(q[3]), "r"(q[4]), "r"(q[5]), "r"(q[6]), "r"(q[7]) : "memory");
-}
-
 // 32 floats of one row as bf16 (64 bytes at p): two 256-bit stores when the output's base
 // pointers are 32-byte aligned (v8, set by the host; the offsets are multiples of 64
 // bytes), else four 16-byte stores.

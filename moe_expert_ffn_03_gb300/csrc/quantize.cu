@@ -14,11 +14,12 @@ namespace moe {
 // SCATTER: source row s (a token) is written to the k rows row_of[s*k + j]
 // (the permuted rows); otherwise to row s itself.
 // ---------------------------------------------------------------------------------
+// v8_src / v8_dst: src / codes are 32-byte aligned (256-bit loads / stores).
 template <bool SCATTER>
 __global__ void __launch_bounds__(256) quant_rowwise_kernel(
     const __nv_bfloat16* __restrict__ src, int64_t n_rows, int cols,
     const int* __restrict__ row_of, int k, int64_t cap,
-    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int* err) {
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int* err, bool v8_src, bool v8_dst) {
   const int lane = threadIdx.x & 31;
   const int64_t s = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (s >= n_rows) return;
@@ -45,14 +46,20 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(
   }
   for (int b = lane; b < nblk; b += 32) {
     uint32_t w[16];
-    const uint4* p4 = reinterpret_cast<const uint4*>(src + s * cols + (int64_t)b * 32);
+    const __nv_bfloat16* blk = src + s * cols + (int64_t)b * 32;
+    if (v8_src) {
+      ld_global_v8(blk, w);
+      ld_global_v8(blk + 16, w + 8);
+    } else {
+      const uint4* p4 = reinterpret_cast<const uint4*>(blk);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 x = p4[i];
-      w[4 * i + 0] = x.x;
-      w[4 * i + 1] = x.y;
-      w[4 * i + 2] = x.z;
-      w[4 * i + 3] = x.w;
+      for (int i = 0; i < 4; ++i) {
+        const uint4 x = p4[i];
+        w[4 * i + 0] = x.x;
+        w[4 * i + 1] = x.y;
+        w[4 * i + 2] = x.z;
+        w[4 * i + 3] = x.w;
+      }
     }
     uint32_t q[8];
     const uint32_t c = mx_quant32_bf16(w, q);
@@ -60,7 +67,7 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(
     for (int j = 0; j < 8; ++j) {
       if (j < nd) {
         const int64_t row = SCATTER ? int64_t(dst[j]) : s;
-        store_codes32(codes + row * cols + (int64_t)b * 32, q);
+        store_codes32(codes + row * cols + (int64_t)b * 32, q, v8_dst);
         scales[sf_offset(row, b, cols)] = uint8_t(c);
       }
     }
@@ -115,7 +122,7 @@ constexpr int QC_PITCH = QC_TILE + 8;                // bf16 per smem row (16 B 
 __global__ void __launch_bounds__(256, 6) quant_colwise_kernel(
     const __nv_bfloat16* __restrict__ src, const int* __restrict__ src_map, int64_t n_src_rows,
     int rows, int cols, const int* __restrict__ split_sizes, int E,
-    uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t, int* err) {
+    uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t, int* err, bool v8) {
   __shared__ __align__(16) __nv_bfloat16 tile[QC_TILE * QC_PITCH];
   __shared__ __align__(16) uint8_t sc_atom[512];
   __shared__ int s_rows_used;
@@ -168,8 +175,8 @@ __global__ void __launch_bounds__(256, 6) quant_colwise_kernel(
     uint32_t q_lo[8], q_hi[8];
     const uint32_t sc = mx_quant32_bf16_colpair(p, QC_PITCH / 2, q_lo, q_hi);
     const int64_t drow = batch * cols + col0 + c;    // row of the transposed tensor
-    store_codes32(codes_t + drow * rows + row0 + rb * 32, q_lo);
-    store_codes32(codes_t + (drow + 1) * rows + row0 + rb * 32, q_hi);
+    store_codes32(codes_t + drow * rows + row0 + rb * 32, q_lo, v8);
+    store_codes32(codes_t + (drow + 1) * rows + row0 + rb * 32, q_hi, v8);
     sc_atom[((c & 31) << 4) + (((c >> 5) & 3) << 2) + rb] = uint8_t(sc);
     sc_atom[(((c + 1) & 31) << 4) + ((((c + 1) >> 5) & 3) << 2) + rb] = uint8_t(sc >> 8);
   }
@@ -192,7 +199,7 @@ __global__ void __launch_bounds__(256, 6) quant_colwise_kernel(
 template <class Src>
 __global__ void __launch_bounds__(256, 6) quant_dual_kernel(
     const __grid_constant__ Src src, int rows, int cols, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ scales, uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t) {
+    uint8_t* __restrict__ scales, uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t, bool v8) {
   __shared__ __align__(16) __nv_bfloat16 tile[QC_TILE * QC_PITCH];
   __shared__ __align__(16) uint8_t sc_row[512];
   __shared__ __align__(16) uint8_t sc_col[512];
@@ -227,7 +234,7 @@ __global__ void __launch_bounds__(256, 6) quant_dual_kernel(
     uint32_t q[8];
     const uint32_t sc = mx_quant32_bf16(w, q);
     const int64_t drow = srow0 + r;
-    store_codes32(codes + drow * cols + col0 + b * 32, q);
+    store_codes32(codes + drow * cols + col0 + b * 32, q, v8);
     sc_row[((r & 31) << 4) + (((r >> 5) & 3) << 2) + b] = uint8_t(sc);
   }
   // colwise: task = (columns c, c+1) x 32-row block rb -- one per thread
@@ -237,8 +244,8 @@ __global__ void __launch_bounds__(256, 6) quant_dual_kernel(
     uint32_t q_lo[8], q_hi[8];
     const uint32_t sc = mx_quant32_bf16_colpair(p, QC_PITCH / 2, q_lo, q_hi);
     const int64_t drow = batch * cols + col0 + c;
-    store_codes32(codes_t + drow * rows + row0 + rb * 32, q_lo);
-    store_codes32(codes_t + (drow + 1) * rows + row0 + rb * 32, q_hi);
+    store_codes32(codes_t + drow * rows + row0 + rb * 32, q_lo, v8);
+    store_codes32(codes_t + (drow + 1) * rows + row0 + rb * 32, q_hi, v8);
     sc_col[((c & 31) << 4) + (((c >> 5) & 3) << 2) + rb] = uint8_t(sc);
     sc_col[(((c + 1) & 31) << 4) + ((((c + 1) >> 5) & 3) << 2) + rb] = uint8_t(sc >> 8);
   }
@@ -262,12 +269,13 @@ cudaError_t launch_quant_rowwise(const void* src, int64_t n_rows, int cols, cons
   if (n_rows == 0) return cudaSuccess;
   const int64_t threads = n_rows * 32;
   const unsigned grid = unsigned((threads + 255) / 256);
+  const bool v8s = aligned32(src), v8d = aligned32(codes);
   if (row_of != nullptr)
     quant_rowwise_kernel<true><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), n_rows, cols,
-                                                     row_of, k, cap, codes, scales, err);
+                                                     row_of, k, cap, codes, scales, err, v8s, v8d);
   else
     quant_rowwise_kernel<false><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), n_rows, cols,
-                                                      nullptr, 1, cap, codes, scales, err);
+                                                      nullptr, 1, cap, codes, scales, err, v8s, v8d);
   return cudaGetLastError();
 }
 
@@ -282,7 +290,7 @@ cudaError_t launch_quant_colwise(const void* src, const int* src_map, int64_t n_
                                  int* err, cudaStream_t st) {
   dim3 grid(rows / QC_TILE, cols / QC_TILE, batch);
   quant_colwise_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), src_map, n_src_rows, rows,
-                                             cols, split_sizes, E, codes_t, scales_t, err);
+                                             cols, split_sizes, E, codes_t, scales_t, err, aligned32(codes_t));
   return cudaGetLastError();
 }
 
@@ -290,14 +298,16 @@ cudaError_t launch_quant_dual(const void* src, int batch, int rows, int cols, ui
                               uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st) {
   dim3 grid(rows / QC_TILE, cols / QC_TILE, batch);
   const StackedSrc s{static_cast<const __nv_bfloat16*>(src), int64_t(rows) * cols};
-  quant_dual_kernel<StackedSrc><<<grid, 256, 0, st>>>(s, rows, cols, codes, scales, codes_t, scales_t);
+  quant_dual_kernel<StackedSrc><<<grid, 256, 0, st>>>(s, rows, cols, codes, scales, codes_t, scales_t,
+                                                      aligned32(codes) && aligned32(codes_t));
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_dual_experts(const ExpertSrc& src, int batch, int rows, int cols, uint8_t* codes,
                                       uint8_t* scales, uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st) {
   dim3 grid(rows / QC_TILE, cols / QC_TILE, batch);
-  quant_dual_kernel<ExpertSrc><<<grid, 256, 0, st>>>(src, rows, cols, codes, scales, codes_t, scales_t);
+  quant_dual_kernel<ExpertSrc><<<grid, 256, 0, st>>>(src, rows, cols, codes, scales, codes_t, scales_t,
+                                                     aligned32(codes) && aligned32(codes_t));
   return cudaGetLastError();
 }
 
