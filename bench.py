@@ -145,7 +145,7 @@ def run_cuda(args):
     import torch
 
     from moe_expert_ffn_03_gb300 import build, configs, synth
-    from moe_expert_ffn_03_gb300.layer import LAUNCHES_PER_FORWARD_STEP, LAUNCHES_PER_TRAINING_STEP, ExpertFFN
+    from moe_expert_ffn_03_gb300.layer import ExpertFFN, launches_per_step
     from moe_expert_ffn_03_gb300.pipeline import HostPipeline
 
     world, rank, local = dist_setup(args.gpus)
@@ -462,7 +462,7 @@ def run_cuda(args):
                 "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                 "api": "HostPipeline.run (copies overlapped on a copy stream)",
                 "serial_copies_ms_per_step": round(serial_ms, 4)},
-        "gpu_launches": (LAUNCHES_PER_TRAINING_STEP if train else LAUNCHES_PER_FORWARD_STEP) * args.steps,
+        "gpu_launches": launches_per_step(wl.T, wl.E, wl.k, train) * args.steps,
         "clocks": clocks,
     }
     line["graph"] = {"ms_per_step": round(graph_ms, 4),

@@ -108,7 +108,9 @@ size_t moe_rows_capacity(const moe_dims* d);
  * (training = 1), and also by grouped_mlp_bwd_bf16 (training = 2) or by
  * grouped_mlp_bwd_fp8_tensor (training = 3).  The workspace is caller memory,
  * 256-byte aligned, zero-filled once before first use (that clears the device
- * error word); it may be reused by later calls on the same stream.  Returns 0
+ * error word and the block counter of the routing launch, which every routing
+ * call leaves at zero again); it may be reused by later calls on the same
+ * stream, not by calls running at the same time on other streams.  Returns 0
  * for invalid sizes or training outside 0..3.  Host only. */
 size_t moe_workspace_size(const moe_dims* d, int32_t training);
 

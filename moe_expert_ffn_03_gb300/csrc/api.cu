@@ -304,11 +304,14 @@ moe_status moe_route_permute(const moe_dims* d, const float* logits, const void*
   int* err = at<int>(workspace, w.err);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t cap = capacity(d);
-  CUDA_TRY(launch_route_permute(logits, d->T, d->E, d->k, d->renormalize, idx, prob, at<uint32_t>(workspace, w.masks),
-                                at<int>(workspace, w.bases), split_sizes, row_of, src_of, prob_perm, err, st),
-           "route_permute");
-  CUDA_TRY(launch_quant_rowwise(x, d->T, d->H, row_of, d->k, cap, xq, xq_scale, err, st), "gather_quant_rowwise");
-  CUDA_TRY(launch_fill_pad_rows(split_sizes, d->E, d->H, xq, xq_scale, st), "fill_pad_rows");
+  uint32_t* masks = at<uint32_t>(workspace, w.masks);
+  int* bases = at<int>(workspace, w.bases);
+  CUDA_TRY(launch_route_scan(logits, d->T, d->E, d->k, d->renormalize, idx, prob, masks, bases, split_sizes,
+                             route_ticket(err), err, st),
+           "route + scan");
+  const PermuteRows pr{idx, prob, masks, bases, split_sizes, d->E, (d->T + 31) / 32, row_of, src_of, prob_perm};
+  CUDA_TRY(launch_permute_quant_rows(x, d->T, d->H, d->k, cap, pr, xq, xq_scale, err, st),
+           "permutation + gather_quant_rowwise + padding rows");
   if (xq_col != nullptr)
     CUDA_TRY(launch_quant_colwise(x, src_of, d->T, 1, int(cap), d->H, split_sizes, d->E, xq_col, xq_col_scale, err,
                                   st),
@@ -332,9 +335,10 @@ moe_status moe_route(const moe_dims* d, const float* logits, int32_t* idx, float
   s = check_ws(d, workspace, workspace_bytes, false);
   if (s != MOE_OK) return s;
   const WsLayout w = ws_layout(d, false);
+  int* err = at<int>(workspace, w.err);
   CUDA_TRY(launch_route_permute(logits, d->T, d->E, d->k, d->renormalize, idx, prob, at<uint32_t>(workspace, w.masks),
                                 at<int>(workspace, w.bases), split_sizes, row_of, src_of, prob_perm,
-                                at<int>(workspace, w.err), static_cast<cudaStream_t>(stream)),
+                                route_ticket(err), err, static_cast<cudaStream_t>(stream)),
            "route");
   return MOE_OK;
 }
@@ -370,8 +374,8 @@ moe_status moe_permute(const moe_dims* d, const int32_t* idx, const float* prob,
   CUDA_TRY(launch_permute_from_idx(idx, prob, d->T, d->E, d->k, at<uint32_t>(workspace, w.masks),
                                    at<int>(workspace, w.bases), split_sizes, row_of, src_of, prob_perm, err, st),
            "permute");
-  CUDA_TRY(launch_quant_rowwise(x, d->T, d->H, row_of, d->k, cap, xq, xq_scale, err, st), "gather_quant_rowwise");
-  CUDA_TRY(launch_fill_pad_rows(split_sizes, d->E, d->H, xq, xq_scale, st), "fill_pad_rows");
+  CUDA_TRY(launch_quant_rowwise(x, d->T, d->H, row_of, d->k, cap, xq, xq_scale, err, st, split_sizes, d->E),
+           "gather_quant_rowwise + padding rows");
   if (xq_col != nullptr)
     CUDA_TRY(launch_quant_colwise(x, src_of, d->T, 1, int(cap), d->H, split_sizes, d->E, xq_col, xq_col_scale, err,
                                   st),
@@ -617,7 +621,7 @@ moe_status moe_fp8_tensor_quantize_tokens(const moe_dims* d, const void* x, cons
   CUDA_TRY(launch_t8_amax_tokens(x, d->T, d->H, idx, d->k, d->E, am, err, st), "per-expert amax of x");
   CUDA_TRY(launch_t8_quant_tokens(x, d->T, d->H, idx, row_of, d->k, d->E, capacity(d), am, xq, err, st),
            "per-tensor quantize of x rows");
-  CUDA_TRY(launch_fill_pad_rows(split_sizes, d->E, d->H, xq, nullptr, st), "padding rows of xq");
+  CUDA_TRY(launch_fill_pad_rows(split_sizes, d->E, d->H, capacity(d), xq, nullptr, err, st), "padding rows of xq");
   return MOE_OK;
 }
 
@@ -957,7 +961,7 @@ moe_status grouped_mlp_bwd_fp8_tensor(const moe_dims* d, const void* dout, const
   CUDA_TRY(launch_t8_amax_tokens(dout, d->T, H, idx, k, E, am_dy, err, st), "per-expert amax of dY");
   CUDA_TRY(launch_t8_quant_tokens(dout, d->T, H, idx, row_of, k, E, cap, am_dy, dyq, err, st),
            "per-tensor quantize of dY rows");
-  CUDA_TRY(launch_fill_pad_rows(split_sizes, E, H, dyq, nullptr, st), "padding rows of dY");
+  CUDA_TRY(launch_fill_pad_rows(split_sizes, E, H, cap, dyq, nullptr, err, st), "padding rows of dY");
   CUDA_TRY(launch_transpose_u8(dyq, 1, int(cap), H, split_sizes, E, dyqc, st), "dY codes transposed");
   // the weights' codes transposed (a per-tensor scale does not depend on the axis)
   CUDA_TRY(launch_transpose_u8(wd_q, E, H, I, nullptr, 0, wdT, st), "W_d codes transposed");
@@ -1098,8 +1102,8 @@ moe_status grouped_mlp_bwd(const moe_dims* d, const void* dout, const int32_t* s
   float* dp = at<float>(workspace, w.dp);
 
   // dY rows: gathered dout quantized along H (dgrad) and along tokens (wgrad)
-  CUDA_TRY(launch_quant_rowwise(dout, d->T, H, row_of, k, cap, dyq, dyq_s, err, st), "dout gather_quant_rowwise");
-  CUDA_TRY(launch_fill_pad_rows(split_sizes, E, H, dyq, dyq_s, st), "dout fill_pad_rows");
+  CUDA_TRY(launch_quant_rowwise(dout, d->T, H, row_of, k, cap, dyq, dyq_s, err, st, split_sizes, E),
+           "dout gather_quant_rowwise + padding rows");
   CUDA_TRY(launch_quant_colwise(dout, src_of, d->T, 1, int(cap), H, split_sizes, E, dyqc, dyqc_s, err, st),
            "dout gather_quant_colwise");
 

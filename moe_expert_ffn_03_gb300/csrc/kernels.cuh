@@ -28,10 +28,32 @@ struct ExpertSrc {
   __device__ __forceinline__ const __nv_bfloat16* mat(int64_t b) const { return p[b]; }
 };
 
+// pad_split (optional, with pad_E experts): the same launch also zeroes the padding rows of
+// every segment of the permuted output (what launch_fill_pad_rows does).
 cudaError_t launch_quant_rowwise(const void* src, int64_t n_rows, int cols, const int* row_of, int k, int64_t cap,
-                                 uint8_t* codes, uint8_t* scales, int* err, cudaStream_t st);
-cudaError_t launch_fill_pad_rows(const int* split_sizes, int E, int cols, uint8_t* codes, uint8_t* scales,
-                                 cudaStream_t st);
+                                 uint8_t* codes, uint8_t* scales, int* err, cudaStream_t st,
+                                 const int* pad_split = nullptr, int pad_E = 0);
+cudaError_t launch_fill_pad_rows(const int* split_sizes, int E, int cols, int64_t cap, uint8_t* codes,
+                                 uint8_t* scales, int* err, cudaStream_t st);
+// The expert-major permutation, finished while x is quantized: the routing's outputs
+// (idx, prob, the per-expert token masks [E][G] with their group prefix sums and
+// split_sizes) in, row_of / src_of / prob_perm out.
+constexpr int kMaxExperts = 256;
+struct PermuteRows {
+  const int* idx;
+  const float* prob;
+  const uint32_t* masks;
+  const int* bases;
+  const int* split_sizes;
+  int E, G;
+  int* row_of;
+  int* src_of;
+  float* prob_perm;
+};
+// x bf16 [T][H] -> MX codes/scales of the permuted rows [cap][H] (padding rows zero, src
+// -1, prob 0) and the permutation maps, in one launch.
+cudaError_t launch_permute_quant_rows(const void* x, int T, int H, int k, int64_t cap, const PermuteRows& p,
+                                      uint8_t* codes, uint8_t* scales, int* err, cudaStream_t st);
 cudaError_t launch_quant_colwise(const void* src, const int* src_map, int64_t n_src_rows, int batch, int rows,
                                  int cols, const int* split_sizes, int E, uint8_t* codes_t, uint8_t* scales_t,
                                  int* err, cudaStream_t st);
@@ -46,9 +68,20 @@ cudaError_t launch_router_fwd(const void* x, const void* w, int T, int H, int E,
 cudaError_t launch_router_bwd(const void* x, const void* w, const float* logits, const int* idx, const float* prob,
                               const float* dprob, int T, int H, int E, int k, int renorm, float* dl, void* dx,
                               float* dw, float* partial, int* err, cudaStream_t st);
+// Top-k routing plus the per-expert scan of the token masks (masks [E][G], bases [E][G],
+// split_sizes [E]).  One launch while E*ceil(T/32) <= 16384 (the last block to finish
+// scans; `ticket` is a zero-initialised counter the launch returns to zero), else two.
+bool route_scan_fused(int T, int E);
+// The ticket of launch_route_scan: word 8 of a workspace's 256-byte error region (the
+// error code and site are words 0 and 1), zero from the workspace's zero fill.
+inline unsigned* route_ticket(int* err) { return reinterpret_cast<unsigned*>(err + 8); }
+cudaError_t launch_route_scan(const float* logits, int T, int E, int k, int renorm, int* idx, float* prob,
+                              uint32_t* masks, int* bases, int* split_sizes, unsigned* ticket, int* err,
+                              cudaStream_t st);
+// launch_route_scan, then the permutation maps alone (row_of, src_of, prob_perm).
 cudaError_t launch_route_permute(const float* logits, int T, int E, int k, int renorm, int* idx, float* prob,
                                  uint32_t* masks, int* bases, int* split_sizes, int* row_of, int* src_of,
-                                 float* prob_perm, int* err, cudaStream_t st);
+                                 float* prob_perm, unsigned* ticket, int* err, cudaStream_t st);
 // The permutation of moe_route_permute for given expert ids idx [T][k] and probabilities.
 cudaError_t launch_permute_from_idx(const int* idx, const float* prob, int T, int E, int k, uint32_t* masks,
                                     int* bases, int* split_sizes, int* row_of, int* src_of, float* prob_perm,

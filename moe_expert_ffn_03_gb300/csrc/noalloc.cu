@@ -144,13 +144,17 @@ extern "C" moe_status moe_route_permute_noalloc(const moe_dims* d, const float* 
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t cap = moe::rows_capacity(d);
-  // the masks and bases are fully rewritten by every call; only the error word starts at zero
-  cudaError_t e = cudaMemsetAsync(err, 0, 8, st);
+  // the masks and bases are fully rewritten by every call; the error word and the routing
+  // launch's block ticket start at zero
+  cudaError_t e = cudaMemsetAsync(err, 0, 64, st);
   if (e == cudaSuccess)
-    e = moe::launch_route_permute(logits, d->T, d->E, d->k, d->renormalize, idx, prob, masks, bases, split_sizes,
-                                  row_of, src_of, prob_perm, err, st);
-  if (e == cudaSuccess) e = moe::launch_quant_rowwise(x, d->T, d->H, row_of, d->k, cap, xq, xq_scale, err, st);
-  if (e == cudaSuccess) e = moe::launch_fill_pad_rows(split_sizes, d->E, d->H, xq, xq_scale, st);
+    e = moe::launch_route_scan(logits, d->T, d->E, d->k, d->renormalize, idx, prob, masks, bases, split_sizes,
+                               moe::route_ticket(err), err, st);
+  if (e == cudaSuccess) {
+    const moe::PermuteRows pr{idx, prob, masks, bases, split_sizes, d->E, (d->T + 31) / 32, row_of, src_of,
+                              prob_perm};
+    e = moe::launch_permute_quant_rows(x, d->T, d->H, d->k, cap, pr, xq, xq_scale, err, st);
+  }
   if (e == cudaSuccess && xq_col != nullptr)
     e = moe::launch_quant_colwise(x, src_of, d->T, 1, int(cap), d->H, split_sizes, d->E, xq_col, xq_col_scale, err,
                                   st);

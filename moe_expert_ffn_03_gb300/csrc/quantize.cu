@@ -11,31 +11,132 @@ namespace moe {
 // ---------------------------------------------------------------------------------
 // Rowwise: blocks of 32 along the contiguous axis.  One warp per source row;
 // lane l takes blocks l, l+32, ... so a warp reads 2 KB contiguous per step.
-// SCATTER: source row s (a token) is written to the k rows row_of[s*k + j]
-// (the permuted rows); otherwise to row s itself.
-// ---------------------------------------------------------------------------------
+// Destination rows of source row s (a token):
+//   ROW_SELF     row s itself;
+//   ROW_GIVEN    the k rows row_of[s*k + j] (the permuted rows);
+//   ROW_PERMUTE  the k rows the permutation assigns, computed here from the routing's
+//                per-expert token masks and their group prefix sums (row = padded start
+//                of expert e + base[e][g] + tokens of e below s in s's 32-token group),
+//                and written to row_of, src_of and prob_perm on the way.
 // v8_src / v8_dst: src / codes are 32-byte aligned (256-bit loads / stores).
-template <bool SCATTER>
+// ---------------------------------------------------------------------------------
+enum RowMode { ROW_SELF = 0, ROW_GIVEN = 1, ROW_PERMUTE = 2 };
+
+// Zero codes and zero scale codes (scales may be null: codes only) for the padding
+// rows of every expert segment (rows split_sizes[e] .. roundup(split_sizes[e],128)-1
+// of segment e); with src_of / prob_perm also src -1 and probability 0 there.
+// Slice `slice` of expert e clears padding rows slice, slice + FP_SLICES, ...
+constexpr int FP_SLICES = 16;
+
+__device__ __forceinline__ void fill_pad_rows_block(const int* __restrict__ split_sizes, int E, int cols,
+                                                    int64_t cap, uint8_t* __restrict__ codes,
+                                                    uint8_t* __restrict__ scales, int* __restrict__ src_of,
+                                                    float* __restrict__ prob_perm, int* err, int e, int slice) {
+  __shared__ int seg_start;
+  if (threadIdx.x < 32) {
+    int acc = 0;
+    for (int i = threadIdx.x; i < e; i += 32) acc += (split_sizes[i] + 127) & ~127;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+    if (threadIdx.x == 0) seg_start = acc;
+  }
+  __syncthreads();
+  const int m = split_sizes[e];
+  const int npad = ((m + 127) & ~127) - m;
+  const int64_t r0 = int64_t(seg_start) + m;
+  if (m < 0 || r0 + npad > cap) {
+    if (threadIdx.x == 0 && slice == 0) report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_QUANT + 2);
+    return;
+  }
+  const int vec_per_row = cols >> 4;                 // uint4 per row
+  const int nblk = cols >> 5;
+  for (int pr = slice; pr < npad; pr += FP_SLICES) {
+    const int64_t r = r0 + pr;
+    uint4* row = reinterpret_cast<uint4*>(codes + r * cols);
+    for (int c = threadIdx.x; c < vec_per_row; c += blockDim.x) row[c] = make_uint4(0, 0, 0, 0);
+    if (scales != nullptr)
+      for (int b = threadIdx.x; b < nblk; b += blockDim.x) scales[sf_offset(r, b, cols)] = 0;
+    if (src_of != nullptr && threadIdx.x == 0) {
+      src_of[r] = -1;
+      prob_perm[r] = 0.f;
+    }
+  }
+}
+
+// pad_split (optional): blocks past the token blocks zero the padding rows of every
+// segment (FP_SLICES blocks per expert); ROW_PERMUTE always has them.
+template <int MODE>
 __global__ void __launch_bounds__(256) quant_rowwise_kernel(
     const __nv_bfloat16* __restrict__ src, int64_t n_rows, int cols,
     const int* __restrict__ row_of, int k, int64_t cap,
-    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int* err, bool v8_src, bool v8_dst) {
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int* err, bool v8_src, bool v8_dst,
+    const int* __restrict__ pad_split, int pad_E, int token_blocks, PermuteRows pr) {
+  if (pad_split != nullptr && int(blockIdx.x) >= token_blocks) {
+    const int pb = blockIdx.x - token_blocks;
+    fill_pad_rows_block(pad_split, pad_E, cols, cap, codes, scales, MODE == ROW_PERMUTE ? pr.src_of : nullptr,
+                        pr.prob_perm, err, pb / FP_SLICES, pb % FP_SLICES);
+    return;
+  }
   const int lane = threadIdx.x & 31;
+  __shared__ int seg_start[kMaxExperts];
+  if (MODE == ROW_PERMUTE) {
+    // padded segment starts: lane l holds experts 8l .. 8l+7
+    if (threadIdx.x < 32) {
+      int v[8], local = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = 8 * lane + i;
+        v[i] = e < pr.E ? (pr.split_sizes[e] + 127) & ~127 : 0;
+        local += v[i];
+      }
+      int incl = local;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      int run = incl - local;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = 8 * lane + i;
+        if (e < pr.E) seg_start[e] = run;
+        run += v[i];
+      }
+    }
+    __syncthreads();
+  }
   const int64_t s = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (s >= n_rows) return;
   const int nblk = cols >> 5;
-  // lane j < k loads the destination row of slot j; every lane then takes all k by
+  // lane j < k finds the destination row of slot j; every lane then takes all k by
   // shuffles here, where the whole warp is present (fewer than 32 lanes enter the
   // block loop below when cols < 1024)
   int nd = 1;
   int dst[8];
-  if (SCATTER) {
+  if (MODE != ROW_SELF) {
     nd = k;
-    int my_dst = 0;
+    int my_dst = -1;
     bool bad = false;
     if (lane < k) {
-      my_dst = row_of[s * k + lane];
+      if (MODE == ROW_GIVEN) {
+        my_dst = row_of[s * k + lane];
+      } else {
+        const int e = pr.idx[s * k + lane];
+        if (e >= 0 && e < pr.E) {
+          const int64_t gi = int64_t(e) * pr.G + (s >> 5);
+          const uint32_t m = pr.masks[gi];
+          const uint32_t bit = 1u << (s & 31);
+          if (m & bit) my_dst = seg_start[e] + pr.bases[gi] + __popc(m & (bit - 1u));
+        }
+      }
       bad = my_dst < 0 || my_dst >= cap;
+      if (MODE == ROW_PERMUTE) {
+        pr.row_of[s * k + lane] = bad ? -1 : my_dst;
+        if (!bad) {
+          pr.src_of[my_dst] = int(s);
+          pr.prob_perm[my_dst] = pr.prob[s * k + lane];
+        }
+      }
     }
     if (__any_sync(0xFFFFFFFFu, bad)) {
       if (lane == 0) report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_QUANT + 1);
@@ -66,7 +167,7 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (j < nd) {
-        const int64_t row = SCATTER ? int64_t(dst[j]) : s;
+        const int64_t row = MODE != ROW_SELF ? int64_t(dst[j]) : s;
         store_codes32(codes + row * cols + (int64_t)b * 32, q, v8_dst);
         scales[sf_offset(row, b, cols)] = uint8_t(c);
       }
@@ -74,37 +175,10 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(
   }
 }
 
-// Zero codes and zero scale codes (scales may be null: codes only) for the
-// padding rows of every expert segment (rows split_sizes[e] ..
-// roundup(split_sizes[e],128)-1 of segment e).
-// Grid (E, FP_SLICES): slice y of expert e clears padding rows y, y + FP_SLICES, ...
-constexpr int FP_SLICES = 16;
-
 __global__ void __launch_bounds__(256) fill_pad_rows_kernel(
-    const int* __restrict__ split_sizes, int E, int cols,
-    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
-  __shared__ int seg_start;
-  const int e = blockIdx.x;
-  if (threadIdx.x < 32) {
-    int acc = 0;
-    for (int i = threadIdx.x; i < e; i += 32) acc += (split_sizes[i] + 127) & ~127;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-    if (threadIdx.x == 0) seg_start = acc;
-  }
-  __syncthreads();
-  const int m = split_sizes[e];
-  const int npad = ((m + 127) & ~127) - m;
-  const int64_t r0 = int64_t(seg_start) + m;
-  const int vec_per_row = cols >> 4;                 // uint4 per row
-  const int nblk = cols >> 5;
-  for (int pr = blockIdx.y; pr < npad; pr += FP_SLICES) {
-    const int64_t r = r0 + pr;
-    uint4* row = reinterpret_cast<uint4*>(codes + r * cols);
-    for (int c = threadIdx.x; c < vec_per_row; c += blockDim.x) row[c] = make_uint4(0, 0, 0, 0);
-    if (scales != nullptr)
-      for (int b = threadIdx.x; b < nblk; b += blockDim.x) scales[sf_offset(r, b, cols)] = 0;
-  }
+    const int* __restrict__ split_sizes, int E, int cols, int64_t cap,
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int* err) {
+  fill_pad_rows_block(split_sizes, E, cols, cap, codes, scales, nullptr, nullptr, err, blockIdx.x, blockIdx.y);
 }
 
 // ---------------------------------------------------------------------------------
@@ -265,23 +339,36 @@ __global__ void __launch_bounds__(256, 6) quant_dual_kernel(
 // host launchers
 // ---------------------------------------------------------------------------------
 cudaError_t launch_quant_rowwise(const void* src, int64_t n_rows, int cols, const int* row_of, int k,
-                                 int64_t cap, uint8_t* codes, uint8_t* scales, int* err, cudaStream_t st) {
-  if (n_rows == 0) return cudaSuccess;
-  const int64_t threads = n_rows * 32;
-  const unsigned grid = unsigned((threads + 255) / 256);
+                                 int64_t cap, uint8_t* codes, uint8_t* scales, int* err, cudaStream_t st,
+                                 const int* pad_split, int pad_E) {
+  if (n_rows == 0 && pad_split == nullptr) return cudaSuccess;
+  const int64_t token_blocks = (n_rows * 32 + 255) / 256;
+  const unsigned grid = unsigned(token_blocks + (pad_split != nullptr ? int64_t(pad_E) * FP_SLICES : 0));
   const bool v8s = aligned32(src), v8d = aligned32(codes);
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(src);
   if (row_of != nullptr)
-    quant_rowwise_kernel<true><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), n_rows, cols,
-                                                     row_of, k, cap, codes, scales, err, v8s, v8d);
+    quant_rowwise_kernel<ROW_GIVEN><<<grid, 256, 0, st>>>(x, n_rows, cols, row_of, k, cap, codes, scales, err, v8s,
+                                                          v8d, pad_split, pad_E, int(token_blocks), PermuteRows{});
   else
-    quant_rowwise_kernel<false><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), n_rows, cols,
-                                                      nullptr, 1, cap, codes, scales, err, v8s, v8d);
+    quant_rowwise_kernel<ROW_SELF><<<grid, 256, 0, st>>>(x, n_rows, cols, nullptr, 1, cap, codes, scales, err, v8s,
+                                                         v8d, pad_split, pad_E, int(token_blocks), PermuteRows{});
   return cudaGetLastError();
 }
 
-cudaError_t launch_fill_pad_rows(const int* split_sizes, int E, int cols, uint8_t* codes, uint8_t* scales,
-                                 cudaStream_t st) {
-  fill_pad_rows_kernel<<<dim3(E, FP_SLICES), 256, 0, st>>>(split_sizes, E, cols, codes, scales);
+cudaError_t launch_permute_quant_rows(const void* x, int T, int H, int k, int64_t cap, const PermuteRows& p,
+                                      uint8_t* codes, uint8_t* scales, int* err, cudaStream_t st) {
+  if (p.E < 1 || p.E > kMaxExperts || k < 1 || k > 8) return cudaErrorInvalidValue;
+  const int64_t token_blocks = (int64_t(T) * 32 + 255) / 256;
+  const unsigned grid = unsigned(token_blocks + int64_t(p.E) * FP_SLICES);
+  quant_rowwise_kernel<ROW_PERMUTE><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), T, H, nullptr, k,
+                                                          cap, codes, scales, err, aligned32(x), aligned32(codes),
+                                                          p.split_sizes, p.E, int(token_blocks), p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_pad_rows(const int* split_sizes, int E, int cols, int64_t cap, uint8_t* codes,
+                                 uint8_t* scales, int* err, cudaStream_t st) {
+  fill_pad_rows_kernel<<<dim3(E, FP_SLICES), 256, 0, st>>>(split_sizes, E, cols, cap, codes, scales, err);
   return cudaGetLastError();
 }
 

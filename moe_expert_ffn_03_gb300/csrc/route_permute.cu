@@ -18,7 +18,7 @@
 namespace moe {
 
 constexpr int kMaxK = 8;
-constexpr int kMaxE = 256;
+constexpr int kMaxE = kMaxExperts;
 
 // Total order of (logit, expert): larger logit first, ties to the lower expert id.
 // A NaN logit ranks below every number (-inf included) and NaNs tie among
@@ -32,6 +32,10 @@ __device__ __forceinline__ bool better(float va, int ea, float vb, int eb) {
 }
 
 constexpr int RT_THREADS = 128;
+// Top-k and the per-expert scan as one launch (the last block scans) while the masks are
+// at most RS_SCAN_MAX_WORDS words; larger ones get the scan kernel with one CTA per expert.
+constexpr int RS_THREADS = 512;
+constexpr int RS_SCAN_MAX_WORDS = 16384;
 
 // Bubble (v, e) into the sorted list (best first); the last entry falls off.
 __device__ __forceinline__ void topk_insert(float v, int e, float (&sv)[kMaxK], int (&se)[kMaxK]) {
@@ -48,67 +52,120 @@ __device__ __forceinline__ void topk_insert(float v, int e, float (&sv)[kMaxK], 
   }
 }
 
-__global__ void __launch_bounds__(RT_THREADS) route_topk_kernel(
-    const float* __restrict__ logits, int T, int E, int k, int renorm,
-    int* __restrict__ idx, float* __restrict__ prob, uint32_t* __restrict__ masks, int G, int* err) {
-  __shared__ uint32_t smask[RT_THREADS / 32][kMaxE];
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int t = blockIdx.x * RT_THREADS + threadIdx.x;
-  const int g = t >> 5;                                // the warp's 32-token group
-  if (g >= G) return;                                  // warp-uniform
-  for (int e = lane; e < E; e += 32) smask[w][e] = 0u;
-  __syncwarp();
-  if (t < T) {
-    float sv[kMaxK];
-    int se[kMaxK];
+// Exclusive scan over groups g of popc(mask[e][g]) for the experts e = warp, warp + nwarps, ...
+// (one warp per expert, 128 groups a step, 4 consecutive groups a lane): base[e][g] and
+// split_sizes[e].  Loads bypass L1: the masks were written by other blocks of this launch.
+__device__ __forceinline__ void scan_experts_by_warps(const uint32_t* masks, int G, int E, int warp, int nwarps,
+                                                      int lane, int* bases, int* split_sizes) {
+  for (int e = warp; e < E; e += nwarps) {
+    const uint32_t* m = masks + (int64_t)e * G;
+    int* b = bases + (int64_t)e * G;
+    int carry = 0;
+    for (int g0 = 0; g0 < G; g0 += 128) {
+      int c[4];
 #pragma unroll
-    for (int s = 0; s < kMaxK; ++s) {
-      sv[s] = __int_as_float(0x7FFFFFFF);              // NaN with the largest id: below every real entry
-      se[s] = 0x7FFFFFFF;
-    }
-    const float* row = logits + (int64_t)t * E;
-    if ((E & 3) == 0) {
-      const float4* row4 = reinterpret_cast<const float4*>(row);
-      for (int e4 = 0; e4 < (E >> 2); ++e4) {
-        const float4 q = row4[e4];
-        topk_insert(q.x, 4 * e4 + 0, sv, se);
-        topk_insert(q.y, 4 * e4 + 1, sv, se);
-        topk_insert(q.z, 4 * e4 + 2, sv, se);
-        topk_insert(q.w, 4 * e4 + 3, sv, se);
+      for (int i = 0; i < 4; ++i) {
+        const int g = g0 + 4 * lane + i;
+        c[i] = g < G ? __popc(__ldcg(m + g)) : 0;
       }
-    } else {
-      for (int e = 0; e < E; ++e) topk_insert(row[e], e, sv, se);
-    }
-    // probabilities: softmax of the selected logits (renorm) or of all E
-    const float m = sv[0];
-    float den = 0.f;
-    if (renorm) {
+      const int local = c[0] + c[1] + c[2] + c[3];
+      int incl = local;
 #pragma unroll
-      for (int s = 0; s < kMaxK; ++s)
-        if (s < k) den += expf(sv[s] - m);
-    } else {
-      for (int e = 0; e < E; ++e) den += expf(row[e] - m);
-    }
-#pragma unroll
-    for (int s = 0; s < kMaxK; ++s) {
-      if (s < k) {
-        // k <= E, so the list holds k real experts; the check keeps a broken invariant
-        // from turning into a shared-memory access out of bounds
-        if (se[s] < 0 || se[s] >= E) {
-          report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_ROUTE);
-          idx[(int64_t)t * k + s] = -1;
-          prob[(int64_t)t * k + s] = 0.f;
-          continue;
-        }
-        idx[(int64_t)t * k + s] = se[s];
-        prob[(int64_t)t * k + s] = expf(sv[s] - m) / den;
-        atomicOr(&smask[w][se[s]], 1u << lane);
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += o;
       }
+      int run = carry + incl - local;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int g = g0 + 4 * lane + i;
+        if (g < G) b[g] = run;
+        run += c[i];
+      }
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
+    if (lane == 0) split_sizes[e] = carry;
   }
-  __syncwarp();
-  // bit l of mask[e][g] = token g*32+l picked expert e
-  for (int e = lane; e < E; e += 32) masks[(int64_t)e * G + g] = smask[w][e];
+}
+
+// NT threads a block, one token a thread.  With SCAN the block that finishes last (a
+// ticket taken after each block's masks are written and fenced) also runs the per-expert
+// scan, so top-k and scan are one launch; atomicInc wraps the ticket back to 0 at the
+// last block, ready for the next launch.  Nothing waits on another block.
+template <int NT, bool SCAN>
+__global__ void __launch_bounds__(NT) route_topk_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int renorm,
+    int* __restrict__ idx, float* __restrict__ prob, uint32_t* __restrict__ masks, int G, int* err,
+    unsigned* ticket, int* __restrict__ bases, int* __restrict__ split_sizes) {
+  __shared__ uint32_t smask[NT / 32][kMaxE];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int t = blockIdx.x * NT + threadIdx.x;
+  const int g = t >> 5;                                // the warp's 32-token group
+  if (g < G) {                                         // warp-uniform
+    for (int e = lane; e < E; e += 32) smask[w][e] = 0u;
+    __syncwarp();
+    if (t < T) {
+      float sv[kMaxK];
+      int se[kMaxK];
+#pragma unroll
+      for (int s = 0; s < kMaxK; ++s) {
+        sv[s] = __int_as_float(0x7FFFFFFF);            // NaN with the largest id: below every real entry
+        se[s] = 0x7FFFFFFF;
+      }
+      const float* row = logits + (int64_t)t * E;
+      if ((E & 3) == 0) {
+        const float4* row4 = reinterpret_cast<const float4*>(row);
+        for (int e4 = 0; e4 < (E >> 2); ++e4) {
+          const float4 q = row4[e4];
+          topk_insert(q.x, 4 * e4 + 0, sv, se);
+          topk_insert(q.y, 4 * e4 + 1, sv, se);
+          topk_insert(q.z, 4 * e4 + 2, sv, se);
+          topk_insert(q.w, 4 * e4 + 3, sv, se);
+        }
+      } else {
+        for (int e = 0; e < E; ++e) topk_insert(row[e], e, sv, se);
+      }
+      // probabilities: softmax of the selected logits (renorm) or of all E
+      const float m = sv[0];
+      float den = 0.f;
+      if (renorm) {
+#pragma unroll
+        for (int s = 0; s < kMaxK; ++s)
+          if (s < k) den += expf(sv[s] - m);
+      } else {
+        for (int e = 0; e < E; ++e) den += expf(row[e] - m);
+      }
+#pragma unroll
+      for (int s = 0; s < kMaxK; ++s) {
+        if (s < k) {
+          // k <= E, so the list holds k real experts; the check keeps a broken invariant
+          // from turning into a shared-memory access out of bounds
+          if (se[s] < 0 || se[s] >= E) {
+            report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_ROUTE);
+            idx[(int64_t)t * k + s] = -1;
+            prob[(int64_t)t * k + s] = 0.f;
+            continue;
+          }
+          idx[(int64_t)t * k + s] = se[s];
+          prob[(int64_t)t * k + s] = expf(sv[s] - m) / den;
+          atomicOr(&smask[w][se[s]], 1u << lane);
+        }
+      }
+    }
+    __syncwarp();
+    // bit l of mask[e][g] = token g*32+l picked expert e
+    for (int e = lane; e < E; e += 32) masks[(int64_t)e * G + g] = smask[w][e];
+  }
+  if (SCAN) {
+    __shared__ bool last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicInc(ticket, gridDim.x - 1) == gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    scan_experts_by_warps(masks, G, E, w, NT / 32, lane, bases, split_sizes);
+  }
 }
 
 // One CTA per expert: exclusive scan over groups of popc(mask).
@@ -236,16 +293,31 @@ cudaError_t launch_permute_from_idx(const int* idx, const float* prob, int T, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_route_permute(const float* logits, int T, int E, int k, int renorm, int* idx, float* prob,
-                                 uint32_t* masks, int* bases, int* split_sizes, int* row_of, int* src_of,
-                                 float* prob_perm, int* err, cudaStream_t st) {
+// ---------------------------------------------------------------------------------
+bool route_scan_fused(int T, int E) { return int64_t(E) * ((int64_t(T) + 31) / 32) <= RS_SCAN_MAX_WORDS; }
+
+cudaError_t launch_route_scan(const float* logits, int T, int E, int k, int renorm, int* idx, float* prob,
+                              uint32_t* masks, int* bases, int* split_sizes, unsigned* ticket, int* err,
+                              cudaStream_t st) {
   const int G = (T + 31) / 32;
-  route_topk_kernel<<<(G * 32 + RT_THREADS - 1) / RT_THREADS, RT_THREADS, 0, st>>>(logits, T, E, k, renorm, idx,
-                                                                                   prob, masks, G, err);
+  if (route_scan_fused(T, E)) {
+    route_topk_kernel<RS_THREADS, true><<<(G * 32 + RS_THREADS - 1) / RS_THREADS, RS_THREADS, 0, st>>>(
+        logits, T, E, k, renorm, idx, prob, masks, G, err, ticket, bases, split_sizes);
+    return cudaGetLastError();
+  }
+  route_topk_kernel<RT_THREADS, false><<<(G * 32 + RT_THREADS - 1) / RT_THREADS, RT_THREADS, 0, st>>>(
+      logits, T, E, k, renorm, idx, prob, masks, G, err, nullptr, nullptr, nullptr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   permute_scan_kernel<<<E, 1024, 0, st>>>(masks, G, bases, split_sizes);
-  e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_permute(const float* logits, int T, int E, int k, int renorm, int* idx, float* prob,
+                                 uint32_t* masks, int* bases, int* split_sizes, int* row_of, int* src_of,
+                                 float* prob_perm, unsigned* ticket, int* err, cudaStream_t st) {
+  const int G = (T + 31) / 32;
+  cudaError_t e = launch_route_scan(logits, T, E, k, renorm, idx, prob, masks, bases, split_sizes, ticket, err, st);
   if (e != cudaSuccess) return e;
   const int token_blocks = (T + 255) / 256;
   permute_scatter_kernel<<<token_blocks + E, 256, 0, st>>>(idx, prob, T, k, E, G, masks, bases, split_sizes,

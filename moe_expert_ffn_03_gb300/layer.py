@@ -14,14 +14,28 @@ from . import binding as B
 
 U8 = torch.uint8
 
-# kernel launches of one training step (quantize_weights + forward + backward):
-# weights 2 (both orientations of W_gu and of W_d), route/permute 6 (top-k, scan, scatter,
-# gather+quantize rows, padding rows, gather+quantize along tokens), forward 2
-# GEMMs, combine 1, backward 8 (dY rowwise, padding rows, dY along tokens, down
-# dgrad, dprob reduce, down wgrad, gate_up dgrad, gate_up wgrad), combine 1.
-LAUNCHES_PER_TRAINING_STEP = 20
-# forward-only step: weights 2, route/permute 5, forward 2, combine 1
-LAUNCHES_PER_FORWARD_STEP = 10
+# Routing: top-k and the per-expert scan of the token masks are one launch while the
+# masks hold at most 16384 words (E * ceil(T/32)), else two; the permutation itself is
+# finished by the launch that gathers and quantizes the x rows.
+ROUTE_SCAN_FUSED_MAX_WORDS = 16384
+
+
+def route_launches(T: int, E: int) -> int:
+    """Launches of routing up to (not including) the row gather-quantize."""
+    return 1 if E * ((T + 31) // 32) <= ROUTE_SCAN_FUSED_MAX_WORDS else 2
+
+
+def launches_per_step(T: int, E: int, k: int, training: bool) -> int:
+    """Kernel launches of one step (quantize_weights + forward [+ backward]).
+
+    weights 2 (both orientations of W_gu and of W_d); routing 1 or 2; permutation with the
+    x rows gathered and quantized (padding rows zeroed in the same launch) 1; forward 2
+    GEMMs; combine 1.  Training adds x along tokens 1 and the backward: dY rows (with
+    padding rows) 1, dY along tokens 1, down dgrad 1, dprob reduce 1, down wgrad 1,
+    gate_up dgrad 1, gate_up wgrad 1, and the dx combine 1.
+    """
+    fwd = 2 + route_launches(T, E) + 1 + 2 + 1
+    return fwd + (1 + 8 if training else 0)
 
 
 class _Range:
