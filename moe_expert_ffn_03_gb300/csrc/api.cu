@@ -84,7 +84,7 @@ WsLayout ws_layout(const moe_dims* d, int mode) {
     w.dhqc = take(2 * I * cap);
     w.dhqc_s = take(2 * I * cap / 32);
     w.dp = take(ntI * 4 * cap * 4);                 // one partial row sum per 64-column group
-    w.rpart = take(router_partial_bytes(d->E, d->H));   // router weight-gradient partials
+    w.rpart = take(router_ws_bytes(d->T, d->E, d->H));  // router backward: dW_r partials, dl hi/lo
   }
   if (mode == 3) {
     w.t8dy = take(cap * H);
@@ -1254,7 +1254,7 @@ moe_status moe_router_bwd(const moe_dims* d, const void* x, const void* w_r, con
   if (s != MOE_OK) return s;
   const WsLayout w = ws_layout(d, true);
   CUDA_TRY(launch_router_bwd(x, w_r, logits, idx, prob, dprob, d->T, d->H, d->E, d->k, d->renormalize, dlogits, dx,
-                             dw_r, at<float>(workspace, w.rpart), at<int>(workspace, w.err),
+                             dw_r, at<uint8_t>(workspace, w.rpart), at<int>(workspace, w.err),
                              static_cast<cudaStream_t>(stream)),
            "router bwd");
   return MOE_OK;

@@ -25,6 +25,7 @@ enum ErrSite : int {
   SITE_GEMM_MMA_ACC = 520,
   SITE_GEMM_EPILOGUE = 530,
   SITE_GEMM_DRAIN = 540,
+  SITE_ROUTER_DW = 600,
 };
 
 __device__ __forceinline__ void report_error(int* err, int code, int site) {

@@ -1364,6 +1364,203 @@ __global__ void __launch_bounds__(MR_THREADS, 1) mma_rate_selftest_kernel(int k_
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// ---- router weight gradient on the tensor cores --------------------------------------
+// dW_r^T[h][e] = sum_t x[t][h] * dl[t][e] (the router's weight gradient, transposed) for
+// one 128-row block of h and one chunk of tokens per CTA, single-CTA MMAs
+// (cta_group::1, M = 128, N = roundup(E, 64)).  x [T][H] and dl [T][N] both keep the
+// MMA's M / N index contiguous, so TMA loads them as they lie into MN-major 128-byte
+// swizzled tiles: 64 tokens (K) x 64 columns per box, boxes of further 64-column blocks
+// LBO apart, 8-token groups 1024 bytes apart (SBO).  dl arrives as two bf16 terms hi + lo
+// (hi = bf16(dl), lo = bf16(dl - hi): dl to about 2^-17 relative); each 16-token step
+// issues hi . x and lo . x into the same f32 accumulator.  Chunk c's tile is written to
+// partial[c][e][h]; the chunks are summed in chunk order by a separate reduction.
+constexpr int RDW_KT = 64;                     // tokens per pipeline stage
+constexpr int RDW_M = 128;                     // hidden rows of a tile
+constexpr int RDW_MAX_STG = 8;
+constexpr uint32_t RDW_SMEM_MAX = 200u * 1024u;
+constexpr uint32_t RDW_A_BYTES = RDW_M * RDW_KT * 2;   // two 64-column boxes of x
+
+struct RouterDwArgs {
+  int H, E, N;            // N = roundup(E, 64): accumulator columns
+  int nst, per;           // 64-token stages in all, and per chunk
+  int stages;             // pipeline depth
+  float* partial;         // [chunks][E][H]
+  int* err;
+};
+
+__device__ __forceinline__ void tma_load_2d_cta(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_cta(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_cta() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_cta(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_commit_cta(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma_bf16_cta(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// MN-major operand with 128-byte swizzle: rows of 128 bytes (64 bf16 of the M or N index)
+// per K index, 8-row groups every 1024 bytes (SBO), 64-column blocks every lbo bytes.
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);
+  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+  d |= uint64_t(1024 >> 4) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
+}
+// kind::f16 instruction descriptor: bf16 x bf16 -> f32, A and B MN-major (transposed).
+__device__ __forceinline__ uint32_t idesc_bf16_mn(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | (uint32_t(N >> 3) << 17) |
+         (uint32_t(M >> 4) << 24);
+}
+
+__global__ void __launch_bounds__(192, 1) router_dw_tc_kernel(const __grid_constant__ CUtensorMap mx,
+                                                              const __grid_constant__ CUtensorMap mhi,
+                                                              const __grid_constant__ CUtensorMap mlo,
+                                                              const RouterDwArgs a) {
+  extern __shared__ uint8_t rdw_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rdw_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t full[RDW_MAX_STG], empty[RDW_MAX_STG], done;
+  __shared__ uint32_t tmem_s;
+  __shared__ int abort_flag;
+  volatile int* abort_s = &abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NB = a.N / 64;
+  const uint32_t b_bytes = uint32_t(a.N) * RDW_KT * 2;
+  const uint32_t stage_bytes = RDW_A_BYTES + 2 * b_bytes;
+  const uint32_t ncols = a.N <= 64 ? 64u : a.N <= 128 ? 128u : 256u;
+  const int h0 = blockIdx.x * RDW_M, c = blockIdx.y;
+  const int s0 = c * a.per;
+  const int n = min(a.nst, s0 + a.per) - s0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&done, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc_cta(&tmem_s, ncols);
+    tmem_relinquish_cta();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_s;
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      prefetch_tmap(&mx);
+      prefetch_tmap(&mhi);
+      prefetch_tmap(&mlo);
+      int last_round[RDW_MAX_STG];
+#pragma unroll
+      for (int s = 0; s < RDW_MAX_STG; ++s) last_round[s] = -1;
+      bool ok = true;
+      for (int i = 0; i < n; ++i) {
+        const int slot = i % a.stages, round = i / a.stages;
+        if (!wait_phase(&empty[slot], (round & 1) ^ 1, abort_s, a.err, SITE_ROUTER_DW, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + size_t(slot) * stage_bytes;
+        mbar_arrive_expect_tx(&full[slot], stage_bytes);
+        const int t = (s0 + i) * RDW_KT;
+        tma_load_2d_cta(st, &mx, h0, t, &full[slot]);
+        tma_load_2d_cta(st + 8192, &mx, h0 + 64, t, &full[slot]);
+        for (int j = 0; j < NB; ++j) {
+          tma_load_2d_cta(st + RDW_A_BYTES + j * 8192, &mhi, 64 * j, t, &full[slot]);
+          tma_load_2d_cta(st + RDW_A_BYTES + b_bytes + j * 8192, &mlo, 64 * j, t, &full[slot]);
+        }
+        last_round[slot] = round;
+      }
+      if (!ok) {
+        // copies already issued land before the CTA exits (bounded)
+        for (int s = 0; s < a.stages; ++s) {
+          if (last_round[s] < 0) continue;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&full[s], last_round[s] & 1) && globaltimer_ns() - t0 < 20000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      const uint32_t idesc = idesc_bf16_mn(RDW_M, a.N);
+      for (int i = 0; i < n; ++i) {
+        const int slot = i % a.stages, round = i / a.stages;
+        if (!wait_phase(&full[slot], round & 1, abort_s, a.err, SITE_ROUTER_DW + 1, kWaitLimitNs)) break;
+        tc_fence_after();
+        const uint32_t st = smem_u32(smem + size_t(slot) * stage_bytes);
+        const uint64_t ad = desc_sw128_mn(st, 8192);
+        const uint64_t bh = desc_sw128_mn(st + RDW_A_BYTES, 8192);
+        const uint64_t bl = desc_sw128_mn(st + RDW_A_BYTES + b_bytes, 8192);
+#pragma unroll
+        for (int kk = 0; kk < RDW_KT / 16; ++kk) {
+          // 16 tokens = two 8-row groups = 2048 bytes, 128 in the descriptor's 16-byte units
+          tc_mma_bf16_cta(tmem, ad + uint64_t(128 * kk), bh + uint64_t(128 * kk), idesc, (i | kk) != 0);
+          tc_mma_bf16_cta(tmem, ad + uint64_t(128 * kk), bl + uint64_t(128 * kk), idesc, 1);
+        }
+        tc_commit_cta(&empty[slot]);
+      }
+      tc_commit_cta(&done);                    // arrives once every MMA issued above is complete
+    }
+  } else {
+    // ---------------- epilogue warps 2..5: warp w reads TMEM lanes 32*(w%4).. ----------------
+    const int q = warp & 3;
+    const int h = h0 + 32 * q + lane;
+    bool ok = wait_phase(&done, 0, abort_s, a.err, SITE_ROUTER_DW + 2, kWaitLimitNs);
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    if (ok) {
+      tc_fence_after();
+      for (int j0 = 0; j0 < a.N; j0 += 16) {
+        uint32_t r[16];
+        tmem_ld16_async(tmem + (uint32_t(32 * q) << 16) + uint32_t(j0), r);
+        tmem_wait_ld<16>(r);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const int e = j0 + jj;
+          if (e < a.E && h < a.H) a.partial[(int64_t(c) * a.E + e) * a.H + h] = __uint_as_float(r[jj]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_s) {
+    // an MMA may still run after a wait gave up: let it finish before the memory goes (bounded)
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(&done, 0) && globaltimer_ns() - t0 < 20000000ull) {
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_cta(tmem, ncols);
+}
+
 // ---- host side -----------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -1559,6 +1756,66 @@ cudaError_t launch_grouped_gemm(int epi, const GemmArgs& args, const void* A, in
     case EPI_B16_F32_OUT: return launch_kind<EPI_B16_F32_OUT>(ma, mb, msfa, msfb, b_experts != nullptr ? &pe_maps : nullptr, a, grid, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+
+// ---- router weight gradient: host side -----------------------------------------------
+int router_dw_cols(int E) { return (E + 63) / 64 * 64; }
+int router_dw_max_chunks(int H) {
+  const int tiles = (H + RDW_M - 1) / RDW_M;
+  const int c = 256 / tiles;
+  return c < 1 ? 1 : c > 32 ? 32 : c;
+}
+
+static bool encode_map_bf16_2d(CUtensorMap* m, const void* base, int64_t inner, int64_t outer) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+  cuuint64_t strides[1] = {cuuint64_t(inner * 2)};
+  cuuint32_t box[2] = {64, cuuint32_t(RDW_KT)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_router_dw_tc(const void* x, const void* dl_hi, const void* dl_lo, int T, int H, int E,
+                                float* partial, int max_chunks, int* chunks_used, int* err, cudaStream_t st) {
+  if (H % RDW_M != 0 || T < 1 || E < 1 || E > 256) return cudaErrorInvalidValue;
+  const int N = router_dw_cols(E);
+  CUtensorMap mx, mhi, mlo;
+  if (!encode_map_bf16_2d(&mx, x, H, T) || !encode_map_bf16_2d(&mhi, dl_hi, N, T) ||
+      !encode_map_bf16_2d(&mlo, dl_lo, N, T))
+    return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int tiles = H / RDW_M;
+  const int nst = (T + RDW_KT - 1) / RDW_KT;
+  int S = sms / tiles;
+  S = S < 1 ? 1 : S;
+  S = S > max_chunks ? max_chunks : S;
+  S = S > nst ? nst : S;
+  const int per = (nst + S - 1) / S;
+  S = (nst + per - 1) / per;                   // every chunk holds at least one stage
+  RouterDwArgs a{};
+  a.H = H;
+  a.E = E;
+  a.N = N;
+  a.nst = nst;
+  a.per = per;
+  a.partial = partial;
+  a.err = err;
+  const uint32_t stage_bytes = RDW_A_BYTES + 2u * uint32_t(N) * RDW_KT * 2u;
+  int stages = int(RDW_SMEM_MAX / stage_bytes);
+  a.stages = stages > RDW_MAX_STG ? RDW_MAX_STG : stages;
+  const size_t smem = size_t(a.stages) * stage_bytes + 1024;
+  e = cudaFuncSetAttribute(router_dw_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  router_dw_tc_kernel<<<dim3(unsigned(tiles), unsigned(S)), 192, smem, st>>>(mx, mhi, mlo, a);
+  *chunks_used = S;
+  return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -62,12 +62,18 @@ cudaError_t launch_quant_dual(const void* src, int batch, int rows, int cols, ui
 // codes_t / scales_t may be null (rows only)
 cudaError_t launch_quant_dual_experts(const ExpertSrc& src, int batch, int rows, int cols, uint8_t* codes,
                                       uint8_t* scales, uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st);
-size_t router_partial_bytes(int E, int H);
+// Router backward workspace (chunk partials of dW_r and dl as bf16 hi + lo) and the
+// tensor-core dW_r launch (partial [chunks][E][H]; *chunks_used chunks written).
+size_t router_ws_bytes(int T, int E, int H);
+int router_dw_cols(int E);
+int router_dw_max_chunks(int H);
+cudaError_t launch_router_dw_tc(const void* x, const void* dl_hi, const void* dl_lo, int T, int H, int E,
+                                float* partial, int max_chunks, int* chunks_used, int* err, cudaStream_t st);
 cudaError_t launch_router_fwd(const void* x, const void* w, int T, int H, int E, float* logits, int* err,
                               cudaStream_t st, char* msg, size_t msg_len);
 cudaError_t launch_router_bwd(const void* x, const void* w, const float* logits, const int* idx, const float* prob,
                               const float* dprob, int T, int H, int E, int k, int renorm, float* dl, void* dx,
-                              float* dw, float* partial, int* err, cudaStream_t st);
+                              float* dw, void* ws, int* err, cudaStream_t st);
 // Top-k routing plus the per-expert scan of the token masks (masks [E][G], bases [E][G],
 // split_sizes [E]).  One launch while E*ceil(T/32) <= 16384 (the last block to finish
 // scans; `ticket` is a zero-initialised counter the launch returns to zero), else two.
