@@ -74,7 +74,8 @@ def test_trainable_layer_with_router(T, H, I, E, k, renorm):
 
 
 @pytest.mark.parametrize("renorm", [1, 0])
-@pytest.mark.parametrize("T,H,E,k", [(8192, 2048, 64, 6), (4096, 4096, 8, 2), (1000, 384, 256, 8), (70, 128, 4, 2)])
+@pytest.mark.parametrize("T,H,E,k", [(8192, 2048, 64, 6), (4096, 4096, 8, 2), (1000, 384, 256, 8), (70, 128, 4, 2),
+                                     (3000, 1280, 100, 4)])
 def test_router_backward_direct(T, H, E, k, renorm):
     """moe_router_bwd alone at the fine-grained and Mixtral hidden sizes (and ragged ones):
     logits, routing and dprob are made on the host (seeded), so dlogits, the router's
