@@ -13,6 +13,10 @@ stream:
 * Two device slots hold the inputs, so the next step's inputs land while this
   step computes.  A slot is refilled only after the step that read it has run
   its backward (or its forward, without training).
+* A step quantizes its weights before it waits for its inputs (the weights are
+  already on the device), and its forward waits only for x and logits: dout has
+  an event of its own and is awaited by the backward.  So the inputs of a step
+  whose predecessor left no time to copy them (the first one) land under work.
 * out and dx are single device buffers.  A step's combine waits until the
   previous step's copy of that buffer has left the device, so a result is
   never overwritten before it is read out.
@@ -41,7 +45,8 @@ class HostPipeline:
         self.slots = [{n: torch.empty(shapes[n][0], dtype=shapes[n][1], device=dev) for n in names}
                       for _ in range(2)]
         ev = lambda: torch.cuda.Event()                                 # noqa: E731
-        self.landed = [ev(), ev()]        # H2D of a slot finished
+        self.landed = [ev(), ev()]        # H2D of a slot's x and logits finished
+        self.landed_dout = [ev(), ev()]   # H2D of a slot's dout finished (training)
         self.released = [ev(), ev()]      # the compute stream is done reading a slot
         self.out_done, self.dx_done = ev(), ev()        # a result is complete on the device
         self.out_copied, self.dx_copied = ev(), ev()    # a result has left the device
@@ -51,9 +56,12 @@ class HostPipeline:
         with torch.cuda.stream(self.copy_in):
             if wait_release:
                 self.copy_in.wait_event(self.released[slot])
-            for n in self.names:
+            for n in ("x", "logits"):
                 self.slots[slot][n].copy_(host[n], non_blocking=True)
             self.landed[slot].record(self.copy_in)
+            if self.train:
+                self.slots[slot]["dout"].copy_(host["dout"], non_blocking=True)
+                self.landed_dout[slot].record(self.copy_in)
 
     def run(self, host_inputs: list, host_outputs: list, after: torch.cuda.Event | None = None):
         """One step per entry of host_inputs (dicts of pinned tensors named x, logits[,
@@ -73,8 +81,8 @@ class HostPipeline:
             if i + 1 < n:
                 self._h2d(1 - s, host_inputs[i + 1], wait_release=not self._first or i >= 1)
             inp = self.slots[s]
-            st.wait_event(self.landed[s])
             L.quantize_weights(self.w_gu, self.w_d, st)
+            st.wait_event(self.landed[s])
             L.route(inp["logits"], inp["x"], st)
             L.ffn_forward(st)
             if not self._first or i > 0:
@@ -82,6 +90,7 @@ class HostPipeline:
             L.combine_out(st)
             self.out_done.record(st)
             if self.train:
+                st.wait_event(self.landed_dout[s])
                 L.ffn_backward(inp["dout"], st)
                 self.released[s].record(st)
                 if not self._first or i > 0:
