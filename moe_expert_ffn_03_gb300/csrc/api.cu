@@ -854,7 +854,8 @@ moe_status grouped_mlp_bwd_bf16(const moe_dims* d, const void* dout, const int32
   CUDA_TRY(launch_grouped_gemm(EPI_B16_BWD_SWIGLU, g3, dy, cap, H, w_dT, int64_t(E) * I, H, (cap / 128) * g3.n_tiles,
                                st, g_msg, sizeof(g_msg)),
            "bf16 down dgrad GEMM");
-  CUDA_TRY(launch_dprob_reduce(dp, g3.n_tiles * 4, cap, row_of, int64_t(d->T) * k, dprob, err, st), "dprob reduce");
+  CUDA_TRY(launch_dprob_reduce(dp, g3.n_tiles * 4, cap, split_sizes, E, src_of, row_of, k, d->T, dprob, err, st),
+           "dprob reduce");
 
   // down wgrad: dW_d[e] = dY_e^T a_e (K = the expert's tokens)
   GemmArgs g4{};
@@ -990,7 +991,8 @@ moe_status grouped_mlp_bwd_fp8_tensor(const moe_dims* d, const void* dout, const
   CUDA_TRY(launch_grouped_gemm(EPI_T8_BWD_SWIGLU, g3, dyq, cap, H, wdT, int64_t(E) * I, H, (cap / 128) * g3.n_tiles,
                                st, g_msg, sizeof(g_msg)),
            "per-tensor FP8 down dgrad GEMM");
-  CUDA_TRY(launch_dprob_reduce(dp, g3.n_tiles * 4, cap, row_of, int64_t(d->T) * k, dprob, err, st), "dprob reduce");
+  CUDA_TRY(launch_dprob_reduce(dp, g3.n_tiles * 4, cap, split_sizes, E, nullptr, row_of, k, d->T, dprob, err, st),
+           "dprob reduce");
   // dH codes with its expert's scale, rows and transposed; x and a codes transposed
   CUDA_TRY(launch_t8_quant_segments(dh16, split_sizes, E, cap, 2 * I, am_dh, dhq, st), "per-tensor quantize of dH");
   CUDA_TRY(launch_transpose_u8(dhq, 1, int(cap), 2 * I, split_sizes, E, dhqc, st), "dH codes transposed");
@@ -1134,7 +1136,8 @@ moe_status grouped_mlp_bwd(const moe_dims* d, const void* dout, const int32_t* s
   CUDA_TRY(launch_grouped_gemm(EPI_BWD_SWIGLU, g3, dyq, cap, H, wdT_q, int64_t(E) * I, H, (cap / 128) * g3.n_tiles,
                                st, g_msg, sizeof(g_msg)),
            "down dgrad GEMM");
-  CUDA_TRY(launch_dprob_reduce(dp, g3.n_tiles * 4, cap, row_of, int64_t(d->T) * k, dprob, err, st), "dprob reduce");
+  CUDA_TRY(launch_dprob_reduce(dp, g3.n_tiles * 4, cap, split_sizes, E, src_of, row_of, k, d->T, dprob, err, st),
+           "dprob reduce");
 
   // down wgrad: dW_d[e] = dY_e^T a_e, K = the expert's tokens
   GemmArgs g4{};

@@ -81,6 +81,63 @@ __global__ void __launch_bounds__(256) dprob_reduce_kernel(
   dprob[i] = acc;
 }
 
+// The same sums by permuted row, for rows with many partials (the Mixtral-shaped 224; the
+// token-ordered kernel above is as fast for few).  A block holds 32 rows and its eight warps
+// split the partials: warp w sums n = w, w + 8, ... of its lane's row (a warp's loads are 128
+// contiguous bytes), then warp 0 adds the eight sums in warp order (a fixed order:
+// deterministic), finds the row's slot j among row_of[src_of[r]][*] and writes
+// dprob[src_of[r]][j].  Rows past the padded total and padding rows (src_of = -1) write nothing.
+constexpr int DPR_WARPS = 8;
+__global__ void __launch_bounds__(32 * DPR_WARPS) dprob_reduce_rows_kernel(
+    const float* __restrict__ dp_part, int n_tiles, int64_t cap, const int* __restrict__ split_sizes, int E,
+    const int* __restrict__ src_of, const int* __restrict__ row_of, int k, int T, float* __restrict__ dprob,
+    int* err) {
+  __shared__ int64_t total_s;
+  __shared__ float part[DPR_WARPS][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (w == 0) {
+    int64_t acc = 0;
+    for (int e = lane; e < E; e += 32) acc += (split_sizes[e] + 127) & ~127;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+    if (lane == 0) total_s = acc;
+  }
+  __syncthreads();
+  const int64_t r = int64_t(blockIdx.x) * 32 + lane;
+  const bool valid = r < total_s && r < cap;
+  float acc = 0.f;
+  if (valid) {
+    int n = w;
+    for (; n + 3 * DPR_WARPS < n_tiles; n += 4 * DPR_WARPS) {
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = dp_part[int64_t(n + j * DPR_WARPS) * cap + r];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc += v[j];
+    }
+    for (; n < n_tiles; n += DPR_WARPS) acc += dp_part[int64_t(n) * cap + r];
+  }
+  part[w][lane] = acc;
+  __syncthreads();
+  if (w != 0 || !valid) return;
+  float sum = part[0][lane];
+#pragma unroll
+  for (int i = 1; i < DPR_WARPS; ++i) sum += part[i][lane];
+  const int t = src_of[r];
+  if (t < 0) return;
+  if (t >= T) {
+    report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_COMBINE + 4);
+    return;
+  }
+  int j = 0;
+  while (j < k && row_of[int64_t(t) * k + j] != r) ++j;
+  if (j == k) {
+    report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_COMBINE + 5);
+    return;
+  }
+  dprob[int64_t(t) * k + j] = sum;
+}
+
 // bf16 path: x_perm[row_of[t][j]] = x[t] (one warp per token, 16-byte copies).
 __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
                                                           const int* __restrict__ row_of, int T, int k, int H,
@@ -142,9 +199,16 @@ cudaError_t launch_combine(const void* y, const int* row_of, const float* prob, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_dprob_reduce(const float* dp_part, int n_tiles, int64_t cap, const int* row_of, int64_t R,
-                                float* dprob, int* err, cudaStream_t st) {
-  dprob_reduce_kernel<<<unsigned((R + 255) / 256), 256, 0, st>>>(dp_part, n_tiles, cap, row_of, R, dprob, err);
+cudaError_t launch_dprob_reduce(const float* dp_part, int n_tiles, int64_t cap, const int* split_sizes, int E,
+                                const int* src_of, const int* row_of, int k, int T, float* dprob, int* err,
+                                cudaStream_t st) {
+  if (src_of != nullptr && n_tiles >= 64) {
+    dprob_reduce_rows_kernel<<<unsigned((cap + 31) / 32), 32 * DPR_WARPS, 0, st>>>(
+        dp_part, n_tiles, cap, split_sizes, E, src_of, row_of, k, T, dprob, err);
+  } else {
+    const int64_t R = int64_t(T) * k;
+    dprob_reduce_kernel<<<unsigned((R + 255) / 256), 256, 0, st>>>(dp_part, n_tiles, cap, row_of, R, dprob, err);
+  }
   return cudaGetLastError();
 }
 

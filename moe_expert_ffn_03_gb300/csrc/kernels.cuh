@@ -129,8 +129,11 @@ cudaError_t launch_transpose_bf16_experts(const ExpertSrc& src, int batch, int r
 // with split_sizes, row tiles past the padded segments are skipped.
 cudaError_t launch_transpose_u8(const uint8_t* src, int batch, int rows, int cols, const int* split_sizes, int E,
                                 uint8_t* out, cudaStream_t st);
-cudaError_t launch_dprob_reduce(const float* dp_part, int n_tiles, int64_t cap, const int* row_of, int64_t R,
-                                float* dprob, int* err, cudaStream_t st);
+// dprob[t][j] = the fixed-order sum of the down dgrad's per-tile partial row sums at
+// row_of[t][j]; with src_of (and split_sizes) and many partials it reduces by permuted row.
+cudaError_t launch_dprob_reduce(const float* dp_part, int n_tiles, int64_t cap, const int* split_sizes, int E,
+                                const int* src_of, const int* row_of, int k, int T, float* dprob, int* err,
+                                cudaStream_t st);
 
 // ---- grouped block-scaled MXFP8 GEMM (tcgen05) ------------------------------------
 // C[M][N] = A[M][K] * B[N][K]^T, both operands K-major MX tensors.

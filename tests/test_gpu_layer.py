@@ -149,6 +149,7 @@ def test_tiny_workload_fwd_bwd():
     (600, 128, 128, 256, 8, "biased"),   # the largest E and k: 256 tiny segments, many empty
     (1, 128, 128, 4, 2, "normal"),       # one token
     (100, 128, 256, 4, 4, "normal"),     # k = E: every token in every expert
+    (256, 128, 4096, 4, 2, "normal"),    # 64 dprob partials per row: the reduce splits them over warps
 ])
 def test_small_workloads_fwd_bwd(T, H, I, E, k, routing):
     wl = configs.small(T, H, I, E, k, routing=routing, backward=True)
