@@ -168,6 +168,78 @@ __global__ void __launch_bounds__(NT) route_topk_kernel(
   }
 }
 
+// Many experts: four lanes per token.  Lane s of a token's quad keeps the sorted top-k of
+// experts s, s+4, s+8, ... (ascending, so a quad reads 16 contiguous bytes at a time), then
+// two shuffle rounds merge the quad's lists (partner lane ^1, then ^2): every lane ends with
+// the token's k best in the total order, the same list one lane over all E would hold, so
+// idx and the renormalised probabilities equal route_topk_kernel's bit for bit; without
+// renormalisation lane 0 sums the row's exponentials in expert order, as that kernel does.
+// A 128-thread block is one 32-token group; its masks are gathered in shared memory.
+constexpr int RQ_THREADS = 128;                      // 32 tokens x 4 lanes
+__global__ void __launch_bounds__(RQ_THREADS) route_topk_quad_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int renorm,
+    int* __restrict__ idx, float* __restrict__ prob, uint32_t* __restrict__ masks, int G, int* err) {
+  __shared__ uint32_t smask[kMaxE];
+  const int lane = threadIdx.x & 31, sub = lane & 3;
+  const int tl = threadIdx.x >> 2;                   // token of this quad inside the group (0..31)
+  const int g = blockIdx.x;
+  const int t = g * 32 + tl;
+  for (int e = threadIdx.x; e < E; e += RQ_THREADS) smask[e] = 0u;
+  __syncthreads();
+  float sv[kMaxK];
+  int se[kMaxK];
+#pragma unroll
+  for (int s = 0; s < kMaxK; ++s) {
+    sv[s] = __int_as_float(0x7FFFFFFF);              // NaN with the largest id: below every real entry
+    se[s] = 0x7FFFFFFF;
+  }
+  const float* row = logits + (int64_t)t * E;
+  if (t < T) {
+#pragma unroll 4
+    for (int e = sub; e < E; e += 4) topk_insert(row[e], e, sv, se);
+  }
+#pragma unroll
+  for (int m = 1; m <= 2; m <<= 1) {
+    float pv[kMaxK];
+    int pe[kMaxK];
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s) {
+      pv[s] = __shfl_xor_sync(0xFFFFFFFFu, sv[s], m);
+      pe[s] = __shfl_xor_sync(0xFFFFFFFFu, se[s], m);
+    }
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s)
+      if (s < k) topk_insert(pv[s], pe[s], sv, se);
+  }
+  if (t < T && sub == 0) {
+    const float m = sv[0];
+    float den = 0.f;
+    if (renorm) {
+#pragma unroll
+      for (int s = 0; s < kMaxK; ++s)
+        if (s < k) den += expf(sv[s] - m);
+    } else {
+      for (int e = 0; e < E; ++e) den += expf(row[e] - m);
+    }
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s) {
+      if (s < k) {
+        if (se[s] < 0 || se[s] >= E) {
+          report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_ROUTE);
+          idx[(int64_t)t * k + s] = -1;
+          prob[(int64_t)t * k + s] = 0.f;
+          continue;
+        }
+        idx[(int64_t)t * k + s] = se[s];
+        prob[(int64_t)t * k + s] = expf(sv[s] - m) / den;
+        atomicOr(&smask[se[s]], 1u << tl);
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += RQ_THREADS) masks[(int64_t)e * G + g] = smask[e];
+}
+
 // One CTA per expert: exclusive scan over groups of popc(mask).
 __global__ void __launch_bounds__(1024) permute_scan_kernel(
     const uint32_t* __restrict__ masks, int G, int* __restrict__ bases, int* __restrict__ split_sizes) {
@@ -305,8 +377,11 @@ cudaError_t launch_route_scan(const float* logits, int T, int E, int k, int reno
         logits, T, E, k, renorm, idx, prob, masks, G, err, ticket, bases, split_sizes);
     return cudaGetLastError();
   }
-  route_topk_kernel<RT_THREADS, false><<<(G * 32 + RT_THREADS - 1) / RT_THREADS, RT_THREADS, 0, st>>>(
-      logits, T, E, k, renorm, idx, prob, masks, G, err, nullptr, nullptr, nullptr);
+  if (E >= 32)
+    route_topk_quad_kernel<<<G, RQ_THREADS, 0, st>>>(logits, T, E, k, renorm, idx, prob, masks, G, err);
+  else
+    route_topk_kernel<RT_THREADS, false><<<(G * 32 + RT_THREADS - 1) / RT_THREADS, RT_THREADS, 0, st>>>(
+        logits, T, E, k, renorm, idx, prob, masks, G, err, nullptr, nullptr, nullptr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   permute_scan_kernel<<<E, 1024, 0, st>>>(masks, G, bases, split_sizes);
