@@ -544,10 +544,6 @@ __device__ __forceinline__ uint2 mx_encode8(const float* v, uint32_t c) {
 // instead of holding every step's precomputed address in registers.
 __device__ __forceinline__ void opaque(uint8_t*& p) { asm volatile("" : "+l"(p)); }
 
-// Row-wise codes of eight columns with known scale code c: 8 bytes at p.
-__device__ __forceinline__ void store_row8(const float* v, uint32_t c, uint8_t* p) {
-  *reinterpret_cast<uint2*>(p) = mx_encode8(v, c);
-}
 
 // Along-token quantization: where lane (c = lane/4, g = lane%4) of a warp whose 32 lanes
 // are the rows row_blk0.. writes the codes of column col + c (rows 8g..8g+7 of its block)
