@@ -3,16 +3,22 @@
 // Training for Biological Foundation Models", section "GroupedLinear": the
 // grouped call takes the tokens collected per expert plus split_sizes).
 //
-// Deterministic without sorting and without global atomics:
+// Deterministic without sorting (the results never depend on the order of atomics):
 //   1. route_topk_kernel: one thread per token keeps its k best (logit,
 //      expert) pairs in a sorted register list (exact comparisons, ties to the
 //      lower expert id); the warp then writes, per expert e and 32-token group
-//      g, the bit mask[e][g] of the group's tokens that picked e.
-//   2. permute_scan_kernel: one CTA per expert scans popc(mask[e][g]) over g:
-//      base[e][g] = tokens of e in groups before g; split_sizes[e] = total.
-//   3. permute_scatter_kernel: row of (t, slot) = padded start of e +
-//      base[e][g] + popc(mask[e][g] & lanes below t) -- ascending token order
-//      inside every expert segment.
+//      g, the bit mask[e][g] of the group's tokens that picked e.  With 32 or
+//      more experts and masks past the one-launch bound, route_topk_quad_kernel
+//      does the same with four lanes per token.
+//   2. the per-expert scan of popc(mask[e][g]) over g: base[e][g] = tokens of e
+//      in groups before g; split_sizes[e] = total.  While the masks hold at most
+//      16384 words, the block of route_topk_kernel that takes the last ticket
+//      (one atomicInc per block) runs it in the same launch; past that bound,
+//      permute_scan_kernel, one CTA per expert.
+//   3. the rows: row of (t, slot) = padded start of e + base[e][g] +
+//      popc(mask[e][g] & lanes below t) -- ascending token order inside every
+//      expert segment.  The row quantizer computes them while it gathers x
+//      (quantize.cu); permute_scatter_kernel writes the maps alone.
 #include "kernels.cuh"
 
 namespace moe {
