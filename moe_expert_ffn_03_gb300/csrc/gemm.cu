@@ -46,6 +46,10 @@
 // Every mbarrier wait is bounded; on expiry the CTA records
 // MOE_ERR_DEVICE_TIMEOUT, stops issuing, drains its copies and MMAs, frees
 // TMEM and returns.
+//
+// The file also holds the router's weight gradient on the tensor cores
+// (router_dw_tc_kernel: single-CTA MMAs on MN-major operands, dl as two bf16
+// terms), which shares these PTX wrappers and the bounded waits.
 #include <cuda.h>
 
 #include <atomic>
