@@ -535,8 +535,9 @@ moe_status moe_router_fwd(const moe_dims* d, const void* x, const void* w_r, flo
  *   logits f32 [T][E], idx int32 [T][k], prob f32 [T][k] (from
  *   moe_route_permute), dprob f32 [T][k]; dlogits out f32 [T][E];
  *   dx in/out bf16 [T][H]: dx[t] += sum_e dlogits[t][e] w_r[e] (f32 sum, one
- *   rounding to bf16); dw_r out f32 [E][H] = dlogits^T x, summed over fixed
- *   token chunks in chunk order (deterministic).
+ *   rounding to bf16); dw_r out f32 [E][H] = dlogits^T x on the tensor cores
+ *   (dlogits as two bf16 terms hi + lo, float32-level accuracy), per fixed
+ *   token chunk, the chunks summed in chunk order (deterministic).
  *   workspace: as for grouped_mlp_bwd (moe_workspace_size with training).
  */
 moe_status moe_router_bwd(const moe_dims* d, const void* x, const void* w_r, const float* logits,
