@@ -92,8 +92,7 @@ constexpr int GU_PITCH = 128;
 // Per-tensor E4M3 kinds: 128 K elements per stage, kind::f8f6f4 MMA, no block scales.
 template <int EPI>
 struct Ops {
-  static constexpr bool B16 = (EPI == EPI_B16_OUT || EPI == EPI_B16_FWD_SWIGLU || EPI == EPI_B16_BWD_SWIGLU ||
-                               EPI == EPI_B16_F32_OUT);
+  static constexpr bool B16 = (EPI == EPI_B16_OUT || EPI == EPI_B16_FWD_SWIGLU || EPI == EPI_B16_BWD_SWIGLU);
   static constexpr bool SWIGLU_BWD = (EPI == EPI_BWD_SWIGLU || EPI == EPI_B16_BWD_SWIGLU || EPI == EPI_T8_BWD_SWIGLU);
   static constexpr bool T8 = (EPI == EPI_T8_OUT || EPI == EPI_T8_FWD_SWIGLU || EPI == EPI_T8_BWD_SWIGLU);
   static constexpr bool NOSF = B16 || T8;         // no scale-factor loads or copies
@@ -814,17 +813,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
   __syncwarp();
   if (lane == 0) mbar_arrive_cluster(tmem_empty_c);
 
-  if (EPI == EPI_B16_F32_OUT) {
-    // f32 output [rows_limit][N]: rows past rows_limit and columns past N are not written
-    if (c0 >= ncols || row >= a.rows_limit) return;
-    float* orow = a.out_f32 + row * a.ldo;
-#pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      const int64_t col = tl.n0 + c0 + i;
-      if (col < a.N) orow[col] = have ? __uint_as_float(r[i]) : 0.f;
-    }
-    return;
-  }
   if (EPI == EPI_BF16 || EPI == EPI_B16_OUT || EPI == EPI_T8_OUT) {
     if (c0 >= ncols) return;
     // per-tensor E4M3 operands: dequantize the accumulator with 1/(s_a s_b) of this expert
@@ -1561,6 +1549,152 @@ __global__ void __launch_bounds__(192, 1) router_dw_tc_kernel(const __grid_const
   if (warp == 1) tmem_dealloc_cta(tmem, ncols);
 }
 
+// ---- router logits on the tensor cores ---------------------------------------------------
+// logits[t][e] = sum_h x[t][h] * W_r[e][h] for 128 tokens per CTA: single-CTA MMAs (M = 128,
+// N = roundup(E, 16) experts, f32 accumulation in TMEM), both operands K-major by TMA (x
+// [T][H] and W_r [E][H] as they lie, 64 bf16 of K per 128-byte swizzled row).  The W_r box
+// holds E rows; rows E..N-1 of the staged tile are stale and feed only output columns past
+// E, which are never written.  Bound by reading x once.
+constexpr int RF_KT = 64;                      // K elements (bf16) per stage
+constexpr int RF_M = 128;                      // tokens per CTA
+constexpr int RF_MAX_STG = 8;
+
+struct RouterFwdArgs {
+  int T, E, N;            // N = roundup(E, 16): accumulator columns
+  int nk;                 // 64-wide K chunks (H / 64)
+  int steps;              // K chunks per pipeline stage (more bytes behind each barrier)
+  int stages;             // pipeline depth
+  float* logits;          // [T][E]
+  int* err;
+};
+
+__device__ __forceinline__ uint32_t idesc_bf16_m128(int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(RF_M >> 4) << 24);
+}
+
+__global__ void __launch_bounds__(192, 1) router_fwd_tc_kernel(const __grid_constant__ CUtensorMap mx,
+                                                               const __grid_constant__ CUtensorMap mw,
+                                                               const RouterFwdArgs a) {
+  extern __shared__ uint8_t rf_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rf_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t full[RF_MAX_STG], empty[RF_MAX_STG], done;
+  __shared__ uint32_t tmem_s;
+  __shared__ int abort_flag;
+  volatile int* abort_s = &abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr uint32_t A_BYTES = RF_M * RF_KT * 2;                     // 16 KB
+  const uint32_t b_slot = (uint32_t(a.N) * RF_KT * 2 + 1023u) & ~1023u;   // the N-row tile of a chunk
+  const uint32_t b_bytes = uint32_t(a.E) * RF_KT * 2;                     // what the E-row box brings
+  const uint32_t chunk_bytes = A_BYTES + b_slot;
+  const uint32_t stage_bytes = uint32_t(a.steps) * chunk_bytes;
+  const int n_st = (a.nk + a.steps - 1) / a.steps;                          // pipeline stages of the CTA
+  const uint32_t ncols = a.N <= 32 ? 32u : a.N <= 64 ? 64u : a.N <= 128 ? 128u : 256u;
+  const int t0 = blockIdx.x * RF_M;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&done, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc_cta(&tmem_s, ncols);
+    tmem_relinquish_cta();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_s;
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      prefetch_tmap(&mx);
+      prefetch_tmap(&mw);
+      int last_round[RF_MAX_STG];
+#pragma unroll
+      for (int s = 0; s < RF_MAX_STG; ++s) last_round[s] = -1;
+      bool ok = true;
+      for (int i = 0; i < n_st; ++i) {
+        const int slot = i % a.stages, round = i / a.stages;
+        if (!wait_phase(&empty[slot], (round & 1) ^ 1, abort_s, a.err, SITE_ROUTER_DW + 10, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + size_t(slot) * stage_bytes;
+        const int c0 = i * a.steps, nc = min(a.steps, a.nk - c0);
+        mbar_arrive_expect_tx(&full[slot], uint32_t(nc) * (A_BYTES + b_bytes));
+        for (int c = 0; c < nc; ++c) {
+          tma_load_2d_cta(st + c * chunk_bytes, &mx, (c0 + c) * RF_KT, t0, &full[slot]);
+          tma_load_2d_cta(st + c * chunk_bytes + A_BYTES, &mw, (c0 + c) * RF_KT, 0, &full[slot]);
+        }
+        last_round[slot] = round;
+      }
+      if (!ok) {
+        for (int s = 0; s < a.stages; ++s) {
+          if (last_round[s] < 0) continue;
+          const uint64_t tw = globaltimer_ns();
+          while (!mbar_try_wait(&full[s], last_round[s] & 1) && globaltimer_ns() - tw < 20000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      const uint32_t idesc = idesc_bf16_m128(a.N);
+      for (int i = 0; i < n_st; ++i) {
+        const int slot = i % a.stages, round = i / a.stages;
+        if (!wait_phase(&full[slot], round & 1, abort_s, a.err, SITE_ROUTER_DW + 11, kWaitLimitNs)) break;
+        tc_fence_after();
+        const int c0 = i * a.steps, nc = min(a.steps, a.nk - c0);
+        for (int c = 0; c < nc; ++c) {
+          const uint32_t st = smem_u32(smem + size_t(slot) * stage_bytes + size_t(c) * chunk_bytes);
+          const uint64_t ad = desc_sw128(st);
+          const uint64_t bd = desc_sw128(st + A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < RF_KT / 16; ++kk)
+            // 16 bf16 of K = 32 bytes inside the 128-byte swizzle row = +2 in the encoded address
+            tc_mma_bf16_cta(tmem, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), idesc, (i | c | kk) != 0);
+        }
+        tc_commit_cta(&empty[slot]);
+      }
+      tc_commit_cta(&done);
+    }
+  } else {
+    // ---------------- epilogue warps 2..5: warp w reads TMEM lanes 32*(w%4).. (tokens) ----------------
+    const int q = warp & 3;
+    const int t = t0 + 32 * q + lane;
+    bool ok = wait_phase(&done, 0, abort_s, a.err, SITE_ROUTER_DW + 12, kWaitLimitNs);
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    if (ok) {
+      tc_fence_after();
+      float* orow = a.logits + int64_t(t) * a.E;
+      for (int j0 = 0; j0 < a.N; j0 += 16) {
+        uint32_t r[16];
+        tmem_ld16_async(tmem + (uint32_t(32 * q) << 16) + uint32_t(j0), r);
+        tmem_wait_ld<16>(r);
+        if (t < a.T) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            if (j0 + jj < a.E) orow[j0 + jj] = __uint_as_float(r[jj]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_s) {
+    const uint64_t tw = globaltimer_ns();
+    while (!mbar_try_wait(&done, 0) && globaltimer_ns() - tw < 20000000ull) {
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_cta(tmem, ncols);
+}
+
 // ---- host side -----------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -1720,8 +1854,7 @@ cudaError_t launch_grouped_gemm(int epi, const GemmArgs& args, const void* A, in
     for (int e = a.E; e < kMaxMapExperts; ++e) pe_maps.m[e] = pe_maps.m[0];
   }
   CUtensorMap ma, mb, msfa, msfb;
-  const bool b16 = (epi == EPI_B16_OUT || epi == EPI_B16_FWD_SWIGLU || epi == EPI_B16_BWD_SWIGLU ||
-                    epi == EPI_B16_F32_OUT);
+  const bool b16 = (epi == EPI_B16_OUT || epi == EPI_B16_FWD_SWIGLU || epi == EPI_B16_BWD_SWIGLU);
   const bool t8 = (epi == EPI_T8_OUT || epi == EPI_T8_FWD_SWIGLU || epi == EPI_T8_BWD_SWIGLU);
   if (!encode_map3(&ma, A, a_rows, a_K, b16) || !encode_map3(&mb, B, b_rows, b_K, b16)) {
     snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed (A %lld x %lld, B %lld x %lld)", (long long)a_rows,
@@ -1753,7 +1886,6 @@ cudaError_t launch_grouped_gemm(int epi, const GemmArgs& args, const void* A, in
     case EPI_T8_FWD_SWIGLU: return launch_kind<EPI_T8_FWD_SWIGLU>(ma, mb, msfa, msfb, b_experts != nullptr ? &pe_maps : nullptr, a, grid, st);
     case EPI_B16_BWD_SWIGLU: return launch_kind<EPI_B16_BWD_SWIGLU>(ma, mb, msfa, msfb, b_experts != nullptr ? &pe_maps : nullptr, a, grid, st);
     case EPI_T8_BWD_SWIGLU: return launch_kind<EPI_T8_BWD_SWIGLU>(ma, mb, msfa, msfb, b_experts != nullptr ? &pe_maps : nullptr, a, grid, st);
-    case EPI_B16_F32_OUT: return launch_kind<EPI_B16_F32_OUT>(ma, mb, msfa, msfb, b_experts != nullptr ? &pe_maps : nullptr, a, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1815,6 +1947,55 @@ cudaError_t launch_router_dw_tc(const void* x, const void* dl_hi, const void* dl
   if (e != cudaSuccess) return e;
   router_dw_tc_kernel<<<dim3(unsigned(tiles), unsigned(S)), 192, smem, st>>>(mx, mhi, mlo, a);
   *chunks_used = S;
+  return cudaGetLastError();
+}
+
+
+// ---- router logits: host side --------------------------------------------------------------
+static bool encode_map_bf16_kmajor(CUtensorMap* m, const void* base, int64_t K, int64_t rows, int box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(K * 2)};
+  cuuint32_t box[2] = {cuuint32_t(RF_KT), cuuint32_t(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_router_fwd_tc(const void* x, const void* w, int T, int H, int E, float* logits, int* err,
+                                 cudaStream_t st) {
+  if (T < 1 || E < 1 || E > 256 || H % RF_KT != 0) return cudaErrorInvalidValue;
+  RouterFwdArgs a{};
+  a.T = T;
+  a.E = E;
+  a.N = (E + 15) / 16 * 16;
+  a.nk = H / RF_KT;
+  a.logits = logits;
+  a.err = err;
+  CUtensorMap mx, mw;
+  if (!encode_map_bf16_kmajor(&mx, x, H, T, RF_M) || !encode_map_bf16_kmajor(&mw, w, H, E, E))
+    return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e0 = cudaGetDevice(&dev);
+  if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e0 != cudaSuccess) return e0;
+  // more CTAs than SMs: half the shared memory each, two CTAs per SM, one wave
+  const int ctas = (T + RF_M - 1) / RF_M;
+  const uint32_t budget = ctas > sms ? RDW_SMEM_MAX / 2 : RDW_SMEM_MAX;
+  const uint32_t chunk = uint32_t(RF_M) * RF_KT * 2 + ((uint32_t(a.N) * RF_KT * 2 + 1023u) & ~1023u);
+  // at least three stages, each with as many 64-wide K chunks as fit (at most four)
+  int steps = int(budget / (3 * chunk));
+  steps = steps < 1 ? 1 : steps > 4 ? 4 : steps;
+  a.steps = steps;
+  const uint32_t stage_bytes = uint32_t(steps) * chunk;
+  const int stages = int(budget / stage_bytes);
+  a.stages = stages > RF_MAX_STG ? RF_MAX_STG : stages;
+  const size_t smem = size_t(a.stages) * stage_bytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(router_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  router_fwd_tc_kernel<<<unsigned((T + RF_M - 1) / RF_M), 192, smem, st>>>(mx, mw, a);
   return cudaGetLastError();
 }
 

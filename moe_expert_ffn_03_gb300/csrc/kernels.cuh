@@ -67,6 +67,9 @@ cudaError_t launch_quant_dual_experts(const ExpertSrc& src, int batch, int rows,
 size_t router_ws_bytes(int T, int E, int H);
 int router_dw_cols(int E);
 int router_dw_max_chunks(int H);
+// Router logits [T][E] f32 = x [T][H] . W_r [E][H]^T on the tensor cores (bf16 operands).
+cudaError_t launch_router_fwd_tc(const void* x, const void* w, int T, int H, int E, float* logits, int* err,
+                                 cudaStream_t st);
 cudaError_t launch_router_dw_tc(const void* x, const void* dl_hi, const void* dl_lo, int T, int H, int E,
                                 float* partial, int max_chunks, int* chunks_used, int* err, cudaStream_t st);
 cudaError_t launch_router_fwd(const void* x, const void* w, int T, int H, int E, float* logits, int* err,
@@ -160,8 +163,6 @@ enum Epilogue : int {
   EPI_B16_BWD_SWIGLU = 7,    // bf16 operands; SwiGLU backward writing bf16 dH to out [cap][2I] and out_t [2I][cap]
   EPI_T8_BWD_SWIGLU = 8,     // per-tensor E4M3 operands; SwiGLU backward writing bf16 dH to out [cap][2I]
                              // and raising every expert's amax of dH into amax_out
-  EPI_B16_F32_OUT = 9,       // bf16 operands; f32 out_f32 [rows_limit][N] (rows and columns past the ends
-                             // masked): the router logits
 };
 
 struct GemmArgs {
@@ -194,7 +195,6 @@ struct GemmArgs {
   const uint32_t* amax_a;    // T8 kinds: per-expert amax (float bits) of A's and B's tensors
   const uint32_t* amax_b;
   uint32_t* amax_out;        // EPI_T8_FWD_SWIGLU: per-expert amax of the bf16 `a` (raised, not set)
-  float* out_f32;            // EPI_B16_F32_OUT output, row stride ldo
   int64_t rows_limit;        // mode 0 with split_sizes == nullptr: one segment of this many rows (E = 1)
   int* err;
   bool out_v8;               // set by launch_grouped_gemm: out, out_t and gu are 32-byte aligned (256-bit stores)

@@ -5,15 +5,17 @@
 // the SwiGLU output).  The forward runs on the tensor cores; the backward
 // kernels run on the CUDA cores with fixed summation orders (deterministic
 // results):
-//   forward                 logits = x W_r^T on the tensor cores: the grouped GEMM
-//                           engine with bf16 operands, one segment of T rows,
-//                           N = E, f32 logits (rows and columns past T and E masked);
+//   forward                 logits = x W_r^T on the tensor cores (router_fwd_tc_kernel,
+//                           gemm.cu): 128 tokens per CTA, N = roundup(E, 16), bf16
+//                           operands, f32 logits (rows and columns past T and E masked);
 //   router_dlogits_kernel   one warp per token, straight-through top-k softmax;
 //   router_dx_kernel        dx[t] += sum_e dl[t][e] W_r[e] (bf16 in place);
 //   dW_r                    dl^T x on the tensor cores (router_dw_tc_kernel): dl split
 //                           into two bf16 terms hi + lo by the dlogits kernel, f32
 //                           accumulation per token chunk, chunks summed in chunk order
 //                           by router_dw_reduce_kernel.
+#include <cstdio>
+
 #include "kernels.cuh"
 
 namespace moe {
@@ -124,21 +126,10 @@ size_t router_ws_bytes(int T, int E, int H) {
 
 cudaError_t launch_router_fwd(const void* x, const void* w, int T, int H, int E, float* logits, int* err,
                               cudaStream_t st, char* msg, size_t msg_len) {
-  // one segment of T rows (E = 1 in the grouped engine's terms), N = the router's experts
-  GemmArgs g{};
-  g.mode = 0;
-  g.E = 1;
-  g.split_sizes = nullptr;
-  g.rows_limit = T;
-  g.K = H;
-  g.N = E;
-  g.n_tiles = (E + 255) / 256;
-  g.b_rows_per_expert = E;
-  g.cap = (int64_t(T) + 127) / 128 * 128;
-  g.out_f32 = logits;
-  g.ldo = E;
-  g.err = err;
-  return launch_grouped_gemm(EPI_B16_F32_OUT, g, x, T, H, w, E, H, (g.cap / 128) * g.n_tiles, st, msg, msg_len);
+  // 128 tokens per CTA, N = roundup(E, 16) on single-CTA tensor-core MMAs (gemm.cu)
+  const cudaError_t e = launch_router_fwd_tc(x, w, T, H, E, logits, err, st);
+  if (e != cudaSuccess && msg != nullptr) snprintf(msg, msg_len, "router logits launch failed: %s", cudaGetErrorString(e));
+  return e;
 }
 
 cudaError_t launch_router_bwd(const void* x, const void* w, const float* logits, const int* idx, const float* prob,
