@@ -29,8 +29,11 @@ def f64(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-@pytest.mark.parametrize("T,H,E", [(300, 256, 8), (70, 128, 64), (1000, 384, 256), (16384, 4096, 8)])
+@pytest.mark.parametrize("T,H,E", [(300, 256, 8), (70, 128, 64), (1000, 384, 256), (16384, 4096, 8),
+                                   (257, 128, 5), (130, 640, 100), (40000, 256, 64)])
 def test_router_logits(T, H, E):
+    """Cases with E not a multiple of 16 (the staged W_r tile has stale rows past E, which must
+    not reach a written column), T not a multiple of 128, and more CTAs than SMs."""
     wl = configs.small(T, H, 128, E, 2, backward=False)
     x = synth.make_inputs(wl, 0, device="cuda")["x"]
     w_r = synth.make_router_weight(wl, 0, device="cuda")
