@@ -148,16 +148,6 @@ struct Lay {
 };
 
 // ---- PTX wrappers -------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
 // Cluster helpers.  A shared::cta address of this CTA is also its shared::cluster
 // address; mapa gives the address of the same offset in another CTA of the cluster.
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -176,17 +166,6 @@ __device__ __forceinline__ void cluster_sync() {
 // arrive on an mbarrier anywhere in the cluster (release at cluster scope)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 // Tensor copy into this CTA's shared memory; completion is signalled on the
 // mbarrier at cluster address bar_c, which may sit in the pair's other CTA.
@@ -1793,6 +1772,21 @@ cudaError_t launch_kind(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
 }
 
 }  // namespace
+
+// 2-D map over a row-major bf16 [rows][cols] tensor for four-row gathers: box one row
+// high and box_cols wide, no swizzle (the rows land back to back in shared memory).
+// A row coordinate >= rows reads zeros.
+bool encode_gather_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_cols) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+  cuuint32_t box[2] = {cuuint32_t(box_cols), 1};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 cudaError_t launch_epilogue_quant_selftest(const float* src, int rows, int cols, uint8_t* codes, uint8_t* scales,
                                            uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st) {

@@ -2,6 +2,8 @@
 // ABI in include/moe_ffn.h, implemented in api.cu).
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -54,6 +56,9 @@ struct PermuteRows {
 // -1, prob 0) and the permutation maps, in one launch.
 cudaError_t launch_permute_quant_rows(const void* x, int T, int H, int k, int64_t cap, const PermuteRows& p,
                                       uint8_t* codes, uint8_t* scales, int* err, cudaStream_t st);
+// Tensor map for tile::gather4 loads of a bf16 [rows][cols] tensor (box: one row of
+// box_cols elements); false when the driver's encoder is missing or refuses it.
+bool encode_gather_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_cols);
 cudaError_t launch_quant_colwise(const void* src, const int* src_map, int64_t n_src_rows, int batch, int rows,
                                  int cols, const int* split_sizes, int E, uint8_t* codes_t, uint8_t* scales_t,
                                  int* err, cudaStream_t st);

@@ -182,83 +182,111 @@ __global__ void __launch_bounds__(256) fill_pad_rows_kernel(
 }
 
 // ---------------------------------------------------------------------------------
-// Colwise: blocks of 32 along the row axis, output transposed.  One CTA per
-// 128x128 tile: the tile is staged in shared memory with 16-byte loads, then
-// thread (column c, row block rb) reduces 32 rows, quantizes them and writes
-// 32 contiguous codes of the transposed row c.  The tile's scales form exactly
-// one 512-byte atom of the transposed tensor.
+// Colwise: blocks of 32 along the row axis, output transposed.  One CTA per tile of
+// 128 rows x 64 columns.  Warp 0 fetches the tile's rows with 32 four-row TMA
+// gathers (tile::gather4: one instruction per four source rows, wherever they lie;
+// a padding row's index points one past the source, and the copy fills it with
+// zeros), then thread (column pair c, row block rb) reduces 32 rows of two columns,
+// quantizes them and writes 32 contiguous codes to each of the transposed rows c
+// and c+1.  The small tiles keep twelve CTAs' loads (192 KB) in flight per SM.
+// The tile's scales are half of a 512-byte atom of the transposed tensor: bytes
+// 0..7 (the atom's first 64 columns) or 8..15 of each of its 16-byte rows.
 //   src row of tile row r: src_map ? src_map[r] (-1 -> zero row) : batch*rows + r
-//   split_sizes (optional): rows at or past the padded total are skipped.
+//   split_sizes (optional): row tiles at or past the padded total are skipped.
 // ---------------------------------------------------------------------------------
 constexpr int QC_TILE = 128;
-constexpr int QC_PITCH = QC_TILE + 8;                // bf16 per smem row (16 B pad)
+constexpr int QC_PITCH = QC_TILE + 8;                // bf16 per smem row of the dual kernel (16 B pad)
+constexpr int QG_ROWS = 128, QG_COLS = 64;           // gathered tile
+constexpr int QG_THREADS = 2 * QG_COLS;              // (column pair, row block) tasks: 32 x 4
 
-__global__ void __launch_bounds__(256, 6) quant_colwise_kernel(
-    const __nv_bfloat16* __restrict__ src, const int* __restrict__ src_map, int64_t n_src_rows,
-    int rows, int cols, const int* __restrict__ split_sizes, int E,
-    uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t, int* err, bool v8) {
-  __shared__ __align__(16) __nv_bfloat16 tile[QC_TILE * QC_PITCH];
-  __shared__ __align__(16) uint8_t sc_atom[512];
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int x, const int (&y)[4],
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y[0]), "r"(y[1]), "r"(y[2]),
+        "r"(y[3]), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__global__ void __launch_bounds__(QG_THREADS, 12) quant_colwise_kernel(
+    const __grid_constant__ CUtensorMap src_rows, const int* __restrict__ src_map, int n_src_rows, int rows,
+    int cols, const int* __restrict__ split_sizes, int E, uint8_t* __restrict__ codes_t,
+    uint8_t* __restrict__ scales_t, int* err, bool v8, uint64_t wait_limit_ns) {
+  __shared__ __align__(1024) __nv_bfloat16 tile[QG_ROWS * QG_COLS];
+  __shared__ __align__(16) uint8_t sc_half[256];
+  __shared__ __align__(8) uint64_t bar;
   __shared__ int s_rows_used;
-  const int row0 = blockIdx.x * QC_TILE;
-  const int col0 = blockIdx.y * QC_TILE;
+  const int row0 = blockIdx.x * QG_ROWS;
+  const int col0 = blockIdx.y * QG_COLS;
   const int64_t batch = blockIdx.z;
-  // Thread stages 16-byte chunk c16 of tile rows rbase + 16*it.  The gather
-  // indices are loaded before the padded total is known, so both round trips
-  // overlap; entries past the total are never used.
-  const int c16 = threadIdx.x & 15, rbase = threadIdx.x >> 4;
-  int sr[QC_TILE / 16];
-  if (src_map != nullptr) {
-#pragma unroll
-    for (int it = 0; it < QC_TILE / 16; ++it) sr[it] = src_map[row0 + rbase + 16 * it];
-  }
-  if (split_sizes != nullptr) {
-    if (threadIdx.x < 32) {
-      int acc = 0;
+  if (threadIdx.x < 32) {
+    int acc = rows;
+    if (split_sizes != nullptr) {
+      acc = 0;
       for (int e = threadIdx.x; e < E; e += 32) acc += (split_sizes[e] + 127) & ~127;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-      if (threadIdx.x == 0) s_rows_used = acc;
     }
-    __syncthreads();
-    if (row0 >= s_rows_used) return;
+    if (threadIdx.x == 0) {
+      s_rows_used = acc;
+      mbar_init(&bar, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
   }
-#pragma unroll
-  for (int it = 0; it < QC_TILE / 16; ++it) {
-    const int r = rbase + 16 * it;
-    int64_t s;
+  __syncthreads();
+  if (row0 >= s_rows_used) return;
+  if (threadIdx.x < 32) {
+    // lane l gathers tile rows 4l .. 4l+3
+    int y[4];
     if (src_map != nullptr) {
-      s = sr[it];
-      if (s >= n_src_rows) {
-        report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_QUANT + 2);
-        s = -1;
+      const int4 s4 = reinterpret_cast<const int4*>(src_map + row0)[threadIdx.x];
+      y[0] = s4.x;
+      y[1] = s4.y;
+      y[2] = s4.z;
+      y[3] = s4.w;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (y[j] >= n_src_rows) {
+          report_error(err, MOE_ERR_DEVICE_BOUNDS, SITE_QUANT + 2);
+          y[j] = -1;
+        }
+        if (y[j] < 0) y[j] = n_src_rows;       // past the source: zeros
       }
     } else {
-      s = batch * rows + row0 + r;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) y[j] = int(batch * rows) + row0 + 4 * int(threadIdx.x) + j;
     }
-    const bool valid = s >= 0;
-    cp_async16(&tile[r * QC_PITCH + c16 * 8], valid ? static_cast<const void*>(src + s * cols + col0 + c16 * 8) : src,
-               valid);
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&bar, QG_ROWS * QG_COLS * 2);
+    __syncwarp();
+    tma_gather4(tile + threadIdx.x * 4 * QG_COLS, &src_rows, col0, y, &bar);
   }
-  cp_async_wait_all();
-  __syncthreads();
-  // task: columns (c, c+1) x 32-row block rb -- one per thread
-  {
-    const int c = 2 * (threadIdx.x & 63), rb = threadIdx.x >> 6;
-    const uint32_t* p = reinterpret_cast<const uint32_t*>(&tile[(rb * 32) * QC_PITCH + c]);
-    uint32_t q_lo[8], q_hi[8];
-    const uint32_t sc = mx_quant32_bf16_colpair(p, QC_PITCH / 2, q_lo, q_hi);
-    const int64_t drow = batch * cols + col0 + c;    // row of the transposed tensor
-    store_codes32(codes_t + drow * rows + row0 + rb * 32, q_lo, v8);
-    store_codes32(codes_t + (drow + 1) * rows + row0 + rb * 32, q_hi, v8);
-    sc_atom[((c & 31) << 4) + (((c >> 5) & 3) << 2) + rb] = uint8_t(sc);
-    sc_atom[(((c + 1) & 31) << 4) + ((((c + 1) >> 5) & 3) << 2) + rb] = uint8_t(sc >> 8);
+  // bounded wait for the tile (the only copies this CTA issues)
+  if (!mbar_try_wait(&bar, 0)) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(&bar, 0)) {
+      if (globaltimer_ns() - t0 > wait_limit_ns) {
+        report_error(err, MOE_ERR_DEVICE_TIMEOUT, SITE_QUANT + 3);
+        return;
+      }
+    }
   }
+  const int c = 2 * (threadIdx.x & 31), rb = threadIdx.x >> 5;
+  const uint32_t* p = reinterpret_cast<const uint32_t*>(&tile[(rb * 32) * QG_COLS + c]);
+  uint32_t q_lo[8], q_hi[8];
+  const uint32_t sc = mx_quant32_bf16_colpair(p, QG_COLS / 2, q_lo, q_hi);
+  const int64_t drow = batch * cols + col0 + c;          // row of the transposed tensor
+  store_codes32(codes_t + drow * rows + row0 + rb * 32, q_lo, v8);
+  store_codes32(codes_t + (drow + 1) * rows + row0 + rb * 32, q_hi, v8);
+  // atom byte of (column cc of the atom's 128, row block rb): 16 (cc & 31) + 4 ((cc >> 5) & 3) + rb;
+  // here (cc >> 5) & 3 = 2 [col0 & 64] + (c >> 5), so the tile fills 8 bytes of each 16-byte row
+  sc_half[((c & 31) << 3) + ((c >> 5) << 2) + rb] = uint8_t(sc);
+  sc_half[(((c + 1) & 31) << 3) + (((c + 1) >> 5) << 2) + rb] = uint8_t(sc >> 8);
   __syncthreads();
-  // the tile's scales are exactly one 512-byte atom of the transposed tensor
   if (threadIdx.x < 32) {
     const int64_t atom = ((batch * cols + col0) >> 7) * (rows >> 7) + (row0 >> 7);
-    reinterpret_cast<uint4*>(scales_t + (atom << 9))[threadIdx.x] = reinterpret_cast<const uint4*>(sc_atom)[threadIdx.x];
+    *reinterpret_cast<uint2*>(scales_t + (atom << 9) + (threadIdx.x << 4) + ((col0 & 64) >> 3)) =
+        reinterpret_cast<const uint2*>(sc_half)[threadIdx.x];
   }
 }
 
@@ -375,9 +403,15 @@ cudaError_t launch_fill_pad_rows(const int* split_sizes, int E, int cols, int64_
 cudaError_t launch_quant_colwise(const void* src, const int* src_map, int64_t n_src_rows, int batch, int rows,
                                  int cols, const int* split_sizes, int E, uint8_t* codes_t, uint8_t* scales_t,
                                  int* err, cudaStream_t st) {
-  dim3 grid(rows / QC_TILE, cols / QC_TILE, batch);
-  quant_colwise_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), src_map, n_src_rows, rows,
-                                             cols, split_sizes, E, codes_t, scales_t, err, aligned32(codes_t));
+  if (rows <= 0 || cols <= 0 || batch <= 0) return cudaSuccess;
+  // row coordinates of the gathers (and the one-past-the-end zero row) are 32-bit
+  if (n_src_rows >= (int64_t(1) << 31) - 1 || rows % QG_ROWS != 0 || cols % QG_COLS != 0)
+    return cudaErrorInvalidValue;
+  CUtensorMap m;
+  if (!encode_gather_rows_map(&m, src, n_src_rows, cols, QG_COLS)) return cudaErrorInvalidValue;
+  dim3 grid(rows / QG_ROWS, cols / QG_COLS, batch);
+  quant_colwise_kernel<<<grid, QG_THREADS, 0, st>>>(m, src_map, int(n_src_rows), rows, cols, split_sizes, E, codes_t,
+                                                    scales_t, err, aligned32(codes_t), kWaitLimitNs);
   return cudaGetLastError();
 }
 

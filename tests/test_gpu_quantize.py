@@ -69,6 +69,22 @@ def test_colwise_every_bf16_pattern(seed):
     assert np.array_equal(got_c, ref_c.T)
 
 
+def test_colwise_many_tiles():
+    """A 16384 x 1024 matrix along its rows: 2048 gathered tiles of 128 x 64, each filling
+    one half of its scale atoms.  Random bf16 bit patterns (NaN, Inf, zeros and
+    subnormals among them) and whole NaN and subnormal blocks, compared with the oracle."""
+    rows, cols = 16384, 1024
+    bits = np.random.default_rng(11).integers(0, 65536, size=(rows, cols), dtype=np.uint32)
+    bits[:32, :5] = 0x7FC0                                        # whole NaN blocks
+    bits[32:64, 7] = 0x0001                                       # a block of the smallest subnormal
+    x = bf16_from_bits(bits)
+    codes, scales = run_quant(x, 1, rows, cols, 1)
+    with np.errstate(invalid="ignore"):
+        ref_c, ref_s = mx.quantize_blocks(as_f64(x), axis=0)
+    assert np.array_equal(untile_scales(scales, cols, rows), ref_s.T)
+    assert np.array_equal(codes.reshape(cols, rows), ref_c.T)
+
+
 @pytest.mark.parametrize("scale_pow", [-60, -20, 0, 12])
 def test_batched_weights_both_axes(scale_pow):
     E, R, C = 3, 256, 384
