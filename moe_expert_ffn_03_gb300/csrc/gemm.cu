@@ -1282,11 +1282,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // block (bx*4 + w) of an f32 [rows][cols] tensor, each lane one row's 32 values, exactly
 // as an epilogue warp holds them, and calls the epilogue's row-wise and along-token
 // quantizers on them.
+// RTO: the row-wise codes the way the SwiGLU backward's pass B makes them: the scale from
+// the float block maximum, the values through a g,u staging slot as bf16 rounded to odd
+// (the epilogue's own store and load), then encoded; no along-token copy.
 constexpr int EQ_WARPS = 4;
+template <bool RTO>
 __global__ void __launch_bounds__(32 * EQ_WARPS) epilogue_quant_selftest_kernel(
     const float* __restrict__ src, int rows, int cols, uint8_t* codes, uint8_t* scales, uint8_t* codes_t,
     uint8_t* scales_t) {
   __shared__ float tr_all[EQ_WARPS * TR_WARP_FLOATS];
+  __shared__ __align__(16) uint8_t gu_all[RTO ? EQ_WARPS * 32 * GU_PITCH : 16];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t blk = int64_t(blockIdx.x) * EQ_WARPS + warp;
   const int cb = cols / 32;
@@ -1303,6 +1308,28 @@ __global__ void __launch_bounds__(32 * EQ_WARPS) epilogue_quant_selftest_kernel(
     v[4 * i + 1] = q.y;
     v[4 * i + 2] = q.z;
     v[4 * i + 3] = q.w;
+  }
+  if (RTO) {
+    uint8_t* gu_s = gu_all + (warp * 32 + lane) * GU_PITCH;
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) amax = amax_raise(amax, v[i], v[i + 1]);
+    const uint32_t c = mx_scale_code(__float_as_uint(amax));
+    uint32_t q[8];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float vg[8], vu[8];
+      store_dgdu_chunk(gu_s, j, lane, v + 16 * j, v + 16 * j + 8);
+      load_dgdu_chunk(gu_s, j, lane, vg, vu);
+      const uint2 eg = mx_encode8(vg, c), eu = mx_encode8(vu, c);
+      q[4 * j] = eg.x;
+      q[4 * j + 1] = eg.y;
+      q[4 * j + 2] = eu.x;
+      q[4 * j + 3] = eu.y;
+    }
+    st_global_v8(codes + row * cols + col, q);
+    scales[sf_offset(row, col >> 5, cols)] = uint8_t(c);
+    return;
   }
   quant_row_block(v, codes, scales, row, col, cols);
   quant_col_block(v, codes_t, scales_t, row_blk0, col, rows, lane, tr_all + warp * TR_WARP_FLOATS);
@@ -1828,8 +1855,17 @@ cudaError_t launch_epilogue_quant_selftest(const float* src, int rows, int cols,
                                            uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st) {
   const int64_t blocks = int64_t(rows / 32) * (cols / 32);
   const int64_t grid = (blocks + EQ_WARPS - 1) / EQ_WARPS;
-  epilogue_quant_selftest_kernel<<<unsigned(grid), 32 * EQ_WARPS, 0, st>>>(src, rows, cols, codes, scales, codes_t,
-                                                                           scales_t);
+  epilogue_quant_selftest_kernel<false><<<unsigned(grid), 32 * EQ_WARPS, 0, st>>>(src, rows, cols, codes, scales,
+                                                                                  codes_t, scales_t);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_epilogue_quant_rto_selftest(const float* src, int rows, int cols, uint8_t* codes, uint8_t* scales,
+                                               cudaStream_t st) {
+  const int64_t blocks = int64_t(rows / 32) * (cols / 32);
+  const int64_t grid = (blocks + EQ_WARPS - 1) / EQ_WARPS;
+  epilogue_quant_selftest_kernel<true><<<unsigned(grid), 32 * EQ_WARPS, 0, st>>>(src, rows, cols, codes, scales,
+                                                                                 nullptr, nullptr);
   return cudaGetLastError();
 }
 
