@@ -13,6 +13,8 @@ template <bool V8>
 __global__ void __launch_bounds__(256) combine_kernel(
     const __nv_bfloat16* __restrict__ y, const int* __restrict__ row_of, const float* __restrict__ prob,
     int T, int k, int H, int64_t cap, __nv_bfloat16* __restrict__ out, int* err) {
+  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
@@ -69,6 +71,8 @@ __global__ void __launch_bounds__(256) combine_kernel(
 __global__ void __launch_bounds__(256) dprob_reduce_kernel(
     const float* __restrict__ dp_part, int n_tiles, int64_t cap, const int* __restrict__ row_of, int64_t R,
     float* __restrict__ dprob, int* err) {
+  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_launch_dependents();
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= R) return;
   const int r = row_of[i];
@@ -92,6 +96,8 @@ __global__ void __launch_bounds__(32 * DPR_WARPS) dprob_reduce_rows_kernel(
     const float* __restrict__ dp_part, int n_tiles, int64_t cap, const int* __restrict__ split_sizes, int E,
     const int* __restrict__ src_of, const int* __restrict__ row_of, int k, int T, float* __restrict__ dprob,
     int* err) {
+  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_launch_dependents();
   __shared__ int64_t total_s;
   __shared__ float part[DPR_WARPS][32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -193,9 +199,11 @@ cudaError_t launch_combine(const void* y, const int* row_of, const float* prob, 
   const __nv_bfloat16* yb = static_cast<const __nv_bfloat16*>(y);
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out);
   if (aligned32(y) && aligned32(out) && H % 16 == 0)
-    combine_kernel<true><<<grid, 256, 0, st>>>(yb, row_of, prob, T, k, H, cap, ob, err);
+    launch_pdl(combine_kernel<true>, dim3(grid), dim3(256), 0, st,
+               yb, row_of, prob, T, k, H, cap, ob, err);
   else
-    combine_kernel<false><<<grid, 256, 0, st>>>(yb, row_of, prob, T, k, H, cap, ob, err);
+    launch_pdl(combine_kernel<false>, dim3(grid), dim3(256), 0, st,
+               yb, row_of, prob, T, k, H, cap, ob, err);
   return cudaGetLastError();
 }
 
@@ -203,11 +211,12 @@ cudaError_t launch_dprob_reduce(const float* dp_part, int n_tiles, int64_t cap, 
                                 const int* src_of, const int* row_of, int k, int T, float* dprob, int* err,
                                 cudaStream_t st) {
   if (src_of != nullptr && n_tiles >= 64) {
-    dprob_reduce_rows_kernel<<<unsigned((cap + 31) / 32), 32 * DPR_WARPS, 0, st>>>(
-        dp_part, n_tiles, cap, split_sizes, E, src_of, row_of, k, T, dprob, err);
+    launch_pdl(dprob_reduce_rows_kernel, dim3(unsigned((cap + 31) / 32)), dim3(32 * DPR_WARPS), 0, st,
+               dp_part, n_tiles, cap, split_sizes, E, src_of, row_of, k, T, dprob, err);
   } else {
     const int64_t R = int64_t(T) * k;
-    dprob_reduce_kernel<<<unsigned((R + 255) / 256), 256, 0, st>>>(dp_part, n_tiles, cap, row_of, R, dprob, err);
+    launch_pdl(dprob_reduce_kernel, dim3(unsigned((R + 255) / 256)), dim3(256), 0, st,
+               dp_part, n_tiles, cap, row_of, R, dprob, err);
   }
   return cudaGetLastError();
 }

@@ -202,6 +202,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: every bounded wait gives up after this
 
+// ---- programmatic dependent launch --------------------------------------------------
+// A kernel launched with programmatic stream serialization (launch_pdl) may start while
+// the kernel before it in the stream is still running.  pdl_wait() returns once that
+// kernel has completed and its memory operations are visible; every such kernel calls
+// it before its first access to global memory that an earlier kernel may write or read.
+// pdl_launch_dependents() lets the next kernel's CTAs be scheduled once every CTA of
+// this one has called it or exited.  Both are no-ops in a kernel launched without the
+// attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- mbarriers (this CTA's shared memory) ----------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

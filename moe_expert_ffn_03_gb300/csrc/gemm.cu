@@ -1067,17 +1067,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     mbar_init(drain, 1);
     *abort_s = 0;
-    int acc = 0, acc_pb = 0;
-    for (int e = 0; e < args.E; ++e) {
-      seg[e] = acc;
-      seg[SEG_PB + e] = acc_pb;
-      const int rows_e = args.split_sizes != nullptr ? args.split_sizes[e] : int(args.rows_limit);
-      const int nblk = (rows_e + 127) >> 7;
-      acc += nblk;
-      acc_pb += (nblk + 1) >> 1;
-    }
-    seg[args.E] = acc;
-    seg[SEG_PB + args.E] = acc_pb;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && lane == 0) {
@@ -1091,6 +1080,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 1) {
     tmem_alloc(tmem_base_s, TMEM_COLS);          // collectively with the peer CTA
     tmem_relinquish();
+  }
+  // Everything above touches only this CTA's shared memory, TMEM and the parameters, so it
+  // overlaps the end of the previous kernel (programmatic stream serialization); from here
+  // on the kernel reads what earlier kernels wrote.  The next kernel is let in once every
+  // CTA's producer has issued its last copy (or the CTA has exited): its CTAs then arrive
+  // during this kernel's last tiles.
+  pdl_wait();
+  if (threadIdx.x == 0) {
+    int acc = 0, acc_pb = 0;
+    for (int e = 0; e < args.E; ++e) {
+      seg[e] = acc;
+      seg[SEG_PB + e] = acc_pb;
+      const int rows_e = args.split_sizes != nullptr ? args.split_sizes[e] : int(args.rows_limit);
+      const int nblk = (rows_e + 127) >> 7;
+      acc += nblk;
+      acc_pb += (nblk + 1) >> 1;
+    }
+    seg[args.E] = acc;
+    seg[SEG_PB + args.E] = acc_pb;
   }
   tc_fence_before();
   __syncthreads();
@@ -1158,6 +1166,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         cur = nxt;
       }
+      pdl_launch_dependents();
       if (!ok && issued_any) {
         // let copies already issued land before the CTA exits: the leader watches the full
         // barriers (which also count the peer's copies); the peer, whose copies signal the
@@ -1809,13 +1818,15 @@ cudaError_t launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = Lay<EPI>::SMEM_BYTES;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // the kernel calls pdl_wait()
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<EPI, PE>, ma, mb, msfa, msfb, bmaps, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -4,9 +4,33 @@
 
 #include <cuda.h>
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace moe {
+
+// Launch with programmatic stream serialization: the kernel may begin (and run up to its
+// pdl_wait()) while the previous kernel in the stream finishes.  Only for kernels that call
+// pdl_wait() before touching global memory an earlier kernel may write or read.  A grid of
+// more than kPdlMaxCtas CTAs runs in many waves, and starting its first one early gains
+// nothing: it is launched the ordinary way (pdl_wait() then returns at once).
+constexpr int64_t kPdlMaxCtas = 2048;
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = int64_t(grid.x) * grid.y * grid.z <= kPdlMaxCtas ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Per-thread text of the last host-side error, returned by moe_last_error_message().
 constexpr size_t kLastErrorBytes = 512;

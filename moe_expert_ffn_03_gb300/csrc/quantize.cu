@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(
     const int* __restrict__ row_of, int k, int64_t cap,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int* err, bool v8_src, bool v8_dst,
     const int* __restrict__ pad_split, int pad_E, int token_blocks, PermuteRows pr) {
+  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_launch_dependents();
   if (pad_split != nullptr && int(blockIdx.x) >= token_blocks) {
     const int pb = blockIdx.x - token_blocks;
     fill_pad_rows_block(pad_split, pad_E, cols, cap, codes, scales, MODE == ROW_PERMUTE ? pr.src_of : nullptr,
@@ -178,6 +180,8 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(
 __global__ void __launch_bounds__(256) fill_pad_rows_kernel(
     const int* __restrict__ split_sizes, int E, int cols, int64_t cap,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int* err) {
+  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_launch_dependents();
   fill_pad_rows_block(split_sizes, E, cols, cap, codes, scales, nullptr, nullptr, err, blockIdx.x, blockIdx.y);
 }
 
@@ -213,6 +217,8 @@ __global__ void __launch_bounds__(QG_THREADS, 12) quant_colwise_kernel(
     const __grid_constant__ CUtensorMap src_rows, const int* __restrict__ src_map, int n_src_rows, int rows,
     int cols, const int* __restrict__ split_sizes, int E, uint8_t* __restrict__ codes_t,
     uint8_t* __restrict__ scales_t, int* err, bool v8, uint64_t wait_limit_ns) {
+  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_launch_dependents();
   __shared__ __align__(1024) __nv_bfloat16 tile[QG_ROWS * QG_COLS];
   __shared__ __align__(16) uint8_t sc_half[256];
   __shared__ __align__(8) uint64_t bar;
@@ -302,6 +308,8 @@ template <class Src>
 __global__ void __launch_bounds__(256, 6) quant_dual_kernel(
     const __grid_constant__ Src src, int rows, int cols, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t, bool v8) {
+  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_launch_dependents();
   __shared__ __align__(16) __nv_bfloat16 tile[QC_TILE * QC_PITCH];
   __shared__ __align__(16) uint8_t sc_row[512];
   __shared__ __align__(16) uint8_t sc_col[512];
@@ -375,11 +383,13 @@ cudaError_t launch_quant_rowwise(const void* src, int64_t n_rows, int cols, cons
   const bool v8s = aligned32(src), v8d = aligned32(codes);
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(src);
   if (row_of != nullptr)
-    quant_rowwise_kernel<ROW_GIVEN><<<grid, 256, 0, st>>>(x, n_rows, cols, row_of, k, cap, codes, scales, err, v8s,
-                                                          v8d, pad_split, pad_E, int(token_blocks), PermuteRows{});
+    launch_pdl(quant_rowwise_kernel<ROW_GIVEN>, dim3(grid), dim3(256), 0, st,
+               x, n_rows, cols, row_of, k, cap, codes, scales, err, v8s, v8d, pad_split, pad_E, int(token_blocks),
+               PermuteRows{});
   else
-    quant_rowwise_kernel<ROW_SELF><<<grid, 256, 0, st>>>(x, n_rows, cols, nullptr, 1, cap, codes, scales, err, v8s,
-                                                         v8d, pad_split, pad_E, int(token_blocks), PermuteRows{});
+    launch_pdl(quant_rowwise_kernel<ROW_SELF>, dim3(grid), dim3(256), 0, st,
+               x, n_rows, cols, nullptr, 1, cap, codes, scales, err, v8s, v8d, pad_split, pad_E, int(token_blocks),
+               PermuteRows{});
   return cudaGetLastError();
 }
 
@@ -388,15 +398,16 @@ cudaError_t launch_permute_quant_rows(const void* x, int T, int H, int k, int64_
   if (p.E < 1 || p.E > kMaxExperts || k < 1 || k > 8) return cudaErrorInvalidValue;
   const int64_t token_blocks = (int64_t(T) * 32 + 255) / 256;
   const unsigned grid = unsigned(token_blocks + int64_t(p.E) * FP_SLICES);
-  quant_rowwise_kernel<ROW_PERMUTE><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), T, H, nullptr, k,
-                                                          cap, codes, scales, err, aligned32(x), aligned32(codes),
-                                                          p.split_sizes, p.E, int(token_blocks), p);
+  launch_pdl(quant_rowwise_kernel<ROW_PERMUTE>, dim3(grid), dim3(256), 0, st,
+             static_cast<const __nv_bfloat16*>(x), T, H, nullptr, k, cap, codes, scales, err, aligned32(x),
+             aligned32(codes), p.split_sizes, p.E, int(token_blocks), p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fill_pad_rows(const int* split_sizes, int E, int cols, int64_t cap, uint8_t* codes,
                                  uint8_t* scales, int* err, cudaStream_t st) {
-  fill_pad_rows_kernel<<<dim3(E, FP_SLICES), 256, 0, st>>>(split_sizes, E, cols, cap, codes, scales, err);
+  launch_pdl(fill_pad_rows_kernel, dim3(E, FP_SLICES), dim3(256), 0, st,
+             split_sizes, E, cols, cap, codes, scales, err);
   return cudaGetLastError();
 }
 
@@ -410,8 +421,9 @@ cudaError_t launch_quant_colwise(const void* src, const int* src_map, int64_t n_
   CUtensorMap m;
   if (!encode_gather_rows_map(&m, src, n_src_rows, cols, QG_COLS)) return cudaErrorInvalidValue;
   dim3 grid(rows / QG_ROWS, cols / QG_COLS, batch);
-  quant_colwise_kernel<<<grid, QG_THREADS, 0, st>>>(m, src_map, int(n_src_rows), rows, cols, split_sizes, E, codes_t,
-                                                    scales_t, err, aligned32(codes_t), kWaitLimitNs);
+  launch_pdl(quant_colwise_kernel, dim3(grid), dim3(QG_THREADS), 0, st,
+             m, src_map, int(n_src_rows), rows, cols, split_sizes, E, codes_t, scales_t, err, aligned32(codes_t),
+             kWaitLimitNs);
   return cudaGetLastError();
 }
 
@@ -419,16 +431,16 @@ cudaError_t launch_quant_dual(const void* src, int batch, int rows, int cols, ui
                               uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st) {
   dim3 grid(rows / QC_TILE, cols / QC_TILE, batch);
   const StackedSrc s{static_cast<const __nv_bfloat16*>(src), int64_t(rows) * cols};
-  quant_dual_kernel<StackedSrc><<<grid, 256, 0, st>>>(s, rows, cols, codes, scales, codes_t, scales_t,
-                                                      aligned32(codes) && aligned32(codes_t));
+  launch_pdl(quant_dual_kernel<StackedSrc>, dim3(grid), dim3(256), 0, st,
+             s, rows, cols, codes, scales, codes_t, scales_t, aligned32(codes) && aligned32(codes_t));
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_dual_experts(const ExpertSrc& src, int batch, int rows, int cols, uint8_t* codes,
                                       uint8_t* scales, uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st) {
   dim3 grid(rows / QC_TILE, cols / QC_TILE, batch);
-  quant_dual_kernel<ExpertSrc><<<grid, 256, 0, st>>>(src, rows, cols, codes, scales, codes_t, scales_t,
-                                                     aligned32(codes) && aligned32(codes_t));
+  launch_pdl(quant_dual_kernel<ExpertSrc>, dim3(grid), dim3(256), 0, st,
+             src, rows, cols, codes, scales, codes_t, scales_t, aligned32(codes) && aligned32(codes_t));
   return cudaGetLastError();
 }
 

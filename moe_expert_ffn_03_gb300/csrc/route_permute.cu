@@ -103,6 +103,8 @@ __global__ void __launch_bounds__(NT) route_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renorm,
     int* __restrict__ idx, float* __restrict__ prob, uint32_t* __restrict__ masks, int G, int* err,
     unsigned* ticket, int* __restrict__ bases, int* __restrict__ split_sizes) {
+  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_launch_dependents();
   __shared__ uint32_t smask[NT / 32][kMaxE];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int t = blockIdx.x * NT + threadIdx.x;
@@ -185,6 +187,8 @@ constexpr int RQ_THREADS = 128;                      // 32 tokens x 4 lanes
 __global__ void __launch_bounds__(RQ_THREADS) route_topk_quad_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renorm,
     int* __restrict__ idx, float* __restrict__ prob, uint32_t* __restrict__ masks, int G, int* err) {
+  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_launch_dependents();
   __shared__ uint32_t smask[kMaxE];
   const int lane = threadIdx.x & 31, sub = lane & 3;
   const int tl = threadIdx.x >> 2;                   // token of this quad inside the group (0..31)
@@ -249,6 +253,8 @@ __global__ void __launch_bounds__(RQ_THREADS) route_topk_quad_kernel(
 // One CTA per expert: exclusive scan over groups of popc(mask).
 __global__ void __launch_bounds__(1024) permute_scan_kernel(
     const uint32_t* __restrict__ masks, int G, int* __restrict__ bases, int* __restrict__ split_sizes) {
+  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_launch_dependents();
   __shared__ int warp_sums[32];
   __shared__ int carry_s;
   const int e = blockIdx.x;
@@ -292,6 +298,8 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
     const uint32_t* __restrict__ masks, const int* __restrict__ bases, const int* __restrict__ split_sizes,
     int* __restrict__ row_of, int* __restrict__ src_of, float* __restrict__ prob_perm, int token_blocks,
     int* err) {
+  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_launch_dependents();
   __shared__ int seg_start[kMaxE + 1];
   if (threadIdx.x == 0) {
     int acc = 0;
@@ -334,6 +342,8 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
 // An id outside 0..E-1 is recorded and its slot skipped (the scatter marks it -1).
 __global__ void __launch_bounds__(RT_THREADS) idx_masks_kernel(const int* __restrict__ idx, int T, int E, int k,
                                                                uint32_t* __restrict__ masks, int G, int* err) {
+  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_launch_dependents();
   __shared__ uint32_t smask[RT_THREADS / 32][kMaxE];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int t = blockIdx.x * RT_THREADS + threadIdx.x;
@@ -359,15 +369,17 @@ cudaError_t launch_permute_from_idx(const int* idx, const float* prob, int T, in
                                     int* bases, int* split_sizes, int* row_of, int* src_of, float* prob_perm,
                                     int* err, cudaStream_t st) {
   const int G = (T + 31) / 32;
-  idx_masks_kernel<<<(G * 32 + RT_THREADS - 1) / RT_THREADS, RT_THREADS, 0, st>>>(idx, T, E, k, masks, G, err);
+  launch_pdl(idx_masks_kernel, dim3((G * 32 + RT_THREADS - 1) / RT_THREADS), dim3(RT_THREADS), 0, st,
+             idx, T, E, k, masks, G, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  permute_scan_kernel<<<E, 1024, 0, st>>>(masks, G, bases, split_sizes);
+  launch_pdl(permute_scan_kernel, dim3(E), dim3(1024), 0, st,
+             masks, G, bases, split_sizes);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int token_blocks = (T + 255) / 256;
-  permute_scatter_kernel<<<token_blocks + E, 256, 0, st>>>(idx, prob, T, k, E, G, masks, bases, split_sizes,
-                                                           row_of, src_of, prob_perm, token_blocks, err);
+  launch_pdl(permute_scatter_kernel, dim3(token_blocks + E), dim3(256), 0, st,
+             idx, prob, T, k, E, G, masks, bases, split_sizes, row_of, src_of, prob_perm, token_blocks, err);
   return cudaGetLastError();
 }
 
@@ -379,18 +391,22 @@ cudaError_t launch_route_scan(const float* logits, int T, int E, int k, int reno
                               cudaStream_t st) {
   const int G = (T + 31) / 32;
   if (route_scan_fused(T, E)) {
-    route_topk_kernel<RS_THREADS, true><<<(G * 32 + RS_THREADS - 1) / RS_THREADS, RS_THREADS, 0, st>>>(
-        logits, T, E, k, renorm, idx, prob, masks, G, err, ticket, bases, split_sizes);
+    launch_pdl(route_topk_kernel<RS_THREADS, true>, dim3((G * 32 + RS_THREADS - 1) / RS_THREADS), dim3(RS_THREADS),
+               0, st,
+               logits, T, E, k, renorm, idx, prob, masks, G, err, ticket, bases, split_sizes);
     return cudaGetLastError();
   }
   if (E >= 32)
-    route_topk_quad_kernel<<<G, RQ_THREADS, 0, st>>>(logits, T, E, k, renorm, idx, prob, masks, G, err);
+    launch_pdl(route_topk_quad_kernel, dim3(G), dim3(RQ_THREADS), 0, st,
+               logits, T, E, k, renorm, idx, prob, masks, G, err);
   else
-    route_topk_kernel<RT_THREADS, false><<<(G * 32 + RT_THREADS - 1) / RT_THREADS, RT_THREADS, 0, st>>>(
-        logits, T, E, k, renorm, idx, prob, masks, G, err, nullptr, nullptr, nullptr);
+    launch_pdl(route_topk_kernel<RT_THREADS, false>, dim3((G * 32 + RT_THREADS - 1) / RT_THREADS), dim3(RT_THREADS),
+               0, st,
+               logits, T, E, k, renorm, idx, prob, masks, G, err, nullptr, nullptr, nullptr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  permute_scan_kernel<<<E, 1024, 0, st>>>(masks, G, bases, split_sizes);
+  launch_pdl(permute_scan_kernel, dim3(E), dim3(1024), 0, st,
+             masks, G, bases, split_sizes);
   return cudaGetLastError();
 }
 
@@ -401,8 +417,8 @@ cudaError_t launch_route_permute(const float* logits, int T, int E, int k, int r
   cudaError_t e = launch_route_scan(logits, T, E, k, renorm, idx, prob, masks, bases, split_sizes, ticket, err, st);
   if (e != cudaSuccess) return e;
   const int token_blocks = (T + 255) / 256;
-  permute_scatter_kernel<<<token_blocks + E, 256, 0, st>>>(idx, prob, T, k, E, G, masks, bases, split_sizes,
-                                                           row_of, src_of, prob_perm, token_blocks, err);
+  launch_pdl(permute_scatter_kernel, dim3(token_blocks + E), dim3(256), 0, st,
+             idx, prob, T, k, E, G, masks, bases, split_sizes, row_of, src_of, prob_perm, token_blocks, err);
   return cudaGetLastError();
 }
 
