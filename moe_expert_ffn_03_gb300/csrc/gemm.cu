@@ -691,15 +691,18 @@ __device__ __forceinline__ void stage_gu(const GemmArgs& a, int64_t row, int64_t
 }
 
 // dA of chunk j of half h of an epilogue warp's 64 columns: columns 0..15 are in registers
-// r, columns 16..63 in the warp's TMEM stash.
-__device__ __forceinline__ void da_chunk(const uint32_t* r, uint32_t stash, int h, int j, uint32_t* d) {
+// r, columns 16..63 in the warp's TMEM stash.  da_issue starts the chunk's load (a copy for
+// the register chunks); da_land waits for it, so the load can run under other work.
+__device__ __forceinline__ void da_issue(const uint32_t* r, uint32_t stash, int h, int j, uint32_t* d) {
   if (h == 0 && j < 2) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) d[i] = r[8 * j + i];
   } else {
     tmem_ld8_async(stash + uint32_t(8 * (4 * h + j - 2)), d);
-    tmem_wait_ld<8>(d);
   }
+}
+__device__ __forceinline__ void da_land(int h, int j, uint32_t* d) {
+  if (!(h == 0 && j < 2)) tmem_wait_ld<8>(d);
 }
 
 // Chunk j (columns 8j..8j+7 of the half starting at col) of this lane's g and u into its
@@ -921,10 +924,15 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
         float amax_g = 0.f, amax_u = 0.f;
         ColDst dst_g = col_dst(a.q_col, a.q_col_s, row_blk0, col, a.cap, lane);
         ColDst dst_u = col_dst(a.q_col, a.q_col_s, row_blk0, a.I + col, a.cap, lane);
+        uint32_t dn[8];                                    // the next chunk's dA, loaded ahead
+        da_issue(r, stash, h, 0, dn);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
+          da_land(h, j, dn);
           uint32_t d[8];
-          da_chunk(r, stash, h, j, d);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) d[i] = dn[i];
+          if (j < 3) da_issue(r, stash, h, j + 1, dn);     // in flight during this chunk's work
           float vg[8], vu[8];
           swiglu_bwd_chunk(d, gu_s, j, lane, p2, vg, vu, &dp2);
           store_dgdu_chunk(gu_s, j, lane, vg, vu);
