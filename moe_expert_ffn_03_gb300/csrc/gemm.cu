@@ -792,17 +792,17 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     tmem_ld32_async(tmem_row + TM_ACC + 128 + cg * 32, r + 32);
     tmem_wait_ld<64>(r);
   } else if (EPI == EPI_BWD_SWIGLU) {
-    // columns 16..63 of this warp's dA go to its TMEM stash (three rounds of 16), columns
+    // columns 16..63 of this warp's dA go to its TMEM stash (32 and 16 columns), columns
     // 0..15 stay in registers; then the accumulator is free for the next tile
     have = c0 < ncols;
     if (have) {
+      // two TMEM round trips before the accumulator is released (it gates the next tile's MMAs)
       const uint32_t stash = tmem_row + TM_DA_STASH + uint32_t(cg) * TM_DA_STASH_W;
-#pragma unroll
-      for (int k = 0; k < 3; ++k) {
-        tmem_ld16_async(tmem_row + TM_ACC + c0 + 16 + 16 * k, r);
-        tmem_wait_ld<16>(r);
-        tmem_st16(stash + 16 * k, r);
-      }
+      tmem_ld32_async(tmem_row + TM_ACC + c0 + 16, r);
+      tmem_ld16_async(tmem_row + TM_ACC + c0 + 48, r + 32);
+      tmem_wait_ld<48>(r);
+      tmem_st32(stash, r);
+      tmem_st16(stash + 32, r + 32);
       tmem_ld16_async(tmem_row + TM_ACC + c0, r);
       tmem_wait_ld<16>(r);
       tmem_wait_st();
