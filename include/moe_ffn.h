@@ -599,23 +599,6 @@ moe_status moe_selftest_epilogue_quant(const float* src, int32_t rows, int32_t c
                                        uint8_t* scales, uint8_t* codes_t, uint8_t* scales_t, moe_stream_t stream);
 
 /*
- * moe_selftest_epilogue_quant_rto -- the row-wise MX quantizer as the SwiGLU
- * backward's epilogue runs it on dg and du (same page and section): the scale
- * from the float32 block maximum, the values kept between the epilogue's two
- * passes as bf16 rounded to odd (high 16 bits, last bit set when a dropped bit
- * is nonzero), then encoded.  Round-to-odd to at least two more bits than E4M3's
- * four makes the second rounding exact, so every code must equal the code of the
- * float32 value itself.
- *   src     f32 [rows][cols] (rows, cols multiples of 128, rows*cols <= 2^31)
- *   codes   out E4M3 [rows][cols] (32-byte aligned), blocks of 32 along cols
- *   scales  out E8M0, tile layout of [rows][cols/32]
- * Errors: MOE_ERR_INVALID_ARG (a NULL pointer), MOE_ERR_ALIGNMENT, MOE_ERR_UNSUPPORTED (sizes),
- * MOE_ERR_CUDA (launch).  Nothing is allocated.
- */
-moe_status moe_selftest_epilogue_quant_rto(const float* src, int32_t rows, int32_t cols, uint8_t* codes,
-                                           uint8_t* scales, moe_stream_t stream);
-
-/*
  * moe_selftest_mma_issue -- the tensor pipe's MXFP8 issue ceiling for the GEMM's
  * instruction mix, a measurement aid with no counterpart in the pages.  One
  * launch of SMs/2 CTA pairs (one CTA per SM); in each pair one thread issues

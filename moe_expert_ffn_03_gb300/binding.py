@@ -21,8 +21,7 @@ EXPORTS = (
     "moe_selftest_wait_timeout", "moe_router_fwd", "moe_router_bwd", "moe_gather_rows", "grouped_mlp_fwd_bf16",
     "fp8_tensor_quantize", "moe_fp8_tensor_quantize_tokens", "grouped_mlp_fwd_fp8_tensor",
     "mxfp8_quantize_experts", "fp8_tensor_quantize_experts", "moe_transpose_bf16", "grouped_mlp_bwd_bf16",
-    "grouped_mlp_bwd_fp8_tensor", "moe_workspace_tensor", "moe_selftest_epilogue_quant", "moe_selftest_epilogue_quant_rto",
-    "moe_selftest_mma_issue",
+    "grouped_mlp_bwd_fp8_tensor", "moe_workspace_tensor", "moe_selftest_epilogue_quant", "moe_selftest_mma_issue",
     "moe_transpose_bf16_experts", "grouped_mlp_fwd_bf16_experts", "moe_route", "moe_permute", "moe_ep_pack",
     "moe_gather_f32",
 )
@@ -99,7 +98,6 @@ def lib() -> ctypes.CDLL:
             "moe_workspace_tensor": ([D, c_int32, c_int32, ctypes.POINTER(c_size_t), ctypes.POINTER(c_size_t)],
                                      c_int32),
             "moe_selftest_epilogue_quant": ([P, c_int32, c_int32, P, P, P, P, P], c_int32),
-            "moe_selftest_epilogue_quant_rto": ([P, c_int32, c_int32, P, P, P], c_int32),
             "moe_selftest_mma_issue": ([c_int32, P, c_size_t, ctypes.POINTER(c_int32), P], c_int32),
             "moe_transpose_bf16_experts": ([ctypes.POINTER(P), c_int32, c_int32, c_int32, P, P], c_int32),
             "moe_route": ([D, P, P, P, P, P, P, P, P, c_size_t, P], c_int32),
@@ -246,10 +244,6 @@ def moe_workspace_tensor(d, training, which):
 def moe_selftest_epilogue_quant(src, rows, cols, codes, scales, codes_t, scales_t, stream=None):
     _check(lib().moe_selftest_epilogue_quant(_p(src), rows, cols, _p(codes), _p(scales), _p(codes_t), _p(scales_t),
                                              _st(stream)))
-
-
-def moe_selftest_epilogue_quant_rto(src, rows, cols, codes, scales, stream=None):
-    _check(lib().moe_selftest_epilogue_quant_rto(_p(src), rows, cols, _p(codes), _p(scales), _st(stream)))
 
 
 def moe_selftest_mma_issue(k_steps, scratch, stream=None):

@@ -1356,20 +1356,6 @@ moe_status moe_selftest_epilogue_quant(const float* src, int32_t rows, int32_t c
   return MOE_OK;
 }
 
-moe_status moe_selftest_epilogue_quant_rto(const float* src, int32_t rows, int32_t cols, uint8_t* codes,
-                                           uint8_t* scales, moe_stream_t stream) {
-  g_msg[0] = 0;
-  REQUIRE_PTR(src);
-  REQUIRE_PTR(codes);
-  REQUIRE_PTR(scales);
-  if (reinterpret_cast<uintptr_t>(codes) & 31u) return fail(MOE_ERR_ALIGNMENT, "codes must be 32-byte aligned");
-  if (rows < 128 || cols < 128 || rows % 128 || cols % 128 || int64_t(rows) * cols > (int64_t(1) << 31))
-    return fail(MOE_ERR_UNSUPPORTED, "rows=%d cols=%d: need multiples of 128, rows*cols <= 2^31", rows, cols);
-  CUDA_TRY(launch_epilogue_quant_rto_selftest(src, rows, cols, codes, scales, static_cast<cudaStream_t>(stream)),
-           "round-to-odd epilogue quantizer self-test");
-  return MOE_OK;
-}
-
 moe_status moe_selftest_mma_issue(int32_t k_steps, void* scratch, size_t scratch_bytes, int32_t* pairs,
                                   moe_stream_t stream) {
   g_msg[0] = 0;

@@ -736,42 +736,6 @@ __device__ __forceinline__ void swiglu_bwd_chunk(const uint32_t* d, const uint8_
   }
 }
 
-// Two floats as a bf16 pair rounded to odd (lo in the low half): the high 16 bits of each,
-// with the last bit set when a dropped bit is nonzero.  Rounding such a value to E4M3
-// (four significant bits, round to nearest even) gives the code of the float itself:
-// round-to-odd to at least two more bits than the final format makes the second rounding
-// exact (S. Boldo and G. Melquiond, "Emulation of FMA and correctly rounded sums: proved
-// algorithms using rounding to odd", IEEE Trans. Computers 57(4), 2008), and scaling by
-// a power of two commutes with both.  NaN stays NaN (its payload bits set the last bit)
-// and a finite value never becomes infinite.
-__device__ __forceinline__ uint32_t pack_bf16x2_rto(float lo, float hi) {
-  const uint32_t a = __float_as_uint(lo), b = __float_as_uint(hi);
-  return __byte_perm(a, b, 0x7632) | __vsetne2(__byte_perm(a, b, 0x5410), 0u);
-}
-// dg and du of chunk j (eight columns each) into the chunk's g and u slots of this lane's
-// staging row, and back.
-__device__ __forceinline__ void store_dgdu_chunk(uint8_t* gu_s, int j, int lane, const float* vg, const float* vu) {
-  *reinterpret_cast<uint4*>(gu_s + ((j ^ (lane & 7)) << 4)) =
-      make_uint4(pack_bf16x2_rto(vg[0], vg[1]), pack_bf16x2_rto(vg[2], vg[3]), pack_bf16x2_rto(vg[4], vg[5]),
-                 pack_bf16x2_rto(vg[6], vg[7]));
-  *reinterpret_cast<uint4*>(gu_s + (((4 + j) ^ (lane & 7)) << 4)) =
-      make_uint4(pack_bf16x2_rto(vu[0], vu[1]), pack_bf16x2_rto(vu[2], vu[3]), pack_bf16x2_rto(vu[4], vu[5]),
-                 pack_bf16x2_rto(vu[6], vu[7]));
-}
-__device__ __forceinline__ void load_dgdu_chunk(const uint8_t* gu_s, int j, int lane, float* vg, float* vu) {
-  const uint4 gw = *reinterpret_cast<const uint4*>(gu_s + ((j ^ (lane & 7)) << 4));
-  const uint4 uw = *reinterpret_cast<const uint4*>(gu_s + (((4 + j) ^ (lane & 7)) << 4));
-  const uint32_t gs[4] = {gw.x, gw.y, gw.z, gw.w};
-  const uint32_t us[4] = {uw.x, uw.y, uw.z, uw.w};
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    vg[2 * t] = bf16_lo(gs[t]);
-    vg[2 * t + 1] = bf16_hi(gs[t]);
-    vu[2 * t] = bf16_lo(us[t]);
-    vu[2 * t + 1] = bf16_hi(us[t]);
-  }
-}
-
 template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl, uint32_t tmem_row, int q, int cg,
                                               int lane, uint32_t tmem_empty_c, float* tr, uint8_t* gu_s) {
@@ -904,13 +868,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     // MXFP8 SwiGLU backward: this warp's 64 columns of dA, as two halves of 32, each in two
     // passes over four chunks of eight columns.  Pass A computes dg and du (packed pairs),
     // runs the along-token quantizer rounds of the chunk (their blocks run over the warp's
-    // 32 rows, so a chunk's eight columns are complete), raises the row-block maxima, sums
-    // dp, and leaves dg and du in the chunk's g,u slot as bf16 rounded to odd.  Pass B
-    // reads them back and writes their row-wise codes with the scales pass A found: the
-    // codes are those of the float values (round-to-odd keeps four more bits than E4M3's
-    // four).  A chunk's dA comes from registers (columns 0..15) or from the TMEM stash;
-    // only one chunk is live at a time, which keeps the epilogue within its registers.
-    // Pass B refills each chunk's slot with the next half's g,u as it frees it.
+    // 32 rows, so a chunk's eight columns are complete), raises the row-block maxima and
+    // sums dp.  Pass B recomputes the same dg and du (the same instructions on the same
+    // inputs: bit-identical) and writes their row-wise codes with the scales pass A found.
+    // A chunk's dA comes from registers (columns 0..15) or from the TMEM stash, loaded one
+    // chunk ahead; only one chunk is processed at a time, which keeps the epilogue within
+    // its registers.  Pass B refills each chunk's g,u slot with the next half's as it frees it.
     float2 dp2 = make_float2(0.f, 0.f);
     if (have) {
       const float p = a.prob_perm[row];
@@ -935,7 +898,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
           if (j < 3) da_issue(r, stash, h, j + 1, dn);     // in flight during this chunk's work
           float vg[8], vu[8];
           swiglu_bwd_chunk(d, gu_s, j, lane, p2, vg, vu, &dp2);
-          store_dgdu_chunk(gu_s, j, lane, vg, vu);
 #pragma unroll
           for (int t = 0; t < 8; t += 2) {
             amax_g = amax_raise(amax_g, vg[t], vg[t + 1]);
@@ -951,10 +913,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
         uint8_t* row_g = a.q_row + row * twoI + col;
         uint8_t* row_u = row_g + a.I;
         uint32_t qg[8], qu[8];
+        da_issue(r, stash, h, 0, dn);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
+          da_land(h, j, dn);
+          uint32_t d[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) d[i] = dn[i];
+          if (j < 3) da_issue(r, stash, h, j + 1, dn);
           float vg[8], vu[8];
-          load_dgdu_chunk(gu_s, j, lane, vg, vu);
+          swiglu_bwd_chunk(d, gu_s, j, lane, p2, vg, vu, nullptr);
           if (h == 0) stage_gu_chunk(a, row, col + 32, gu_s, lane & 7, j);   // the next half's chunk j
           const uint2 eg = mx_encode8(vg, c_g), eu = mx_encode8(vu, c_u);
           qg[2 * j] = eg.x;
@@ -1299,16 +1267,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // block (bx*4 + w) of an f32 [rows][cols] tensor, each lane one row's 32 values, exactly
 // as an epilogue warp holds them, and calls the epilogue's row-wise and along-token
 // quantizers on them.
-// RTO: the row-wise codes the way the SwiGLU backward's pass B makes them: the scale from
-// the float block maximum, the values through a g,u staging slot as bf16 rounded to odd
-// (the epilogue's own store and load), then encoded; no along-token copy.
 constexpr int EQ_WARPS = 4;
-template <bool RTO>
 __global__ void __launch_bounds__(32 * EQ_WARPS) epilogue_quant_selftest_kernel(
     const float* __restrict__ src, int rows, int cols, uint8_t* codes, uint8_t* scales, uint8_t* codes_t,
     uint8_t* scales_t) {
   __shared__ float tr_all[EQ_WARPS * TR_WARP_FLOATS];
-  __shared__ __align__(16) uint8_t gu_all[RTO ? EQ_WARPS * 32 * GU_PITCH : 16];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t blk = int64_t(blockIdx.x) * EQ_WARPS + warp;
   const int cb = cols / 32;
@@ -1325,28 +1288,6 @@ __global__ void __launch_bounds__(32 * EQ_WARPS) epilogue_quant_selftest_kernel(
     v[4 * i + 1] = q.y;
     v[4 * i + 2] = q.z;
     v[4 * i + 3] = q.w;
-  }
-  if (RTO) {
-    uint8_t* gu_s = gu_all + (warp * 32 + lane) * GU_PITCH;
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; i += 2) amax = amax_raise(amax, v[i], v[i + 1]);
-    const uint32_t c = mx_scale_code(__float_as_uint(amax));
-    uint32_t q[8];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float vg[8], vu[8];
-      store_dgdu_chunk(gu_s, j, lane, v + 16 * j, v + 16 * j + 8);
-      load_dgdu_chunk(gu_s, j, lane, vg, vu);
-      const uint2 eg = mx_encode8(vg, c), eu = mx_encode8(vu, c);
-      q[4 * j] = eg.x;
-      q[4 * j + 1] = eg.y;
-      q[4 * j + 2] = eu.x;
-      q[4 * j + 3] = eu.y;
-    }
-    st_global_v8(codes + row * cols + col, q);
-    scales[sf_offset(row, col >> 5, cols)] = uint8_t(c);
-    return;
   }
   quant_row_block(v, codes, scales, row, col, cols);
   quant_col_block(v, codes_t, scales_t, row_blk0, col, rows, lane, tr_all + warp * TR_WARP_FLOATS);
@@ -1874,17 +1815,8 @@ cudaError_t launch_epilogue_quant_selftest(const float* src, int rows, int cols,
                                            uint8_t* codes_t, uint8_t* scales_t, cudaStream_t st) {
   const int64_t blocks = int64_t(rows / 32) * (cols / 32);
   const int64_t grid = (blocks + EQ_WARPS - 1) / EQ_WARPS;
-  epilogue_quant_selftest_kernel<false><<<unsigned(grid), 32 * EQ_WARPS, 0, st>>>(src, rows, cols, codes, scales,
-                                                                                  codes_t, scales_t);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_epilogue_quant_rto_selftest(const float* src, int rows, int cols, uint8_t* codes, uint8_t* scales,
-                                               cudaStream_t st) {
-  const int64_t blocks = int64_t(rows / 32) * (cols / 32);
-  const int64_t grid = (blocks + EQ_WARPS - 1) / EQ_WARPS;
-  epilogue_quant_selftest_kernel<true><<<unsigned(grid), 32 * EQ_WARPS, 0, st>>>(src, rows, cols, codes, scales,
-                                                                                 nullptr, nullptr);
+  epilogue_quant_selftest_kernel<<<unsigned(grid), 32 * EQ_WARPS, 0, st>>>(src, rows, cols, codes, scales, codes_t,
+                                                                           scales_t);
   return cudaGetLastError();
 }
 

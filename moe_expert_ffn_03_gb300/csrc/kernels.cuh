@@ -241,10 +241,6 @@ cudaError_t launch_epilogue_quant_selftest(const float* src, int rows, int cols,
 // The MXFP8 MMA issue ceiling: one launch of SMs/2 CTA pairs, each issuing k_steps
 // K steps of the GEMM's MMAs (M=256, N=256, K=128 per step, with its scale copies)
 // on resident zero operands; *pairs = the pairs launched.  err: device error word.
-// The row-wise quantizer as the SwiGLU backward's second pass runs it (values stored
-// between the passes as bf16 rounded to odd): codes [rows][cols], scales in the tile layout.
-cudaError_t launch_epilogue_quant_rto_selftest(const float* src, int rows, int cols, uint8_t* codes, uint8_t* scales,
-                                               cudaStream_t st);
 cudaError_t launch_mma_rate_selftest(int k_steps, int* err, int* pairs, cudaStream_t st);
 
 // b_experts (host array of E pointers, E <= 128; the bf16 forward kinds only): B is one

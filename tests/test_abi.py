@@ -186,9 +186,6 @@ def test_selftest_entry_points_check_their_arguments(lib):
     assert lib.moe_selftest_mma_issue(10, p, 64, ctypes.byref(pairs), None) == 4          # scratch too small
     assert lib.moe_selftest_epilogue_quant(p, 128, 100, p, p, p, p, None) == 2           # cols % 128
     assert lib.moe_selftest_epilogue_quant(None, 128, 128, p, p, p, p, None) == 1
-    assert lib.moe_selftest_epilogue_quant_rto(p, 128, 100, p, p, None) == 2               # cols % 128
-    assert lib.moe_selftest_epilogue_quant_rto(None, 128, 128, p, p, None) == 1
-    assert lib.moe_selftest_epilogue_quant_rto(p, 128, 128, ctypes.c_void_p(272), p, None) == 3   # codes % 32
 
 
 def test_noalloc_names_the_bad_field(lib):

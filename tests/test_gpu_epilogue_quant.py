@@ -78,7 +78,7 @@ def f32_from_bits(bits):
     return np.asarray(bits, dtype=np.uint32).view(np.float32)
 
 
-def hand_placed():
+def test_scale_boundary_and_rounding_ties():
     """Hand-placed float32 values (128 x 128): block maxima with significand 1.75 (0x600000,
     the largest that keeps e = E - 8) and one ulp above it; elements that sit exactly half
     way between two E4M3 codes after scaling (ties to even), in the normal and the
@@ -129,49 +129,8 @@ def hand_placed():
             | (rng.integers(0, 2, size=(128, 64), dtype=np.int64) << 31)).astype(np.uint32)
     v[:, 64:] = bits.view(np.float32)
     assert np.all(np.isfinite(v))
-    return v
-
-
-def test_scale_boundary_and_rounding_ties():
-    v = hand_placed()
     check_bit_exact(v, "hand-placed")
     check_bit_exact(np.ascontiguousarray(v.T), "hand-placed, transposed")
-
-
-def run_device_rto(v32):
-    rows, cols = v32.shape
-    src = torch.from_numpy(np.ascontiguousarray(v32, dtype=np.float32)).cuda()
-    codes = torch.full((rows, cols), 0xA5, dtype=torch.uint8, device="cuda")
-    scales = torch.full((rows * cols // 32,), 0xA5, dtype=torch.uint8, device="cuda")
-    B.moe_selftest_epilogue_quant_rto(src, rows, cols, codes, scales)
-    torch.cuda.synchronize()
-    return codes.cpu().numpy(), untile_scales(scales.cpu().numpy(), rows, cols)
-
-
-def check_rto_bit_exact(v32, name):
-    v = np.asarray(v32, dtype=np.float32).astype(np.float64)
-    c, s = run_device_rto(v32)
-    ref_c, ref_s = mx.quantize_blocks(v, axis=1)
-    assert np.array_equal(s, ref_s), f"{name}: row scales"
-    assert np.array_equal(c, ref_c), f"{name}: row codes ({np.count_nonzero(c != ref_c)} differ)"
-
-
-@pytest.mark.parametrize("wl", [configs.get(configs.TINY),
-                                configs.small(300, 256, 384, 6, 2, routing="biased", backward=True)],
-                         ids=["tiny", "ragged_T300_I384_E6"])
-def test_round_to_odd_pass_codes_equal_the_float_codes(wl):
-    """The SwiGLU backward keeps dg and du between its two passes as bf16 rounded to odd;
-    its row-wise codes must still be the codes of the float32 values: the oracle's own dH,
-    the hand-placed ties and boundaries (a tie one float32 ulp off is where a plain bf16
-    rounding would break it), and random float32 over many binades."""
-    _, dH = oracle_intermediates(wl)
-    check_rto_bit_exact(dH.astype(np.float32), "dH")
-    v = hand_placed()
-    check_rto_bit_exact(v, "hand-placed")
-    check_rto_bit_exact(np.ascontiguousarray(v.T), "hand-placed, transposed")
-    rng = np.random.default_rng(5)
-    r = (rng.standard_normal((256, 512)) * np.exp2(rng.integers(-40, 40, (256, 512)))).astype(np.float32)
-    check_rto_bit_exact(r, "random binades")
 
 
 def test_host_checks():
