@@ -163,9 +163,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// arrive on an mbarrier anywhere in the cluster (release at cluster scope)
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+// Arrive on an mbarrier anywhere in the cluster, without release semantics: the arrival
+// does not wait for this thread's earlier global stores to be performed.  For handing the
+// accumulator back to the MMA warp, which needs only this warp's TMEM reads finished:
+// tcgen05.wait::ld has returned (the values are in registers) and
+// tcgen05.fence::before_thread_sync orders them before the arrival.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 // Tensor copy into this CTA's shared memory; completion is signalled on the
 // mbarrier at cluster address bar_c, which may sit in the pair's other CTA.
@@ -741,7 +745,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
                                               int lane, uint32_t tmem_empty_c, float* tr, uint8_t* gu_s) {
   if (!tl.valid) {
     __syncwarp();
-    if (lane == 0) mbar_arrive_cluster(tmem_empty_c);
+    if (lane == 0) mbar_arrive_cluster_relaxed(tmem_empty_c);
     return;
   }
   const int64_t row = tl.out_row + q * 32 + lane;        // output / permuted row of this thread
@@ -793,7 +797,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
   }
   tc_fence_before();
   __syncwarp();
-  if (lane == 0) mbar_arrive_cluster(tmem_empty_c);
+  if (lane == 0) mbar_arrive_cluster_relaxed(tmem_empty_c);
 
   if (EPI == EPI_BF16 || EPI == EPI_B16_OUT || EPI == EPI_T8_OUT) {
     if (c0 >= ncols) return;
