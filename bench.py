@@ -36,10 +36,10 @@ WORKLOAD = "mixtral_fwdbwd_T16384_H4096_I14336_E8_k2"
 METRIC = "grouped expert-MLP fwd+bwd TFLOP/s (MXFP8, algorithmic 18*R*H*I per step)"
 # dram__bytes_read.sum + dram__bytes_write.sum of the six grouped-GEMM launches of
 # one step of the default workload, like `achieved` (which is over the same six
-# launches): 5.593 GB from an ncu capture at T=4096, E=2 (every expert with the
+# launches): 5.558 GB from an ncu capture at T=4096, E=2 (every expert with the
 # full workload's 4096 rows), times 4 for E=8 (profiles/ holds the summary).
 # Set to None when the GEMM kernel changes, until it is captured again.
-GEMM_TRAFFIC_BYTES = 22_372_000_000
+GEMM_TRAFFIC_BYTES = 22_233_000_000
 
 
 def read_peaks():
