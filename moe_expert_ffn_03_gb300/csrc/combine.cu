@@ -13,7 +13,7 @@ template <bool V8>
 __global__ void __launch_bounds__(256) combine_kernel(
     const __nv_bfloat16* __restrict__ y, const int* __restrict__ row_of, const float* __restrict__ prob,
     int T, int k, int H, int64_t cap, __nv_bfloat16* __restrict__ out, int* err) {
-  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_wait();                 // may start early (programmatic stream serialization)
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
 __global__ void __launch_bounds__(256) dprob_reduce_kernel(
     const float* __restrict__ dp_part, int n_tiles, int64_t cap, const int* __restrict__ row_of, int64_t R,
     float* __restrict__ dprob, int* err) {
-  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_wait();                 // may start early (programmatic stream serialization)
   pdl_launch_dependents();
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= R) return;
@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(32 * DPR_WARPS) dprob_reduce_rows_kernel(
     const float* __restrict__ dp_part, int n_tiles, int64_t cap, const int* __restrict__ split_sizes, int E,
     const int* __restrict__ src_of, const int* __restrict__ row_of, int k, int T, float* __restrict__ dprob,
     int* err) {
-  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_wait();                 // may start early (programmatic stream serialization)
   pdl_launch_dependents();
   __shared__ int64_t total_s;
   __shared__ float part[DPR_WARPS][32];

@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(
     const int* __restrict__ row_of, int k, int64_t cap,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int* err, bool v8_src, bool v8_dst,
     const int* __restrict__ pad_split, int pad_E, int token_blocks, PermuteRows pr) {
-  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_wait();                 // may start early (programmatic stream serialization)
   pdl_launch_dependents();
   if (pad_split != nullptr && int(blockIdx.x) >= token_blocks) {
     const int pb = blockIdx.x - token_blocks;
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(
 __global__ void __launch_bounds__(256) fill_pad_rows_kernel(
     const int* __restrict__ split_sizes, int E, int cols, int64_t cap,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int* err) {
-  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_wait();                 // may start early (programmatic stream serialization)
   pdl_launch_dependents();
   fill_pad_rows_block(split_sizes, E, cols, cap, codes, scales, nullptr, nullptr, err, blockIdx.x, blockIdx.y);
 }
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(QG_THREADS, 12) quant_colwise_kernel(
     const __grid_constant__ CUtensorMap src_rows, const int* __restrict__ src_map, int n_src_rows, int rows,
     int cols, const int* __restrict__ split_sizes, int E, uint8_t* __restrict__ codes_t,
     uint8_t* __restrict__ scales_t, int* err, bool v8, uint64_t wait_limit_ns) {
-  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_wait();                 // may start early (programmatic stream serialization)
   pdl_launch_dependents();
   __shared__ __align__(1024) __nv_bfloat16 tile[QG_ROWS * QG_COLS];
   __shared__ __align__(16) uint8_t sc_half[256];
@@ -308,7 +308,7 @@ template <class Src>
 __global__ void __launch_bounds__(256, 6) quant_dual_kernel(
     const __grid_constant__ Src src, int rows, int cols, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t, bool v8) {
-  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_wait();                 // may start early (programmatic stream serialization)
   pdl_launch_dependents();
   __shared__ __align__(16) __nv_bfloat16 tile[QC_TILE * QC_PITCH];
   __shared__ __align__(16) uint8_t sc_row[512];

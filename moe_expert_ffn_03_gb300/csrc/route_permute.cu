@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(NT) route_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renorm,
     int* __restrict__ idx, float* __restrict__ prob, uint32_t* __restrict__ masks, int G, int* err,
     unsigned* ticket, int* __restrict__ bases, int* __restrict__ split_sizes) {
-  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_wait();                 // may start early (programmatic stream serialization)
   pdl_launch_dependents();
   __shared__ uint32_t smask[NT / 32][kMaxE];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -187,7 +187,7 @@ constexpr int RQ_THREADS = 128;                      // 32 tokens x 4 lanes
 __global__ void __launch_bounds__(RQ_THREADS) route_topk_quad_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renorm,
     int* __restrict__ idx, float* __restrict__ prob, uint32_t* __restrict__ masks, int G, int* err) {
-  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_wait();                 // may start early (programmatic stream serialization)
   pdl_launch_dependents();
   __shared__ uint32_t smask[kMaxE];
   const int lane = threadIdx.x & 31, sub = lane & 3;
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(RQ_THREADS) route_topk_quad_kernel(
 // One CTA per expert: exclusive scan over groups of popc(mask).
 __global__ void __launch_bounds__(1024) permute_scan_kernel(
     const uint32_t* __restrict__ masks, int G, int* __restrict__ bases, int* __restrict__ split_sizes) {
-  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_wait();                 // may start early (programmatic stream serialization)
   pdl_launch_dependents();
   __shared__ int warp_sums[32];
   __shared__ int carry_s;
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
     const uint32_t* __restrict__ masks, const int* __restrict__ bases, const int* __restrict__ split_sizes,
     int* __restrict__ row_of, int* __restrict__ src_of, float* __restrict__ prob_perm, int token_blocks,
     int* err) {
-  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_wait();                 // may start early (programmatic stream serialization)
   pdl_launch_dependents();
   __shared__ int seg_start[kMaxE + 1];
   if (threadIdx.x == 0) {
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
 // An id outside 0..E-1 is recorded and its slot skipped (the scatter marks it -1).
 __global__ void __launch_bounds__(RT_THREADS) idx_masks_kernel(const int* __restrict__ idx, int T, int E, int k,
                                                                uint32_t* __restrict__ masks, int G, int* err) {
-  pdl_wait();                 // launched with programmatic stream serialization
+  pdl_wait();                 // may start early (programmatic stream serialization)
   pdl_launch_dependents();
   __shared__ uint32_t smask[RT_THREADS / 32][kMaxE];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
